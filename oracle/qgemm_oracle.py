@@ -1,0 +1,163 @@
+"""Plain CPU oracle of the quantized-weight GEMM  Y = X . dequant(Wq)^T.
+
+TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the CPU legs of
+bench.py may import this module.  It shares no code, table or constant with the CUDA
+library and never calls it.
+
+What it computes, and where that comes from:
+  * "Humming wird angekündigt" (vLLM blog, German edition), section "Eine einheitliche
+    Quantisierungsdarstellung": a weight is described by its format, scale granularity
+    (group size), scale dtype, zero points and secondary scales; activations have their own
+    format.  Example given there: group-wise INT4 weights paired with BF16 activations.
+  * Same page, sections "WnA16" and "W8A8 / W4A8 / W4A4": W4A16 (4-bit weights, BF16
+    activations) and W4A8-MXFP4 (MXFP4 weights, FP8 activations), each dense and as an MoE
+    grouped path; section "End-to-End-Inferenzleistung": FP8 activations are tokenwise.
+  * "蚂蚁与vLLM开源量化推理内核Humming", paragraph 支持矩阵: symmetric INT weights and INT
+    weights with zero points; FP4 e2m1 weights.
+  * Same page, paragraph 架构设计 and the German page's "Gemeinsam genutzte
+    CUDA-Komponenten": dequantization and scaling are fused into the GEMM and scaling can be
+    fused into the output stage (the secondary per-channel scale below).
+
+Readings where the pages are silent (each is listed in the design notes):
+  * canonical codes: uint8 [N, K/2], element k of row n in byte k//2, even k in the low
+    nibble;
+  * INT4 symmetric: the nibble is a two's-complement q in [-8, 7], w = q * s[n, k//g];
+  * INT4 with zero point: q, z in [0, 15], w = (q - z) * s[n, k//g] (no "+1" offset);
+  * MXFP4: w = e2m1(q) * 2^(e[n, k//32] - 127);
+  * secondary scale: optional float32 c[n] multiplying output column n;
+  * FP8 activation quantization: per row m, s_m = amax_m / 448 in float32 (1.0 when the row
+    is all zero), codes = e4m3 round-to-nearest-even with saturation of x / s_m computed in
+    float32.
+
+The matmul accumulates in float64 from the exact dequantized weights; nothing is blocked,
+fused or reordered beyond the plain definition.
+"""
+import numpy as np
+
+from . import formats as F
+
+WFMTS = ("int4_sym", "uint4_zp", "mxfp4")
+
+
+def unpack_nibbles(codes):
+    """uint8 [N, K/2] -> uint8 [N, K] with element k taken from byte k//2, even k low."""
+    codes = np.asarray(codes, dtype=np.uint8)
+    n, kh = codes.shape
+    out = np.empty((n, 2 * kh), dtype=np.uint8)
+    out[:, 0::2] = codes & 0xF
+    out[:, 1::2] = codes >> 4
+    return out
+
+
+def scale_values(wfmt, scales):
+    """Per-group scale values as float64: BF16 bit patterns, or E8M0 exponents for MXFP4."""
+    if wfmt == "mxfp4":
+        return F.e8m0_to_float(scales)
+    return F.bf16_bits_to_float(scales)
+
+
+def dequant(wfmt, group, codes, scales, zeros=None):
+    """Exact dequantized weights W [N, K] in float64.
+
+    wfmt: "int4_sym" | "uint4_zp" | "mxfp4"; group: K-elements per scale (32 for mxfp4);
+    codes: uint8 [N, K/2]; scales: uint16 bf16 bits [N, K/group] (uint8 E8M0 for mxfp4);
+    zeros: uint8 [N, K/group] in [0, 15] for "uint4_zp", else None.
+    """
+    if wfmt not in WFMTS:
+        raise ValueError(wfmt)
+    q = unpack_nibbles(codes)
+    n, k = q.shape
+    if k % group:
+        raise ValueError("K must be a multiple of the group size")
+    gidx = np.arange(k) // group                       # group of each K position
+    s = scale_values(wfmt, scales)[:, gidx]            # [N, K]
+    if wfmt == "int4_sym":
+        return F.int4_signed(q).astype(np.float64) * s
+    if wfmt == "uint4_zp":
+        z = np.asarray(zeros).astype(np.int64)[:, gidx]
+        return (q.astype(np.int64) - z).astype(np.float64) * s
+    return F.e2m1_to_float(q) * s
+
+
+def dequant_bf16(wfmt, group, codes, scales, zeros=None):
+    """The weights as a kernel must feed them to a BF16 tensor core: RNE_bf16(W_exact)."""
+    return F.round_to_bf16(dequant(wfmt, group, codes, scales, zeros))
+
+
+def gemm(x, w, chan_scale=None, tok_scale=None):
+    """y[m, n] = tok_scale[m] * chan_scale[n] * sum_k x[m, k] * w[n, k], in float64.
+
+    x: activation values [M, K] (any real dtype, used exactly); w: exact weights [N, K].
+    """
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+    if tok_scale is not None:
+        y = y * np.asarray(tok_scale, dtype=np.float64)[:, None]
+    if chan_scale is not None:
+        y = y * np.asarray(chan_scale, dtype=np.float64)[None, :]
+    return y
+
+
+def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+    """Dense W4A16: BF16 activations (bit patterns [M, K]) times dequantized weights."""
+    x = F.bf16_bits_to_float(x_bits)
+    return gemm(x, dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+
+
+def quant_act_fp8(x_bits):
+    """Tokenwise FP8 e4m3 activation quantization of BF16 rows.
+
+    Returns (codes uint8 [M, K], scale float32 [M]).  Decisions are taken in float32: the
+    row maximum, s = amax / 448, and the quotient x / s that is rounded to e4m3.
+    """
+    x = F.bf16_bits_to_float(x_bits).astype(np.float32)
+    amax = np.max(np.abs(x), axis=1) if x.shape[1] else np.zeros(x.shape[0], np.float32)
+    s = (amax.astype(np.float32) / np.float32(F.E4M3_MAX)).astype(np.float32)
+    s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
+    v = (x / s[:, None]).astype(np.float32)            # IEEE float32 quotient
+    return F.e4m3_encode(F.round_to_e4m3_satfinite(v.astype(np.float64))), s
+
+
+def w4a8(xq, tok_scale, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+    """Dense W4A8: y = s_tok[m] * sum_k e4m3(xq[m, k]) * W[n, k]  (times c[n] if given)."""
+    x = F.e4m3_to_float(xq)
+    return gemm(x, dequant(wfmt, group, codes, scales, zeros),
+                chan_scale=chan_scale, tok_scale=tok_scale)
+
+
+def moe_grouped(x_rows, offsets, experts, tok_scale=None, chan_scales=None):
+    """MoE grouped GEMM over expert-sorted rows.
+
+    x_rows: activation values [R, K] sorted by expert; offsets: int [E+1], rows
+    offsets[e]..offsets[e+1] belong to expert e; experts: list of E exact weights [N, K].
+    Each expert's block of rows is an ordinary dense GEMM with that expert's weights
+    ("Humming wird angekündigt", section "WnA16": tokens are distributed over experts and
+    the work per expert varies with the load).
+    """
+    x_rows = np.asarray(x_rows, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    n = experts[0].shape[0]
+    y = np.zeros((x_rows.shape[0], n), dtype=np.float64)
+    for e, w in enumerate(experts):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            ts = None if tok_scale is None else np.asarray(tok_scale)[a:b]
+            cs = None if chan_scales is None else chan_scales[e]
+            y[a:b] = gemm(x_rows[a:b], w, chan_scale=cs, tok_scale=ts)
+    return y
+
+
+def tolerance_ok(y, y_ref, rel):
+    """The parity bar: |y - y_ref| <= rel * max(|y_ref|, rms(y_ref)) elementwise.
+
+    Returns (ok, worst ratio of error to the allowed bound)."""
+    y = np.asarray(y, dtype=np.float64)
+    y_ref = np.asarray(y_ref, dtype=np.float64)
+    if y_ref.size == 0:
+        return True, 0.0
+    rms = float(np.sqrt(np.mean(y_ref * y_ref)))
+    bound = rel * np.maximum(np.abs(y_ref), rms)
+    err = np.abs(y - y_ref)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        ratio = np.where(bound > 0, err / bound, np.where(err > 0, np.inf, 0.0))
+    worst = float(np.max(ratio))
+    return bool(worst <= 1.0 and np.all(np.isfinite(y))), worst

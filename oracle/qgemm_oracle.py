@@ -29,8 +29,9 @@ Readings where the pages are silent (each is listed in the design notes):
     is all zero), codes = e4m3 round-to-nearest-even with saturation of x / s_m computed in
     float32.
 
-The matmul accumulates in float64 from the exact dequantized weights; nothing is blocked,
-fused or reordered beyond the plain definition.
+The matmul accumulates in float64; W4A16 uses the dequantized weights as BF16 values (the
+operand of a 16-bit tensor core), W4A8 the exact e2m1 x E8M0 values (exact in FP8 with a
+block scale).  Nothing is blocked, fused or reordered beyond the plain definition.
 """
 import numpy as np
 
@@ -98,9 +99,14 @@ def gemm(x, w, chan_scale=None, tok_scale=None):
 
 
 def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None):
-    """Dense W4A16: BF16 activations (bit patterns [M, K]) times dequantized weights."""
+    """Dense W4A16: BF16 activations (bit patterns [M, K]) times the dequantized weights.
+
+    W4A16 computes on 16-bit tensor cores ("Humming wird angekündigt", section "WnA16":
+    low-bit weights combined with FP16/BF16 activations, using the widely available 16-bit
+    compute), so the dequantized weight is the BF16 value RNE_bf16(W_exact) -- the same
+    weights the dequantization must reproduce bit for bit.  The sum runs in float64."""
     x = F.bf16_bits_to_float(x_bits)
-    return gemm(x, dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+    return gemm(x, dequant_bf16(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
 
 
 def quant_act_fp8(x_bits):

@@ -36,6 +36,17 @@ def test_worked_int4_examples(name):
     np.testing.assert_array_equal(Y, np.array(g["Y"], dtype=np.float64))
 
 
+def test_worked_bf16_weight_rounding():
+    g, wfmt, group, codes, scales, zeros = _golden_weights("worked_bf16_weights.txt")
+    np.testing.assert_array_equal(oracle.dequant(wfmt, group, codes, scales, zeros),
+                                  np.array(g["Wexact"], dtype=np.float64))
+    np.testing.assert_array_equal(oracle.dequant_bf16(wfmt, group, codes, scales, zeros),
+                                  np.array(g["W"], dtype=np.float64))
+    xb = F.float_to_bf16_bits(np.array(g["X"], dtype=np.float64))
+    Y = oracle.w4a16(xb, wfmt, group, codes, scales, zeros)
+    np.testing.assert_array_equal(Y, np.array(g["Y"], dtype=np.float64))
+
+
 def test_worked_mxfp4_example():
     g, wfmt, group, codes, scales, zeros = _golden_weights("worked_mxfp4.txt")
     W = oracle.dequant(wfmt, group, codes, scales)
@@ -112,7 +123,7 @@ def test_integer_brute_force(wfmt, group):
 
 def test_one_hot_reproduces_weight_columns():
     x, w = WL.tiny_dense(seed=3)
-    W = oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros)
     K = w.K
     for k in (0, 1, 127, 128, 129, K - 1):
         onehot = np.zeros((1, K))

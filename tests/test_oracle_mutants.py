@@ -19,6 +19,7 @@ PINS = [
     lambda: TG.test_worked_int4_examples("worked_uint4_zp.txt"),
     lambda: TG.test_worked_int4_examples("worked_int4_sym.txt"),
     TG.test_worked_mxfp4_example, TG.test_nibble_order_low_is_even,
+    TG.test_worked_bf16_weight_rounding,
     lambda: TG.test_integer_brute_force("int4_sym", 32),
     lambda: TG.test_integer_brute_force("uint4_zp", 64),
     lambda: TG.test_integer_brute_force("mxfp4", 32),
@@ -91,6 +92,11 @@ def _gemm_transposed(x, w, chan_scale=None, tok_scale=None):
     return y
 
 
+def _w4a16_exact_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+    x = F.bf16_bits_to_float(x_bits)
+    return Q.gemm(x, Q.dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+
+
 def _gemm_drop_tok_scale(x, w, chan_scale=None, tok_scale=None):
     return _orig_gemm(x, w, chan_scale=chan_scale, tok_scale=None)
 
@@ -115,6 +121,7 @@ MUTANTS = {
     "group index shifted": (Q, "dequant", _dequant_group_shift),
     "output columns permuted": (Q, "gemm", _gemm_transposed),
     "token scale dropped": (Q, "gemm", _gemm_drop_tok_scale),
+    "w4a16 without bf16 weights": (Q, "w4a16", _w4a16_exact_weights),
     "zero row not guarded": (Q, "quant_act_fp8", _quant_no_zero_guard),
 }
 

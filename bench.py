@@ -1,0 +1,346 @@
+"""Benchmark of the quantized-weight GEMM on one GB300 (or N replicas).
+
+Workload (one step): the dense W4A16 asymmetric-INT4 sweep -- uint4 codes with uint4 zero
+points and BF16 scales per group of 128, shapes N x K = 28672 x 8192 and 8192 x 28672,
+M = 1, 2, 4, ..., 8192 -- 28 GEMM calls, each timed alone with CUDA events after an L2
+flush (a 256 MiB device write, outside the events), mirroring the protocol of "Humming
+wird angekündigt" (vLLM blog, German edition), section "Leistung".
+
+value   = sum of 2*M*N*K over the step / sum of the event-timed call durations (TFLOP/s)
+e2e     = the same calls through the public API with X copied from pinned host memory and
+          Y copied back to pinned host memory inside the timed region
+roofline: dominant kernel = the 256-token-tile variant (M >= 256, tensor bound); small-M
+          (M <= 16, HBM bound) is reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (float64 numpy, one thread) on a bounded sample of
+the same workload.  Multi-GPU runs (torchrun) execute independent replicas (weak scaling);
+the GEMM has no exchange step.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "quantized GEMM TFLOP/s + weight GB/s vs M=1..8192, % of roofline (1 GB300)"
+SHAPES = ((28672, 8192), (8192, 28672))
+M_SWEEP = tuple(2 ** i for i in range(14))
+GROUP = 128
+WORKLOAD = ("dense W4A16 asymmetric INT4 (uint4 codes + uint4 zero points, BF16 scales, "
+            "group 128), N x K in {28672 x 8192, 8192 x 28672}, M = 1..8192 (powers of two)")
+FLUSH_BYTES = 256 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def weight_bytes(N, K, g=GROUP):
+    return N * K // 2 + N * (K // g) * 2 + N * (K // g) // 2
+
+
+def alg_bytes(M, N, K):
+    return weight_bytes(N, K) + M * K * 2 + M * N * 2
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- ours
+def build_inputs(device):
+    import numpy as np
+    import torch
+    import workloads as WL
+    import quantized_weight_gemm_gb300 as qg
+
+    cases = []
+    for (N, K) in SHAPES:
+        x, w = WL.int4_asym_shape(N, K, max(M_SWEEP), seed=0)
+        d = qg.WeightDesc("uint4_zp", N, K, GROUP)
+        packed = qg.repack(d, torch.from_numpy(w.codes).to(device),
+                           torch.from_numpy(w.scales.view(np.int16)).to(device),
+                           torch.from_numpy(w.zeros).to(device))
+        X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        Y = torch.empty(max(M_SWEEP), N, dtype=torch.bfloat16, device=device)
+        ws = qg.workspace(d, max(M_SWEEP), device)
+        cases.append({"N": N, "K": K, "desc": d, "packed": packed, "X": X, "Y": Y, "ws": ws,
+                      "x_host": torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory(),
+                      "y_host": torch.empty(max(M_SWEEP), N, dtype=torch.bfloat16).pin_memory()})
+        del x, w
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("repack reported a device error")
+    return cases
+
+
+def run_step(cases, flush, e2e=False):
+    """One pass over the sweep; returns [(N, K, M, ms)] from CUDA events per call."""
+    import torch
+    import quantized_weight_gemm_gb300 as qg
+    out = []
+    st = torch.cuda.current_stream()
+    for c in cases:
+        for M in M_SWEEP:
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(st)
+            if e2e:
+                c["X"][:M].copy_(c["x_host"][:M], non_blocking=True)
+            qg.w4a16(c["desc"], c["packed"], c["X"][:M], out=c["Y"][:M], ws=c["ws"])
+            if e2e:
+                c["y_host"][:M].copy_(c["Y"][:M], non_blocking=True)
+            e1.record(st)
+            out.append((c["N"], c["K"], M, e0, e1))
+    torch.cuda.synchronize()
+    return [(N, K, M, e0.elapsed_time(e1)) for (N, K, M, e0, e1) in out]
+
+
+def cpu_sample(seconds=12.0, threads=1):
+    """Time the oracle on a bounded sample in a fresh single-threaded process."""
+    env = dict(os.environ)
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        env[v] = str(threads)
+    code = f"""
+import json, sys, time
+sys.path.insert(0, {ROOT!r})
+import numpy as np
+import oracle, workloads as WL
+N, K, M, g = 28672, 8192, 16, 128
+x, w = WL.int4_asym_shape(N, K, M, seed=0)
+done_rows, flops, t_total = 0, 0.0, 0.0
+chunk = 512
+while done_rows < N and t_total < {seconds}:
+    a, b = done_rows, min(N, done_rows + chunk)
+    t0 = time.perf_counter()
+    y = oracle.w4a16(x, w.wfmt, w.group, w.codes[a:b], w.scales[a:b], w.zeros[a:b])
+    t_total += time.perf_counter() - t0
+    flops += 2.0 * M * (b - a) * K
+    done_rows = b
+print(json.dumps({{"flops": flops, "seconds": t_total, "rows": done_rows}}))
+"""
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                       timeout=600)
+    if r.returncode != 0:
+        raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["flops"] / d["seconds"] / 1e12, "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle",
+            "sample": (f"float64 numpy oracle, N x K = 28672 x 8192, M = 16, the first "
+                       f"{d['rows']} of 28672 weight rows (dequantize + matmul), "
+                       f"{d['seconds']:.1f} s, 1 thread")}
+
+
+def bench_ours(args):
+    import torch
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    import __graft_entry__ as ge
+    ge.build()
+    import quantized_weight_gemm_gb300 as qg
+    peaks, peak_kind = load_peaks()
+    device = torch.device("cuda", local)
+    cases = build_inputs(device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+
+    for _ in range(args.warmup):
+        run_step(cases, flush)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.perf_counter()
+    steps = [run_step(cases, flush) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    e2e_steps = [run_step(cases, flush, e2e=True) for _ in range(max(1, args.steps))]
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("a GEMM reported a device error")
+
+    flops_step = sum(2.0 * M * N * K for (N, K) in SHAPES for M in M_SWEEP)
+    step_ms = [sum(r[3] for r in s) for s in steps]
+    e2e_ms = [sum(r[3] for r in s) for s in e2e_steps]
+    local_ms = statistics.mean(step_ms)
+    local_e2e = statistics.mean(e2e_ms)
+    if dist is not None:
+        t = torch.tensor([local_ms, local_e2e], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        local_ms, local_e2e = float(t[0]), float(t[1])
+    value = ws * flops_step / (local_ms * 1e-3) / 1e12
+    e2e_value = ws * flops_step / (local_e2e * 1e-3) / 1e12
+
+    # per-call table (median over steps)
+    per = {}
+    for s in steps:
+        for (N, K, M, ms) in s:
+            per.setdefault((N, K, M), []).append(ms)
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    sweep = []
+    for (N, K, M), v in sorted(per.items(), key=lambda kv: (kv[0][0], kv[0][2])):
+        ms = statistics.median(v)
+        rt = max(alg_bytes(M, N, K) / bw, 2.0 * M * N * K / tc)
+        sweep.append({"N": N, "K": K, "M": M, "us": round(ms * 1e3, 2),
+                      "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2),
+                      "weight_gbs": round(weight_bytes(N, K) / (ms * 1e-3) / 1e9, 1),
+                      "roofline_frac": round(rt / (ms * 1e-3), 3),
+                      "bound": "hbm" if alg_bytes(M, N, K) / bw > 2.0 * M * N * K / tc else "tensor"})
+    big = [r for r in sweep if r["M"] >= 256]
+    big_time = sum(r["us"] for r in big) * 1e-6
+    big_flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in big)
+    achieved_tc = big_flops / big_time / 1e12
+    small = [r for r in sweep if r["M"] <= 16]
+    small_time = sum(r["us"] for r in small) * 1e-6
+    small_bytes = sum(alg_bytes(r["M"], r["N"], r["K"]) for r in small)
+    achieved_bw = small_bytes / small_time / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(local_ms, 3),
+        "wall_ms_per_step": round(wall * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: X ~ N(0,1) bf16, uint4 codes U[0,15], zero points U[6,9], "
+                "scales U[0.005,0.02] bf16)",
+        "config": {"workload": WORKLOAD, "shapes": [list(s) for s in SHAPES], "M": list(M_SWEEP),
+                   "l2": "flushed before every timed call (256 MiB device write outside the events)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "impl": "ours",
+        "roofline": {"bound": "tensor", "achieved": round(achieved_tc, 1),
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": round(achieved_tc / peaks["bf16_tflops"], 3), "traffic": None,
+                     "kernel": "qgemm_tc_kernel<256, bf16> (M >= 256 calls)",
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}"},
+        "roofline_small_m": {"bound": "hbm", "achieved": round(achieved_bw, 1),
+                             "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                             "frac": round(achieved_bw / peaks["hbm_gbs"], 3),
+                             "kernel": "qgemm_tc_kernel<16, bf16> (M <= 16 calls, split-K)",
+                             "peak_source": f"hbm_gbs of {peak_kind}"},
+        "sweep": sweep,
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": sum(M * K * 2 for (N, K) in SHAPES for M in M_SWEEP),
+                "d2h_bytes_per_step": sum(M * N * 2 for (N, K) in SHAPES for M in M_SWEEP)},
+        "gpu_launches": len(SHAPES) * len(M_SWEEP) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_sample()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def bench_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        cpu_sample(seconds=2.0)
+    t0 = time.perf_counter()
+    samples = [cpu_sample(seconds=8.0) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    v = statistics.mean(s["value"] for s in samples)
+    cb = dict(samples[-1])
+    cb["value"] = round(v, 6)
+    line = {
+        "metric": METRIC, "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(wall * 1e3 / args.steps, 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "shapes": [list(s) for s in SHAPES], "M": list(M_SWEEP),
+                   "l2": "n/a (CPU)", "parallelism": "single process"},
+        "impl": "reference", "cpu_baseline": cb,
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

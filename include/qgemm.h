@@ -1,0 +1,201 @@
+/*
+ * qgemm.h -- C ABI of the GB300 (sm_103a) quantized-weight GEMM library.
+ *
+ * The library computes Y = X . dequant(Wq)^T where the weights are 4-bit codes that are
+ * dequantized inside the kernel:
+ *   - INT4, symmetric: two's-complement q in [-8, 7], w = q * s[n, k/g], BF16 scales;
+ *   - INT4 with zero points: q, z in [0, 15], w = (q - z) * s[n, k/g], BF16 scales;
+ *   - MXFP4: e2m1 codes with one E8M0 exponent e per 32 K-elements, w = e2m1(q) * 2^(e-127).
+ * Activations are BF16 (W4A16) or FP8 e4m3 with one float32 scale per token (W4A8).
+ * There is a dense form and an MoE grouped form over expert-sorted rows.
+ *
+ * The problem statement follows "Humming wird angekündigt" (vLLM blog, German edition):
+ * section "Eine einheitliche Quantisierungsdarstellung" (weight format, scale granularity,
+ * scale dtype, zero points and secondary scales as separate parameters; activations with
+ * their own format), section "Tuning und JIT-Kompilierung für jeden Workload" (a
+ * preprocessing step validates, pads and repacks weights into a kernel layout; a layer is
+ * described by shapes, dtypes and quantization parameters), and sections "WnA16" and
+ * "W8A8 / W4A8 / W4A4" (dense and MoE grouped paths).
+ *
+ * Conventions for every call:
+ *   - Pointers named as device pointers must be CUDA device memory of the current device;
+ *     the caller owns all memory.  The library allocates nothing.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).  Calls are
+ *     asynchronous on it.  Argument errors are returned synchronously before any launch;
+ *     a failed launch returns QGEMM_ERR_CUDA.
+ *   - Conditions that only the GPU can see (a packed buffer whose header does not match
+ *     the descriptor, an invalid scale or zero point found by qgemm_repack, a bounded wait
+ *     that gave up) are recorded in a per-device status word; read it with
+ *     qgemm_device_status() after synchronizing.
+ *   - Matrices are row-major with an explicit leading dimension counted in elements.
+ *   - Y is overwritten (no accumulation into Y).  M = 0 is a no-op that returns QGEMM_OK.
+ *   - Concurrent calls on different streams are safe when they use separate workspaces.
+ */
+#ifndef QGEMM_H
+#define QGEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QGEMM_OK = 0,
+  QGEMM_ERR_INVALID_ARG = 1,   /* bad pointer, size, stride or descriptor field        */
+  QGEMM_ERR_UNSUPPORTED = 2,   /* valid but not implemented combination                */
+  QGEMM_ERR_ALIGNMENT = 3,     /* pointer or leading dimension misaligned for TMA      */
+  QGEMM_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required           */
+  QGEMM_ERR_BAD_PACKED = 5,    /* (device status) packed header does not match desc    */
+  QGEMM_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed                 */
+  QGEMM_ERR_TIMEOUT = 7,       /* (device status) a bounded device wait gave up        */
+  QGEMM_ERR_NO_DEVICE = 8,     /* no sm_103 device is current                          */
+  QGEMM_ERR_BAD_VALUE = 9      /* (device status) repack met an E8M0 of 255, a non-finite
+                                  BF16 scale or a zero point above 15                  */
+} qgemm_status;
+
+typedef enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2 } qgemm_wfmt;
+typedef enum { QGEMM_SCALE_BF16 = 0, QGEMM_SCALE_E8M0 = 1 } qgemm_sdtype;
+typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1 } qgemm_afmt;
+
+/*
+ * Weight descriptor ("layer config"): one quantized weight matrix W of logical shape
+ * [N, K] (Y = X . W^T).  Supported combinations:
+ *   wfmt INT4_SYM : sdtype BF16, has_zp 0, group_size 32 or a multiple of 64, K % group == 0
+ *   wfmt UINT4_ZP : sdtype BF16, has_zp 1, group_size as above
+ *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32
+ * K must be a multiple of 32; N >= 1 is arbitrary (the packed form pads it).
+ * afmt names the activation format the packed weights will be multiplied with.
+ */
+typedef struct {
+  int32_t wfmt;        /* qgemm_wfmt   */
+  int32_t sdtype;      /* qgemm_sdtype */
+  int32_t group_size;  /* K elements per scale */
+  int32_t has_zp;      /* 1 iff wfmt == QGEMM_W_UINT4_ZP */
+  int32_t afmt;        /* qgemm_afmt   */
+  int32_t reserved;    /* must be 0    */
+  int64_t N;
+  int64_t K;
+} qgemm_wdesc;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t qgemm_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qgemm_status_str(qgemm_status s);
+
+/* Validate a descriptor without touching any device (QGEMM_OK if supported). */
+qgemm_status qgemm_check_desc(const qgemm_wdesc* desc);
+
+/*
+ * Size in bytes of the packed (repacked) form of one weight matrix, or 0 if `desc` is
+ * invalid.  For an MoE layer, expert e's packed weights start at e * qgemm_packed_bytes().
+ * The size is a multiple of 256.
+ */
+size_t qgemm_packed_bytes(const qgemm_wdesc* desc);
+
+/*
+ * Offline preprocessing ("Humming wird angekündigt", section "Tuning und
+ * JIT-Kompilierung für jeden Workload": validate parameters, pad dimensions, repack into
+ * the kernel layout).  Reads the canonical weight tensors and writes the packed form.
+ *   codes  : device uint8 [N, K/2]; element k of row n is in byte k/2, even k in the low
+ *            nibble.  INT4_SYM nibbles are two's complement; UINT4_ZP nibbles are 0..15;
+ *            MXFP4 nibbles are e2m1 codes (bit 3 sign).
+ *   scales : device [N, K/group] row-major: uint16 BF16 bit patterns, or uint8 E8M0.
+ *   zeros  : device uint8 [N, K/group] with values 0..15 (UINT4_ZP), else NULL.
+ *   packed : device buffer of qgemm_packed_bytes(desc) bytes, 256-byte aligned.
+ * Values the format forbids (E8M0 = 255, a NaN/Inf BF16 scale, a zero point > 15) set
+ * QGEMM_ERR_BAD_VALUE in the device status word.
+ */
+qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const void* scales,
+                          const uint8_t* zeros, void* packed, void* stream);
+
+/*
+ * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max (split-K partial
+ * sums and tile counters).  The workspace must be 256-byte aligned and zero-filled
+ * before its first use; every successful call leaves it zero-filled again, so one
+ * zero-filled buffer can be reused by consecutive calls on one stream.
+ */
+size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);
+
+/*
+ * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k]   (c = 1 when chan_scale == NULL)
+ *   packed     : device, from qgemm_repack with desc->afmt == QGEMM_A_BF16
+ *   X          : device BF16 [M, ldx], 16-byte aligned, ldx % 8 == 0, ldx >= K
+ *   chan_scale : device float32 [N] secondary per-channel scale, or NULL
+ *   Y          : device BF16 [M, ldy], 4-byte aligned, ldy >= N, ldy even
+ *   ws         : device workspace (see qgemm_workspace_bytes), may be NULL when
+ *                qgemm_workspace_bytes(desc, M) == 0
+ * "Humming wird angekündigt", section "WnA16"; fused output scaling: section
+ * "Gemeinsam genutzte CUDA-Komponenten".
+ */
+qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void* X, int64_t M,
+                         int64_t ldx, const float* chan_scale, void* Y, int64_t ldy, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * Tokenwise FP8 activation quantization (the input of W4A8): per row m,
+ * s[m] = max_k |X[m, k]| / 448 (1 when the row is zero) and Xq[m, k] = e4m3 code of
+ * X[m, k] / s[m], rounded to nearest even with saturation, all in float32.
+ *   X : device BF16 [M, ldx];  Xq : device uint8 [M, ldq];  tok_scale : device float32 [M]
+ * "Humming wird angekündigt", section "End-to-End-Inferenzleistung" (tokenwise FP8).
+ */
+qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                 int64_t ldq, float* tok_scale, void* stream);
+
+/*
+ * Dense W4A8 (MXFP4 weights x tokenwise FP8 activations):
+ *   Y[m, n] = tok_scale[m] * c[n] * sum_k e4m3(Xq[m, k]) * W[n, k]
+ *   packed : device, from qgemm_repack with desc->wfmt == MXFP4, desc->afmt == FP8E4M3_TOKEN
+ *   Xq     : device uint8 e4m3 [M, ldx], 16-byte aligned, ldx % 16 == 0
+ *   tok_scale : device float32 [M];  other arguments as for qgemm_w4a16.
+ * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4".
+ */
+qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
+                        int64_t ldx, const float* tok_scale, const float* chan_scale, void* Y,
+                        int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * MoE grouped GEMM over expert-sorted rows: for each expert e, rows
+ * expert_offsets[e] .. expert_offsets[e+1]-1 of X are multiplied by expert e's weights.
+ *   desc           : per-expert weight descriptor (all experts share it)
+ *   packed         : device, E packed matrices, expert e at e * qgemm_packed_bytes(desc)
+ *   afmt           : QGEMM_A_BF16 (X is BF16) or QGEMM_A_FP8E4M3_TOKEN (X is e4m3 and
+ *                    tok_scale holds one float32 per row)
+ *   X              : device [R, ldx] sorted rows; padding rows should be zero
+ *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
+ *   Y              : device BF16 [R, ldy]; rows of every expert are written
+ * "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths; tokens are
+ * distributed over experts and the work per expert varies with the load).
+ */
+qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
+                               int32_t afmt, const void* X, int64_t R, int64_t ldx,
+                               const float* tok_scale, const int32_t* expert_offsets,
+                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Test hook: unpack a packed matrix back to BF16 W[n, k] = RNE_bf16(dequant) through the
+ * same register decode the GEMM kernels use.  W_out: device BF16 [N, K] (row stride K).
+ */
+qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,
+                                 void* stream);
+
+/*
+ * Read (and, if clear != 0, reset) the current device's status word: QGEMM_OK or the
+ * first device-side error recorded since the last reset.  Synchronizes the device.
+ */
+qgemm_status qgemm_device_status(int32_t clear);
+
+/*
+ * Tuning override for tests and sweeps: force the token tile (16, 32, 64, 128 or 256) and
+ * the split-K factor (>= 1) of the dense kernels; 0 restores the built-in heuristic.
+ * Process-wide, not thread-safe.
+ */
+qgemm_status qgemm_force_config(int32_t token_tile, int32_t splits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMM_H */

@@ -1,0 +1,257 @@
+"""Python binding of the qgemm C ABI (include/qgemm.h): argument marshalling only.
+
+Every computation runs in libqgemm.so's sm_103a kernels; this module only checks
+tensor dtypes/devices, passes raw pointers and the current CUDA stream, and turns status
+codes into exceptions.  There is no fallback: if the library is missing, every call
+raises.
+"""
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+__all__ = [
+    "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
+    "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
+    "force_config", "check_desc", "WFMT", "AFMT", "EXPORTS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libqgemm.so")
+
+WFMT = {"int4_sym": 0, "uint4_zp": 1, "mxfp4": 2}
+AFMT = {"bf16": 0, "fp8": 1}
+EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
+           "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
+           "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
+           "qgemm_force_config")
+
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
+          5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
+
+
+class QGemmError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = int(status)
+        super().__init__(f"qgemm: {what}: status {status} ({STATUS.get(int(status), '?')})")
+
+
+class _WDesc(ctypes.Structure):
+    _fields_ = [("wfmt", ctypes.c_int32), ("sdtype", ctypes.c_int32),
+                ("group_size", ctypes.c_int32), ("has_zp", ctypes.c_int32),
+                ("afmt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+@dataclass(frozen=True)
+class WeightDesc:
+    """One quantized weight matrix [N, K]: format, group size and activation format."""
+    wfmt: str
+    N: int
+    K: int
+    group: int = 128
+    afmt: str = "bf16"
+
+    def c(self):
+        w = WFMT[self.wfmt]
+        return _WDesc(w, 1 if self.wfmt == "mxfp4" else 0, self.group,
+                      1 if self.wfmt == "uint4_zp" else 0, AFMT[self.afmt], 0, self.N, self.K)
+
+
+_lib = None
+
+
+def lib_path():
+    return _LIB_PATH
+
+
+def lib():
+    """Load libqgemm.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(f"libqgemm.so not built ({_LIB_PATH}); run "
+                           "`python -m quantized_weight_gemm_gb300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    P = ctypes.c_void_p
+    I32, I64, SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    D = ctypes.POINTER(_WDesc)
+    sigs = {
+        "qgemm_version": (I32, []),
+        "qgemm_status_str": (ctypes.c_char_p, [ctypes.c_int]),
+        "qgemm_check_desc": (ctypes.c_int, [D]),
+        "qgemm_packed_bytes": (SZ, [D]),
+        "qgemm_repack": (ctypes.c_int, [D, P, P, P, P, P]),
+        "qgemm_workspace_bytes": (SZ, [D, I64]),
+        "qgemm_w4a16": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P]),
+        "qgemm_w4a8": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_quant_act_fp8": (ctypes.c_int, [P, I64, I64, I64, P, I64, P, P]),
+        "qgemm_moe_grouped": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_dequant_debug": (ctypes.c_int, [D, P, P, P]),
+        "qgemm_device_status": (ctypes.c_int, [I32]),
+        "qgemm_force_config": (ctypes.c_int, [I32, I32]),
+    }
+    for name, (res, args) in sigs.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    _lib = L
+    return L
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(status, what):
+    if status != 0:
+        raise QGemmError(status, what)
+
+
+def _need(t, name, dtype, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _row_major(t, name):
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+
+
+def check_desc(desc):
+    d = desc.c()
+    return lib().qgemm_check_desc(ctypes.byref(d))
+
+
+def packed_bytes(desc):
+    d = desc.c()
+    n = lib().qgemm_packed_bytes(ctypes.byref(d))
+    if n == 0:
+        raise QGemmError(1, "packed_bytes")
+    return int(n)
+
+
+def repack(desc, codes, scales, zeros=None, out=None, num_experts=1):
+    """Canonical (codes uint8 [N, K/2], scales bf16-bits/E8M0 [N, K/g], zeros) -> packed.
+
+    For an MoE layer pass tensors with a leading expert dimension and num_experts=E."""
+    nb = packed_bytes(desc)
+    if out is None:
+        out = torch.empty(nb * num_experts, dtype=torch.uint8, device=codes.device)
+    L = lib()
+    d = desc.c()
+    for e in range(num_experts):
+        c = codes[e] if num_experts > 1 else codes
+        s = scales[e] if num_experts > 1 else scales
+        z = None if zeros is None else (zeros[e] if num_experts > 1 else zeros)
+        c, s = c.contiguous(), s.contiguous()
+        z = None if z is None else z.contiguous()
+        _check(L.qgemm_repack(ctypes.byref(d), _ptr(c), _ptr(s), _ptr(z),
+                              ctypes.c_void_p(out.data_ptr() + e * nb), _stream()), "repack")
+    return out
+
+
+def workspace_bytes(desc, M_max):
+    d = desc.c()
+    return int(lib().qgemm_workspace_bytes(ctypes.byref(d), int(M_max)))
+
+
+def workspace(desc, M_max, device="cuda"):
+    """A zero-filled workspace for calls with M <= M_max (reusable across calls)."""
+    n = workspace_bytes(desc, M_max)
+    return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
+
+
+def w4a16(desc, packed, X, chan_scale=None, out=None, ws=None):
+    """Y = X . dequant(W)^T (* chan_scale[n]) with BF16 X [M, K]."""
+    _need(X, "X", torch.bfloat16)
+    _row_major(X, "X")
+    M = X.shape[0]
+    if out is None:
+        out = torch.empty(M, desc.N, dtype=torch.bfloat16, device=X.device)
+    _need(out, "out", torch.bfloat16)
+    _row_major(out, "out")
+    if chan_scale is not None:
+        _need(chan_scale, "chan_scale", torch.float32)
+    if ws is None:
+        ws = workspace(desc, M, X.device)
+    d = desc.c()
+    _check(lib().qgemm_w4a16(ctypes.byref(d), _ptr(packed), _ptr(X), M, X.stride(0),
+                             _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(ws),
+                             ws.numel() * ws.element_size(), _stream()), "w4a16")
+    return out
+
+
+def quant_act_fp8(X, out=None, scale=None):
+    """Tokenwise FP8 e4m3 quantization of BF16 X [M, K] -> (codes uint8 [M, K], s fp32 [M])."""
+    _need(X, "X", torch.bfloat16)
+    _row_major(X, "X")
+    M, K = X.shape
+    if out is None:
+        out = torch.empty(M, K, dtype=torch.uint8, device=X.device)
+    if scale is None:
+        scale = torch.empty(M, dtype=torch.float32, device=X.device)
+    _check(lib().qgemm_quant_act_fp8(_ptr(X), M, K, X.stride(0), _ptr(out), out.stride(0),
+                                     _ptr(scale), _stream()), "quant_act_fp8")
+    return out, scale
+
+
+def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None):
+    """Y = diag(tok_scale) . e4m3(Xq) . dequant(W)^T (* chan_scale[n])."""
+    _need(Xq, "Xq", torch.uint8)
+    _row_major(Xq, "Xq")
+    _need(tok_scale, "tok_scale", torch.float32)
+    M = Xq.shape[0]
+    if out is None:
+        out = torch.empty(M, desc.N, dtype=torch.bfloat16, device=Xq.device)
+    if ws is None:
+        ws = workspace(desc, M, Xq.device)
+    d = desc.c()
+    _check(lib().qgemm_w4a8(ctypes.byref(d), _ptr(packed), _ptr(Xq), M, Xq.stride(0),
+                            _ptr(tok_scale), _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(ws),
+                            ws.numel() * ws.element_size(), _stream()), "w4a8")
+    return out
+
+
+def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None):
+    """MoE grouped GEMM over expert-sorted rows X [R, K] (BF16, or uint8 e4m3 with
+    tok_scale); offsets: int32 [E+1] on the device."""
+    fp8 = X.dtype == torch.uint8
+    _need(offsets, "offsets", torch.int32)
+    _row_major(X, "X")
+    R = X.shape[0]
+    if out is None:
+        out = torch.empty(R, desc.N, dtype=torch.bfloat16, device=X.device)
+    d = desc.c()
+    _check(lib().qgemm_moe_grouped(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
+                                   _ptr(X), R, X.stride(0), _ptr(tok_scale), _ptr(offsets),
+                                   _ptr(out), out.stride(0), None, 0, _stream()), "moe_grouped")
+    return out
+
+
+def dequant_debug(desc, packed):
+    """BF16 W [N, K] decoded from the packed form by the GEMM's own register decoders."""
+    out = torch.empty(desc.N, desc.K, dtype=torch.bfloat16, device=packed.device)
+    d = desc.c()
+    _check(lib().qgemm_dequant_debug(ctypes.byref(d), _ptr(packed), _ptr(out), _stream()),
+           "dequant_debug")
+    return out
+
+
+def device_status(clear=True):
+    """First device-side error since the last reset (0 = none); synchronizes."""
+    return int(lib().qgemm_device_status(1 if clear else 0))
+
+
+def force_config(token_tile=0, splits=0):
+    _check(lib().qgemm_force_config(int(token_tile), int(splits)), "force_config")

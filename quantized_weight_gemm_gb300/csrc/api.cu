@@ -1,0 +1,367 @@
+// C ABI entry points: argument validation, the dispatch heuristic and kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "../../include/qgemm.h"
+#include "kernels.h"
+#include "qgemm_internal.h"
+
+using namespace qgemm;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kSplitMaxM = 1024;          // split-K is considered only up to this M
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+
+struct DeviceInfo {
+  bool init = false;
+  bool ok = false;
+  int sms = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+int g_force_tile = 0;
+int g_force_splits = 0;
+
+bool current_device(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.init) {
+    d.init = true;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    d.status = device_status_ptr();
+    d.ok = (major == 10 && minor == 3) && d.sms > 0 && d.status != nullptr;
+  }
+  *out = &d;
+  return d.ok;
+}
+
+int sms_or_default() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+    return sms;
+  return 152;
+}
+
+bool layout_of(const qgemm_wdesc* d, Layout* L) {
+  if (d == nullptr || d->reserved != 0) return false;
+  return make_layout(d->wfmt, d->sdtype, d->group_size, d->has_zp, d->afmt, d->N, d->K, L);
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// ---------------------------------------------------------------- dispatch heuristic
+// Token tile from M; split-K when the (m, n) tiles cannot fill every SM.
+GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
+  GemmPlan p;
+  int tt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  if (g_force_tile) tt = g_force_tile;
+  p.token_tile = tt;
+  const int64_t m_tiles = (M + tt - 1) / tt;
+  const int64_t base = m_tiles * L.n_tiles;
+  int splits = 1;
+  if (g_force_splits) {
+    splits = int(std::min<int64_t>(g_force_splits, L.k_blocks));
+  } else if (M <= kSplitMaxM) {
+    double best = double(base) / (double((base + sms - 1) / sms) * sms);
+    for (int s = 2; s <= 32 && best < 0.9 && L.k_blocks / s >= 4; ++s) {
+      const int64_t units = base * s;
+      const double eff = double(units) / (double((units + sms - 1) / sms) * sms);
+      if (eff > best + 0.02) { best = eff; splits = s; }
+      if (best >= 0.95) break;
+    }
+  }
+  p.splits = splits;
+  const int64_t units = base * splits;
+  p.grid = int(std::min<int64_t>(units, sms));
+  return p;
+}
+
+int64_t split_ws_bytes(const Layout& L, int64_t M, const GemmPlan& p) {
+  if (p.splits <= 1) return 0;
+  const int64_t m_tiles = (M + p.token_tile - 1) / p.token_tile;
+  const int64_t partial = round_up(m_tiles * p.token_tile * L.N_pad * 4, 256);
+  return partial + round_up(m_tiles * L.n_tiles * 4, 256);
+}
+
+typedef PFN_cuTensorMapEncodeTiled_v12000 EncodeFn;
+
+EncodeFn encode_fn() {
+  static EncodeFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess && q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeFn>(p);
+  });
+  return fn;
+}
+
+// X as a 2-D tensor [rows, K] with row stride ldx elements; box = stage depth x token tile,
+// 128-byte swizzle (the layout the MMA's shared-memory descriptor expects).
+bool make_x_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx,
+                int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int esize = fp8 ? 1 : 2;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ldx) * esize};
+  cuuint32_t box[2] = {cuuint32_t(128 / esize), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+qgemm_status check_x(const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx) {
+  if (X == nullptr || rows < 0 || rows >= (int64_t(1) << 31) || ldx < K) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(X, 16) || (ldx * (fp8 ? 1 : 2)) % 16 != 0) return QGEMM_ERR_ALIGNMENT;
+  return QGEMM_OK;
+}
+
+qgemm_status check_y(const void* Y, int64_t N, int64_t ldy) {
+  if (Y == nullptr || ldy < N) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(Y, 2)) return QGEMM_ERR_ALIGNMENT;
+  return QGEMM_OK;
+}
+
+qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
+                       int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
+                       void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  Layout L;
+  if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
+  if ((L.afmt == A_FP8) != fp8) return QGEMM_ERR_INVALID_ARG;
+  if (fp8 && L.wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
+  if (M < 0) return QGEMM_ERR_INVALID_ARG;
+  if (packed == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256)) return QGEMM_ERR_ALIGNMENT;
+  qgemm_status s = check_x(X, fp8, M, L.K, ldx);
+  if (s != QGEMM_OK) return s;
+  if ((s = check_y(Y, L.N, ldy)) != QGEMM_OK) return s;
+  if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if ((chan_scale && !aligned(chan_scale, 4)) || (tok_scale && !aligned(tok_scale, 4)))
+    return QGEMM_ERR_ALIGNMENT;
+  if (M == 0) return QGEMM_OK;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  const GemmPlan plan = plan_dense(L, M, dev->sms);
+  const int64_t need = split_ws_bytes(L, M, plan);
+  if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need)) return QGEMM_ERR_WORKSPACE;
+  if (need > 0 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+  CUtensorMap tmap;
+  if (!make_x_map(&tmap, X, fp8, M, L.K, ldx, plan.token_tile)) return QGEMM_ERR_CUDA;
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.M = M;
+  a.m_tiles = int((M + plan.token_tile - 1) / plan.token_tile);
+  a.splits = plan.splits;
+  a.num_units = int(int64_t(a.m_tiles) * L.n_tiles * plan.splits);
+  a.chan_scale = chan_scale;
+  a.tok_scale = tok_scale;
+  a.Y = Y;
+  a.ldy = ldy;
+  if (need > 0) {
+    a.ws = static_cast<float*>(ws);
+    a.ws_ld = L.N_pad;
+    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
+                                            round_up(int64_t(a.m_tiles) * plan.token_tile * L.N_pad * 4, 256));
+  }
+  a.status = dev->status;
+  a.timeout_ns = kTimeoutNs;
+  cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t qgemm_version(void) { return 100; }
+
+const char* qgemm_status_str(qgemm_status s) {
+  switch (s) {
+    case QGEMM_OK: return "ok";
+    case QGEMM_ERR_INVALID_ARG: return "invalid argument";
+    case QGEMM_ERR_UNSUPPORTED: return "unsupported combination";
+    case QGEMM_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+    case QGEMM_ERR_WORKSPACE: return "workspace missing or too small";
+    case QGEMM_ERR_BAD_PACKED: return "packed weights do not match the descriptor";
+    case QGEMM_ERR_CUDA: return "CUDA error";
+    case QGEMM_ERR_TIMEOUT: return "device wait timed out";
+    case QGEMM_ERR_NO_DEVICE: return "no sm_103 device is current";
+    case QGEMM_ERR_BAD_VALUE: return "invalid value in weights, scales, zero points or offsets";
+  }
+  return "unknown status";
+}
+
+qgemm_status qgemm_check_desc(const qgemm_wdesc* desc) {
+  Layout L;
+  return layout_of(desc, &L) ? QGEMM_OK : QGEMM_ERR_INVALID_ARG;
+}
+
+size_t qgemm_packed_bytes(const qgemm_wdesc* desc) {
+  Layout L;
+  if (!layout_of(desc, &L)) return 0;
+  return size_t(L.total_bytes);
+}
+
+qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const void* scales,
+                          const uint8_t* zeros, void* packed, void* stream) {
+  Layout L;
+  if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
+  if (codes == nullptr || scales == nullptr || packed == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (L.has_zp && zeros == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(codes, 4) || !aligned(scales, L.scale_bytes) || !aligned(packed, 256))
+    return QGEMM_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  cudaError_t e = launch_repack(L, codes, scales, L.has_zp ? zeros : nullptr, packed,
+                                static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
+  Layout L;
+  if (!layout_of(desc, &L) || M_max <= 0) return 0;
+  const int sms = sms_or_default();
+  int64_t best = 0;
+  const int64_t top = std::min<int64_t>(M_max, kSplitMaxM);
+  for (int64_t M = 1; M <= top; ++M) best = std::max(best, split_ws_bytes(L, M, plan_dense(L, M, sms)));
+  best = std::max(best, split_ws_bytes(L, M_max, plan_dense(L, M_max, sms)));
+  return size_t(best);
+}
+
+qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void* X, int64_t M,
+                         int64_t ldx, const float* chan_scale, void* Y, int64_t ldy, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return run_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, Y, ldy, ws, ws_bytes,
+                   stream);
+}
+
+qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
+                        int64_t ldx, const float* tok_scale, const float* chan_scale, void* Y,
+                        int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(desc, true, packed, Xq, M, ldx, tok_scale, chan_scale, Y, ldy, ws, ws_bytes,
+                   stream);
+}
+
+qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                 int64_t ldq, float* tok_scale, void* stream) {
+  if (X == nullptr || Xq == nullptr || tok_scale == nullptr || M < 0 || K < 1 || ldx < K ||
+      ldq < K || M >= (int64_t(1) << 31))
+    return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(X, 2) || !aligned(tok_scale, 4)) return QGEMM_ERR_ALIGNMENT;
+  if (M == 0) return QGEMM_OK;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  cudaError_t e = launch_quant_act_fp8(X, M, K, ldx, Xq, ldq, tok_scale,
+                                       static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
+                               int32_t afmt, const void* X, int64_t R, int64_t ldx,
+                               const float* tok_scale, const int32_t* expert_offsets,
+                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  Layout L;
+  if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
+  const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
+  if (afmt != QGEMM_A_BF16 && !fp8) return QGEMM_ERR_INVALID_ARG;
+  if (L.afmt != afmt) return QGEMM_ERR_INVALID_ARG;
+  if (E < 1 || E > 1024 || packed == nullptr || expert_offsets == nullptr || R < 0)
+    return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(expert_offsets, 4)) return QGEMM_ERR_ALIGNMENT;
+  qgemm_status s = check_x(X, fp8, R, L.K, ldx);
+  if (s != QGEMM_OK) return s;
+  if ((s = check_y(Y, L.N, ldy)) != QGEMM_OK) return s;
+  if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (R == 0) return QGEMM_OK;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  GemmPlan plan;
+  const int64_t avg = R / E;
+  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  if (g_force_tile) tt = g_force_tile;
+  plan.token_tile = tt;
+  plan.splits = 1;
+  plan.grid = dev->sms;
+  CUtensorMap tmap;
+  if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt)) return QGEMM_ERR_CUDA;
+  GemmArgs a;
+  memset(&a, 0, sizeof(a));
+  a.L = L;
+  a.packed = static_cast<const uint8_t*>(packed);
+  a.expert_stride = L.total_bytes;
+  a.offsets = expert_offsets;
+  a.E = E;
+  a.M = R;
+  a.splits = 1;
+  a.tok_scale = tok_scale;
+  a.Y = Y;
+  a.ldy = ldy;
+  a.status = dev->status;
+  a.timeout_ns = kTimeoutNs;
+  cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,
+                                 void* stream) {
+  Layout L;
+  if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
+  if (packed == nullptr || W_out == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(W_out, 16)) return QGEMM_ERR_ALIGNMENT;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  cudaError_t e = launch_dequant_debug(L, packed, W_out, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+qgemm_status qgemm_device_status(int32_t clear) {
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  if (cudaDeviceSynchronize() != cudaSuccess) return QGEMM_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, dev->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return QGEMM_ERR_CUDA;
+  if (clear) {
+    const int zero = 0;
+    if (cudaMemcpy(dev->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return QGEMM_ERR_CUDA;
+  }
+  return static_cast<qgemm_status>(v);
+}
+
+qgemm_status qgemm_force_config(int32_t token_tile, int32_t splits) {
+  if (token_tile != 0 && token_tile != 16 && token_tile != 32 && token_tile != 64 &&
+      token_tile != 128 && token_tile != 256)
+    return QGEMM_ERR_INVALID_ARG;
+  if (splits < 0 || splits > 64) return QGEMM_ERR_INVALID_ARG;
+  g_force_tile = token_tile;
+  g_force_splits = splits;
+  return QGEMM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,80 @@
+// Register-level decoding of packed 4-bit weight words.  The GEMM kernels and the
+// dequant-debug kernel call exactly these functions.
+//
+// BF16 activations (tensor-core operand BF16): a 32-bit word holds K-elements 8j..8j+7 of
+// one weight row with nibbles ordered [e0, e2, e4, e6, e1, e3, e5, e7] from bit 0, so pair
+// i = (e_2i, e_2i+1) sits in nibble i (bits 4i..) and nibble 4+i (bits 16+4i..) and one
+// 0x000F000F mask of (word >> 4i) yields both 16-bit lanes.
+//   INT4: the nibble u is ORed into the mantissa of 128.0 (bf16 0x4300), giving 128 + u
+//   exactly; subtracting 128 + z gives the exact integer u - z; one BF16 multiply by the
+//   group scale s then rounds (u - z) * s to nearest even, the value a BF16 MMA consumes.
+//   Symmetric INT4 is stored as u = q + 8 and decoded with z = 8 (the "magic number"
+//   construction of Kim et al., "Who Says Elephants Can't Run?", 2022, restated from the
+//   bfloat16 format definition).
+//   MXFP4: the e2m1 magnitude bits (e1 e0 m) are moved to bf16 bits 8..6 and the sign to
+//   bit 15, which is the bf16 number e2m1(q) * 2^-126 (a subnormal for e = 0); multiplying
+//   by 2^(E-1) (or by 2^127 and then 2^(E-128) when E > 128) gives e2m1(q) * 2^(E-127),
+//   exact unless it overflows bf16.
+//
+// FP8 activations (tensor-core operand E4M3 with block scales): a word holds K-elements
+// 8j..8j+7 with nibbles [e0, e4, e1, e5, e2, e6, e3, e7], so masking low nibbles gives
+// bytes for e0..e3 and high nibbles bytes for e4..e7.  An e2m1 code s e1 e0 m becomes the
+// e4m3 byte s 0 0 e1 e0 m 0 0, whose value is exactly e2m1(q) * 2^-6 (also for the
+// subnormal code); the factor 2^6 is returned through the activation-side block scale.
+#pragma once
+
+#include <stdint.h>
+
+#include "ptx.cuh"
+
+namespace qgemm {
+
+// INT4 word -> 4 bf16x2 (pairs 0..3).  zz = bf16x2(128 + z), s2 = bf16x2(scale).
+__device__ __forceinline__ void decode_int4_word(uint32_t w, uint32_t zz, uint32_t s2,
+                                                 uint32_t* out) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ptx::lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x43004300u);
+    out[i] = ptx::bf16x2_mul(ptx::bf16x2_sub(t, zz), s2);
+  }
+}
+
+// MXFP4 word -> 4 bf16x2.  sa, sb: bf16x2 factors (sb == 0 means single multiply).
+__device__ __forceinline__ void decode_mxfp4_word(uint32_t w, uint32_t sa, uint32_t sb,
+                                                  bool two_step, uint32_t* out) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = (w >> (4 * i)) & 0x000F000Fu;
+    const uint32_t v = (t * 0x1040u) & 0x81C081C0u;   // sign -> bit 15, e1 e0 m -> bits 8..6
+    uint32_t r = ptx::bf16x2_mul(v, sa);
+    if (two_step) r = ptx::bf16x2_mul(r, sb);
+    out[i] = r;
+  }
+}
+
+// bf16x2 factors applying 2^(E-127) to the subnormal-offset e2m1 value (see above).
+__device__ __forceinline__ void mxfp4_factors(uint32_t E, uint32_t& sa, uint32_t& sb,
+                                              bool& big) {
+  big = E > 128u;
+  const uint32_t a = big ? 0x7F00u : ((E + 126u) << 7);      // 2^127   or 2^(E-1)
+  const uint32_t b = big ? ((E - 1u) << 7) : 0x3F80u;        // 2^(E-128) or 1
+  sa = a | (a << 16);
+  sb = b | (b << 16);
+}
+
+// MXFP4 word (FP8 nibble order) -> two 32-bit words of four e4m3 bytes each.
+__device__ __forceinline__ void decode_e2m1_to_e4m3_word(uint32_t w, uint32_t& lo,
+                                                         uint32_t& hi) {
+  const uint32_t a = w & 0x0F0F0F0Fu;
+  const uint32_t b = (w >> 4) & 0x0F0F0F0Fu;
+  lo = ((a & 0x07070707u) << 2) | ((a & 0x08080808u) << 4);
+  hi = ((b & 0x07070707u) << 2) | ((b & 0x08080808u) << 4);
+}
+
+// ------------------------------------------------------------------------ layout helpers
+// Position of K-element e (0..7) of a word in the nibble order used for BF16 activations.
+__host__ __device__ constexpr int nibble_pos_a16(int e) { return (e & 1) ? 4 + (e >> 1) : (e >> 1); }
+// ... and for FP8 activations.
+__host__ __device__ constexpr int nibble_pos_a8(int e) { return (e < 4) ? 2 * e : 2 * (e - 4) + 1; }
+
+}  // namespace qgemm

@@ -1,0 +1,282 @@
+// Offline repack, dequant-debug and tokenwise FP8 activation quantization kernels.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dequant.cuh"
+#include "kernels.h"
+#include "qgemm_internal.h"
+
+namespace qgemm {
+
+__device__ int g_status = 0;
+
+__device__ __forceinline__ void set_status(int code) { atomicCAS(&g_status, 0, code); }
+
+int* device_status_ptr() {
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+  return static_cast<int*>(p);
+}
+
+// ------------------------------------------------------------------------------ repack
+// One thread writes one 16-byte chunk-row (four words) of one code tile.
+__global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
+                                    uint8_t* __restrict__ packed) {
+  const int chunks = L.bk / 32;
+  const int64_t total = L.n_tiles * L.k_blocks * chunks * kTileN;
+  const int64_t Kh = L.K / 2;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int r = int(idx % kTileN);
+    int64_t t = idx / kTileN;
+    const int c = int(t % chunks);
+    t /= chunks;
+    const int64_t kb = t % L.k_blocks;
+    const int64_t nt = t / L.k_blocks;
+    const int64_t n = nt * kTileN + r;
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int64_t k0 = kb * L.bk + c * 32 + j * 8;
+      uint32_t src = 0;
+      bool pad = (n >= L.N) || (k0 >= L.K);
+      if (!pad) src = *reinterpret_cast<const uint32_t*>(codes + n * Kh + k0 / 2);
+      uint32_t w = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        uint32_t nib = pad ? 0u : (src >> (4 * e)) & 0xFu;   // even k in the low nibble
+        if (L.wfmt == W_INT4_SYM) nib ^= 8u;                 // two's complement -> q + 8
+        const int pos = (L.afmt == A_FP8) ? nibble_pos_a8(e) : nibble_pos_a16(e);
+        w |= nib << (4 * pos);
+      }
+      out[j] = w;
+    }
+    uint8_t* dst = packed + L.off_codes + (nt * L.k_blocks + kb) * L.code_tile_bytes +
+                   int64_t(c) * kTileN * 16 + int64_t(r) * 16;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+// One thread per scale entry (and per zero-point byte).
+__global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
+                                     const uint8_t* __restrict__ zeros,
+                                     uint8_t* __restrict__ packed) {
+  const int G = L.groups_per_tile;
+  const int64_t ngroups = L.K / L.group;
+  const int64_t total = L.n_tiles * L.scale_tiles * kTileN * G;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int j = int(idx % G);
+    int64_t t = idx / G;
+    const int r = int(t % kTileN);
+    t /= kTileN;
+    const int64_t tile = t % L.scale_tiles;
+    const int64_t nt = t / L.scale_tiles;
+    const int64_t n = nt * kTileN + r;
+    const int64_t grp = tile * G + j;
+    const bool valid = n < L.N && grp < ngroups;
+    if (L.sdtype == 0) {
+      uint16_t v = 0;
+      if (valid) {
+        v = static_cast<const uint16_t*>(scales)[n * ngroups + grp];
+        if ((v & 0x7F80u) == 0x7F80u) set_status(kStatusBadValue);   // NaN / Inf
+      }
+      reinterpret_cast<uint16_t*>(packed + L.off_scales)[idx] = v;
+    } else {
+      uint8_t v = 127;
+      if (valid) {
+        v = static_cast<const uint8_t*>(scales)[n * ngroups + grp];
+        if (v == 255) set_status(kStatusBadValue);
+      }
+      (packed + L.off_scales)[idx] = v;
+    }
+    if (L.has_zp && (idx & 1) == 0) {
+      // nibble idx (this entry) and idx + 1 (the next entry) share one byte
+      uint8_t byte = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int64_t id2 = idx + h;
+        const int j2 = int(id2 % G);
+        int64_t t2 = id2 / G;
+        const int r2 = int(t2 % kTileN);
+        t2 /= kTileN;
+        const int64_t tile2 = t2 % L.scale_tiles;
+        const int64_t nt2 = t2 / L.scale_tiles;
+        const int64_t n2 = nt2 * kTileN + r2;
+        const int64_t g2 = tile2 * G + j2;
+        uint8_t z = 0;
+        if (id2 < total && n2 < L.N && g2 < ngroups) {
+          z = zeros[n2 * ngroups + g2];
+          if (z > 15) { set_status(kStatusBadValue); z &= 15; }
+        }
+        byte |= uint8_t(z << (4 * h));
+      }
+      (packed + L.off_zeros)[idx / 2] = byte;
+    }
+  }
+}
+
+__global__ void write_header_kernel(Layout L, uint8_t* packed) {
+  PackedHeader h;
+  h.magic = kPackedMagic;
+  h.version = kPackedVersion;
+  h.wfmt = L.wfmt; h.sdtype = L.sdtype; h.group = L.group; h.has_zp = L.has_zp;
+  h.afmt = L.afmt; h.bk = L.bk;
+  h.N = L.N; h.K = L.K;
+  h.n_tiles = L.n_tiles; h.k_blocks = L.k_blocks; h.scale_tiles = L.scale_tiles;
+  h.code_tile_bytes = L.code_tile_bytes; h.scale_tile_bytes = L.scale_tile_bytes;
+  h.zero_tile_bytes = L.zero_tile_bytes;
+  h.off_codes = L.off_codes; h.off_scales = L.off_scales; h.off_zeros = L.off_zeros;
+  h.total_bytes = L.total_bytes;
+  *reinterpret_cast<PackedHeader*>(packed) = h;
+}
+
+cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* scales,
+                          const uint8_t* zeros, void* packed, cudaStream_t st) {
+  uint8_t* p = static_cast<uint8_t*>(packed);
+  write_header_kernel<<<1, 1, 0, st>>>(L, p);
+  const int64_t ncode = L.n_tiles * L.k_blocks * (L.bk / 32) * kTileN;
+  const int blocks_c = int((ncode + 255) / 256 < 65536 ? (ncode + 255) / 256 : 65536);
+  repack_codes_kernel<<<blocks_c, 256, 0, st>>>(L, codes, p);
+  const int64_t nsc = L.n_tiles * L.scale_tiles * kTileN * L.groups_per_tile;
+  const int blocks_s = int((nsc + 255) / 256 < 65536 ? (nsc + 255) / 256 : 65536);
+  repack_scales_kernel<<<blocks_s, 256, 0, st>>>(L, scales, zeros, p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ header check
+__device__ bool header_matches(const uint8_t* packed, const Layout& L) {
+  const PackedHeader* h = reinterpret_cast<const PackedHeader*>(packed);
+  return h->magic == kPackedMagic && h->version == kPackedVersion && h->wfmt == L.wfmt &&
+         h->sdtype == L.sdtype && h->group == L.group && h->has_zp == L.has_zp &&
+         h->afmt == L.afmt && h->N == L.N && h->K == L.K && h->total_bytes == L.total_bytes;
+}
+
+// ------------------------------------------------------------------------ dequant debug
+// One thread decodes one packed word (8 K-elements of one row) through the GEMM decoders.
+__global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packed,
+                                     __nv_bfloat16* __restrict__ W) {
+  __shared__ int ok;
+  if (threadIdx.x == 0) {
+    ok = header_matches(packed, L);
+    if (!ok && blockIdx.x == 0) set_status(kStatusBadPacked);
+  }
+  __syncthreads();
+  if (!ok) return;
+  const int chunks = L.bk / 32;
+  const int64_t total = L.n_tiles * L.k_blocks * chunks * kTileN * 4;
+  const int G = L.groups_per_tile;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int j = int(idx % 4);
+    int64_t t = idx / 4;
+    const int r = int(t % kTileN);
+    t /= kTileN;
+    const int c = int(t % chunks);
+    t /= chunks;
+    const int64_t kb = t % L.k_blocks;
+    const int64_t nt = t / L.k_blocks;
+    const int64_t n = nt * kTileN + r;
+    const int64_t k0 = kb * L.bk + c * 32 + j * 8;
+    if (n >= L.N || k0 >= L.K) continue;
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(
+        packed + L.off_codes + (nt * L.k_blocks + kb) * L.code_tile_bytes +
+        int64_t(c) * kTileN * 16 + int64_t(r) * 16 + j * 4);
+    // scale tile and entry of this stage / group, exactly as the GEMM producer selects them
+    const int64_t kk = kb * L.bk + c * 32 + j * 8;           // first K of the word
+    int64_t tile, jg;
+    if (G == 1) { tile = kk / L.group; jg = 0; }
+    else { tile = kb; jg = (kk - kb * L.bk) / L.group; }
+    const int64_t sidx = ((nt * L.scale_tiles + tile) * kTileN + r) * G + jg;
+    __nv_bfloat16* dst = W + n * L.K + k0;
+    if (L.afmt == A_FP8) {
+      // e2m1 -> e4m3 byte shuffle, then value = e4m3 * 2^6 * 2^(E-127) (exact in bf16)
+      const uint32_t E = (packed + L.off_scales)[sidx];
+      uint32_t lo, hi;
+      decode_e2m1_to_e4m3_word(w, lo, hi);
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t b = ((e < 4 ? lo : hi) >> (8 * (e & 3))) & 0xFFu;
+        const uint32_t ex = (b >> 3) & 0xFu, m = b & 7u;
+        float v = ex == 0 ? ldexpf(float(m) / 8.0f, -6) : ldexpf(1.0f + float(m) / 8.0f, int(ex) - 7);
+        v = ldexpf(v, 6 + int(E) - 127);
+        if (b & 0x80u) v = -v;
+        dst[e] = __float2bfloat16_rn(v);
+      }
+      continue;
+    }
+    uint32_t out[4];
+    if (L.wfmt == W_MXFP4) {
+      const uint32_t E = (packed + L.off_scales)[sidx];
+      uint32_t sa, sb;
+      bool big;
+      mxfp4_factors(E, sa, sb, big);
+      decode_mxfp4_word(w, sa, sb, big, out);
+    } else {
+      const uint32_t s = reinterpret_cast<const uint16_t*>(packed + L.off_scales)[sidx];
+      uint32_t z = 8;
+      if (L.has_zp) {
+        const uint8_t zb = (packed + L.off_zeros)[sidx / 2];
+        z = (zb >> (4 * (sidx & 1))) & 0xFu;
+      }
+      const uint32_t zz = (0x4300u | z) * 0x00010001u;
+      decode_int4_word(w, zz, s * 0x00010001u, out);
+    }
+    // pair i = elements (2i, 2i+1): low half is the even element
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);    // k0 % 8 == 0 -> 16-byte aligned
+    *reinterpret_cast<uint4*>(d32) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+}
+
+cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, cudaStream_t st) {
+  const int64_t total = L.n_tiles * L.k_blocks * (L.bk / 32) * kTileN * 4;
+  const int blocks = int((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
+  dequant_debug_kernel<<<blocks, 256, 0, st>>>(L, static_cast<const uint8_t*>(packed),
+                                               static_cast<__nv_bfloat16*>(W));
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------ FP8 act quantization
+// One block of 256 threads per row: float32 row maximum, s = amax / 448, code = e4m3
+// RNE-satfinite of x / s (IEEE float32 division).
+__global__ void __launch_bounds__(256) quant_act_fp8_kernel(const __nv_bfloat16* __restrict__ X,
+                                                            int64_t K, int64_t ldx,
+                                                            uint8_t* __restrict__ Xq, int64_t ldq,
+                                                            float* __restrict__ s_out) {
+  const int64_t m = blockIdx.x;
+  const __nv_bfloat16* x = X + m * ldx;
+  float amax = 0.0f;
+  for (int64_t k = threadIdx.x; k < K; k += blockDim.x) amax = fmaxf(amax, fabsf(__bfloat162float(x[k])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[8];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float v = threadIdx.x < 8 ? red[threadIdx.x] : 0.0f;
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if (threadIdx.x == 0) red[0] = v;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
+  if (threadIdx.x == 0) s_out[m] = s;
+  uint8_t* q = Xq + m * ldq;
+  for (int64_t k = 2 * threadIdx.x; k < K; k += 2 * blockDim.x) {
+    const float a = __fdiv_rn(__bfloat162float(x[k]), s);
+    const float b = (k + 1 < K) ? __fdiv_rn(__bfloat162float(x[k + 1]), s) : 0.0f;
+    const uint16_t pair = ptx::cvt_e4m3x2_f32(a, b);
+    q[k] = uint8_t(pair & 0xFF);
+    if (k + 1 < K) q[k + 1] = uint8_t(pair >> 8);
+  }
+}
+
+cudaError_t launch_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                 int64_t ldq, float* s, cudaStream_t st) {
+  quant_act_fp8_kernel<<<unsigned(M), 256, 0, st>>>(static_cast<const __nv_bfloat16*>(X), K, ldx,
+                                                    Xq, ldq, s);
+  return cudaGetLastError();
+}
+
+}  // namespace qgemm

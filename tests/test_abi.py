@@ -1,0 +1,107 @@
+"""CPU-side checks of the C ABI: the library loads, exports every declared entry point,
+and its host logic (descriptor validation, sizes, argument errors) behaves as documented.
+No test here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_weight_gemm_gb300 as qg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "qgemm.h"), encoding="utf-8") as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return set(re.findall(r"\b(qgemm_[a-z0-9_]+)\s*\(", text))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from quantized_weight_gemm_gb300 import build
+    build.build()
+    return qg.lib()
+
+
+def test_exports_match_header(L):
+    declared = _declared_functions()
+    assert declared == set(qg.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for s in range(10):
+        assert L.qgemm_status_str(s)
+    assert L.qgemm_version() >= 100
+
+
+@pytest.mark.parametrize("wfmt,group,afmt,ok", [
+    ("int4_sym", 128, "bf16", True), ("uint4_zp", 128, "bf16", True),
+    ("int4_sym", 32, "bf16", True), ("uint4_zp", 64, "bf16", True),
+    ("mxfp4", 32, "bf16", True), ("mxfp4", 32, "fp8", True),
+    ("int4_sym", 48, "bf16", False), ("mxfp4", 64, "bf16", False),
+    ("int4_sym", 128, "fp8", False),
+])
+def test_check_desc(L, wfmt, group, afmt, ok):
+    d = qg.WeightDesc(wfmt, 256, 512, group, afmt)
+    assert (qg.check_desc(d) == 0) == ok
+
+
+def test_packed_bytes_accounting(L):
+    # INT4 asym 28672 x 8192, group 128: codes + scales + packed uint4 zero points
+    d = qg.WeightDesc("uint4_zp", 28672, 8192, 128)
+    n = qg.packed_bytes(d)
+    codes, scales, zeros = 28672 * 8192 // 2, 28672 * 64 * 2, 28672 * 64 // 2
+    assert n >= codes + scales + zeros
+    assert n - (codes + scales + zeros) < 4096
+    assert n % 256 == 0
+    # MXFP4 4096 x 7168: codes + one E8M0 byte per 32
+    d = qg.WeightDesc("mxfp4", 4096, 7168, 32)
+    assert qg.packed_bytes(d) - (4096 * 7168 // 2 + 4096 * 7168 // 32) < 4096
+    # ragged N and K pad to the tile
+    d = qg.WeightDesc("int4_sym", 130, 96, 32)
+    assert qg.packed_bytes(d) >= 256 * 128 // 2
+
+
+def test_bad_descriptors_give_zero(L):
+    for d in [qg.WeightDesc("int4_sym", 0, 512), qg.WeightDesc("int4_sym", 16, 500),
+              qg.WeightDesc("int4_sym", 16, 512, 100)]:
+        assert L.qgemm_packed_bytes(ctypes.byref(d.c())) == 0
+
+
+def test_workspace_bytes(L):
+    d = qg.WeightDesc("uint4_zp", 28672, 8192, 128)
+    assert qg.workspace_bytes(d, 1) > 0                # decode-sized M splits K
+    big = qg.workspace_bytes(d, 8192)
+    assert big >= qg.workspace_bytes(d, 1)
+    assert big < 256 * 1024 * 1024
+
+
+def test_argument_errors_before_any_launch(L):
+    d = qg.WeightDesc("int4_sym", 256, 512, 128).c()
+    P = ctypes.c_void_p
+    # null X, null packed, negative M, ldx < K, misaligned X
+    assert L.qgemm_w4a16(ctypes.byref(d), None, P(256), 16, 512, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), None, 16, 512, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), -1, 512, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 256, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(258), 16, 512, None, P(256), 256, None, 0, None) == 3
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 516, None, P(256), 256, None, 0, None) == 3
+    # M = 0 is a no-op (returns before touching any device)
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 0, 512, None, P(256), 256, None, 0, None) == 0
+    # FP8 entry point with a BF16-activation descriptor
+    assert L.qgemm_w4a8(ctypes.byref(d), P(256), P(256), 4, 512, P(256), None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_force_config(48, 0) == 1
+    assert L.qgemm_force_config(0, 0) == 0
+
+
+def test_product_package_does_not_import_oracle():
+    pkg = os.path.join(ROOT, "quantized_weight_gemm_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert "oracle" not in text.replace("the oracle", ""), f

@@ -1,0 +1,214 @@
+"""Dense W4A16 / W4A8 parity of the CUDA path against the float64 oracle.
+
+Bar: |y - y_ref| <= 8e-3 * max(|y_ref|, rms(y_ref)) for BF16 activations and 2e-2 for
+FP8 activations, element by element; exact equality where the arithmetic is exact
+(integer-valued inputs with power-of-two scales, one-hot activations)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import formats as F
+import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+TOL_A16 = 8e-3
+TOL_A8 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from quantized_weight_gemm_gb300 import build
+    build.build()
+    import quantized_weight_gemm_gb300 as qg
+    qg.force_config(0, 0)
+    qg.device_status(clear=True)
+    yield
+    qg.force_config(0, 0)
+    assert qg.device_status(clear=True) == 0
+
+
+def _qg():
+    import quantized_weight_gemm_gb300 as qg
+    return qg
+
+
+def _run_a16(x_bits, w, chan=None):
+    from tests import gpu_util as G
+    qg = _qg()
+    d, packed = G.pack(w)
+    X = G.bf16_tensor(x_bits)
+    cs = None if chan is None else torch.from_numpy(chan.astype(np.float32)).cuda()
+    y = qg.w4a16(d, packed, X, chan_scale=cs)
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    return G.to_f64(y)
+
+
+def _assert_close(y, ref, tol):
+    ok, worst = oracle.tolerance_ok(y, ref, tol)
+    if ok:
+        return
+    rms = np.sqrt(np.mean(ref * ref))
+    ratio = np.abs(y - ref) / (tol * np.maximum(np.abs(ref), rms))
+    bad = np.argwhere(~(ratio <= 1.0))
+    m, n = (int(v) for v in np.unravel_index(np.nanargmax(np.where(np.isfinite(ratio), ratio, 1e30)), ratio.shape))
+    rows = sorted(set(int(b[0]) for b in bad))
+    cols = sorted(set(int(b[1]) for b in bad))
+    raise AssertionError(
+        f"worst error / bound = {worst:.3f} at (m={m}, n={n}): y={y[m, n]!r} ref={ref[m, n]!r}; "
+        f"{len(bad)} of {ratio.size} bad; rows {rows[:12]}{'...' if len(rows) > 12 else ''} "
+        f"({len(rows)}); cols {cols[:12]}{'...' if len(cols) > 12 else ''} ({len(cols)}); "
+        f"bad n-tiles {sorted(set(c // 128 for c in cols))[:8]}")
+
+
+def test_tiny_dense_workload():
+    x, w = WL.tiny_dense(seed=0)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales)
+    _assert_close(_run_a16(x, w), ref, TOL_A16)
+
+
+@pytest.mark.parametrize("wfmt,group,M,N,K", [
+    ("uint4_zp", 128, 37, 300, 1024),
+    ("uint4_zp", 128, 1, 512, 2048),
+    ("int4_sym", 128, 129, 256, 512),
+    ("int4_sym", 32, 200, 129, 96),
+    ("uint4_zp", 64, 300, 640, 512),
+    ("uint4_zp", 256, 65, 384, 768),
+    ("mxfp4", 32, 5, 520, 2048),
+    ("mxfp4", 32, 17, 1024, 1024),
+    ("mxfp4", 32, 260, 256, 416),
+    ("mxfp4", 32, 600, 384, 640),
+])
+def test_dense_a16_parity(wfmt, group, M, N, K):
+    r = WL.rng(21)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, wfmt, N, K, group=group)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    _assert_close(_run_a16(x, w), ref, TOL_A16)
+
+
+def test_chan_scale():
+    r = WL.rng(22)
+    x = WL.gen_x(r, 48, 512)
+    w = WL.gen_weights(r, "uint4_zp", 200, 512)
+    chan = r.uniform(0.5, 2.0, 200).astype(np.float32)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros, chan_scale=chan)
+    _assert_close(_run_a16(x, w, chan), ref, TOL_A16)
+
+
+@pytest.mark.parametrize("wfmt,group", [("int4_sym", 128), ("uint4_zp", 64), ("mxfp4", 32)])
+def test_integer_inputs_exact(wfmt, group):
+    """Integer X and power-of-two scales: every partial sum is exact in fp32, so the
+    output must be exactly RNE_bf16 of the oracle's exact result."""
+    r = WL.rng(23)
+    M, N, K = 8, 256, 256
+    x = WL.to_bf16_bits(r.integers(-4, 5, size=(M, K)).astype(np.float32))
+    w = WL.gen_weights(r, wfmt, N, K, group=group)
+    if wfmt == "mxfp4":
+        w.scales[:] = r.integers(124, 130, size=w.scales.shape, dtype=np.uint8)
+    else:
+        w.scales[:] = F.float_to_bf16_bits(np.ldexp(1.0, r.integers(-3, 3, size=w.scales.shape)))
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    y = _run_a16(x, w)
+    np.testing.assert_array_equal(y, F.round_to_bf16(ref))
+
+
+@pytest.mark.parametrize("wfmt,group", [("uint4_zp", 128), ("mxfp4", 32)])
+def test_one_hot_columns_exact(wfmt, group):
+    r = WL.rng(24)
+    N, K = 384, 512
+    w = WL.gen_weights(r, wfmt, N, K, group=group)
+    ks = np.array([0, 1, 31, 32, 63, 64, 127, 128, 255, 511])
+    x = np.zeros((len(ks), K), dtype=np.float32)
+    x[np.arange(len(ks)), ks] = 1.0
+    y = _run_a16(WL.to_bf16_bits(x), w)
+    W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    np.testing.assert_array_equal(y, W[:, ks].T)
+
+
+@pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+def test_every_dispatch_entry(tile, splits):
+    """Each (token tile, split-K) configuration the dispatcher can pick, forced."""
+    qg = _qg()
+    r = WL.rng(25)
+    M, N, K = 100, 384, 1024
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    qg.force_config(tile, splits)
+    try:
+        y = _run_a16(x, w)
+        y2 = _run_a16(x, w)            # the workspace must come back zeroed
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A16)
+    _assert_close(y2, ref, TOL_A16)
+
+
+# ------------------------------------------------------------------------------- W4A8
+
+def test_quant_act_fp8_bitexact():
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(26)
+    x = WL.gen_x(r, 67, 1000, outliers=True)
+    x[5] = 0                                         # an all-zero row
+    codes, s = qg.quant_act_fp8(G.bf16_tensor(x))
+    ref_codes, ref_s = oracle.quant_act_fp8(x)
+    np.testing.assert_array_equal(s.cpu().numpy(), ref_s)
+    np.testing.assert_array_equal(codes.cpu().numpy(), ref_codes)
+
+
+def _run_a8(xq, s, w, chan=None):
+    from tests import gpu_util as G
+    qg = _qg()
+    d, packed = G.pack(w, afmt="fp8")
+    cs = None if chan is None else torch.from_numpy(chan.astype(np.float32)).cuda()
+    y = qg.w4a8(d, packed, G.u8_tensor(xq), torch.from_numpy(s).cuda(), chan_scale=cs)
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    return G.to_f64(y)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 256, 512), (16, 300, 1024), (40, 512, 2048),
+                                   (130, 256, 384), (300, 640, 1024)])
+def test_dense_a8_parity(M, N, K):
+    r = WL.rng(27)
+    x = WL.gen_x(r, M, K, outliers=True)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    xq, s = oracle.quant_act_fp8(x)
+    ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
+    _assert_close(_run_a8(xq, s, w), ref, TOL_A8)
+
+
+def test_a8_integer_inputs_exact():
+    r = WL.rng(28)
+    M, N, K = 8, 256, 256
+    xq = F.e4m3_encode(r.integers(-4, 5, size=(M, K)).astype(np.float64))
+    s = np.ones(M, dtype=np.float32)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    w.scales[:] = r.integers(124, 130, size=w.scales.shape, dtype=np.uint8)
+    ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
+    np.testing.assert_array_equal(_run_a8(xq, s, w), F.round_to_bf16(ref))
+
+
+@pytest.mark.parametrize("tile", [16, 64, 256])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_a8_dispatch_entries(tile, splits):
+    qg = _qg()
+    r = WL.rng(29)
+    M, N, K = 100, 384, 1024
+    x = WL.gen_x(r, M, K, outliers=True)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    xq, s = oracle.quant_act_fp8(x)
+    chan = r.uniform(0.5, 2, N).astype(np.float32)
+    ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales, chan_scale=chan)
+    qg.force_config(tile, splits)
+    try:
+        y = _run_a8(xq, s, w, chan)
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A8)

@@ -188,6 +188,31 @@ qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, vo
 qgemm_status qgemm_device_status(int32_t clear);
 
 /*
+ * Size of the device scratch built into the library for qgemm_w4a16_noalloc (8 MiB).
+ */
+#define QGEMM_NOALLOC_SCRATCH_BYTES (8u * 1024u * 1024u)
+
+/*
+ * Dense W4A16 for callers that cannot allocate a workspace -- for example code whose
+ * device memory is entirely owned by another allocator (a serving framework's reserved
+ * pool), or a latency-critical path that must not call cudaMalloc and its implicit
+ * device synchronization.  The pages have no counterpart; this is a library convenience.
+ * Same arguments and result as qgemm_w4a16 without `ws`/`ws_bytes`: the split-K scratch
+ * is a fixed QGEMM_NOALLOC_SCRATCH_BYTES device array inside the library, held by every
+ * GPU that loads it until the process exits.  Calls whose plan needs more scratch than
+ * that return QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a workspace for them.
+ * Allocates nothing: no cudaMalloc/cudaFree or allocating library routine.  The first
+ * call on a device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  Each call zeroes the
+ * part of the array it uses, on `stream`.  All calls share the one array, so calls that
+ * may overlap on the GPU (different streams, or different host threads) race and give
+ * wrong results; serialize them on one stream.
+ */
+qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, const void* X,
+                                 int64_t M, int64_t ldx, const float* chan_scale, void* Y,
+                                 int64_t ldy, void* stream);
+
+/*
  * Tuning override for tests and sweeps: force the token tile (16, 32, 64, 128 or 256) and
  * the split-K factor (>= 1) of the dense kernels; 0 restores the built-in heuristic.
  * Process-wide, not thread-safe.

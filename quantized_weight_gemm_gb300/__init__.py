@@ -25,7 +25,7 @@ AFMT = {"bf16": 0, "fp8": 1}
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
-           "qgemm_force_config")
+           "qgemm_force_config", "qgemm_w4a16_noalloc")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -92,6 +92,7 @@ def lib():
         "qgemm_dequant_debug": (ctypes.c_int, [D, P, P, P]),
         "qgemm_device_status": (ctypes.c_int, [I32]),
         "qgemm_force_config": (ctypes.c_int, [I32, I32]),
+        "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)

@@ -3,7 +3,8 @@
 Workload (one step): the dense W4A16 asymmetric-INT4 sweep -- uint4 codes with uint4 zero
 points and BF16 scales per group of 128, shapes N x K = 28672 x 8192 and 8192 x 28672,
 M = 1, 2, 4, ..., 8192 -- 28 GEMM calls, each timed alone with CUDA events after an L2
-flush (a 256 MiB device write, outside the events), mirroring the protocol of "Humming
+flush (a 256 MiB device write, outside the events) and a ~0.1 ms device-side spin that
+keeps host launch latency out of the events, mirroring the protocol of "Humming
 wird angekündigt" (vLLM blog, German edition), section "Leistung".
 
 value   = sum of 2*M*N*K over the step / sum of the event-timed call durations (TFLOP/s)
@@ -36,6 +37,7 @@ GROUP = 128
 WORKLOAD = ("dense W4A16 asymmetric INT4 (uint4 codes + uint4 zero points, BF16 scales, "
             "group 128), N x K in {28672 x 8192, 8192 x 28672}, M = 1..8192 (powers of two)")
 FLUSH_BYTES = 256 * 1024 * 1024
+HOLD_CYCLES = 200000            # ~0.1 ms device-side spin before each timed call
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -146,6 +148,11 @@ def run_step(cases, flush, e2e=False):
     for c in cases:
         for M in M_SWEEP:
             flush.zero_()
+            if not e2e:
+                # keep the GPU busy while the host enqueues the call, so that host-side
+                # launch latency does not show up between the events of the kernel-only
+                # timing; the end-to-end timing keeps it
+                torch.cuda._sleep(HOLD_CYCLES)
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(st)
@@ -275,6 +282,7 @@ def bench_ours(args):
                 "scales U[0.005,0.02] bf16)",
         "config": {"workload": WORKLOAD, "shapes": [list(s) for s in SHAPES], "M": list(M_SWEEP),
                    "l2": "flushed before every timed call (256 MiB device write outside the events)",
+                   "launch": "0.1 ms device spin before each call so host latency is not timed",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "impl": "ours",
         "roofline": {"bound": "tensor", "achieved": round(achieved_tc, 1),
@@ -300,6 +308,55 @@ def bench_ours(args):
         print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
+
+
+def bench_case(args):
+    """One GEMM shape, timed alone (profiling aid): --case N,K,M[,wfmt[,afmt]]."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import __graft_entry__ as ge
+    ge.build()
+    import quantized_weight_gemm_gb300 as qg
+    parts = args.case.split(",")
+    N, K, M = int(parts[0]), int(parts[1]), int(parts[2])
+    wfmt = parts[3] if len(parts) > 3 else "uint4_zp"
+    afmt = parts[4] if len(parts) > 4 else "bf16"
+    r = WL.rng(0)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, wfmt, N, K)
+    d = qg.WeightDesc(wfmt, N, K, w.group, afmt)
+    scales = torch.from_numpy(w.scales.view(np.int16) if w.scales.dtype == np.uint16 else w.scales)
+    packed = qg.repack(d, torch.from_numpy(w.codes).cuda(), scales.cuda(),
+                       None if w.zeros is None else torch.from_numpy(w.zeros).cuda())
+    X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
+    if afmt == "fp8":
+        Xq, ts = qg.quant_act_fp8(X)
+    ws = qg.workspace(d, M)
+    Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda._sleep(HOLD_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        if afmt == "fp8":
+            qg.w4a8(d, packed, Xq, ts, out=Y, ws=ws)
+        else:
+            qg.w4a16(d, packed, X, out=Y, ws=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("device error")
+    ms = statistics.median(times)
+    wb = qg.packed_bytes(d)
+    print(json.dumps({"case": args.case, "us": round(ms * 1e3, 2),
+                      "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1),
+                      "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1)}), flush=True)
 
 
 def bench_reference(args):
@@ -335,8 +392,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="N,K,M[,wfmt[,afmt]]: time one GEMM shape")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.case:
+        bench_case(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_ours(args)

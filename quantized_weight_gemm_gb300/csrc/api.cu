@@ -8,7 +8,7 @@
 #include <algorithm>
 #include <mutex>
 
-#include "../../include/qgemm.h"
+#include "qgemm.h"
 #include "kernels.h"
 #include "qgemm_internal.h"
 
@@ -78,7 +78,7 @@ GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
     splits = int(std::min<int64_t>(g_force_splits, L.k_blocks));
   } else if (M <= kSplitMaxM) {
     double best = double(base) / (double((base + sms - 1) / sms) * sms);
-    for (int s = 2; s <= 32 && best < 0.9 && L.k_blocks / s >= 4; ++s) {
+    for (int s = 2; s <= 32 && best < 0.9 && L.k_blocks / s >= 2; ++s) {
       const int64_t units = base * s;
       const double eff = double(units) / (double((units + sms - 1) / sms) * sms);
       if (eff > best + 0.02) { best = eff; splits = s; }
@@ -113,21 +113,39 @@ EncodeFn encode_fn() {
   return fn;
 }
 
-// X as a 2-D tensor [rows, K] with row stride ldx elements; box = stage depth x token tile,
-// 128-byte swizzle (the layout the MMA's shared-memory descriptor expects).
+// The map of X the kernel loads with 128-byte swizzle (the layout the MMA's shared-memory
+// descriptor expects).  When K is a whole number of 128-byte slabs, X is described as a
+// 3-D tensor [K / slab][rows][slab] so that one load brings several slabs (several
+// pipeline stages for narrow token tiles); otherwise as a 2-D tensor [rows][K] loaded one
+// slab at a time.  Sets *is_3d accordingly.
 bool make_x_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx,
-                int box_rows) {
+                int box_rows, int* is_3d) {
   EncodeFn enc = encode_fn();
   if (enc == nullptr) return false;
   const int esize = fp8 ? 1 : 2;
+  const int64_t slab = 128 / esize;                        // elements per 128-byte slab
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int box_slabs = gemm_x_box_slabs(fp8, box_rows);
+  if (K % slab == 0 && box_slabs > 0) {
+    cuuint64_t dims[3] = {cuuint64_t(slab), cuuint64_t(rows), cuuint64_t(K / slab)};
+    cuuint64_t strides[2] = {cuuint64_t(ldx) * esize, 128};
+    cuuint32_t box[3] = {cuuint32_t(slab), cuuint32_t(box_rows), cuuint32_t(box_slabs)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(m, dt, 3, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS) {
+      *is_3d = 1;
+      return true;
+    }
+  }
   cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
   cuuint64_t strides[1] = {cuuint64_t(ldx) * esize};
-  cuuint32_t box[2] = {cuuint32_t(128 / esize), cuuint32_t(box_rows)};
+  cuuint32_t box[2] = {cuuint32_t(slab), cuuint32_t(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                   const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, dt, 2, const_cast<void*>(X), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  *is_3d = 0;
   return r == CUDA_SUCCESS;
 }
 
@@ -167,9 +185,11 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need)) return QGEMM_ERR_WORKSPACE;
   if (need > 0 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
   CUtensorMap tmap;
-  if (!make_x_map(&tmap, X, fp8, M, L.K, ldx, plan.token_tile)) return QGEMM_ERR_CUDA;
+  int x3d = 0;
+  if (!make_x_map(&tmap, X, fp8, M, L.K, ldx, plan.token_tile, &x3d)) return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
+  a.x_3d = x3d;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.M = M;
@@ -308,9 +328,11 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   plan.splits = 1;
   plan.grid = dev->sms;
   CUtensorMap tmap;
-  if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt)) return QGEMM_ERR_CUDA;
+  int x3d = 0;
+  if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d)) return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
+  a.x_3d = x3d;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.expert_stride = L.total_bytes;

@@ -1,29 +1,39 @@
 // The tcgen05 quantized-weight GEMM kernel (dense and MoE grouped), sm_103a.
 //
-// Design (one persistent CTA per SM, warp-specialised):
-//   warp 0     producer: per pipeline stage, one TMA 2-D tile of X (token_tile rows x
-//              128 bytes, 128-byte swizzle) plus bulk copies of the packed weight tile
-//              (128 rows x BK K-elements, 4 bits each), its scale tile and zero-point tile;
-//              all complete on the stage's `full` mbarrier.
-//   warps 2-5  dequant: thread r owns weight row r (= tensor-memory lane r).  It decodes
-//              its row's BK codes in registers (dequant.cuh) and stores them with
-//              tcgen05.st into the stage's A-operand columns of tensor memory.  The
-//              dequantized weights never touch shared memory, which stays free for the
-//              activation operand.
-//   warp 1     MMA issuer (one thread): tcgen05.mma with A = weights in tensor memory
-//              (M = 128 weight rows), B = activation tile in shared memory (N = token_tile
-//              rows of X), accumulating FP32 in tensor memory (the "swap-AB" orientation:
-//              the weights fill the 128-row side, so small batches still run full-height
-//              MMAs).  BF16 activations use kind::f16; FP8 activations use
-//              kind::mxf8f6f4 with the E8M0 weight scales as block scale factors.
-//   warps 6-9  epilogue: tcgen05.ld of the accumulator, fused per-channel / per-token
-//              scaling, BF16 store of Y (or FP32 split-K reduction through a workspace;
-//              the last CTA of a tile converts and re-zeroes the workspace).
-// Data-dependent parts of the pages this follows: "Humming wird angekündigt", sections
-// "Gemeinsam genutzte CUDA-Komponenten" (task scheduling, data movement with TMA,
-// dequantization and scaling fused into the kernel, tensor-core compute, output stage
-// with fused scaling; dense vs MoE scheduling), "Leistungsoptimierung basierend auf
-// Geräteparametern" (fast MXFP4 -> FP8 conversion for W4A8; Stream-K style scheduling).
+// One persistent CTA per SM, warp-specialised (16 warps).  A "stage" is 128 K-elements of
+// one work unit (a 128-row weight tile x a token tile, over a range of K); the 256-token
+// BF16 variant uses half stages (64 K) so that its 32 KB activation tiles fit.
+//
+//   warps 0, 16 record producers (one thread each, alternate stages): one bulk copy per
+//               stage of the packed weight record (codes, scales and zero points of 128
+//               weight rows x 128 K, see qgemm_internal.h) into the record ring, which is
+//               deep (up to 16 slots) so that many weight bytes are in flight: small batches
+//               are bound by HBM.  Every copy costs its issuing thread a few hundred cycles
+//               whatever its size, so two threads share the stream.
+//   warp 15     activation producer (one thread): TMA tiles of X (token_tile rows x 128
+//               bytes per 64-K slab, 128-byte swizzle) into the X ring; for narrow token
+//               tiles one 3-D load brings several stages at once, for the same reason.
+//   warps 2-5,  dequant, two warpgroups taking alternate stages: thread r owns weight row r
+//   warps 6-9   (= tensor-memory lane r), decodes its row's codes from the record ring in
+//               registers (dequant.cuh), releases the record slot, and writes the weights
+//               with tcgen05.st into the stage's A-operand columns of tensor memory.  The
+//               dequantized weights never touch shared memory.
+//   warps 1, 14 MMA issuers (one thread each): tcgen05.mma with A = weights in tensor
+//               memory (M = 128 weight rows) and B = the X tile (N = token_tile rows of X),
+//               FP32 accumulators in tensor memory.  The weights fill the 128-row side
+//               ("swap AB"), so small batches still run full-height MMAs.  A thread issues
+//               an MMA only every few dozen cycles whatever its size, so narrow token tiles
+//               use both issuers on alternate stages, each into its own partial
+//               accumulator.  BF16 activations use kind::f16; FP8 activations use
+//               block-scaled kind::mxf8f6f4 with the E8M0 weight scales as scale factors.
+//   warps 10-13 epilogue: tcgen05.ld of the accumulator(s), fused per-channel / per-token
+//               scaling, BF16 store of Y; or, under split-K, an FP32 reduction through the
+//               workspace whose last contributor converts the tile and re-zeroes it.
+// This follows "Humming wird angekündigt" (vLLM blog, German edition), section "Gemeinsam
+// genutzte CUDA-Komponenten" (task scheduling, TMA data movement, dequantization and
+// scaling fused into the kernel, tensor-core compute, output stage with fused scaling,
+// dense versus MoE scheduling) and section "Leistungsoptimierung basierend auf
+// Geräteparametern" (fast MXFP4 -> FP8 conversion for W4A8; Stream-K style split of K).
 #pragma once
 
 #include <cuda.h>
@@ -38,39 +48,71 @@
 
 namespace qgemm {
 
-constexpr int kThreads = 320;
+constexpr int kWarps = 17;
+constexpr int kThreads = kWarps * 32;
+constexpr int kIssuerWarp1 = 14;     // second MMA issuer (narrow token tiles)
+constexpr int kXProducerWarp = 15;
+constexpr int kRecProducerWarp1 = 16;  // second record producer
 constexpr int kMaxExperts = 1024;
-constexpr int kScaleSlot = 512;      // bytes reserved per stage for a scale tile
-constexpr int kZeroSlot = 128;       // bytes reserved per stage for a zero-point tile
+// Sleep between polls of a barrier, per role (ns): roles on the critical path poll often,
+// the others sleep longer so the dequant warps keep the issue slots.
+constexpr uint32_t kSleepDequant = 32, kSleepMma = 32, kSleepProducer = 128, kSleepEpilogue = 256;
+constexpr int kRecTail = kTileN * 4 * 2 + kTileN * 4 / 2;           // largest scales + zeros
 
 template <int BNT, bool A8>
 struct GemmCfg {
-  static constexpr int kStageK = A8 ? 128 : 64;                  // K-elements per stage
-  static constexpr int kActBytes = BNT * 128;                      // one 128-byte row per token
-  static constexpr int kCodeBytes = kTileN * kStageK / 2;
-  static constexpr int kNumAcc = (BNT <= 128) ? 2 : 1;
-  static constexpr int kStages = BNT >= 256 ? 5 : (BNT >= 128 ? (A8 ? 6 : 8) : (BNT >= 64 ? 10 : 12));
-  static constexpr int kAccCols = kNumAcc * BNT;
+  // 32-K chunks per stage: full records, except BF16 x 256 tokens (half records).
+  static constexpr int kChunks = (!A8 && BNT >= 256) ? 2 : 4;
+  static constexpr int kSubStages = 4 / kChunks;                 // stages per record
+  static constexpr int kRecSlot = kChunks * kTileN * 16 + kRecTail; // codes + tail
+  static constexpr int kSlabs = A8 ? 1 : kChunks / 2;           // 128-byte-wide X slabs
+  static constexpr int kSlabBytes = BNT * 128;
+  static constexpr int kXBytes = kSlabs * kSlabBytes;
+  static constexpr int kACols = A8 ? 32 : kChunks * 16;          // A-operand columns / stage
+  static constexpr int kMmaPerStage = A8 ? kChunks : 2 * kChunks;
+  static constexpr int kIssuers = BNT <= 64 ? 2 : 1;
+  static constexpr int kNumSub = kIssuers;                       // partial accumulators
+  static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
+  static constexpr int kAccCols = kNumAcc * kNumSub * BNT;
+  // A/X ring depth: what tensor memory holds next to the accumulators (FP8 also needs
+  // 4 scale-factor columns per stage and 8 constant ones), capped by shared memory.
+  static constexpr int kSfCols = A8 ? 4 : 0;
+  static constexpr int kATmemMax = (512 - kAccCols - (A8 ? 8 : 0)) / (kACols + kSfCols);
+  static constexpr int kAStages =
+      A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
+         : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
+  // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
+  static constexpr int kXChunk = BNT <= 32 ? 4 : BNT == 64 ? 2 : 1;
+  static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
+  static constexpr int kXSlotBytes = kXChunk * kXBytes;
+  static constexpr int kXBoxSlabs = kXChunk * kSlabs;
+  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4;
+  static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
+  static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
+                                kAStages * kBarBytesPerA + kMiscBytes + 64;
+  static constexpr int kRMax = (227 * 1024 - kFixed) / (kRecSlot + kBarBytesPerR);
+  static constexpr int kRStages = kRMax < 16 ? kRMax : 16;
   static constexpr int kACol0 = (kAccCols + 31) / 32 * 32;
-  // Block-scale factors (FP8 activations only): per stage one 4-column slot for the
+  // Block-scale factors (FP8 activations only): per A stage one 4-column slot for the
   // weight-side factors (a row's four E8M0 bytes, one per 32 K, replicated over the four
   // columns of its lane), then 8 columns holding the constant activation-side factor.
-  static constexpr int kSfaCol0 = kACol0 + kStages * 32;
-  static constexpr int kSfbCol0 = (kSfaCol0 + (A8 ? 4 * kStages : 0) + 7) / 8 * 8;
+  static constexpr int kSfaCol0 = kACol0 + kAStages * kACols;
+  static constexpr int kSfbCol0 = (kSfaCol0 + kSfCols * kAStages + 7) / 8 * 8;
   static constexpr int kUsedCols = kSfbCol0 + (A8 ? 8 : 0);
   static constexpr int kTmemCols = kUsedCols <= 32 ? 32 : kUsedCols <= 64 ? 64 :
                                    kUsedCols <= 128 ? 128 : kUsedCols <= 256 ? 256 : 512;
   static_assert(kUsedCols <= 512, "tensor memory budget");
-  static constexpr int kStageBytes = kActBytes + kCodeBytes + kScaleSlot + kZeroSlot;
-  static constexpr int kBarBytes = (3 * kStages + 2 * kNumAcc + 2) * 8;
-  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4;
-  static constexpr int kSmemBytes = 1024 + kStages * kStageBytes + kBarBytes + kMiscBytes;
+  static_assert(kAStages >= 3 && kRStages >= 4, "pipeline depth");
+  static constexpr int kBarBytes = kRStages * kBarBytesPerR + kAStages * kBarBytesPerA +
+                                   kXSlots * kBarBytesPerX + (2 * kNumAcc + 2) * 8;
+  static constexpr int kSmemBytes =
+      1024 + kXSlots * kXSlotBytes + kRStages * kRecSlot + kBarBytes + kMiscBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
 struct Unit {
   int nt, mt, split, expert;
-  int kb0, kb1;
+  int kb0, kb1;            // record range [kb0, kb1)
   int64_t row0, row_end;
 };
 
@@ -110,28 +152,103 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& a, int bnt, c
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
 
-template <int BNT, bool A8>
+// One arrival per warp once every lane got here (barriers of warp roles count warps, not
+// threads: 128 per-thread arrivals would serialise on the barrier's shared-memory word).
+__device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
+  __syncwarp();
+  if (lane == 0) ptx::mbar_arrive(bar);
+}
+
+// Position in a ring of `n` slots: slot index and the parity of its current use.
+struct Ring {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ __forceinline__ void next(int n) {
+    if (++slot == n) { slot = 0; phase ^= 1u; }
+  }
+};
+
+// Decode modes: the kernel is compiled per weight format so that the decode loop holds
+// only the code it runs.  "G1": one scale (and zero point) per row per record, i.e. a
+// group of 128 K or longer, so they are read once per record.
+enum DecodeMode : int { DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3 };
+
+// Decode two 32-K chunks of weight row r into 32 bf16x2 registers (pair order).  The codes
+// come from slot chunks `slot0`, `slot0 + 1` of the staged record; their scales and zero
+// points are the record's entries for record chunks `rchunk0`, `rchunk0 + 1`.
+template <int DM>
+__device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int tail, int slot0,
+                                                      int rchunk0, int r, int has_zp, int G,
+                                                      int zoff, uint32_t (&regs)[32]) {
+  if constexpr (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1) {
+    const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[r];
+    uint32_t z = 8;
+    if constexpr (DM == DM_INT4_ZP_G1) z = (rec[tail + zoff + (r >> 1)] >> (4 * (r & 1))) & 0xFu;
+    const uint32_t zz = (0x4300u | z) * 0x00010001u;
+    const uint32_t s2 = s * 0x00010001u;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 q = *reinterpret_cast<const uint4*>(rec + (slot0 + c) * (kTileN * 16) + r * 16);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const uint4 q = *reinterpret_cast<const uint4*>(rec + (slot0 + c) * (kTileN * 16) + r * 16);
+      const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
+      if constexpr (DM == DM_MXFP4) {
+        const uint32_t E = rec[tail + r * 4 + rchunk0 + c];   // one E8M0 per 32 K
+        uint32_t sa, sb;
+        bool big;
+        mxfp4_factors(E, sa, sb, big);
+        const bool two = __any_sync(0xffffffffu, big);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) decode_mxfp4_word(wd[j], sa, sb, two, &regs[16 * c + 4 * j]);
+      } else {
+        const int ent = r * G + ((rchunk0 + c) * G) / 4;      // scale entry of this chunk
+        const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[ent];
+        uint32_t z = 8;
+        if (has_zp) z = (rec[tail + zoff + (ent >> 1)] >> (4 * (ent & 1))) & 0xFu;
+        const uint32_t zz = (0x4300u | z) * 0x00010001u;
+        const uint32_t s2 = s * 0x00010001u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+      }
+    }
+  }
+}
+
+template <int BNT, bool A8, int DM>
 __global__ void __launch_bounds__(kThreads, 1)
-qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
+qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   using C = GemmCfg<BNT, A8>;
-  constexpr int S = C::kStages;
+  constexpr int SA = C::kAStages;
+  constexpr int SR = C::kRStages;
+  constexpr int SX = C::kXSlots;
+  constexpr int XQ = C::kXChunk;
+  constexpr int CH = C::kChunks;
+  constexpr int kSub = C::kSubStages;
+  constexpr int kTail = CH * kTileN * 16;                // scales + zeros inside a slot
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* s_act = smem;
-  uint8_t* s_code = s_act + S * C::kActBytes;
-  uint8_t* s_scale = s_code + S * C::kCodeBytes;
-  uint8_t* s_zero = s_scale + S * kScaleSlot;
-  uint64_t* full = reinterpret_cast<uint64_t*>(s_zero + S * kZeroSlot);
-  uint64_t* afull = full + S;
-  uint64_t* empty = afull + S;
-  uint64_t* accfull = empty + S;
+  uint8_t* s_x = smem;                                   // [SX][kXSlotBytes], 1024-aligned
+  uint8_t* s_rec = s_x + SX * C::kXSlotBytes;            // [SR][kRecSlot]
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(s_rec + SR * C::kRecSlot);
+  uint64_t* rempty = rfull + SR;
+  uint64_t* xfull = rempty + SR;
+  uint64_t* xempty = xfull + SX;
+  uint64_t* afull = xempty + SX;
+  uint64_t* aempty = afull + SA;
+  uint64_t* accfull = aempty + SA;
   uint64_t* accempty = accfull + C::kNumAcc;
   uint64_t* drain = accempty + C::kNumAcc;
-  uint64_t* epibar = drain + 1;                    // epilogue-warps rendezvous (split-K)
-  int* misc = reinterpret_cast<int*>(epibar + 1);  // [0] tmem base [1] abort [2] ok [3] units
-  int* prefix = misc + 16;                         // MoE: m-tiles before expert e
-  int* offs = prefix + (kMaxExperts + 1);          // MoE: row offsets
+  uint64_t* epibar = drain + 1;                          // epilogue rendezvous (split-K)
+  int* misc = reinterpret_cast<int*>(epibar + 1);        // [0] tmem [1] abort [2] ok [3] units [4] last
+  int* prefix = misc + 16;                               // MoE: m-tiles before expert e
+  int* offs = prefix + (kMaxExperts + 1);                // MoE: row offsets
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -151,21 +268,28 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
     }
     if (!ok) atomicCAS(a.status, 0, kStatusBadPacked);
     misc[2] = ok ? 1 : 0;
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(&full[s], 1);
-      ptx::mbar_init(&afull[s], 128);
-      ptx::mbar_init(&empty[s], 1);
+    for (int s = 0; s < SR; ++s) {
+      ptx::mbar_init(&rfull[s], 1);
+      ptx::mbar_init(&rempty[s], 4);     // one arrival per dequant warp
+    }
+    for (int s = 0; s < SX; ++s) {
+      ptx::mbar_init(&xfull[s], 1);
+      ptx::mbar_init(&xempty[s], C::kIssuers);
+    }
+    for (int s = 0; s < SA; ++s) {
+      ptx::mbar_init(&afull[s], 4);
+      ptx::mbar_init(&aempty[s], 1);
     }
     for (int i = 0; i < C::kNumAcc; ++i) {
-      ptx::mbar_init(&accfull[i], 1);
-      ptx::mbar_init(&accempty[i], 128);
+      ptx::mbar_init(&accfull[i], C::kIssuers);
+      ptx::mbar_init(&accempty[i], 4);  // one arrival per epilogue warp
     }
-    ptx::mbar_init(drain, 1);
-    ptx::mbar_init(epibar, 128);
+    ptx::mbar_init(drain, C::kIssuers);
+    ptx::mbar_init(epibar, 4);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
-  if (warp == 0 && lane == 0) ptx::prefetch_tmap(&tmap_x);
+  if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
   int num_units = a.num_units;
   if (a.offsets != nullptr && warp == 2) {
     // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).
@@ -213,7 +337,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
   volatile int* abort_flag = &misc[1];
   const uint64_t T = a.timeout_ns;
 
-  if (A8 && warp >= 6) {
+  if (A8 && warp >= 10 && warp < 14) {
     // Activation-side block scale: a constant 2^6 (E8M0 133) that returns the factor 2^-6
     // of the e2m1 -> e4m3 byte shuffle.  Filled over every lane of its columns.
     const uint32_t tl = tbase + (uint32_t((warp & 3) * 32) << 16);
@@ -225,164 +349,219 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
   __syncthreads();
   ptx::tc_fence_after();
 
-  if (warp == 0) {
-    // ---------------------------------------------------------------- producer
+  if (warp == 0 || warp == kRecProducerWarp1) {
+    // ---------------------------------------------------------------- record producers
+    const int rp = (warp == 0) ? 0 : 1;     // takes the stages g with g % 2 == rp
     if (lane == 0) {
-      const uint64_t pol_w = ptx::policy_evict_first();
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t issued_parity[S];
-      bool issued[S];
-      for (int s = 0; s < S; ++s) issued[s] = false;
+      const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+      const uint32_t rec_bytes = uint32_t(L.record_bytes);
+      const uint32_t tail_bytes = rec_bytes - uint32_t(kCodeBytes);     // scales + zeros
+      const uint32_t stage_tx = CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
+      Ring rr;
+      uint32_t pending = 0, pending_parity = 0;   // copies in flight, for the wind-down
+      uint32_t g = 0;                             // stage counter of this CTA
       bool alive = true;
       for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
         const Unit w = decode_unit(u, a, BNT, prefix, offs);
-        const uint8_t* P = a.packed + int64_t(w.expert) * a.expert_stride;
-        const uint8_t* codes = P + L.off_codes + int64_t(w.nt) * L.k_blocks * L.code_tile_bytes;
-        const int64_t st_base = int64_t(w.nt) * L.scale_tiles;
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, abort_flag, T)) { alive = false; break; }
-          const int64_t stile = L.groups_per_tile == 1 ? (int64_t(kb) * C::kStageK) / L.group : kb;
-          const uint32_t bytes = uint32_t(C::kActBytes + L.code_tile_bytes + L.scale_tile_bytes +
-                                          (L.has_zp ? L.zero_tile_bytes : 0));
-          ptx::mbar_arrive_expect_tx(&full[stage], bytes);
-          ptx::tma_load_2d(s_act + stage * C::kActBytes, &tmap_x, kb * C::kStageK,
-                           int32_t(w.row0), &full[stage]);
-          ptx::bulk_g2s(s_code + stage * C::kCodeBytes, codes + int64_t(kb) * L.code_tile_bytes,
-                        uint32_t(L.code_tile_bytes), &full[stage], pol_w);
-          ptx::bulk_g2s(s_scale + stage * kScaleSlot,
-                        P + L.off_scales + (st_base + stile) * L.scale_tile_bytes,
-                        uint32_t(L.scale_tile_bytes), &full[stage], pol_w);
-          if (L.has_zp)
-            ptx::bulk_g2s(s_zero + stage * kZeroSlot,
-                          P + L.off_zeros + (st_base + stile) * L.zero_tile_bytes,
-                          uint32_t(L.zero_tile_bytes), &full[stage], pol_w);
-          issued[stage] = true;
-          issued_parity[stage] = phase;
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+        const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
+                             (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
+        for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
+#pragma unroll 1
+          for (int h = 0; h < kSub; ++h, ++g) {
+            if ((g & 1u) != uint32_t(rp)) { rr.next(SR); continue; }
+            if (!ptx::mbar_wait(&rempty[rr.slot], rr.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
+            uint8_t* sr = s_rec + rr.slot * C::kRecSlot;
+            ptx::mbar_arrive_expect_tx(&rfull[rr.slot], stage_tx);
+            if (CH == 4) {
+              ptx::bulk_g2s(sr, rec, rec_bytes, &rfull[rr.slot], pol_w);
+            } else {
+              // half record: codes of record chunks 2h, 2h+1, then the scales and zeros
+              ptx::bulk_g2s(sr, rec + h * (kCodeBytes / 2), kCodeBytes / 2, &rfull[rr.slot], pol_w);
+              ptx::bulk_g2s(sr + kTail, rec + kCodeBytes, tail_bytes, &rfull[rr.slot], pol_w);
+            }
+            pending |= 1u << rr.slot;
+            pending_parity = (pending_parity & ~(1u << rr.slot)) | (rr.phase << rr.slot);
+            rr.next(SR);
+          }
         }
       }
       if (!alive) {
-        // Wind down: let every copy this thread issued land before the CTA exits.
-        volatile int no_abort = 0;
-        for (int s = 0; s < S; ++s)
-          if (issued[s]) ptx::mbar_wait(&full[s], issued_parity[s], &no_abort, 200000000ull);
+        volatile int no_abort = 0;      // let every copy this thread issued land first
+        for (int s = 0; s < SR; ++s)
+          if (pending & (1u << s))
+            ptx::mbar_wait(&rfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
       }
     }
-  } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+  } else if (warp == kXProducerWarp) {
+    // ---------------------------------------------------------------- activation producer
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      Ring rx;
+      uint32_t pending = 0, pending_parity = 0;
+      bool alive = true;
+      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
+        const Unit w = decode_unit(u, a, BNT, prefix, offs);
+        const int32_t row0 = int32_t(w.row0);
+        const int nst = (w.kb1 - w.kb0) * kSub;
+        for (int i0 = 0; i0 < nst; i0 += XQ) {
+          if (!ptx::mbar_wait(&xempty[rx.slot], rx.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
+          uint8_t* sx = s_x + rx.slot * C::kXSlotBytes;
+          // K offset (elements) of the chunk's first stage: records kb0.., sub-stage h
+          const int k0 = w.kb0 * kStageK + i0 * (kStageK / kSub);
+          ptx::mbar_arrive_expect_tx(&xfull[rx.slot], uint32_t(C::kXSlotBytes));
+          if (a.x_3d) {
+            // box {slab, token_tile rows, kXBoxSlabs slabs}; slab index = K / slab width
+            ptx::tma_load_3d(sx, &tmap_x, 0, row0, k0 / (A8 ? 128 : 64), &xfull[rx.slot]);
+          } else {
+#pragma unroll 1
+            for (int sl = 0; sl < C::kXBoxSlabs; ++sl)
+              ptx::tma_load_2d(sx + sl * C::kSlabBytes, &tmap_x, k0 + sl * (A8 ? 128 : 64), row0,
+                               &xfull[rx.slot]);
+          }
+          pending |= 1u << rx.slot;
+          pending_parity = (pending_parity & ~(1u << rx.slot)) | (rx.phase << rx.slot);
+          rx.next(SX);
+        }
+      }
+      if (!alive) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < SX; ++s)
+          if (pending & (1u << s))
+            ptx::mbar_wait(&xfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
+      }
+    }
+  } else if (warp == 1 || warp == kIssuerWarp1) {
+    // ---------------------------------------------------------------- MMA issuer(s)
+    // Issuer j takes the stages i of each unit with i % kIssuers == j (the stages of
+    // dequant warpgroup j when there are two) and accumulates into partial accumulator j.
+    const int issuer = (warp == 1) ? 0 : 1;
+    if (lane == 0 && issuer < C::kIssuers) {
+      Ring ra, rx;
       int ui = 0;
       bool alive = true;
+      const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
       for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x, ++ui) {
         const Unit w = decode_unit(u, a, BNT, prefix, offs);
         const int acc = ui % C::kNumAcc;
         const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
-        if (!ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T)) break;
+        if (!ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma)) break;
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tbase + uint32_t(acc * BNT);
-        for (int kb = w.kb0; kb < w.kb1; ++kb) {
-          if (!ptx::mbar_wait(&afull[stage], phase, abort_flag, T)) { alive = false; break; }
-          ptx::tc_fence_after();
-          const uint64_t bdesc = ptx::desc_kmajor_sw128(ptx::smem_u32(s_act + stage * C::kActBytes));
-          const uint32_t a_tmem = tbase + uint32_t(C::kACol0 + stage * 32);
+        const uint32_t d_tmem = tbase + uint32_t((acc * C::kNumSub + issuer) * BNT);
+        const int nst = (w.kb1 - w.kb0) * kSub;
+        bool first = true;                  // this issuer's first MMA of the unit overwrites
+        bool x_ready = false;               // waited for the current X slot
+        for (int i = 0; i < nst; ++i) {
+          const Ring cur = ra;
+          ra.next(SA);
+          const int xj = i % XQ;            // stage inside the X slot
+          if (xj == 0) x_ready = false;
+          const bool mine = (i % C::kIssuers) == issuer;
+          if (mine) {
+            if (!x_ready) {
+              if (!ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma)) { alive = false; break; }
+              x_ready = true;
+            }
+            if (!ptx::mbar_wait(&afull[cur.slot], cur.phase, abort_flag, T, kSleepMma)) { alive = false; break; }
+            ptx::tc_fence_after();
+            const uint64_t bdesc =
+                desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
+          const uint32_t a_tmem = tbase + uint32_t(C::kACol0 + cur.slot * C::kACols);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t accum = (kb > w.kb0 || kk > 0) ? 1u : 0u;
+          for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
+            const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
             if constexpr (A8) {
               ptx::mma_mxf8f6f4_ts(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2),
                                    ptx::idesc_mxf8_e4m3(128, BNT, kk, 0),
-                                   tbase + uint32_t(C::kSfaCol0 + 4 * stage),
+                                   tbase + uint32_t(C::kSfaCol0 + 4 * cur.slot),
                                    tbase + uint32_t(C::kSfbCol0), accum);
             } else {
-              ptx::mma_f16_ts(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2),
+              // slab kk / 4, 32-byte K step kk % 4 inside the 128-byte swizzled row
+              ptx::mma_f16_ts(d_tmem, a_tmem + kk * 8,
+                              bdesc + uint64_t(((kk >> 2) * C::kSlabBytes) >> 4) +
+                                  uint64_t((kk & 3) * 2),
                               ptx::idesc_bf16(128, BNT), accum);
             }
           }
-          ptx::mma_commit(&empty[stage]);
-          if (++stage == S) { stage = 0; phase ^= 1u; }
+            first = false;
+            ptx::mma_commit(&aempty[cur.slot]);   // frees the stage's A columns
+          }
+          if (xj == XQ - 1 || i == nst - 1) {
+            ptx::mma_commit(&xempty[rx.slot]);    // every issuer releases every X slot
+            rx.next(SX);
+          }
         }
         if (!alive) break;
-        ptx::mma_commit(&accfull[acc]);
+        ptx::mma_commit(&accfull[acc]);      // every issuer arrives once per unit
       }
       // Every MMA issued above has completed once `drain` flips.
       ptx::mma_commit(drain);
       volatile int no_abort = 0;
       ptx::mbar_wait(drain, 0, &no_abort, 200000000ull);
     }
-  } else if (warp < 6) {
-    // ---------------------------------------------------------------- dequant
+  } else if (warp < 10) {
+    // ---------------------------------------------------------------- dequant (2 WGs)
+    const int wg = (warp - 2) >> 2;                        // takes stages with i % 2 == wg
     const int r = (warp & 3) * 32 + lane;                  // weight row = TMEM lane
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
-    int stage = 0;
-    uint32_t phase = 0;
-    const int G = L.groups_per_tile;
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x) {
+    const int G = L.groups_per_record;
+    const int zoff = L.off_zeros - L.off_scales;
+    Ring rr, ra;
+    bool alive = true;
+    for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
       const Unit w = decode_unit(u, a, BNT, prefix, offs);
-      bool alive = true;
-      for (int kb = w.kb0; kb < w.kb1; ++kb) {
-        if (!warp_all(ptx::mbar_wait(&full[stage], phase, abort_flag, T))) { alive = false; break; }
-        const uint8_t* cs = s_code + stage * C::kCodeBytes;
-        const uint8_t* ss = s_scale + stage * kScaleSlot;
-        uint32_t regs[32];
+      const int nst = (w.kb1 - w.kb0) * kSub;
+      for (int i = 0; i < nst; ++i) {
+        const Ring cr = rr, ca = ra;
+        rr.next(SR);
+        ra.next(SA);
+        if ((i & 1) != wg) continue;
+        if (!warp_all(ptx::mbar_wait(&rfull[cr.slot], cr.phase, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        const uint8_t* rec = s_rec + cr.slot * C::kRecSlot;
+        const uint32_t a_col = t_lane + uint32_t(C::kACol0 + ca.slot * C::kACols);
         if constexpr (A8) {
+          uint32_t regs[32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const uint4 q = *reinterpret_cast<const uint4*>(cs + c * 2048 + r * 16);
+            const uint4 q = *reinterpret_cast<const uint4*>(rec + c * (kTileN * 16) + r * 16);
             const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               decode_e2m1_to_e4m3_word(wd[j], regs[8 * c + 2 * j], regs[8 * c + 2 * j + 1]);
           }
-          const uint32_t sf = *reinterpret_cast<const uint32_t*>(ss + r * 4);   // 4 x E8M0
-          ptx::tmem_st4(t_lane + uint32_t(C::kSfaCol0 + 4 * stage), sf, sf, sf, sf);
+          const uint32_t sf = *reinterpret_cast<const uint32_t*>(rec + kTail + r * 4);
+          warp_arrive(&rempty[cr.slot], lane);           // record consumed
+          if (!warp_all(ptx::mbar_wait(&aempty[ca.slot], ca.phase ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+          ptx::tc_fence_after();
+          ptx::tmem_st4(t_lane + uint32_t(C::kSfaCol0 + 4 * ca.slot), sf, sf, sf, sf);
+          ptx::tmem_st32(a_col, regs);
         } else {
-#pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            const uint4 q = *reinterpret_cast<const uint4*>(cs + c * 2048 + r * 16);
-            const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
-            const int ge = (G == 1) ? 0 : c;                  // group entry of this chunk
-            if (L.wfmt == W_MXFP4) {
-              const uint32_t E = ss[r * G + ge];
-              uint32_t sa, sb;
-              bool big;
-              mxfp4_factors(E, sa, sb, big);
-              const bool two = __any_sync(0xffffffffu, big);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) decode_mxfp4_word(wd[j], sa, sb, two, &regs[16 * c + 4 * j]);
-            } else {
-              const uint32_t s = reinterpret_cast<const uint16_t*>(ss)[r * G + ge];
-              uint32_t z = 8;
-              if (L.has_zp) {
-                const int zi = r * G + ge;
-                z = (s_zero[stage * kZeroSlot + (zi >> 1)] >> (4 * (zi & 1))) & 0xFu;
-              }
-              const uint32_t zz = (0x4300u | z) * 0x00010001u;
-              const uint32_t s2 = s * 0x00010001u;
-#pragma unroll
-              for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], zz, s2, &regs[16 * c + 4 * j]);
-            }
+          // A half record holds record chunks 2h, 2h + 1 (h = i % 2) in slot chunks 0, 1.
+          const int rbase = (CH == 4) ? 0 : 2 * (i & 1);
+          uint32_t regs[32];
+          decode_two_chunks_a16<DM>(rec, kTail, 0, rbase, r, L.has_zp, G, zoff, regs);
+          if (CH == 2) warp_arrive(&rempty[cr.slot], lane);
+          if (!warp_all(ptx::mbar_wait(&aempty[ca.slot], ca.phase ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+          ptx::tc_fence_after();
+          ptx::tmem_st32(a_col, regs);
+          if (CH == 4) {
+            decode_two_chunks_a16<DM>(rec, kTail, 2, 2, r, L.has_zp, G, zoff, regs);
+            warp_arrive(&rempty[cr.slot], lane);
+            ptx::tmem_st32(a_col + 32u, regs);
           }
         }
-        ptx::tmem_st32(t_lane + uint32_t(C::kACol0 + stage * 32), regs);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
-        ptx::mbar_arrive(&afull[stage]);
-        if (++stage == S) { stage = 0; phase ^= 1u; }
+        warp_arrive(&afull[ca.slot], lane);
       }
-      if (!alive) break;
     }
-  } else {
+  } else if (warp < 14) {
     // ---------------------------------------------------------------- epilogue
     const int r = (warp & 3) * 32 + lane;
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
     uint32_t epi_phase = 0;
     // Bounded rendezvous of the 128 epilogue threads (a named barrier could not give up).
     auto epi_sync = [&]() -> bool {
-      ptx::mbar_arrive(epibar);
-      const bool ok = ptx::mbar_wait(epibar, epi_phase, abort_flag, T);
+      warp_arrive(epibar, lane);
+      const bool ok = ptx::mbar_wait(epibar, epi_phase, abort_flag, T, kSleepEpilogue);
       epi_phase ^= 1u;
       return warp_all(ok);
     };
@@ -391,29 +570,49 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
       const Unit w = decode_unit(u, a, BNT, prefix, offs);
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
-      if (!warp_all(ptx::mbar_wait(&accfull[acc], acc_par, abort_flag, T))) break;
+      if (!warp_all(ptx::mbar_wait(&accfull[acc], acc_par, abort_flag, T, kSleepEpilogue))) break;
       ptx::tc_fence_after();
       const int64_t n = int64_t(w.nt) * kTileN + r;
       const bool n_ok = n < L.N;
       const bool split = a.splits > 1;
       const float cs = (n_ok && a.chan_scale != nullptr && !split) ? a.chan_scale[n] : 1.0f;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
+      // partial accumulators of the issuers that had a stage in this unit
+      const int active = min(C::kNumSub, (w.kb1 - w.kb0) * kSub);
       constexpr int kChunk = BNT < 32 ? BNT : 32;
 #pragma unroll 1
       for (int c = 0; c < BNT / kChunk; ++c) {
         uint32_t v[32];
+        const uint32_t col = t_lane + uint32_t(acc * C::kNumSub * BNT + c * kChunk);
         if constexpr (kChunk == 32) {
-          ptx::tmem_ld32(t_lane + uint32_t(acc * BNT + c * 32), v);
+          ptx::tmem_ld32(col, v);
         } else {
           uint32_t v16[16];
-          ptx::tmem_ld16(t_lane + uint32_t(acc * BNT), v16);
+          ptx::tmem_ld16(col, v16);
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = v16[j];
+        }
+#pragma unroll
+        for (int sub = 1; sub < C::kNumSub; ++sub) {
+          if (sub >= active) break;
+          uint32_t p[32];
+          if constexpr (kChunk == 32) {
+            ptx::tmem_ld32(col + uint32_t(sub * BNT), p);
+          } else {
+            uint32_t p16[16];
+            ptx::tmem_ld16(col + uint32_t(sub * BNT), p16);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) p[j] = p16[j];
+          }
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < kChunk; ++j)
+            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(p[j]));
         }
         ptx::tmem_wait_ld();
         if (c == BNT / kChunk - 1) {
           ptx::tc_fence_before();
-          ptx::mbar_arrive(&accempty[acc]);
+          warp_arrive(&accempty[acc], lane);
         }
         if (n_ok) {
 #pragma unroll
@@ -448,12 +647,22 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
           if (n_ok) {
             const float cs2 = a.chan_scale != nullptr ? a.chan_scale[n] : 1.0f;
             const int64_t m_end = w.row0 + BNT < w.row_end ? w.row0 + BNT : w.row_end;
-            for (int64_t m = w.row0; m < m_end; ++m) {
-              float* p = a.ws + m * a.ws_ld + n;
-              float y = __ldcg(p) * cs2;
-              if (A8) y *= a.tok_scale[m];
-              Y[m * a.ldy + n] = __float2bfloat16_rn(y);
-              __stcg(p, 0.0f);
+            // 8 independent loads in flight per thread; rows of one warp are coalesced.
+            for (int64_t m0 = w.row0; m0 < m_end; m0 += 8) {
+              float v[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                v[j] = (m0 + j < m_end) ? __ldcg(a.ws + (m0 + j) * a.ws_ld + n) : 0.0f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const int64_t m = m0 + j;
+                if (m < m_end) {
+                  float y = v[j] * cs2;
+                  if (A8) y *= a.tok_scale[m];
+                  Y[m * a.ldy + n] = __float2bfloat16_rn(y);
+                  __stcg(a.ws + m * a.ws_ld + n, 0.0f);
+                }
+              }
             }
           }
         }
@@ -470,7 +679,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const GemmArgs a) {
   if (warp == 1) ptx::tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int BNT, bool A8>
+template <int BNT, bool A8, int DM>
 cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                            cudaStream_t st) {
   using C = GemmCfg<BNT, A8>;
@@ -479,25 +688,44 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
   constexpr int kSmem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<BNT, A8>,
+    cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<BNT, A8, DM>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  qgemm_tc_kernel<BNT, A8><<<plan.grid, kThreads, kSmem, st>>>(tmap, args);
+  qgemm_tc_kernel<BNT, A8, DM><<<plan.grid, kThreads, kSmem, st>>>(tmap, args);
   return cudaGetLastError();
 }
 
-template <bool A8>
+template <bool A8, int DM>
 cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                              cudaStream_t st) {
   switch (plan.token_tile) {
-    case 16: return launch_variant<16, A8>(plan, tmap, args, st);
-    case 32: return launch_variant<32, A8>(plan, tmap, args, st);
-    case 64: return launch_variant<64, A8>(plan, tmap, args, st);
-    case 128: return launch_variant<128, A8>(plan, tmap, args, st);
-    case 256: return launch_variant<256, A8>(plan, tmap, args, st);
+    case 16: return launch_variant<16, A8, DM>(plan, tmap, args, st);
+    case 32: return launch_variant<32, A8, DM>(plan, tmap, args, st);
+    case 64: return launch_variant<64, A8, DM>(plan, tmap, args, st);
+    case 128: return launch_variant<128, A8, DM>(plan, tmap, args, st);
+    case 256: return launch_variant<256, A8, DM>(plan, tmap, args, st);
     default: return cudaErrorInvalidValue;
+  }
+}
+
+// Decode mode of a packed layout (BF16 activations).
+inline int decode_mode(const Layout& L) {
+  if (L.wfmt == W_MXFP4) return DM_MXFP4;
+  if (L.groups_per_record == 1) return L.has_zp ? DM_INT4_ZP_G1 : DM_INT4_SYM_G1;
+  return DM_INT4_ANY;
+}
+
+template <bool A8>
+int x_box_slabs_impl(int bnt) {
+  switch (bnt) {
+    case 16: return GemmCfg<16, A8>::kXBoxSlabs;
+    case 32: return GemmCfg<32, A8>::kXBoxSlabs;
+    case 64: return GemmCfg<64, A8>::kXBoxSlabs;
+    case 128: return GemmCfg<128, A8>::kXBoxSlabs;
+    case 256: return GemmCfg<256, A8>::kXBoxSlabs;
+    default: return -1;
   }
 }
 

@@ -35,6 +35,7 @@ struct GemmArgs {
   int64_t ws_ld;
   int* status;
   uint64_t timeout_ns;
+  int32_t x_3d;                // X map is 3-D (a box covers several stages); else 2-D
 };
 
 struct GemmPlan {
@@ -44,11 +45,16 @@ struct GemmPlan {
 };
 
 // Launch the tcgen05 GEMM for the given plan.  tmap describes X (BF16 or E4M3, K-major,
-// 128-byte swizzle, box = stage depth x token_tile).
+// 128-byte swizzle): either 2-D with box {one 128-byte slab, token_tile rows}, or (args.x_3d)
+// 3-D [K / slab][rows][slab] with box {slab, token_tile, gemm_x_box_slabs()}.
 cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
                         const GemmArgs& args, cudaStream_t st);
 
 // Dynamic shared memory bytes of a variant (for occupancy checks / attributes).
 int gemm_smem_bytes(bool fp8, int token_tile);
+
+// Number of 128-byte X slabs one 3-D activation load covers (several stages' worth for
+// narrow token tiles, one stage otherwise).
+int gemm_x_box_slabs(bool fp8, int token_tile);
 
 }  // namespace qgemm

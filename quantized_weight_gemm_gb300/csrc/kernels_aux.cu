@@ -20,27 +20,31 @@ int* device_status_ptr() {
 }
 
 // ------------------------------------------------------------------------------ repack
-// One thread writes one 16-byte chunk-row (four words) of one code tile.
+__device__ __forceinline__ uint8_t* record_ptr(const Layout& L, uint8_t* packed, int64_t nt,
+                                               int64_t kb) {
+  return packed + kHeaderBytes + (nt * L.k_blocks + kb) * int64_t(L.record_bytes);
+}
+
+// One thread writes one 16-byte chunk-row (four words) of one record's codes.
 __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
                                     uint8_t* __restrict__ packed) {
-  const int chunks = L.bk / 32;
-  const int64_t total = L.n_tiles * L.k_blocks * chunks * kTileN;
+  const int64_t total = L.n_tiles * L.k_blocks * 4 * kTileN;
   const int64_t Kh = L.K / 2;
   for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int r = int(idx % kTileN);
     int64_t t = idx / kTileN;
-    const int c = int(t % chunks);
-    t /= chunks;
+    const int c = int(t % 4);
+    t /= 4;
     const int64_t kb = t % L.k_blocks;
     const int64_t nt = t / L.k_blocks;
     const int64_t n = nt * kTileN + r;
     uint32_t out[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int64_t k0 = kb * L.bk + c * 32 + j * 8;
+      const int64_t k0 = kb * kStageK + c * 32 + j * 8;
       uint32_t src = 0;
-      bool pad = (n >= L.N) || (k0 >= L.K);
+      const bool pad = (n >= L.N) || (k0 >= L.K);
       if (!pad) src = *reinterpret_cast<const uint32_t*>(codes + n * Kh + k0 / 2);
       uint32_t w = 0;
 #pragma unroll
@@ -52,68 +56,81 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
       }
       out[j] = w;
     }
-    uint8_t* dst = packed + L.off_codes + (nt * L.k_blocks + kb) * L.code_tile_bytes +
-                   int64_t(c) * kTileN * 16 + int64_t(r) * 16;
+    uint8_t* dst = record_ptr(L, packed, nt, kb) + c * (kTileN * 16) + r * 16;
     *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
-// One thread per scale entry (and per zero-point byte).
+// Group of scale entry j of a record: G > 1 splits the record's 128 K into G groups; with
+// G == 1 the record lies inside one group (which may span several records).
+__device__ __forceinline__ int64_t record_group(const Layout& L, int64_t kb, int j) {
+  return L.groups_per_record > 1 ? kb * L.groups_per_record + j : (kb * kStageK) / L.group;
+}
+
+// One thread per scale entry.
 __global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
-                                     const uint8_t* __restrict__ zeros,
                                      uint8_t* __restrict__ packed) {
-  const int G = L.groups_per_tile;
+  const int G = L.groups_per_record;
   const int64_t ngroups = L.K / L.group;
-  const int64_t total = L.n_tiles * L.scale_tiles * kTileN * G;
+  const int64_t total = L.n_tiles * L.k_blocks * kTileN * G;
   for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int j = int(idx % G);
     int64_t t = idx / G;
     const int r = int(t % kTileN);
     t /= kTileN;
-    const int64_t tile = t % L.scale_tiles;
-    const int64_t nt = t / L.scale_tiles;
+    const int64_t kb = t % L.k_blocks;
+    const int64_t nt = t / L.k_blocks;
     const int64_t n = nt * kTileN + r;
-    const int64_t grp = tile * G + j;
+    const int64_t grp = record_group(L, kb, j);
     const bool valid = n < L.N && grp < ngroups;
+    uint8_t* dst = record_ptr(L, packed, nt, kb) + L.off_scales;
     if (L.sdtype == 0) {
       uint16_t v = 0;
       if (valid) {
         v = static_cast<const uint16_t*>(scales)[n * ngroups + grp];
         if ((v & 0x7F80u) == 0x7F80u) set_status(kStatusBadValue);   // NaN / Inf
       }
-      reinterpret_cast<uint16_t*>(packed + L.off_scales)[idx] = v;
+      reinterpret_cast<uint16_t*>(dst)[r * G + j] = v;
     } else {
       uint8_t v = 127;
       if (valid) {
         v = static_cast<const uint8_t*>(scales)[n * ngroups + grp];
         if (v == 255) set_status(kStatusBadValue);
       }
-      (packed + L.off_scales)[idx] = v;
+      dst[r * G + j] = v;
     }
-    if (L.has_zp && (idx & 1) == 0) {
-      // nibble idx (this entry) and idx + 1 (the next entry) share one byte
-      uint8_t byte = 0;
+  }
+}
+
+// One thread per zero-point byte (two entries).
+__global__ void repack_zeros_kernel(Layout L, const uint8_t* __restrict__ zeros,
+                                    uint8_t* __restrict__ packed) {
+  const int G = L.groups_per_record;
+  const int64_t ngroups = L.K / L.group;
+  const int bytes_per_rec = kTileN * G / 2;
+  const int64_t total = L.n_tiles * L.k_blocks * bytes_per_rec;
+  for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * blockDim.x) {
+    const int b = int(idx % bytes_per_rec);
+    const int64_t t = idx / bytes_per_rec;
+    const int64_t kb = t % L.k_blocks;
+    const int64_t nt = t / L.k_blocks;
+    uint8_t byte = 0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t id2 = idx + h;
-        const int j2 = int(id2 % G);
-        int64_t t2 = id2 / G;
-        const int r2 = int(t2 % kTileN);
-        t2 /= kTileN;
-        const int64_t tile2 = t2 % L.scale_tiles;
-        const int64_t nt2 = t2 / L.scale_tiles;
-        const int64_t n2 = nt2 * kTileN + r2;
-        const int64_t g2 = tile2 * G + j2;
-        uint8_t z = 0;
-        if (id2 < total && n2 < L.N && g2 < ngroups) {
-          z = zeros[n2 * ngroups + g2];
-          if (z > 15) { set_status(kStatusBadValue); z &= 15; }
-        }
-        byte |= uint8_t(z << (4 * h));
+    for (int h = 0; h < 2; ++h) {
+      const int e = 2 * b + h;               // entry r * G + j
+      const int r = e / G, j = e % G;
+      const int64_t n = nt * kTileN + r;
+      const int64_t grp = record_group(L, kb, j);
+      uint8_t z = 0;
+      if (n < L.N && grp < ngroups) {
+        z = zeros[n * ngroups + grp];
+        if (z > 15) { set_status(kStatusBadValue); z &= 15; }
       }
-      (packed + L.off_zeros)[idx / 2] = byte;
+      byte |= uint8_t(z << (4 * h));
     }
+    record_ptr(L, packed, nt, kb)[L.off_zeros + b] = byte;
   }
 }
 
@@ -122,26 +139,28 @@ __global__ void write_header_kernel(Layout L, uint8_t* packed) {
   h.magic = kPackedMagic;
   h.version = kPackedVersion;
   h.wfmt = L.wfmt; h.sdtype = L.sdtype; h.group = L.group; h.has_zp = L.has_zp;
-  h.afmt = L.afmt; h.bk = L.bk;
+  h.afmt = L.afmt; h.groups_per_record = L.groups_per_record;
   h.N = L.N; h.K = L.K;
-  h.n_tiles = L.n_tiles; h.k_blocks = L.k_blocks; h.scale_tiles = L.scale_tiles;
-  h.code_tile_bytes = L.code_tile_bytes; h.scale_tile_bytes = L.scale_tile_bytes;
-  h.zero_tile_bytes = L.zero_tile_bytes;
-  h.off_codes = L.off_codes; h.off_scales = L.off_scales; h.off_zeros = L.off_zeros;
-  h.total_bytes = L.total_bytes;
+  h.n_tiles = L.n_tiles; h.k_blocks = L.k_blocks; h.record_bytes = L.record_bytes;
+  h.off_scales = L.off_scales; h.off_zeros = L.off_zeros; h.total_bytes = L.total_bytes;
   *reinterpret_cast<PackedHeader*>(packed) = h;
+}
+
+static int grid_for(int64_t n) {
+  const int64_t b = (n + 255) / 256;
+  return int(b < 65536 ? (b > 0 ? b : 1) : 65536);
 }
 
 cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* scales,
                           const uint8_t* zeros, void* packed, cudaStream_t st) {
   uint8_t* p = static_cast<uint8_t*>(packed);
   write_header_kernel<<<1, 1, 0, st>>>(L, p);
-  const int64_t ncode = L.n_tiles * L.k_blocks * (L.bk / 32) * kTileN;
-  const int blocks_c = int((ncode + 255) / 256 < 65536 ? (ncode + 255) / 256 : 65536);
-  repack_codes_kernel<<<blocks_c, 256, 0, st>>>(L, codes, p);
-  const int64_t nsc = L.n_tiles * L.scale_tiles * kTileN * L.groups_per_tile;
-  const int blocks_s = int((nsc + 255) / 256 < 65536 ? (nsc + 255) / 256 : 65536);
-  repack_scales_kernel<<<blocks_s, 256, 0, st>>>(L, scales, zeros, p);
+  repack_codes_kernel<<<grid_for(L.n_tiles * L.k_blocks * 4 * kTileN), 256, 0, st>>>(L, codes, p);
+  repack_scales_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record), 256, 0,
+                         st>>>(L, scales, p);
+  if (L.has_zp)
+    repack_zeros_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record / 2),
+                          256, 0, st>>>(L, zeros, p);
   return cudaGetLastError();
 }
 
@@ -164,35 +183,29 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
   }
   __syncthreads();
   if (!ok) return;
-  const int chunks = L.bk / 32;
-  const int64_t total = L.n_tiles * L.k_blocks * chunks * kTileN * 4;
-  const int G = L.groups_per_tile;
+  const int64_t total = L.n_tiles * L.k_blocks * 4 * kTileN * 4;
+  const int G = L.groups_per_record;
   for (int64_t idx = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * blockDim.x) {
     const int j = int(idx % 4);
     int64_t t = idx / 4;
     const int r = int(t % kTileN);
     t /= kTileN;
-    const int c = int(t % chunks);
-    t /= chunks;
+    const int c = int(t % 4);
+    t /= 4;
     const int64_t kb = t % L.k_blocks;
     const int64_t nt = t / L.k_blocks;
     const int64_t n = nt * kTileN + r;
-    const int64_t k0 = kb * L.bk + c * 32 + j * 8;
+    const int64_t k0 = kb * kStageK + c * 32 + j * 8;
     if (n >= L.N || k0 >= L.K) continue;
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(
-        packed + L.off_codes + (nt * L.k_blocks + kb) * L.code_tile_bytes +
-        int64_t(c) * kTileN * 16 + int64_t(r) * 16 + j * 4);
-    // scale tile and entry of this stage / group, exactly as the GEMM producer selects them
-    const int64_t kk = kb * L.bk + c * 32 + j * 8;           // first K of the word
-    int64_t tile, jg;
-    if (G == 1) { tile = kk / L.group; jg = 0; }
-    else { tile = kb; jg = (kk - kb * L.bk) / L.group; }
-    const int64_t sidx = ((nt * L.scale_tiles + tile) * kTileN + r) * G + jg;
+    const uint8_t* rec = packed + kHeaderBytes + (nt * L.k_blocks + kb) * int64_t(L.record_bytes);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + c * (kTileN * 16) + r * 16 + j * 4);
+    const int js = c * G / 4;                          // scale entry of chunk c
+    const int ent = r * G + js;
     __nv_bfloat16* dst = W + n * L.K + k0;
     if (L.afmt == A_FP8) {
       // e2m1 -> e4m3 byte shuffle, then value = e4m3 * 2^6 * 2^(E-127) (exact in bf16)
-      const uint32_t E = (packed + L.off_scales)[sidx];
+      const uint32_t E = rec[L.off_scales + ent];
       uint32_t lo, hi;
       decode_e2m1_to_e4m3_word(w, lo, hi);
       for (int e = 0; e < 8; ++e) {
@@ -207,32 +220,27 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
     }
     uint32_t out[4];
     if (L.wfmt == W_MXFP4) {
-      const uint32_t E = (packed + L.off_scales)[sidx];
+      const uint32_t E = rec[L.off_scales + ent];
       uint32_t sa, sb;
       bool big;
       mxfp4_factors(E, sa, sb, big);
       decode_mxfp4_word(w, sa, sb, big, out);
     } else {
-      const uint32_t s = reinterpret_cast<const uint16_t*>(packed + L.off_scales)[sidx];
+      const uint32_t s = reinterpret_cast<const uint16_t*>(rec + L.off_scales)[ent];
       uint32_t z = 8;
-      if (L.has_zp) {
-        const uint8_t zb = (packed + L.off_zeros)[sidx / 2];
-        z = (zb >> (4 * (sidx & 1))) & 0xFu;
-      }
+      if (L.has_zp) z = (rec[L.off_zeros + ent / 2] >> (4 * (ent & 1))) & 0xFu;
       const uint32_t zz = (0x4300u | z) * 0x00010001u;
       decode_int4_word(w, zz, s * 0x00010001u, out);
     }
     // pair i = elements (2i, 2i+1): low half is the even element
-    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);    // k0 % 8 == 0 -> 16-byte aligned
-    *reinterpret_cast<uint4*>(d32) = make_uint4(out[0], out[1], out[2], out[3]);
+    *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
 cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, cudaStream_t st) {
-  const int64_t total = L.n_tiles * L.k_blocks * (L.bk / 32) * kTileN * 4;
-  const int blocks = int((total + 255) / 256 < 65536 ? (total + 255) / 256 : 65536);
-  dequant_debug_kernel<<<blocks, 256, 0, st>>>(L, static_cast<const uint8_t*>(packed),
-                                               static_cast<__nv_bfloat16*>(W));
+  const int64_t total = L.n_tiles * L.k_blocks * 4 * kTileN * 4;
+  dequant_debug_kernel<<<grid_for(total), 256, 0, st>>>(L, static_cast<const uint8_t*>(packed),
+                                                       static_cast<__nv_bfloat16*>(W));
   return cudaGetLastError();
 }
 

@@ -11,7 +11,7 @@
 
 #include <mutex>
 
-#include "../../include/qgemm.h"
+#include "qgemm.h"
 
 namespace {
 

@@ -58,16 +58,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is incomplete
+// (it resumes as soon as the phase completes), so waiting warps do not take issue slots.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred P;\n mbarrier.try_wait.parity.shared::cta.b64 P, [%1], %2, %3;\n"
+      " selp.b32 %0, 1, 0, P;\n}\n"
+      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns) : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Returns false if the
 // shared abort flag was raised or `limit_ns` elapsed; in the latter case raises the flag.
+// Between polls the warp sleeps `sleep_ns`, so that waiting warps leave the issue slots
+// to the warps doing arithmetic on the same sub-partition.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, uint64_t limit_ns) {
+                                          volatile int* abort_flag, uint64_t limit_ns,
+                                          uint32_t sleep_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   uint32_t spins = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 63u) == 0) {
+    if (sleep_ns) __nanosleep(sleep_ns);
+    if ((++spins & 15u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > limit_ns) { *abort_flag = 1; return false; }
     }
@@ -93,6 +109,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
       :: "r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(smem_u32(bar)) : "memory");
 }
 
+// 3-D tiled tensor copy global -> shared (coordinates innermost first, in elements).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
@@ -100,6 +125,12 @@ __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 

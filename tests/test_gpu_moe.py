@@ -1,0 +1,214 @@
+"""MoE grouped GEMM parity of the CUDA path against the float64 oracle.
+
+Rows X_sorted[offsets[e]:offsets[e+1]] are multiplied by expert e's weights ("Humming wird
+angekündigt", section "WnA16": tokens are distributed over the experts and the work per
+expert varies with the load).  Covered: empty experts, counts that are not a multiple of
+the token tile, the padded blocks the router produces, E = 1 reducing to the dense call,
+both activation formats, every token tile, and sampled rows of the DeepSeek-V3-like layer
+(E = 256, top-8, hidden 7168, expert intermediate 2048)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as WL
+
+pytestmark = pytest.mark.gpu
+
+TOL_A16 = 8e-3
+TOL_A8 = 2e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from quantized_weight_gemm_gb300 import build
+    build.build()
+    import quantized_weight_gemm_gb300 as qg
+    qg.force_config(0, 0)
+    qg.device_status(clear=True)
+    yield
+    qg.force_config(0, 0)
+    assert qg.device_status(clear=True) == 0
+
+
+def _stack(ws, field):
+    a = [getattr(w, field) for w in ws]
+    if a[0] is None:
+        return None
+    return np.stack(a)
+
+
+def _pack_experts(ws, afmt="bf16"):
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    d = G.desc_of(ws[0], afmt)
+    codes = G.u8_tensor(_stack(ws, "codes"))
+    sc = _stack(ws, "scales")
+    sc = torch.from_numpy(sc.view(np.int16) if sc.dtype == np.uint16 else sc).cuda()
+    z = _stack(ws, "zeros")
+    z = None if z is None else G.u8_tensor(z)
+    return d, qg.repack(d, codes, sc, z, num_experts=len(ws))
+
+
+def _experts_bf16(ws):
+    return [oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros) for w in ws]
+
+
+def _experts_exact(ws):
+    return [oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros) for w in ws]
+
+
+def _run_moe(ws, x_bits, offsets, afmt="bf16", tok_scale=None, out_fill=None):
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    d, packed = _pack_experts(ws, afmt)
+    off = torch.tensor(np.asarray(offsets, dtype=np.int32), device="cuda")
+    R = x_bits.shape[0]
+    out = torch.empty(R, ws[0].N, dtype=torch.bfloat16, device="cuda")
+    if out_fill is not None:
+        out.fill_(out_fill)
+    if afmt == "bf16":
+        X = G.bf16_tensor(x_bits)
+        y = qg.moe_grouped(d, packed, len(ws), X, off, out=out)
+    else:
+        X = G.u8_tensor(x_bits)
+        ts = torch.from_numpy(np.asarray(tok_scale, dtype=np.float32)).cuda()
+        y = qg.moe_grouped(d, packed, len(ws), X, off, tok_scale=ts, out=out)
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    return G.to_f64(y)
+
+
+def _assert_close(y, ref, tol, rows=None):
+    if rows is not None:
+        y, ref = y[rows], ref[rows]
+    ok, worst = oracle.tolerance_ok(y, ref, tol)
+    assert ok, f"worst error / bound = {worst:.3f}"
+
+
+def _offsets(counts):
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+
+
+@pytest.mark.parametrize("wfmt,counts,N,K", [
+    ("mxfp4", [5, 0, 37, 16, 0, 1, 130, 8], 256, 512),
+    ("mxfp4", [0, 0, 0, 64], 384, 1024),
+    ("uint4_zp", [17, 300, 0, 3], 300, 768),
+    ("int4_sym", [1, 1, 1, 1, 1, 1, 1, 1, 1, 1], 128, 256),
+])
+def test_moe_a16_parity(wfmt, counts, N, K):
+    r = WL.rng(41)
+    off = _offsets(counts)
+    R = int(off[-1])
+    x = WL.gen_x(r, R, K)
+    ws = [WL.gen_weights(r, wfmt, N, K) for _ in counts]
+    ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+    _assert_close(_run_moe(ws, x, off), ref, TOL_A16)
+
+
+def F_bits(x_bits):
+    from oracle import formats as F
+    return F.bf16_bits_to_float(x_bits)
+
+
+@pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
+def test_moe_every_token_tile(tile):
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(42)
+    counts = [3, 70, 0, 129, 16, 33]
+    off = _offsets(counts)
+    R = int(off[-1])
+    N, K = 256, 640
+    x = WL.gen_x(r, R, K)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+    qg.force_config(tile, 0)
+    try:
+        y = _run_moe(ws, x, off)
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A16)
+
+
+def test_moe_single_expert_equals_dense():
+    """E = 1 over all rows is the dense call (same kernel schedule reduced to one group)."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(43)
+    M, N, K = 77, 384, 512
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    y_moe = _run_moe([w], x, [0, M])
+    d, packed = G.pack(w)
+    qg.force_config(0, 1)
+    try:
+        y_dense = G.to_f64(qg.w4a16(d, packed, G.bf16_tensor(x)))
+    finally:
+        qg.force_config(0, 0)
+    np.testing.assert_array_equal(y_moe, y_dense)
+
+
+def test_moe_rows_outside_groups_untouched():
+    """Rows before offsets[0] and after offsets[E] are not written."""
+    r = WL.rng(44)
+    counts = [9, 0, 20]
+    off = _offsets(counts) + 5
+    R = int(off[-1]) + 7
+    N, K = 256, 256
+    x = WL.gen_x(r, R, K)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    y = _run_moe(ws, x, off, out_fill=3.0)
+    assert np.all(y[:5] == 3.0) and np.all(y[int(off[-1]):] == 3.0)
+    ref = oracle.moe_grouped(F_bits(x)[5:int(off[-1])], off - 5, _experts_bf16(ws))
+    _assert_close(y[5:int(off[-1])], ref, TOL_A16)
+
+
+def test_moe_a8_parity():
+    r = WL.rng(45)
+    counts = [12, 0, 41, 200, 1]
+    off = _offsets(counts)
+    R = int(off[-1])
+    N, K = 512, 1024
+    x = WL.gen_x(r, R, K, outliers=True)
+    xq, s = oracle.quant_act_fp8(x)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    from oracle import formats as F
+    ref = oracle.moe_grouped(F.e4m3_to_float(xq), off, _experts_exact(ws), tok_scale=s)
+    _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=s), ref, TOL_A8)
+
+
+def test_moe_router_workload_sampled():
+    """The DeepSeek-V3-like layer's gate_up GEMM (E = 256 MXFP4 experts of 4096 x 7168)
+    at T = 128 tokens routed top-8 with the skewed logits, in the default launch
+    configuration: 32 sampled rows (each against its own expert) plus every row of the two
+    largest experts."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    case = WL.moe_case(128, seed=0, skewed=True)
+    E, N, K = WL.MOE_E, 2 * WL.MOE_INTER, WL.MOE_HIDDEN
+    off = np.asarray(case.offsets, dtype=np.int64)
+    R = int(off[-1])
+    r = WL.rng(46)
+    rows = set(int(v) for v in r.choice(R, size=32, replace=False))
+    for e in np.argsort(-np.diff(off), kind="stable")[:2]:
+        rows.update(range(int(off[e]), int(off[e + 1])))
+    rows = sorted(rows)
+    expert_of = np.searchsorted(off, np.asarray(rows), side="right") - 1
+    d = qg.WeightDesc("mxfp4", N, K, 32)
+    nb = qg.packed_bytes(d)
+    packed = torch.empty(nb * E, dtype=torch.uint8, device="cuda")
+    xf = F_bits(case.x_bits)
+    ref = np.zeros((len(rows), N))
+    for e, w in enumerate(WL.iter_moe_weights(E, N, K, seed=0)):
+        qg.repack(d, G.u8_tensor(w.codes), G.u8_tensor(w.scales), None,
+                  out=packed[e * nb:(e + 1) * nb])
+        mine = np.nonzero(expert_of == e)[0]
+        if len(mine):
+            W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales)
+            ref[mine] = oracle.gemm(xf[[rows[i] for i in mine]], W)
+    X = G.bf16_tensor(case.x_bits)
+    y = qg.moe_grouped(d, packed, E, X, torch.tensor(off.astype(np.int32), device="cuda"))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    y = G.to_f64(y)
+    _assert_close(y[rows], ref, TOL_A16)

@@ -173,8 +173,19 @@ def moe_case(T, seed=0, skewed=False, E=MOE_E, topk=MOE_TOPK, hidden=MOE_HIDDEN,
     return case
 
 
-def moe_weights(E, N, K, seed=0, wfmt="mxfp4"):
-    """E stacked experts' weights of one GEMM (gate_up: N=2*inter, K=hidden; down:
-    N=hidden, K=inter), drawn expert by expert from one generator."""
+def iter_moe_weights(E, N, K, seed=0):
+    """The E experts' MXFP4 weights of one GEMM (gate_up: N=2*inter, K=hidden; down:
+    N=hidden, K=inter), yielded expert by expert from one generator so that a caller can
+    repack each and drop it.  Codes are drawn as whole bytes uniform over 0..255, which
+    is two independent nibbles uniform over all 16 e2m1 codes; then the E8M0 exponents,
+    uniform in [118, 126], one per 32 K-elements."""
     r = rng(seed + 1000)
-    return [gen_weights(r, wfmt, N, K) for _ in range(E)]
+    for _ in range(E):
+        codes = np.frombuffer(bytearray(r.bytes(N * K // 2)), dtype=np.uint8).reshape(N, K // 2)
+        scales = r.integers(118, 127, size=(N, K // 32), dtype=np.uint8)
+        yield WeightCase("mxfp4", 32, N, K, codes, scales)
+
+
+def moe_weights(E, N, K, seed=0):
+    """All E experts of iter_moe_weights() as a list."""
+    return list(iter_moe_weights(E, N, K, seed))

@@ -10,8 +10,12 @@ wird angekündigt" (vLLM blog, German edition), section "Leistung".
 value   = sum of 2*M*N*K over the step / sum of the event-timed call durations (TFLOP/s)
 e2e     = the same calls through the public API with X copied from pinned host memory and
           Y copied back to pinned host memory inside the timed region
-roofline: dominant kernel = the 256-token-tile variant (M >= 256, tensor bound); small-M
-          (M <= 16, HBM bound) is reported beside it.
+roofline: the dominant launch (the call with the largest share of the step time, a
+          tensor-bound M = 8192 call): 2*M*N*K / its event time against the measured bf16
+          peak; the HBM-bound small-M calls (M <= 16: weight + X + Y bytes / time against
+          the measured copy bandwidth) are reported beside it
+other_workloads: the MXFP4 W4A16, MXFP4 W4A8 and MoE grouped sweeps, measured once after
+          the timed region (--no-extra skips them)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -56,6 +60,31 @@ def weight_bytes(N, K, g=GROUP):
 
 def alg_bytes(M, N, K):
     return weight_bytes(N, K) + M * K * 2 + M * N * 2
+
+
+# DRAM bytes (read + write) per launch from one ncu capture of the same call, keyed by
+# (N, K, M), with the digest of the kernel sources they were taken on; a changed kernel
+# reports null until it is captured again.
+CAPTURED_TRAFFIC = {"csrc_sha256": None, "launches": {}}
+
+
+def csrc_digest():
+    import hashlib
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "quantized_weight_gemm_gb300", "csrc")
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    with open(os.path.join(ROOT, "include", "qgemm.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()
+
+
+def captured_traffic(N, K, M):
+    if CAPTURED_TRAFFIC["csrc_sha256"] != csrc_digest():
+        return None
+    return CAPTURED_TRAFFIC["launches"].get(f"{N},{K},{M}")
 
 
 def dist_env():
@@ -202,6 +231,138 @@ print(json.dumps({{"flops": flops, "seconds": t_total, "rows": done_rows}}))
                        f"{d['seconds']:.1f} s, 1 thread")}
 
 
+# --------------------------------------------------------------------------- other workloads
+MX_SHAPES = ((4096, 7168), (7168, 2048))
+
+
+def mx_weight_bytes(N, K):
+    return N * K // 2 + N * K // 32
+
+
+def time_one(fn, flush, reps=5, warm=3):
+    """Median CUDA-event time (ms) of fn() after an L2 flush and a device spin."""
+    import torch
+    st = torch.cuda.current_stream()
+    ts = []
+    for i in range(warm + reps):
+        flush.zero_()
+        torch.cuda._sleep(HOLD_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        fn()
+        e1.record(st)
+        torch.cuda.synchronize()
+        if i >= warm:
+            ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def _row(N, K, M, ms, wbytes, abytes, flops, bw, tc):
+    rt = max(abytes / bw, flops / tc)
+    return {"N": N, "K": K, "M": M, "us": round(ms * 1e3, 2),
+            "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
+            "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
+            "roofline_frac": round(rt / (ms * 1e-3), 3),
+            "bound": "hbm" if abytes / bw > flops / tc else "tensor"}
+
+
+def sweep_mxfp4(device, flush, peaks, fp8):
+    """The MXFP4 dense sweep: W4A16 (BF16 X) or W4A8 (per-token FP8 X with 1% outliers),
+    N x K in {4096 x 7168, 7168 x 2048}, M = 1..8192."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import quantized_weight_gemm_gb300 as qg
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12 * (2.0 if fp8 else 1.0)   # fp8 dense = 2x bf16 nominal
+    rows = []
+    Mmax = max(M_SWEEP)
+    for (N, K) in MX_SHAPES:
+        x, w = WL.mxfp4_shape(N, K, Mmax, seed=0, outliers=fp8)
+        d = qg.WeightDesc("mxfp4", N, K, 32, "fp8" if fp8 else "bf16")
+        packed = qg.repack(d, torch.from_numpy(w.codes).to(device),
+                           torch.from_numpy(w.scales).to(device))
+        X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        Y = torch.empty(Mmax, N, dtype=torch.bfloat16, device=device)
+        ws = qg.workspace(d, Mmax, device)
+        if fp8:
+            Xq, ts = qg.quant_act_fp8(X)
+            Xq2, ts2 = torch.empty_like(Xq), torch.empty_like(ts)
+        wb = mx_weight_bytes(N, K)
+        for M in M_SWEEP:
+            if fp8:
+                ms = time_one(lambda: qg.w4a8(d, packed, Xq[:M], ts[:M], out=Y[:M], ws=ws), flush)
+                ab = wb + M * K + 4 * M + M * N * 2
+            else:
+                ms = time_one(lambda: qg.w4a16(d, packed, X[:M], out=Y[:M], ws=ws), flush)
+                ab = wb + M * K * 2 + M * N * 2
+            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc)
+            if fp8:
+                qms = time_one(lambda: qg.quant_act_fp8(X[:M], out=Xq2[:M], scale=ts2[:M]), flush)
+                r["quant_act_us"] = round(qms * 1e3, 2)
+            rows.append(r)
+        del packed, X, Y, ws
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("an MXFP4 GEMM reported a device error")
+    return rows
+
+
+def sweep_moe(device, flush, peaks):
+    """The MoE layer (E = 256 MXFP4 experts, top-8, hidden 7168, intermediate 2048):
+    gate_up [4096 x 7168] and down [7168 x 2048] grouped GEMMs over expert-sorted rows,
+    T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import quantized_weight_gemm_gb300 as qg
+    E, H, I = WL.MOE_E, WL.MOE_HIDDEN, WL.MOE_INTER
+    shapes = {"gate_up": (2 * I, H, 0), "down": (H, I, 1)}
+    descs, packs = {}, {}
+    for name, (N, K, seed) in shapes.items():
+        d = qg.WeightDesc("mxfp4", N, K, 32)
+        nb = qg.packed_bytes(d)
+        p = torch.empty(nb * E, dtype=torch.uint8, device=device)
+        for e, w in enumerate(WL.iter_moe_weights(E, N, K, seed=seed)):
+            qg.repack(d, torch.from_numpy(w.codes).to(device), torch.from_numpy(w.scales).to(device),
+                      None, out=p[e * nb:(e + 1) * nb])
+        descs[name], packs[name] = d, p
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    rows = []
+    for skewed in (False, True):
+        for T in WL.MOE_T:
+            case = WL.moe_case(T, seed=0, skewed=skewed)
+            off = torch.from_numpy(np.asarray(case.offsets, dtype=np.int32)).to(device)
+            R = len(case.valid)
+            valid = int(case.valid.sum())
+            active = int((np.asarray(case.counts) > 0).sum())
+            ins = {"gate_up": case.x_bits, "down": case.down_bits}
+            r = {"T": T, "skewed": skewed, "rows": R, "active_experts": active}
+            tot_ms, tot_flops, tot_w, tot_b = 0.0, 0.0, 0, 0
+            for name, (N, K, _) in shapes.items():
+                X = torch.from_numpy(ins[name].view(np.int16)).view(torch.bfloat16).to(device)
+                Y = torch.empty(R, N, dtype=torch.bfloat16, device=device)
+                d, p = descs[name], packs[name]
+                ms = time_one(lambda: qg.moe_grouped(d, p, E, X, off, out=Y), flush)
+                wb = active * mx_weight_bytes(N, K)
+                r[name + "_us"] = round(ms * 1e3, 2)
+                tot_ms += ms
+                tot_flops += 2.0 * valid * N * K
+                tot_w += wb
+                tot_b += wb + valid * K * 2 + valid * N * 2
+            r.update({"us": round(tot_ms * 1e3, 2),
+                      "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 2),
+                      "weight_gbs": round(tot_w / (tot_ms * 1e-3) / 1e9, 1),
+                      "roofline_frac": round(max(tot_b / bw, tot_flops / tc) / (tot_ms * 1e-3), 3)})
+            rows.append(r)
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("an MoE GEMM reported a device error")
+    return rows
+
+
 def bench_ours(args):
     import torch
     ws, rank, local = dist_env()
@@ -234,6 +395,13 @@ def bench_ours(args):
     clocks = sampler.stop()
     e2e_steps = [run_step(cases, flush, e2e=True) for _ in range(max(1, args.steps))]
     torch.cuda.synchronize()
+    extra = None
+    if not args.no_extra:
+        del cases
+        torch.cuda.empty_cache()
+        extra = {"mxfp4_a16": sweep_mxfp4(device, flush, peaks, fp8=False),
+                 "mxfp4_a8": sweep_mxfp4(device, flush, peaks, fp8=True),
+                 "moe": sweep_moe(device, flush, peaks)}
     if qg.device_status(clear=True) != 0:
         raise RuntimeError("a GEMM reported a device error")
 
@@ -265,14 +433,15 @@ def bench_ours(args):
                       "weight_gbs": round(weight_bytes(N, K) / (ms * 1e-3) / 1e9, 1),
                       "roofline_frac": round(rt / (ms * 1e-3), 3),
                       "bound": "hbm" if alg_bytes(M, N, K) / bw > 2.0 * M * N * K / tc else "tensor"})
-    big = [r for r in sweep if r["M"] >= 256]
-    big_time = sum(r["us"] for r in big) * 1e-6
-    big_flops = sum(2.0 * r["M"] * r["N"] * r["K"] for r in big)
-    achieved_tc = big_flops / big_time / 1e12
+    # dominant launch: the call with the largest share of the step's time
+    dom = max(sweep, key=lambda r: r["us"])
+    dom_flops = 2.0 * dom["M"] * dom["N"] * dom["K"]
+    achieved_tc = dom_flops / (dom["us"] * 1e-6) / 1e12
     small = [r for r in sweep if r["M"] <= 16]
     small_time = sum(r["us"] for r in small) * 1e-6
     small_bytes = sum(alg_bytes(r["M"], r["N"], r["K"]) for r in small)
     achieved_bw = small_bytes / small_time / 1e9
+    traffic = captured_traffic(dom["N"], dom["K"], dom["M"])
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(local_ms, 3),
@@ -285,11 +454,14 @@ def bench_ours(args):
                    "launch": "0.1 ms device spin before each call so host latency is not timed",
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "impl": "ours",
-        "roofline": {"bound": "tensor", "achieved": round(achieved_tc, 1),
+        "roofline": {"bound": dom["bound"], "achieved": round(achieved_tc, 1),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": round(achieved_tc / peaks["bf16_tflops"], 3), "traffic": None,
-                     "kernel": "qgemm_tc_kernel<256, bf16> (M >= 256 calls)",
-                     "peak_source": f"bf16_tflops (burst) of {peak_kind}"},
+                     "frac": round(achieved_tc / peaks["bf16_tflops"], 3), "traffic": traffic,
+                     "kernel": (f"qgemm_tc_kernel, 256-token tile, uint4+zp BF16: the "
+                                f"N={dom['N']} K={dom['K']} M={dom['M']} call, "
+                                f"{dom['us'] / sum(r['us'] for r in sweep):.0%} of the step"),
+                     "algorithmic": "2*M*N*K flops per launch",
+                     "peak_source": f"bf16_tflops (burst; each call is timed alone) of {peak_kind}"},
         "roofline_small_m": {"bound": "hbm", "achieved": round(achieved_bw, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(achieved_bw / peaks["hbm_gbs"], 3),
@@ -302,6 +474,20 @@ def bench_ours(args):
         "gpu_launches": len(SHAPES) * len(M_SWEEP) * args.steps,
         "clocks": clocks,
     }
+    if extra is not None:
+        line["other_workloads"] = {
+            "note": ("measured once after the timed region, each call alone with a cold L2 "
+                     "(median of 5); not part of value"),
+            "mxfp4_a16": {"workload": "dense W4A16 MXFP4, N x K in {4096 x 7168, 7168 x 2048}",
+                          "sweep": extra["mxfp4_a16"]},
+            "mxfp4_a8": {"workload": ("dense W4A8 MXFP4 x per-token FP8 e4m3 (1% outliers x20), "
+                                      "same shapes; quant_act_us = the separate quantization call; "
+                                      "roofline tensor peak = 2 x measured bf16"),
+                         "sweep": extra["mxfp4_a8"]},
+            "moe": {"workload": ("MoE grouped W4A16 MXFP4, E=256 top-8, gate_up 4096 x 7168 + "
+                                 "down 7168 x 2048, expert-sorted rows padded to 8; flops and "
+                                 "bytes on routed (unpadded) rows and active experts"),
+                    "sweep": extra["moe"]}}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_sample()
     if rank == 0:
@@ -392,6 +578,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the MXFP4, W4A8 and MoE sweeps reported beside the main line")
     ap.add_argument("--case", default=None, help="N,K,M[,wfmt[,afmt]]: time one GEMM shape")
     args = ap.parse_args()
     if args.case:

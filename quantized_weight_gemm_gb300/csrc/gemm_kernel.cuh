@@ -1,34 +1,40 @@
 // The tcgen05 quantized-weight GEMM kernel (dense and MoE grouped), sm_103a.
 //
-// One persistent CTA per SM, warp-specialised (16 warps).  A "stage" is 128 K-elements of
-// one work unit (a 128-row weight tile x a token tile, over a range of K); the 256-token
-// BF16 variant uses half stages (64 K) so that its 32 KB activation tiles fit.
+// One persistent CTA per SM, warp-specialised.  A "stage" is 128 K-elements of one work
+// unit (a 128-row weight tile x a token tile, over a range of K); the 256-token BF16 variant
+// uses half stages (64 K) so that its 32 KB activation tiles fit.  Warp roles, in order:
 //
-//   warps 0, 16 record producers (one thread each, alternate stages): one bulk copy per
-//               stage of the packed weight record (codes, scales and zero points of 128
-//               weight rows x 128 K, see qgemm_internal.h) into the record ring, which is
-//               deep (up to 16 slots) so that many weight bytes are in flight: small batches
-//               are bound by HBM.  Every copy costs its issuing thread a few hundred cycles
-//               whatever its size, so two threads share the stream.
-//   warp 15     activation producer (one thread): TMA tiles of X (token_tile rows x 128
-//               bytes per 64-K slab, 128-byte swizzle) into the X ring; for narrow token
-//               tiles one 3-D load brings several stages at once, for the same reason.
-//   warps 2-5,  dequant, two warpgroups taking alternate stages: thread r owns weight row r
-//   warps 6-9   (= tensor-memory lane r), decodes its row's codes from the record ring in
-//               registers (dequant.cuh), releases the record slot, and writes the weights
-//               with tcgen05.st into the stage's A-operand columns of tensor memory.  The
-//               dequantized weights never touch shared memory.
-//   warps 1, 14 MMA issuers (one thread each): tcgen05.mma with A = weights in tensor
-//               memory (M = 128 weight rows) and B = the X tile (N = token_tile rows of X),
-//               FP32 accumulators in tensor memory.  The weights fill the 128-row side
-//               ("swap AB"), so small batches still run full-height MMAs.  A thread issues
-//               an MMA only every few dozen cycles whatever its size, so narrow token tiles
-//               use both issuers on alternate stages, each into its own partial
-//               accumulator.  BF16 activations use kind::f16; FP8 activations use
-//               block-scaled kind::mxf8f6f4 with the E8M0 weight scales as scale factors.
-//   warps 10-13 epilogue: tcgen05.ld of the accumulator(s), fused per-channel / per-token
+//   dequant     W warpgroups (4 for 16-token tiles, else 2) taking the CTA's stages
+//               round-robin: thread r owns weight row r (= tensor-memory lane r), decodes
+//               its row's codes from the record ring in registers (dequant.cuh), releases
+//               the record slot, and writes the weights with tcgen05.st into the stage's
+//               A-operand columns of tensor memory.  The weights never touch shared memory.
+//   epilogue    4 warps: tcgen05.ld of the accumulator(s), fused per-channel / per-token
 //               scaling, BF16 store of Y; or, under split-K, an FP32 reduction through the
 //               workspace whose last contributor converts the tile and re-zeroes it.
+//   MMA issuers I warps (4 for token tiles up to 64, else 1), each a converged warp whose
+//               elected lane issues tcgen05.mma with A = weights in tensor memory (M = 128
+//               weight rows) and B = the X tile (N = token_tile rows of X), FP32
+//               accumulators in tensor memory.  The weights fill the 128-row side ("swap
+//               AB"), so small batches still run full-height MMAs.  A warp needs a few dozen
+//               cycles per MMA whatever its size, so narrow token tiles spread the stages
+//               over I issuers, each with its own partial accumulator.  BF16 activations use
+//               kind::f16; FP8 activations use block-scaled kind::mxf8f6f4 with the E8M0
+//               weight scales as scale factors.
+//   activation  1 warp (one thread): TMA tiles of X (token_tile rows x 128 bytes per 64-K
+//   producer    slab, 128-byte swizzle) into the X ring; for narrow token tiles one 3-D load
+//               brings several stages at once.
+//   record      2 warps (one thread each, alternate stages): one bulk copy per stage of the
+//   producers   packed weight record (codes, scales and zero points of 128 weight rows x
+//               128 K, see qgemm_internal.h) into the record ring, which is deep (up to 16
+//               slots) so that many weight bytes are in flight: small batches are bound by
+//               HBM.
+//
+// Stage g of a CTA (counted over all its units) belongs to dequant warpgroup g % W and to
+// issuer g % I, and every ring's depth is a multiple of the number of its owners, so each
+// slot is always written and read by the same warps.  A waiter that shared a slot with
+// another could run two uses ahead, and a one-bit mbarrier parity cannot tell the phase it
+// needs from the one before it.
 // This follows "Humming wird angekündigt" (vLLM blog, German edition), section "Gemeinsam
 // genutzte CUDA-Komponenten" (task scheduling, TMA data movement, dequantization and
 // scaling fused into the kernel, tensor-core compute, output stage with fused scaling,
@@ -48,16 +54,38 @@
 
 namespace qgemm {
 
-constexpr int kWarps = 17;
-constexpr int kThreads = kWarps * 32;
-constexpr int kIssuerWarp1 = 14;     // second MMA issuer (narrow token tiles)
-constexpr int kXProducerWarp = 15;
-constexpr int kRecProducerWarp1 = 16;  // second record producer
+#ifndef QGEMM_DEQ_WGS_NARROW
+#define QGEMM_DEQ_WGS_NARROW 4
+#endif
+#ifndef QGEMM_ISSUERS_NARROW
+#define QGEMM_ISSUERS_NARROW 4
+#endif
+// Warp roles, in this order: the dequant warpgroups, the four epilogue warps, the MMA
+// issuers, the activation producer and the two record producers.  Groups of four start at a
+// multiple of 4, so `warp & 3` is the tensor-memory lane quarter a warp may access.  Every
+// SM sub-partition holds a quarter of the warps and of the 64 K registers, so more warps
+// leave fewer registers per thread.
+template <int BNT>
+struct Roles {
+  static constexpr int kDeqWGs = BNT <= 16 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
+  // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
+  // tiles spread the stages over several issuing warps, each with a partial accumulator.
+  static constexpr int kIssuers = BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
+  static constexpr int kEpiWarp0 = 4 * kDeqWGs;
+  static constexpr int kIssuerWarp0 = kEpiWarp0 + 4;
+  static constexpr int kXProducerWarp = kIssuerWarp0 + kIssuers;
+  static constexpr int kRecProducerWarp0 = kXProducerWarp + 1;
+  static constexpr int kWarps = kRecProducerWarp0 + 2;
+  static constexpr int kThreads = kWarps * 32;
+};
 constexpr int kMaxExperts = 1024;
 // Sleep between polls of a barrier, per role (ns): roles on the critical path poll often,
 // the others sleep longer so the dequant warps keep the issue slots.
 constexpr uint32_t kSleepDequant = 32, kSleepMma = 32, kSleepProducer = 128, kSleepEpilogue = 256;
 constexpr int kRecTail = kTileN * 4 * 2 + kTileN * 4 / 2;           // largest scales + zeros
+
+constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
+constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
 
 template <int BNT, bool A8>
 struct GemmCfg {
@@ -70,7 +98,7 @@ struct GemmCfg {
   static constexpr int kXBytes = kSlabs * kSlabBytes;
   static constexpr int kACols = A8 ? 32 : kChunks * 16;          // A-operand columns / stage
   static constexpr int kMmaPerStage = A8 ? kChunks : 2 * kChunks;
-  static constexpr int kIssuers = BNT <= 64 ? 2 : 1;
+  static constexpr int kIssuers = Roles<BNT>::kIssuers;
   static constexpr int kNumSub = kIssuers;                       // partial accumulators
   static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
   static constexpr int kAccCols = kNumAcc * kNumSub * BNT;
@@ -78,9 +106,16 @@ struct GemmCfg {
   // 4 scale-factor columns per stage and 8 constant ones), capped by shared memory.
   static constexpr int kSfCols = A8 ? 4 : 0;
   static constexpr int kATmemMax = (512 - kAccCols - (A8 ? 8 : 0)) / (kACols + kSfCols);
-  static constexpr int kAStages =
+  static constexpr int kAStagesMax =
       A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
          : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
+  // Stage g of the CTA goes to dequant warpgroup g % kDeqWGs and to issuer g % kIssuers.
+  // A ring slot must always have the same two owners: a waiter that is not the slot's only
+  // consumer could run two uses ahead, where a one-bit mbarrier phase parity cannot tell
+  // the phase it needs from the one before.  So the depth is a multiple of both counts.
+  static constexpr int kDeqWGs = Roles<BNT>::kDeqWGs;
+  static constexpr int kALcm = lcm_int(kDeqWGs, kIssuers);
+  static constexpr int kAStages = kAStagesMax / kALcm * kALcm;
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
   static constexpr int kXChunk = BNT <= 32 ? 4 : BNT == 64 ? 2 : 1;
   static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
@@ -90,8 +125,11 @@ struct GemmCfg {
   static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
   static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
                                 kAStages * kBarBytesPerA + kMiscBytes + 64;
-  static constexpr int kRMax = (227 * 1024 - kFixed) / (kRecSlot + kBarBytesPerR);
-  static constexpr int kRStages = kRMax < 16 ? kRMax : 16;
+  static constexpr int kRMax0 = (227 * 1024 - kFixed) / (kRecSlot + kBarBytesPerR);
+  // record ring: producer g % 2, dequant warpgroup g % kDeqWGs (same rule as above)
+  static constexpr int kRLcm = lcm_int(2, kDeqWGs);
+  static constexpr int kRMax = kRMax0 / kRLcm * kRLcm;
+  static constexpr int kRStages = kRMax < 16 / kRLcm * kRLcm ? kRMax : 16 / kRLcm * kRLcm;
   static constexpr int kACol0 = (kAccCols + 31) / 32 * 32;
   // Block-scale factors (FP8 activations only): per A stage one 4-column slot for the
   // weight-side factors (a row's four E8M0 bytes, one per 32 K, replicated over the four
@@ -103,6 +141,7 @@ struct GemmCfg {
                                    kUsedCols <= 128 ? 128 : kUsedCols <= 256 ? 256 : 512;
   static_assert(kUsedCols <= 512, "tensor memory budget");
   static_assert(kAStages >= 3 && kRStages >= 4, "pipeline depth");
+  static_assert(kAStages % kALcm == 0 && kRStages % kRLcm == 0, "ring slots need fixed owners");
   static constexpr int kBarBytes = kRStages * kBarBytesPerR + kAStages * kBarBytesPerA +
                                    kXSlots * kBarBytesPerX + (2 * kNumAcc + 2) * 8;
   static constexpr int kSmemBytes =
@@ -221,9 +260,13 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
 }
 
 template <int BNT, bool A8, int DM>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Roles<BNT>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   using C = GemmCfg<BNT, A8>;
+  using RO = Roles<BNT>;
+  constexpr int kEpiWarp0 = RO::kEpiWarp0;
+  constexpr int kDeqWGs = RO::kDeqWGs;
+  constexpr int kXProducerWarp = RO::kXProducerWarp;
   constexpr int SA = C::kAStages;
   constexpr int SR = C::kRStages;
   constexpr int SX = C::kXSlots;
@@ -291,7 +334,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   }
   if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
   int num_units = a.num_units;
-  if (a.offsets != nullptr && warp == 2) {
+  if (a.offsets != nullptr && warp == 0) {
     // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).
     int carry = 0;
     bool bad = false;
@@ -326,7 +369,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   if (a.offsets != nullptr) num_units = misc[3] * int(L.n_tiles);
   if (!misc[2] || int(blockIdx.x) >= num_units) return;     // nothing allocated yet
 
-  if (warp == 1) {
+  if (warp == kEpiWarp0) {
     ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&misc[0]), C::kTmemCols);
     ptx::tmem_relinquish();
   }
@@ -337,7 +380,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   volatile int* abort_flag = &misc[1];
   const uint64_t T = a.timeout_ns;
 
-  if (A8 && warp >= 10 && warp < 14) {
+  if (A8 && warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
     // Activation-side block scale: a constant 2^6 (E8M0 133) that returns the factor 2^-6
     // of the e2m1 -> e4m3 byte shuffle.  Filled over every lane of its columns.
     const uint32_t tl = tbase + (uint32_t((warp & 3) * 32) << 16);
@@ -349,9 +392,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   __syncthreads();
   ptx::tc_fence_after();
 
-  if (warp == 0 || warp == kRecProducerWarp1) {
+  if (warp >= RO::kRecProducerWarp0) {
     // ---------------------------------------------------------------- record producers
-    const int rp = (warp == 0) ? 0 : 1;     // takes the stages g with g % 2 == rp
+    const int rp = warp - RO::kRecProducerWarp0;   // takes the stages g with g % 2 == rp
     if (lane == 0) {
       const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
       const uint32_t rec_bytes = uint32_t(L.record_bytes);
@@ -429,91 +472,87 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             ptx::mbar_wait(&xfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
       }
     }
-  } else if (warp == 1 || warp == kIssuerWarp1) {
-    // ---------------------------------------------------------------- MMA issuer(s)
-    // Issuer j takes the stages i of each unit with i % kIssuers == j (the stages of
-    // dequant warpgroup j when there are two) and accumulates into partial accumulator j.
-    const int issuer = (warp == 1) ? 0 : 1;
-    if (lane == 0 && issuer < C::kIssuers) {
-      Ring ra, rx;
-      int ui = 0;
-      bool alive = true;
-      const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
-      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x, ++ui) {
-        const Unit w = decode_unit(u, a, BNT, prefix, offs);
-        const int acc = ui % C::kNumAcc;
-        const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
-        if (!ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma)) break;
-        ptx::tc_fence_after();
-        const uint32_t d_tmem = tbase + uint32_t((acc * C::kNumSub + issuer) * BNT);
-        const int nst = (w.kb1 - w.kb0) * kSub;
-        bool first = true;                  // this issuer's first MMA of the unit overwrites
-        bool x_ready = false;               // waited for the current X slot
-        for (int i = 0; i < nst; ++i) {
-          const Ring cur = ra;
-          ra.next(SA);
-          const int xj = i % XQ;            // stage inside the X slot
-          if (xj == 0) x_ready = false;
-          const bool mine = (i % C::kIssuers) == issuer;
-          if (mine) {
-            if (!x_ready) {
-              if (!ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma)) { alive = false; break; }
-              x_ready = true;
-            }
-            if (!ptx::mbar_wait(&afull[cur.slot], cur.phase, abort_flag, T, kSleepMma)) { alive = false; break; }
-            ptx::tc_fence_after();
-            const uint64_t bdesc =
-                desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
+  } else if (warp >= RO::kIssuerWarp0 && warp < kXProducerWarp) {
+    // ---------------------------------------------------------------- MMA issuers
+    // Issuer j takes the stages g of this CTA with g % kIssuers == j and accumulates into
+    // partial accumulator j.  The whole warp runs the loop and one elected lane issues: a
+    // converged warp issues tcgen05 instructions faster than a lone diverged lane.
+    const int issuer = warp - RO::kIssuerWarp0;
+    Ring ra, rx;
+    int ui = 0;
+    uint32_t g = 0;                       // stage counter of this CTA
+    bool alive = true;
+    const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
+    for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x, ++ui) {
+      const Unit w = decode_unit(u, a, BNT, prefix, offs);
+      const int acc = ui % C::kNumAcc;
+      const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
+      if (!warp_all(ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma))) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tbase + uint32_t((acc * C::kNumSub + issuer) * BNT);
+      const int nst = (w.kb1 - w.kb0) * kSub;
+      uint32_t first = 1;                 // this issuer's first MMA of the unit overwrites
+      for (int i = 0; i < nst; ++i, ++g) {
+        const Ring cur = ra;
+        ra.next(SA);
+        const int xj = i % XQ;            // stage inside the X slot
+        // Every issuer waits for every X slot, even one without a stage of its own: its
+        // release of the slot below must count towards this fill of the slot, not the next.
+        if (xj == 0 && !warp_all(ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
+        if (int(g % C::kIssuers) == issuer) {
+          if (!warp_all(ptx::mbar_wait(&afull[cur.slot], cur.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
+          ptx::tc_fence_after();
+          const uint64_t bdesc = desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
           const uint32_t a_tmem = tbase + uint32_t(C::kACol0 + cur.slot * C::kACols);
 #pragma unroll
           for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
-            const uint32_t accum = (!first || kk > 0) ? 1u : 0u;
+            const uint32_t accum = kk > 0 ? 1u : (first ^ 1u);
             if constexpr (A8) {
-              ptx::mma_mxf8f6f4_ts(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2),
-                                   ptx::idesc_mxf8_e4m3(128, BNT, kk, 0),
-                                   tbase + uint32_t(C::kSfaCol0 + 4 * cur.slot),
-                                   tbase + uint32_t(C::kSfbCol0), accum);
+              ptx::mma_mxf8f6f4_ts_elect(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2),
+                                         ptx::idesc_mxf8_e4m3(128, BNT, kk, 0),
+                                         tbase + uint32_t(C::kSfaCol0 + 4 * cur.slot),
+                                         tbase + uint32_t(C::kSfbCol0), accum);
             } else {
               // slab kk / 4, 32-byte K step kk % 4 inside the 128-byte swizzled row
-              ptx::mma_f16_ts(d_tmem, a_tmem + kk * 8,
-                              bdesc + uint64_t(((kk >> 2) * C::kSlabBytes) >> 4) +
-                                  uint64_t((kk & 3) * 2),
-                              ptx::idesc_bf16(128, BNT), accum);
+              ptx::mma_f16_ts_elect(d_tmem, a_tmem + kk * 8,
+                                    bdesc + uint64_t(((kk >> 2) * C::kSlabBytes) >> 4) +
+                                        uint64_t((kk & 3) * 2),
+                                    ptx::idesc_bf16(128, BNT), accum);
             }
           }
-            first = false;
-            ptx::mma_commit(&aempty[cur.slot]);   // frees the stage's A columns
-          }
-          if (xj == XQ - 1 || i == nst - 1) {
-            ptx::mma_commit(&xempty[rx.slot]);    // every issuer releases every X slot
-            rx.next(SX);
-          }
+          first = 0;
+          ptx::mma_commit_elect(&aempty[cur.slot]);   // frees the stage's A columns
         }
-        if (!alive) break;
-        ptx::mma_commit(&accfull[acc]);      // every issuer arrives once per unit
+        if (xj == XQ - 1 || i == nst - 1) {
+          ptx::mma_commit_elect(&xempty[rx.slot]);    // every issuer releases every X slot
+          rx.next(SX);
+        }
       }
-      // Every MMA issued above has completed once `drain` flips.
-      ptx::mma_commit(drain);
-      volatile int no_abort = 0;
-      ptx::mbar_wait(drain, 0, &no_abort, 200000000ull);
+      if (!alive) break;
+      ptx::mma_commit_elect(&accfull[acc]);      // every issuer arrives once per unit
     }
-  } else if (warp < 10) {
+    // Every MMA issued above has completed once `drain` flips.
+    ptx::mma_commit_elect(drain);
+    volatile int no_abort = 0;
+    warp_all(ptx::mbar_wait(drain, 0, &no_abort, 200000000ull));
+  } else if (warp < kEpiWarp0) {
     // ---------------------------------------------------------------- dequant (2 WGs)
-    const int wg = (warp - 2) >> 2;                        // takes stages with i % 2 == wg
+    const int wg = warp >> 2;                              // takes the stages g % kDeqWGs == wg
     const int r = (warp & 3) * 32 + lane;                  // weight row = TMEM lane
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
     const int G = L.groups_per_record;
     const int zoff = L.off_zeros - L.off_scales;
     Ring rr, ra;
+    uint32_t g = 0;                                        // stage counter of this CTA
     bool alive = true;
     for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
       const Unit w = decode_unit(u, a, BNT, prefix, offs);
       const int nst = (w.kb1 - w.kb0) * kSub;
-      for (int i = 0; i < nst; ++i) {
+      for (int i = 0; i < nst; ++i, ++g) {
         const Ring cr = rr, ca = ra;
         rr.next(SR);
         ra.next(SA);
-        if ((i & 1) != wg) continue;
+        if (int(g % kDeqWGs) != wg) continue;
         if (!warp_all(ptx::mbar_wait(&rfull[cr.slot], cr.phase, abort_flag, T, kSleepDequant))) { alive = false; break; }
         const uint8_t* rec = s_rec + cr.slot * C::kRecSlot;
         const uint32_t a_col = t_lane + uint32_t(C::kACol0 + ca.slot * C::kACols);
@@ -553,7 +592,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         warp_arrive(&afull[ca.slot], lane);
       }
     }
-  } else if (warp < 14) {
+  } else if (warp < kEpiWarp0 + 4) {
     // ---------------------------------------------------------------- epilogue
     const int r = (warp & 3) * 32 + lane;
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
@@ -566,10 +605,14 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       return warp_all(ok);
     };
     int ui = 0;
+    uint32_t g = 0;                       // stage counter of this CTA at the unit's start
     for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++ui) {
       const Unit w = decode_unit(u, a, BNT, prefix, offs);
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
+      const int nst = (w.kb1 - w.kb0) * kSub;
+      const uint32_t g0 = g;
+      g += uint32_t(nst);
       if (!warp_all(ptx::mbar_wait(&accfull[acc], acc_par, abort_flag, T, kSleepEpilogue))) break;
       ptx::tc_fence_after();
       const int64_t n = int64_t(w.nt) * kTileN + r;
@@ -577,24 +620,27 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const bool split = a.splits > 1;
       const float cs = (n_ok && a.chan_scale != nullptr && !split) ? a.chan_scale[n] : 1.0f;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
-      // partial accumulators of the issuers that had a stage in this unit
-      const int active = min(C::kNumSub, (w.kb1 - w.kb0) * kSub);
+      // Partial accumulators of the issuers that had a stage in this unit: the unit's
+      // stages g0, g0 + 1, ... went to issuers (g0 + d) % kIssuers.
+      const int active = min(C::kNumSub, nst);
+      const int sub0 = int(g0 % uint32_t(C::kNumSub));
       constexpr int kChunk = BNT < 32 ? BNT : 32;
 #pragma unroll 1
       for (int c = 0; c < BNT / kChunk; ++c) {
         uint32_t v[32];
         const uint32_t col = t_lane + uint32_t(acc * C::kNumSub * BNT + c * kChunk);
         if constexpr (kChunk == 32) {
-          ptx::tmem_ld32(col, v);
+          ptx::tmem_ld32(col + uint32_t(sub0 * BNT), v);
         } else {
           uint32_t v16[16];
-          ptx::tmem_ld16(col, v16);
+          ptx::tmem_ld16(col + uint32_t(sub0 * BNT), v16);
 #pragma unroll
           for (int j = 0; j < 16; ++j) v[j] = v16[j];
         }
 #pragma unroll
-        for (int sub = 1; sub < C::kNumSub; ++sub) {
-          if (sub >= active) break;
+        for (int d = 1; d < C::kNumSub; ++d) {
+          if (d >= active) break;
+          const int sub = (sub0 + d) % C::kNumSub;
           uint32_t p[32];
           if constexpr (kChunk == 32) {
             ptx::tmem_ld32(col + uint32_t(sub * BNT), p);
@@ -676,7 +722,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 1) ptx::tmem_dealloc(tbase, C::kTmemCols);
+  if (warp == kEpiWarp0) ptx::tmem_dealloc(tbase, C::kTmemCols);
 }
 
 template <int BNT, bool A8, int DM>
@@ -693,7 +739,7 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  qgemm_tc_kernel<BNT, A8, DM><<<plan.grid, kThreads, kSmem, st>>>(tmap, args);
+  qgemm_tc_kernel<BNT, A8, DM><<<plan.grid, Roles<BNT>::kThreads, kSmem, st>>>(tmap, args);
   return cudaGetLastError();
 }
 

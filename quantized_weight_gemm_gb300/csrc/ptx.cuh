@@ -182,6 +182,35 @@ __device__ __forceinline__ void mma_mxf8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem
          "r"(accumulate) : "memory");
 }
 
+// The same two MMAs and the commit below, executed by a whole converged warp: one lane
+// (elect.sync) issues, the others only take part in the election.
+__device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P, E;\n setp.ne.b32 P, %4, 0;\n elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, P;\n}\n"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_mxf8f6f4_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
+                                                      uint64_t b_desc, uint32_t idesc,
+                                                      uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P, E;\n setp.ne.b32 P, %6, 0;\n elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+      " [%0], [%1], %2, %3, [%4], [%5], P;\n}\n"
+      :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate) : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
+  asm volatile(
+      "{\n .reg .pred E;\n elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n"
+      :: "r"(smem_u32(bar)) : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile(

@@ -150,6 +150,25 @@ def test_every_dispatch_entry(tile, splits):
 
 # ------------------------------------------------------------------------------- W4A8
 
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_many_units_with_odd_stage_counts(splits):
+    """Many units per CTA whose stage counts are odd or differ between units: the stage
+    to warp assignment runs on across unit boundaries and must keep every ring slot with
+    fixed owners (a slot shared by two waiters lets one of them pass a wait a phase early)."""
+    qg = _qg()
+    r = WL.rng(30)
+    M, N, K = 16, 28672, 1152                         # 224 weight tiles x 9 K-blocks
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    qg.force_config(16, splits)
+    try:
+        y = _run_a16(x, w)
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A16)
+
+
 def test_quant_act_fp8_bitexact():
     from tests import gpu_util as G
     qg = _qg()

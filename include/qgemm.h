@@ -113,8 +113,9 @@ qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const v
 
 /*
  * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max (split-K partial
- * sums and tile counters).  The workspace must be 256-byte aligned and zero-filled
- * before its first use; every successful call leaves it zero-filled again, so one
+ * sums, one FP32 slice per split, and tile arrival counters).  The workspace must be
+ * 256-byte aligned and zero-filled before its first use; every successful call leaves the
+ * counters zero again (the partial sums are overwritten by every call), so one
  * zero-filled buffer can be reused by consecutive calls on one stream.
  */
 size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);

@@ -64,37 +64,72 @@ bool layout_of(const qgemm_wdesc* d, Layout* L) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// ---------------------------------------------------------------- dispatch heuristic
-// Token tile from M; split-K when the (m, n) tiles cannot fill every SM.
+// ---------------------------------------------------------------- dispatch
+// Token tile and split-K factor from a cost model of one call on a persistent grid:
+//   time ~ T0 + ceil(units / SMs) * (ceil(k_blocks / splits) * stage(tile) + unit(tile)
+//                                   + [splits > 1] splits * tile * reduce)
+// where units = m_tiles * n_tiles * splits; the last term is the last-arriving split's
+// sum over the splits' partial tiles.  The constants were fitted (least squares on log
+// time) to event-timed calls of every tile and split count on one GB300, over the INT4 and
+// MXFP4 shapes N x K = 28672 x 8192, 8192 x 28672, 4096 x 7168, 7168 x 2048 and
+// M = 1 ... 2048; the model's choice was within 0.5% of the fastest measured one on
+// average (13% in the worst case).
+namespace {
+constexpr int kTiles[5] = {16, 32, 64, 128, 256};
+constexpr double kStageUs[5] = {0.326, 0.330, 0.353, 0.401, 0.657};  // per 128-K block
+constexpr double kUnitUs[5] = {3.08, 6.11, 7.88, 10.05, 17.59};      // per unit
+constexpr double kReduceUsPerSplitRow = 0.0716;
+constexpr double kCallUs = 6.44;
+}  // namespace
+
+double plan_cost_us(const Layout& L, int64_t M, int ti, int splits, int sms) {
+  const int64_t tt = kTiles[ti];
+  const int64_t m_tiles = (M + tt - 1) / tt;
+  const int64_t units = m_tiles * L.n_tiles * splits;
+  const int64_t per_cta = (units + sms - 1) / sms;
+  const int64_t kpu = (L.k_blocks + splits - 1) / splits;
+  double unit = double(kpu) * kStageUs[ti] + kUnitUs[ti];
+  if (splits > 1) unit += double(splits) * double(tt) * kReduceUsPerSplitRow;
+  return kCallUs + double(per_cta) * unit;
+}
+
 GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
   GemmPlan p;
-  int tt = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
-  if (g_force_tile) tt = g_force_tile;
-  p.token_tile = tt;
-  const int64_t m_tiles = (M + tt - 1) / tt;
-  const int64_t base = m_tiles * L.n_tiles;
-  int splits = 1;
-  if (g_force_splits) {
-    splits = int(std::min<int64_t>(g_force_splits, L.k_blocks));
-  } else if (M <= kSplitMaxM) {
-    double best = double(base) / (double((base + sms - 1) / sms) * sms);
-    for (int s = 2; s <= 32 && best < 0.9 && L.k_blocks / s >= 2; ++s) {
-      const int64_t units = base * s;
-      const double eff = double(units) / (double((units + sms - 1) / sms) * sms);
-      if (eff > best + 0.02) { best = eff; splits = s; }
-      if (best >= 0.95) break;
+  p.token_tile = 16;
+  p.splits = 1;
+  double best = 1e300;
+  for (int ti = 0; ti < 5; ++ti) {
+    const int tt = kTiles[ti];
+    if (g_force_tile ? tt != g_force_tile : (tt > 16 && tt > 2 * M)) continue;
+    for (int s : {1, 2, 3, 4, 6, 8}) {
+      if (g_force_splits) {
+        if (s != 1) break;
+        s = int(std::min<int64_t>(g_force_splits, L.k_blocks));
+      } else if (s > 1 && (M > kSplitMaxM || L.k_blocks / s < 2)) {
+        break;
+      }
+      const double c = plan_cost_us(L, M, ti, s, sms);
+      if (c < best) { best = c; p.token_tile = tt; p.splits = s; }
+      if (g_force_splits) break;
     }
   }
-  p.splits = splits;
-  const int64_t units = base * splits;
+  if (g_force_tile) p.token_tile = g_force_tile;
+  const int64_t units = (M + p.token_tile - 1) / p.token_tile * L.n_tiles * p.splits;
   p.grid = int(std::min<int64_t>(units, sms));
   return p;
+}
+
+// Split-K workspace: one FP32 partial-sum slice per split (plain stores, no atomics), then
+// one arrival counter per output tile.
+int64_t split_slice_floats(const Layout& L, int64_t M, const GemmPlan& p) {
+  const int64_t m_tiles = (M + p.token_tile - 1) / p.token_tile;
+  return round_up(m_tiles * p.token_tile * L.N_pad, 64);
 }
 
 int64_t split_ws_bytes(const Layout& L, int64_t M, const GemmPlan& p) {
   if (p.splits <= 1) return 0;
   const int64_t m_tiles = (M + p.token_tile - 1) / p.token_tile;
-  const int64_t partial = round_up(m_tiles * p.token_tile * L.N_pad * 4, 256);
+  const int64_t partial = int64_t(p.splits) * split_slice_floats(L, M, p) * 4;
   return partial + round_up(m_tiles * L.n_tiles * 4, 256);
 }
 
@@ -203,8 +238,9 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   if (need > 0) {
     a.ws = static_cast<float*>(ws);
     a.ws_ld = L.N_pad;
+    a.ws_slice = split_slice_floats(L, M, plan);
     a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
-                                            round_up(int64_t(a.m_tiles) * plan.token_tile * L.N_pad * 4, 256));
+                                            int64_t(plan.splits) * a.ws_slice * 4);
   }
   a.status = dev->status;
   a.timeout_ns = kTimeoutNs;

@@ -10,8 +10,9 @@
 //               the record slot, and writes the weights with tcgen05.st into the stage's
 //               A-operand columns of tensor memory.  The weights never touch shared memory.
 //   epilogue    4 warps: tcgen05.ld of the accumulator(s), fused per-channel / per-token
-//               scaling, BF16 store of Y; or, under split-K, an FP32 reduction through the
-//               workspace whose last contributor converts the tile and re-zeroes it.
+//               scaling, BF16 store of Y; or, under split-K, a store of the FP32 partial
+//               tile into the split's slice of the workspace, after which the last of the
+//               tile's splits to arrive sums the slices in split order and converts.
 //   MMA issuers I warps (4 for token tiles up to 64, else 1), each a converged warp whose
 //               elected lane issues tcgen05.mma with A = weights in tensor memory (M = 128
 //               weight rows) and B = the X tile (N = token_tile rows of X), FP32
@@ -667,7 +668,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             if (m < w.row_end) {
               float y = __uint_as_float(v[j]);
               if (split) {
-                ptx::red_add_f32(a.ws + m * a.ws_ld + n, y);
+                __stcg(a.ws + int64_t(w.split) * a.ws_slice + m * a.ws_ld + n, y);
               } else {
                 y *= cs;
                 if (A8) y *= a.tok_scale[m];
@@ -689,6 +690,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         }
         if (!epi_sync()) break;
         if (misc[4]) {
+          // Sum the slices in split order (a fixed order: the result does not depend on
+          // which split arrived last), scale, convert.
           __threadfence();
           if (n_ok) {
             const float cs2 = a.chan_scale != nullptr ? a.chan_scale[n] : 1.0f;
@@ -697,8 +700,13 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             for (int64_t m0 = w.row0; m0 < m_end; m0 += 8) {
               float v[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                v[j] = (m0 + j < m_end) ? __ldcg(a.ws + (m0 + j) * a.ws_ld + n) : 0.0f;
+              for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+              for (int sl = 0; sl < a.splits; ++sl) {
+                const float* src = a.ws + int64_t(sl) * a.ws_slice + n;
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (m0 + j < m_end) v[j] += __ldcg(src + (m0 + j) * a.ws_ld);
+              }
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 const int64_t m = m0 + j;
@@ -706,7 +714,6 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
                   float y = v[j] * cs2;
                   if (A8) y *= a.tok_scale[m];
                   Y[m * a.ldy + n] = __float2bfloat16_rn(y);
-                  __stcg(a.ws + m * a.ws_ld + n, 0.0f);
                 }
               }
             }

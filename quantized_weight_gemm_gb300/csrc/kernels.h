@@ -30,9 +30,10 @@ struct GemmArgs {
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
-  float* ws;                   // split-K partial sums [m_tiles * tile_m, ws_ld]
+  float* ws;                   // split-K partial sums [splits][m_tiles * tile_m][ws_ld]
   int32_t* counters;           // split-K arrival counters [m_tiles * n_tiles]
   int64_t ws_ld;
+  int64_t ws_slice;            // floats per split slice of ws
   int* status;
   uint64_t timeout_ns;
   int32_t x_3d;                // X map is 3-D (a box covers several stages); else 2-D

@@ -54,7 +54,8 @@ extern "C" qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void*
   void* scratch = nullptr;
   const qgemm_status s = scratch_address(&scratch);
   if (s != QGEMM_OK) return s;
-  // The array keeps whatever the previous call left; the split-K path needs zeros.
+  // The array keeps whatever the previous call left; the split-K tile counters must
+  // start at zero.
   if (need > 0 && cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return QGEMM_ERR_CUDA;
   return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, Y, ldy, scratch,

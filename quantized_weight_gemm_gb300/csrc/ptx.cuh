@@ -327,9 +327,5 @@ __device__ __forceinline__ uint16_t cvt_e4m3x2_f32(float lo, float hi) {
   return d;
 }
 
-__device__ __forceinline__ void red_add_f32(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" :: "l"(p), "f"(v) : "memory");
-}
-
 }  // namespace ptx
 }  // namespace qgemm

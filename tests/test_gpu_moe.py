@@ -138,10 +138,10 @@ def test_moe_single_expert_equals_dense():
     M, N, K = 77, 384, 512
     x = WL.gen_x(r, M, K)
     w = WL.gen_weights(r, "uint4_zp", N, K)
-    y_moe = _run_moe([w], x, [0, M])
     d, packed = G.pack(w)
-    qg.force_config(0, 1)
+    qg.force_config(128, 1)                 # the same token tile and no split in both calls
     try:
+        y_moe = _run_moe([w], x, [0, M])
         y_dense = G.to_f64(qg.w4a16(d, packed, G.bf16_tensor(x)))
     finally:
         qg.force_config(0, 0)

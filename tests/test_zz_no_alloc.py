@@ -39,7 +39,7 @@ def qg():
     q.force_config(0, 0)
 
 
-@pytest.mark.parametrize("wfmt,M,N,K", [("uint4_zp", 16, 4096, 4096), ("mxfp4", 1, 28672, 2048),
+@pytest.mark.parametrize("wfmt,M,N,K", [("uint4_zp", 16, 4096, 4096), ("mxfp4", 1, 4096, 7168),
                                         ("int4_sym", 64, 1024, 2048)])
 def test_noalloc_matches_workspace_entry_point(qg, wfmt, M, N, K):
     from tests import gpu_util as G

@@ -536,8 +536,9 @@ def bench_case(args):
         torch.cuda.synchronize()
         if i >= args.warmup:
             times.append(e0.elapsed_time(e1))
-    if qg.device_status(clear=True) != 0:
-        raise RuntimeError("device error")
+    st = qg.device_status(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
     ms = statistics.median(times)
     wb = qg.packed_bytes(d)
     print(json.dumps({"case": args.case, "us": round(ms * 1e3, 2),

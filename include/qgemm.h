@@ -49,7 +49,8 @@ typedef enum {
   QGEMM_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required           */
   QGEMM_ERR_BAD_PACKED = 5,    /* (device status) packed header does not match desc    */
   QGEMM_ERR_CUDA = 6,          /* a CUDA runtime call or launch failed                 */
-  QGEMM_ERR_TIMEOUT = 7,       /* (device status) a bounded device wait gave up        */
+  QGEMM_ERR_TIMEOUT = 7,       /* (device status) a bounded device wait gave up (limit:
+                                  4 s, or QGEMM_TIMEOUT_MS milliseconds from the env)  */
   QGEMM_ERR_NO_DEVICE = 8,     /* no sm_103 device is current                          */
   QGEMM_ERR_BAD_VALUE = 9      /* (device status) repack met an E8M0 of 255, a non-finite
                                   BF16 scale or a zero point above 15                  */

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <mutex>
 
 #include "qgemm.h"
@@ -18,12 +19,28 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int64_t kSplitMaxM = 1024;          // split-K is considered only up to this M
-constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kTimeoutNs = 4000000000ull;     // default limit of one device wait
+
+// Limit of every bounded wait inside a kernel: QGEMM_TIMEOUT_MS in the environment (read
+// once; a profiler that replays each launch many times needs a longer limit), else 4 s.
+uint64_t timeout_ns() {
+  static const uint64_t v = []() -> uint64_t {
+    const char* e = std::getenv("QGEMM_TIMEOUT_MS");
+    if (e != nullptr) {
+      char* end = nullptr;
+      const unsigned long long ms = std::strtoull(e, &end, 10);
+      if (end != e && ms > 0 && ms < 86400000ull) return uint64_t(ms) * 1000000ull;
+    }
+    return kTimeoutNs;
+  }();
+  return v;
+}
 
 struct DeviceInfo {
   bool init = false;
   bool ok = false;
   int sms = 0;
+  int64_t l2_bytes = 0;
   int* status = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
@@ -42,6 +59,9 @@ bool current_device(DeviceInfo** out) {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    int l2 = 0;
+    cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev);
+    d.l2_bytes = l2 > 0 ? l2 : (64ll << 20);
     d.status = device_status_ptr();
     d.ok = (major == 10 && minor == 3) && d.sms > 0 && d.status != nullptr;
   }
@@ -231,6 +251,13 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   a.m_tiles = int((M + plan.token_tile - 1) / plan.token_tile);
   a.splits = plan.splits;
   a.num_units = int(int64_t(a.m_tiles) * L.n_tiles * plan.splits);
+  // Token tiles per rasterization group: as many as keep the group's activation rows
+  // within about half of L2, so that they are read from DRAM once.
+  {
+    const int64_t x_tile_bytes = int64_t(plan.token_tile) * L.K * (fp8 ? 1 : 2);
+    const int64_t gm = std::max<int64_t>(1, (dev->l2_bytes / 2) / std::max<int64_t>(1, x_tile_bytes));
+    a.group_m = int(std::min<int64_t>(gm, a.m_tiles));
+  }
   a.chan_scale = chan_scale;
   a.tok_scale = tok_scale;
   a.Y = Y;
@@ -243,7 +270,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
                                             int64_t(plan.splits) * a.ws_slice * 4);
   }
   a.status = dev->status;
-  a.timeout_ns = kTimeoutNs;
+  a.timeout_ns = timeout_ns();
   cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }
@@ -380,7 +407,7 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   a.Y = Y;
   a.ldy = ldy;
   a.status = dev->status;
-  a.timeout_ns = kTimeoutNs;
+  a.timeout_ns = timeout_ns();
   cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }

@@ -72,8 +72,11 @@ struct Roles {
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
   static constexpr int kIssuers = BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
+  // Wide token tiles have one accumulator buffer (or two of 128 columns): two epilogue
+  // warps per lane quarter drain it twice as fast, so the MMA waits less for it.
+  static constexpr int kEpiWarps = BNT >= 128 ? 8 : 4;
   static constexpr int kEpiWarp0 = 4 * kDeqWGs;
-  static constexpr int kIssuerWarp0 = kEpiWarp0 + 4;
+  static constexpr int kIssuerWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kXProducerWarp = kIssuerWarp0 + kIssuers;
   static constexpr int kRecProducerWarp0 = kXProducerWarp + 1;
   static constexpr int kWarps = kRecProducerWarp0 + 2;
@@ -162,10 +165,17 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& a, int bnt, c
   const int n_tiles = int(a.L.n_tiles);
   const int k_blocks = int(a.L.k_blocks);
   if (a.offsets == nullptr) {
+    // Splits of a tile are consecutive units.  Tiles run in groups of group_m token tiles:
+    // inside a group the token tile changes fastest, so the CTAs running at one time share
+    // a few weight tiles and the group's activation rows, which stay in L2.
     w.split = u % a.splits;
     const int tile = u / a.splits;
-    w.nt = tile % n_tiles;
-    w.mt = tile / n_tiles;
+    const int per_group = a.group_m * n_tiles;
+    const int first_mt = (tile / per_group) * a.group_m;
+    const int gm = min(a.group_m, a.m_tiles - first_mt);
+    const int in = tile - (tile / per_group) * per_group;
+    w.mt = first_mt + in % gm;
+    w.nt = in / gm;
     w.expert = 0;
     w.row0 = int64_t(w.mt) * bnt;
     w.row_end = a.M;
@@ -326,10 +336,10 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     }
     for (int i = 0; i < C::kNumAcc; ++i) {
       ptx::mbar_init(&accfull[i], C::kIssuers);
-      ptx::mbar_init(&accempty[i], 4);  // one arrival per epilogue warp
+      ptx::mbar_init(&accempty[i], RO::kEpiWarps);  // one arrival per epilogue warp
     }
     ptx::mbar_init(drain, C::kIssuers);
-    ptx::mbar_init(epibar, 4);
+    ptx::mbar_init(epibar, RO::kEpiWarps);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
   }
@@ -381,7 +391,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   volatile int* abort_flag = &misc[1];
   const uint64_t T = a.timeout_ns;
 
-  if (A8 && warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
+  if (A8 && warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {    // first lane quarter set
     // Activation-side block scale: a constant 2^6 (E8M0 133) that returns the factor 2^-6
     // of the e2m1 -> e4m3 byte shuffle.  Filled over every lane of its columns.
     const uint32_t tl = tbase + (uint32_t((warp & 3) * 32) << 16);
@@ -439,6 +449,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer
     if (lane == 0) {
+      // every X tile is read by all weight tiles of its group: keep it in L2
+      const uint64_t pol_x = ptx::policy_evict_last();
       Ring rx;
       uint32_t pending = 0, pending_parity = 0;
       bool alive = true;
@@ -454,12 +466,12 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           ptx::mbar_arrive_expect_tx(&xfull[rx.slot], uint32_t(C::kXSlotBytes));
           if (a.x_3d) {
             // box {slab, token_tile rows, kXBoxSlabs slabs}; slab index = K / slab width
-            ptx::tma_load_3d(sx, &tmap_x, 0, row0, k0 / (A8 ? 128 : 64), &xfull[rx.slot]);
+            ptx::tma_load_3d(sx, &tmap_x, 0, row0, k0 / (A8 ? 128 : 64), &xfull[rx.slot], pol_x);
           } else {
 #pragma unroll 1
             for (int sl = 0; sl < C::kXBoxSlabs; ++sl)
               ptx::tma_load_2d(sx + sl * C::kSlabBytes, &tmap_x, k0 + sl * (A8 ? 128 : 64), row0,
-                               &xfull[rx.slot]);
+                               &xfull[rx.slot], pol_x);
           }
           pending |= 1u << rx.slot;
           pending_parity = (pending_parity & ~(1u << rx.slot)) | (rx.phase << rx.slot);
@@ -593,17 +605,54 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         warp_arrive(&afull[ca.slot], lane);
       }
     }
-  } else if (warp < kEpiWarp0 + 4) {
+  } else if (warp < kEpiWarp0 + RO::kEpiWarps) {
     // ---------------------------------------------------------------- epilogue
+    // Warp e covers tensor-memory lanes 32 (e % 4) ... (its 32 weight rows) and the
+    // accumulator columns (tokens) [eh * kCols, (eh + 1) * kCols) of its column half eh.
+    constexpr int kHalves = RO::kEpiWarps / 4;
+    constexpr int kCols = BNT / kHalves;
+    constexpr int kChunk = kCols < 32 ? kCols : 32;
+    const int eh = (warp - kEpiWarp0) >> 2;
     const int r = (warp & 3) * 32 + lane;
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
     uint32_t epi_phase = 0;
-    // Bounded rendezvous of the 128 epilogue threads (a named barrier could not give up).
+    // Bounded rendezvous of the epilogue threads (a named barrier could not give up).
     auto epi_sync = [&]() -> bool {
       warp_arrive(epibar, lane);
       const bool ok = ptx::mbar_wait(epibar, epi_phase, abort_flag, T, kSleepEpilogue);
       epi_phase ^= 1u;
       return warp_all(ok);
+    };
+    // This warp's accumulator chunk c (kChunk columns), partial accumulators summed.
+    auto load_chunk = [&](int acc, int sub0, int active, int c, uint32_t (&v)[32]) {
+      const uint32_t col = t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * kChunk);
+      if constexpr (kChunk == 32) {
+        ptx::tmem_ld32(col + uint32_t(sub0 * BNT), v);
+      } else {
+        uint32_t v16[16];
+        ptx::tmem_ld16(col + uint32_t(sub0 * BNT), v16);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = v16[j];
+      }
+#pragma unroll
+      for (int d = 1; d < C::kNumSub; ++d) {
+        if (d >= active) break;
+        const int sub = (sub0 + d) % C::kNumSub;
+        uint32_t p[32];
+        if constexpr (kChunk == 32) {
+          ptx::tmem_ld32(col + uint32_t(sub * BNT), p);
+        } else {
+          uint32_t p16[16];
+          ptx::tmem_ld16(col + uint32_t(sub * BNT), p16);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) p[j] = p16[j];
+        }
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < kChunk; ++j)
+          v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(p[j]));
+      }
+      ptx::tmem_wait_ld();
     };
     int ui = 0;
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
@@ -619,58 +668,125 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const int64_t n = int64_t(w.nt) * kTileN + r;
       const bool n_ok = n < L.N;
       const bool split = a.splits > 1;
-      const float cs = (n_ok && a.chan_scale != nullptr && !split) ? a.chan_scale[n] : 1.0f;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
       // Partial accumulators of the issuers that had a stage in this unit: the unit's
       // stages g0, g0 + 1, ... went to issuers (g0 + d) % kIssuers.
       const int active = min(C::kNumSub, nst);
       const int sub0 = int(g0 % uint32_t(C::kNumSub));
-      constexpr int kChunk = BNT < 32 ? BNT : 32;
-#pragma unroll 1
-      for (int c = 0; c < BNT / kChunk; ++c) {
-        uint32_t v[32];
-        const uint32_t col = t_lane + uint32_t(acc * C::kNumSub * BNT + c * kChunk);
-        if constexpr (kChunk == 32) {
-          ptx::tmem_ld32(col + uint32_t(sub0 * BNT), v);
-        } else {
-          uint32_t v16[16];
-          ptx::tmem_ld16(col + uint32_t(sub0 * BNT), v16);
+      const int64_t m_first = w.row0 + int64_t(eh) * kCols;   // first row of this warp
+      if constexpr (kHalves > 1) {
+        if (!split) {
+          // Wide tiles: scale and round every column of this warp to BF16 in registers,
+          // hand the accumulator back to the MMA at once, then store.
+          const float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+          uint32_t packed[kCols / 2];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = v16[j];
-        }
+          for (int c = 0; c < kCols / 16; ++c) {
+            uint32_t v[16];
+            ptx::tmem_ld16(t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * 16), v);
+            ptx::tmem_wait_ld();
 #pragma unroll
-        for (int d = 1; d < C::kNumSub; ++d) {
-          if (d >= active) break;
-          const int sub = (sub0 + d) % C::kNumSub;
-          uint32_t p[32];
-          if constexpr (kChunk == 32) {
-            ptx::tmem_ld32(col + uint32_t(sub * BNT), p);
-          } else {
-            uint32_t p16[16];
-            ptx::tmem_ld16(col + uint32_t(sub * BNT), p16);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) p[j] = p16[j];
+            for (int j = 0; j < 16; j += 2)
+              packed[(c * 16 + j) / 2] =
+                  ptx::pack_bf16x2(__uint_as_float(v[j]) * cs, __uint_as_float(v[j + 1]) * cs);
           }
-          ptx::tmem_wait_ld();
+          ptx::tc_fence_before();
+          warp_arrive(&accempty[acc], lane);
+          if (n_ok) {
+            uint16_t* Yh = reinterpret_cast<uint16_t*>(Y) + n;
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j)
-            v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(p[j]));
+            for (int j = 0; j < kCols; ++j) {
+              const int64_t m = m_first + j;
+              if (m < w.row_end) {
+                uint16_t h = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
+                if (A8) {
+                  // per-token scale after the rounding above would round twice: redo it
+                  const float y = __uint_as_float(uint32_t(h) << 16);
+                  h = uint16_t(ptx::pack_bf16x2(y * a.tok_scale[m], 0.0f) & 0xFFFFu);
+                }
+                Yh[m * a.ldy] = h;
+              }
+            }
+          }
+          continue;
         }
-        ptx::tmem_wait_ld();
-        if (c == BNT / kChunk - 1) {
+      }
+      if (!split) {
+        // Narrow tiles (double-buffered accumulators): convert and store chunk by chunk.
+        const float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+#pragma unroll 1
+        for (int c = 0; c < kCols / kChunk; ++c) {
+          uint32_t v[32];
+          load_chunk(acc, sub0, active, c, v);
+          if (c == kCols / kChunk - 1) {
+            ptx::tc_fence_before();
+            warp_arrive(&accempty[acc], lane);
+          }
+          if (n_ok) {
+#pragma unroll
+            for (int j = 0; j < kChunk; ++j) {
+              const int64_t m = m_first + c * kChunk + j;
+              if (m < w.row_end) {
+                float y = __uint_as_float(v[j]) * cs;
+                if (A8) y *= a.tok_scale[m];
+                Y[m * a.ldy + n] = __float2bfloat16_rn(y);
+              }
+            }
+          }
+        }
+        continue;
+      }
+      // Split-K: store this split's FP32 partial tile into its slice of the workspace.
+#pragma unroll 1
+      for (int c = 0; c < kCols / kChunk; ++c) {
+        uint32_t v[32];
+        load_chunk(acc, sub0, active, c, v);
+        if (c == kCols / kChunk - 1) {
           ptx::tc_fence_before();
           warp_arrive(&accempty[acc], lane);
         }
         if (n_ok) {
 #pragma unroll
           for (int j = 0; j < kChunk; ++j) {
-            const int64_t m = w.row0 + c * kChunk + j;
-            if (m < w.row_end) {
-              float y = __uint_as_float(v[j]);
-              if (split) {
-                __stcg(a.ws + int64_t(w.split) * a.ws_slice + m * a.ws_ld + n, y);
-              } else {
-                y *= cs;
+            const int64_t m = m_first + c * kChunk + j;
+            if (m < w.row_end)
+              __stcg(a.ws + int64_t(w.split) * a.ws_slice + m * a.ws_ld + n, __uint_as_float(v[j]));
+          }
+        }
+      }
+      // The last of the tile's splits to arrive sums the slices and converts.
+      __threadfence();
+      if (!epi_sync()) break;
+      if (r == 0 && eh == 0) {
+        const int tile = w.mt * int(L.n_tiles) + w.nt;
+        const int prev = atomicAdd(&a.counters[tile], 1);
+        misc[4] = (prev == a.splits - 1) ? 1 : 0;
+        if (prev == a.splits - 1) a.counters[tile] = 0;
+      }
+      if (!epi_sync()) break;
+      if (misc[4]) {
+        // Sum the slices in split order (a fixed order: the result does not depend on
+        // which split arrived last), scale, convert.
+        __threadfence();
+        if (n_ok) {
+          const float cs2 = a.chan_scale != nullptr ? a.chan_scale[n] : 1.0f;
+          const int64_t m_lim = m_first + kCols < w.row_end ? m_first + kCols : w.row_end;
+          // 8 independent loads in flight per thread; rows of one warp are coalesced.
+          for (int64_t m0 = m_first; m0 < m_lim; m0 += 8) {
+            float v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
+            for (int sl = 0; sl < a.splits; ++sl) {
+              const float* src = a.ws + int64_t(sl) * a.ws_slice + n;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (m0 + j < m_lim) v[j] += __ldcg(src + (m0 + j) * a.ws_ld);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int64_t m = m0 + j;
+              if (m < m_lim) {
+                float y = v[j] * cs2;
                 if (A8) y *= a.tok_scale[m];
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }
@@ -678,49 +794,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           }
         }
       }
-      if (split) {
-        // Split-K: the last of the `splits` CTAs that reduce this tile converts it.
-        __threadfence();
-        if (!epi_sync()) break;
-        if (r == 0) {
-          const int tile = w.mt * int(L.n_tiles) + w.nt;
-          const int prev = atomicAdd(&a.counters[tile], 1);
-          misc[4] = (prev == a.splits - 1) ? 1 : 0;
-          if (prev == a.splits - 1) a.counters[tile] = 0;
-        }
-        if (!epi_sync()) break;
-        if (misc[4]) {
-          // Sum the slices in split order (a fixed order: the result does not depend on
-          // which split arrived last), scale, convert.
-          __threadfence();
-          if (n_ok) {
-            const float cs2 = a.chan_scale != nullptr ? a.chan_scale[n] : 1.0f;
-            const int64_t m_end = w.row0 + BNT < w.row_end ? w.row0 + BNT : w.row_end;
-            // 8 independent loads in flight per thread; rows of one warp are coalesced.
-            for (int64_t m0 = w.row0; m0 < m_end; m0 += 8) {
-              float v[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-              for (int sl = 0; sl < a.splits; ++sl) {
-                const float* src = a.ws + int64_t(sl) * a.ws_slice + n;
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                  if (m0 + j < m_end) v[j] += __ldcg(src + (m0 + j) * a.ws_ld);
-              }
-#pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int64_t m = m0 + j;
-                if (m < m_end) {
-                  float y = v[j] * cs2;
-                  if (A8) y *= a.tok_scale[m];
-                  Y[m * a.ldy + n] = __float2bfloat16_rn(y);
-                }
-              }
-            }
-          }
-        }
-        if (!epi_sync()) break;
-      }
+      if (!epi_sync()) break;
     }
   }
 

@@ -26,6 +26,7 @@ struct GemmArgs {
   int32_t E;
   int64_t M;                   // dense rows (M) or MoE rows (R)
   int32_t m_tiles, splits, num_units;   // dense schedule
+  int32_t group_m;             // dense: token tiles per rasterization group (>= 1)
   const float* chan_scale;     // [N] or nullptr
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   void* Y;                     // bf16 [M, ldy]

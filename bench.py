@@ -65,7 +65,11 @@ def alg_bytes(M, N, K):
 # DRAM bytes (read + write) per launch from one ncu capture of the same call, keyed by
 # (N, K, M), with the digest of the kernel sources they were taken on; a changed kernel
 # reports null until it is captured again.
-CAPTURED_TRAFFIC = {"csrc_sha256": None, "launches": {}}
+CAPTURED_TRAFFIC = {
+    # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
+    "csrc_sha256": "2faed61f1d28d79a4dccd3982bdb87b30d4abc0348f57c89a1fcaf9041b2cdbf",
+    "launches": {"28672,8192,8192": 3265377000 + 901497600},
+}
 
 
 def csrc_digest():
@@ -100,32 +104,47 @@ class ClockSampler:
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 20
 
     def __init__(self, index):
         self.index = index
         self.proc = None
 
     def start(self):
+        """Start sampling (before the warm-up, so the sampler is running when timing starts);
+        each line read is stamped with the host clock by a reader thread."""
+        import threading
+        self.lines = []
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+            return
 
-    def stop(self):
+        def reader():
+            for line in self.proc.stdout:
+                self.lines.append((time.perf_counter(), line))
+        self.thread = threading.Thread(target=reader, daemon=True)
+        self.thread.start()
+
+    def stop(self, t0, t1):
+        """Samples taken within the host-time window [t0, t1] of the timed region."""
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         self.proc.terminate()
         try:
-            out, _ = self.proc.communicate(timeout=5)
+            self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-            out, _ = self.proc.communicate()
+        self.thread.join(timeout=5)
         sm, smax, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in out.strip().splitlines():
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
@@ -138,7 +157,7 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "samples": len(sm), "period_ms": self.PERIOD_MS, "reasons": sorted(reasons)}
 
 
 # --------------------------------------------------------------------------- ours
@@ -210,13 +229,14 @@ N, K, M, g = 28672, 8192, 16, 128
 x, w = WL.int4_asym_shape(N, K, M, seed=0)
 done_rows, flops, t_total = 0, 0.0, 0.0
 chunk = 512
-while done_rows < N and t_total < {seconds}:
-    a, b = done_rows, min(N, done_rows + chunk)
+while t_total < {seconds}:
+    a = done_rows % N
+    b = min(N, a + chunk)
     t0 = time.perf_counter()
     y = oracle.w4a16(x, w.wfmt, w.group, w.codes[a:b], w.scales[a:b], w.zeros[a:b])
     t_total += time.perf_counter() - t0
     flops += 2.0 * M * (b - a) * K
-    done_rows = b
+    done_rows += b - a
 print(json.dumps({{"flops": flops, "seconds": t_total, "rows": done_rows}}))
 """
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
@@ -226,8 +246,8 @@ print(json.dumps({{"flops": flops, "seconds": t_total, "rows": done_rows}}))
     d = json.loads(r.stdout.strip().splitlines()[-1])
     return {"value": d["flops"] / d["seconds"] / 1e12, "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle",
-            "sample": (f"float64 numpy oracle, N x K = 28672 x 8192, M = 16, the first "
-                       f"{d['rows']} of 28672 weight rows (dequantize + matmul), "
+            "sample": (f"float64 numpy oracle, N x K = 28672 x 8192, M = 16: {d['rows']} weight "
+                       f"rows dequantized and multiplied (cycling over the 28672), "
                        f"{d['seconds']:.1f} s, 1 thread")}
 
 
@@ -379,20 +399,21 @@ def bench_ours(args):
     cases = build_inputs(device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
 
+    sampler = ClockSampler(local)
+    sampler.start()
     for _ in range(args.warmup):
         run_step(cases, flush)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    sampler = ClockSampler(local)
-    sampler.start()
     t0 = time.perf_counter()
     steps = [run_step(cases, flush) for _ in range(args.steps)]
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-    wall = time.perf_counter() - t0
-    clocks = sampler.stop()
+    t1 = time.perf_counter()
+    wall = t1 - t0
+    clocks = sampler.stop(t0, t1)
     e2e_steps = [run_step(cases, flush, e2e=True) for _ in range(max(1, args.steps))]
     torch.cuda.synchronize()
     extra = None
@@ -575,7 +596,7 @@ def bench_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -67,9 +67,16 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "2faed61f1d28d79a4dccd3982bdb87b30d4abc0348f57c89a1fcaf9041b2cdbf",
+    "csrc_sha256": "209244b9d4af4e72b4484afdd69480809a4bc0545628e247cd3ee57e0b9584a9",
     "launches": {"28672,8192,8192": 3265377000 + 901497600},
 }
+
+
+# Sources that define the GEMM kernel and its launch plan (not the repack, quantization or
+# no-alloc wrappers).
+GEMM_SOURCES = ("api.cu", "dequant.cuh", "gemm_a16_any.cu", "gemm_a16_mxfp4.cu",
+                "gemm_a16_sym_g1.cu", "gemm_a16_zp_g1.cu", "gemm_a8.cu", "gemm_kernel.cuh",
+                "kernels.h", "ptx.cuh", "qgemm_internal.h")
 
 
 def csrc_digest():
@@ -77,7 +84,7 @@ def csrc_digest():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_weight_gemm_gb300", "csrc")
     for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h")):
+        if f in GEMM_SOURCES:
             with open(os.path.join(d, f), "rb") as fh:
                 h.update(f.encode() + b"\0" + fh.read())
     with open(os.path.join(ROOT, "include", "qgemm.h"), "rb") as fh:

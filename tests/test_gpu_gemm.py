@@ -169,12 +169,15 @@ def test_many_units_with_odd_stage_counts(splits):
     _assert_close(y, ref, TOL_A16)
 
 
-def test_quant_act_fp8_bitexact():
+@pytest.mark.parametrize("M,K", [(67, 1000), (3, 1001), (5, 28672), (2, 7168), (9, 24)])
+def test_quant_act_fp8_bitexact(M, K):
+    """Vector path (K % 8 == 0; rows longer than the register-kept part re-read) and the
+    scalar path (K = 1001)."""
     from tests import gpu_util as G
     qg = _qg()
     r = WL.rng(26)
-    x = WL.gen_x(r, 67, 1000, outliers=True)
-    x[5] = 0                                         # an all-zero row
+    x = WL.gen_x(r, M, K, outliers=True)
+    x[min(1, M - 1)] = 0                             # an all-zero row
     codes, s = qg.quant_act_fp8(G.bf16_tensor(x))
     ref_codes, ref_s = oracle.quant_act_fp8(x)
     np.testing.assert_array_equal(s.cpu().numpy(), ref_s)

@@ -491,9 +491,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     // partial accumulator j.  The whole warp runs the loop and one elected lane issues: a
     // converged warp issues tcgen05 instructions faster than a lone diverged lane.
     const int issuer = warp - RO::kIssuerWarp0;
-    Ring ra, rx;
+    Ring rx;
     int ui = 0;
-    uint32_t g = 0;                       // stage counter of this CTA
+    uint32_t g0 = 0;                      // CTA stage counter at the unit start
     bool alive = true;
     const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
     for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x, ++ui) {
@@ -505,14 +505,21 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const uint32_t d_tmem = tbase + uint32_t((acc * C::kNumSub + issuer) * BNT);
       const int nst = (w.kb1 - w.kb0) * kSub;
       uint32_t first = 1;                 // this issuer's first MMA of the unit overwrites
-      for (int i = 0; i < nst; ++i, ++g) {
-        const Ring cur = ra;
-        ra.next(SA);
-        const int xj = i % XQ;            // stage inside the X slot
+      for (int x0 = 0; x0 < nst && alive; x0 += XQ) {
         // Every issuer waits for every X slot, even one without a stage of its own: its
         // release of the slot below must count towards this fill of the slot, not the next.
-        if (xj == 0 && !warp_all(ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
-        if (int(g % C::kIssuers) == issuer) {
+        if (!warp_all(ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
+        const int x1 = x0 + XQ < nst ? x0 + XQ : nst;
+        // this issuer's stages in [x0, x1): CTA stage g0 + i with (g0 + i) % kIssuers == issuer
+        const uint32_t gx = g0 + uint32_t(x0);
+        int i = x0 + int((uint32_t(issuer) + uint32_t(C::kIssuers) - gx % uint32_t(C::kIssuers)) %
+                         uint32_t(C::kIssuers));
+        for (; i < x1; i += C::kIssuers) {
+          const uint32_t g = g0 + uint32_t(i);
+          const int xj = i - x0;          // stage inside the X slot
+          Ring cur;
+          cur.slot = int(g % uint32_t(SA));
+          cur.phase = (g / uint32_t(SA)) & 1u;
           if (!warp_all(ptx::mbar_wait(&afull[cur.slot], cur.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
           ptx::tc_fence_after();
           const uint64_t bdesc = desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
@@ -536,11 +543,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           first = 0;
           ptx::mma_commit_elect(&aempty[cur.slot]);   // frees the stage's A columns
         }
-        if (xj == XQ - 1 || i == nst - 1) {
-          ptx::mma_commit_elect(&xempty[rx.slot]);    // every issuer releases every X slot
-          rx.next(SX);
-        }
+        if (!alive) break;
+        ptx::mma_commit_elect(&xempty[rx.slot]);      // every issuer releases every X slot
+        rx.next(SX);
       }
+      g0 += uint32_t(nst);
       if (!alive) break;
       ptx::mma_commit_elect(&accfull[acc]);      // every issuer arrives once per unit
     }
@@ -555,17 +562,23 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
     const int G = L.groups_per_record;
     const int zoff = L.off_zeros - L.off_scales;
-    Ring rr, ra;
-    uint32_t g = 0;                                        // stage counter of this CTA
+    uint32_t g0 = 0;                                       // CTA stage counter at the unit start
     bool alive = true;
     for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
       const Unit w = decode_unit(u, a, BNT, prefix, offs);
       const int nst = (w.kb1 - w.kb0) * kSub;
-      for (int i = 0; i < nst; ++i, ++g) {
-        const Ring cr = rr, ca = ra;
-        rr.next(SR);
-        ra.next(SA);
-        if (int(g % kDeqWGs) != wg) continue;
+      // Visit only this warpgroup's stages; ring slots and phases follow from the stage
+      // counter (the ring depths are compile-time constants).
+      const uint32_t g1 = g0 + uint32_t(nst);
+      uint32_t g = g0 + (uint32_t(wg) + uint32_t(kDeqWGs) - g0 % uint32_t(kDeqWGs)) % uint32_t(kDeqWGs);
+      g0 = g1;
+      for (; g < g1; g += uint32_t(kDeqWGs)) {
+        const int i = int(g - (g1 - uint32_t(nst)));       // stage index inside the unit
+        Ring cr, ca;
+        cr.slot = int(g % uint32_t(SR));
+        cr.phase = (g / uint32_t(SR)) & 1u;
+        ca.slot = int(g % uint32_t(SA));
+        ca.phase = (g / uint32_t(SA)) & 1u;
         if (!warp_all(ptx::mbar_wait(&rfull[cr.slot], cr.phase, abort_flag, T, kSleepDequant))) { alive = false; break; }
         const uint8_t* rec = s_rec + cr.slot * C::kRecSlot;
         const uint32_t a_col = t_lane + uint32_t(C::kACol0 + ca.slot * C::kACols);

@@ -309,19 +309,17 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   const Layout& L = a.L;
 
   // ------------------------------------------------------------------ prologue
+  // The header loads are issued first and checked after the barrier set-up, and tensor
+  // memory is allocated at the same time, so that their latencies overlap.
   if (threadIdx.x == 0) {
-    misc[1] = 0;
     const PackedHeader* h = reinterpret_cast<const PackedHeader*>(a.packed);
-    bool ok = h->magic == kPackedMagic && h->version == kPackedVersion && h->wfmt == L.wfmt &&
-              h->group == L.group && h->has_zp == L.has_zp && h->afmt == L.afmt &&
-              h->N == L.N && h->K == L.K && h->total_bytes == L.total_bytes;
-    if (ok && a.offsets != nullptr && a.E > 1) {
-      const PackedHeader* hl =
-          reinterpret_cast<const PackedHeader*>(a.packed + int64_t(a.E - 1) * a.expert_stride);
-      ok = hl->magic == kPackedMagic && hl->N == L.N && hl->K == L.K && hl->afmt == L.afmt;
-    }
-    if (!ok) atomicCAS(a.status, 0, kStatusBadPacked);
-    misc[2] = ok ? 1 : 0;
+    const PackedHeader hd = *h;
+    const PackedHeader* hl = reinterpret_cast<const PackedHeader*>(
+        a.packed + int64_t(a.offsets != nullptr && a.E > 1 ? a.E - 1 : 0) * a.expert_stride);
+    const uint32_t hl_magic = hl->magic;
+    const int64_t hl_N = hl->N, hl_K = hl->K;
+    const int32_t hl_afmt = hl->afmt;
+    misc[1] = 0;
     for (int s = 0; s < SR; ++s) {
       ptx::mbar_init(&rfull[s], 1);
       ptx::mbar_init(&rempty[s], 4);     // one arrival per dequant warp
@@ -342,6 +340,17 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     ptx::mbar_init(epibar, RO::kEpiWarps);
     ptx::fence_barrier_init();
     ptx::fence_proxy_async_smem();
+    bool ok = hd.magic == kPackedMagic && hd.version == kPackedVersion && hd.wfmt == L.wfmt &&
+              hd.group == L.group && hd.has_zp == L.has_zp && hd.afmt == L.afmt &&
+              hd.N == L.N && hd.K == L.K && hd.total_bytes == L.total_bytes;
+    // MoE: the last expert's header as well
+    ok = ok && hl_magic == kPackedMagic && hl_N == L.N && hl_K == L.K && hl_afmt == L.afmt;
+    if (!ok) atomicCAS(a.status, 0, kStatusBadPacked);
+    misc[2] = ok ? 1 : 0;
+  }
+  if (warp == kEpiWarp0) {
+    ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&misc[0]), C::kTmemCols);
+    ptx::tmem_relinquish();
   }
   if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
   int num_units = a.num_units;
@@ -376,18 +385,15 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (bad) atomicCAS(a.status, 0, kStatusBadValue);
     }
   }
-  __syncthreads();
-  if (a.offsets != nullptr) num_units = misc[3] * int(L.n_tiles);
-  if (!misc[2] || int(blockIdx.x) >= num_units) return;     // nothing allocated yet
-
-  if (warp == kEpiWarp0) {
-    ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&misc[0]), C::kTmemCols);
-    ptx::tmem_relinquish();
-  }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (a.offsets != nullptr) num_units = misc[3] * int(L.n_tiles);
   const uint32_t tbase = static_cast<uint32_t>(misc[0]);
+  if (!misc[2] || int(blockIdx.x) >= num_units) {           // nothing to do: give TMEM back
+    if (warp == kEpiWarp0) ptx::tmem_dealloc(tbase, C::kTmemCols);
+    return;
+  }
   volatile int* abort_flag = &misc[1];
   const uint64_t T = a.timeout_ns;
 

@@ -355,18 +355,30 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
   int num_units = a.num_units;
   if (a.offsets != nullptr && warp == 0) {
-    // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).
+    // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).  All offsets
+    // are loaded first (independent loads, one memory latency), then scanned from shared
+    // memory.
+    for (int base = 0; base <= a.E; base += 32 * 8) {
+      int v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = base + j * 32 + lane;
+        v[j] = e <= a.E ? __ldg(a.offsets + e) : 0;
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int e = base + j * 32 + lane;
+        if (e <= a.E) offs[e] = v[j];
+      }
+    }
+    __syncwarp();
     int carry = 0;
     bool bad = false;
     for (int base = 0; base <= a.E; base += 32) {
       const int e = base + lane;
-      int o = 0, t = 0;
-      if (e <= a.E) {
-        o = a.offsets[e];
-        offs[e] = o;
-      }
+      int t = 0;
       if (e < a.E) {
-        const int o1 = a.offsets[e + 1];
+        const int o = offs[e], o1 = offs[e + 1];
         if (o1 < o || o < 0 || o1 > a.M) bad = true;
         t = (o1 > o) ? (o1 - o + BNT - 1) / BNT : 0;
       }

@@ -113,8 +113,10 @@ qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const v
                           const uint8_t* zeros, void* packed, void* stream);
 
 /*
- * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max (split-K partial
- * sums, one FP32 slice per split, and tile arrival counters).  The workspace must be
+ * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max: the FP32 partial
+ * sums of the output tiles whose K range the schedule cuts over several CTAs (split-K or
+ * stream-K; one 128 x token-tile slot per contributing CTA) and one arrival counter per
+ * cut tile; 0 when no M <= M_max cuts a tile.  The workspace must be
  * 256-byte aligned and zero-filled before its first use; every successful call leaves the
  * counters zero again (the partial sums are overwritten by every call), so one
  * zero-filled buffer can be reused by consecutive calls on one stream.
@@ -215,9 +217,19 @@ qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, co
                                  int64_t ldy, void* stream);
 
 /*
+ * The schedule qgemm_w4a16 / qgemm_w4a8 would run for M rows on the current device (152
+ * SMs assumed when no device is visible): out[0] token tile, out[1] uniform K cut (1 = none),
+ * out[2] stream-K tiles (0 = none), out[3] partial-sum slots per cut tile, out[4] CTAs.
+ * Host-only (launches nothing); honours qgemm_force_config.
+ */
+qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]);
+
+/*
  * Tuning override for tests and sweeps: force the token tile (16, 32, 64, 128 or 256) and
- * the split-K factor (>= 1) of the dense kernels; 0 restores the built-in heuristic.
- * Process-wide, not thread-safe.
+ * the schedule of the dense kernels: splits >= 1 cuts every tile's K range into that many
+ * equal parts (1 = no cut), splits = -1 selects the stream-K schedule (an even share of the
+ * leftover tiles' K blocks per CTA, then whole tiles; falls back to no cut where it does not
+ * apply); 0 restores the built-in heuristic for that part.  Process-wide, not thread-safe.
  */
 qgemm_status qgemm_force_config(int32_t token_tile, int32_t splits);
 

@@ -14,7 +14,7 @@ import torch
 __all__ = [
     "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
-    "force_config", "check_desc", "WFMT", "AFMT", "EXPORTS",
+    "force_config", "plan", "check_desc", "WFMT", "AFMT", "EXPORTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -25,7 +25,7 @@ AFMT = {"bf16": 0, "fp8": 1}
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
-           "qgemm_force_config", "qgemm_w4a16_noalloc")
+           "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -93,6 +93,7 @@ def lib():
         "qgemm_device_status": (ctypes.c_int, [I32]),
         "qgemm_force_config": (ctypes.c_int, [I32, I32]),
         "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
+        "qgemm_plan": (ctypes.c_int, [D, I64, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -255,4 +256,13 @@ def device_status(clear=True):
 
 
 def force_config(token_tile=0, splits=0):
+    """splits: >= 1 uniform K cut, -1 stream-K, 0 heuristic (see qgemm_force_config)."""
     _check(lib().qgemm_force_config(int(token_tile), int(splits)), "force_config")
+
+
+def plan(desc, M):
+    """The dense schedule for M rows: dict(token_tile, splits, sk_tiles, max_contrib, grid)."""
+    out = (ctypes.c_int32 * 5)()
+    d = desc.c()
+    _check(lib().qgemm_plan(ctypes.byref(d), int(M), out), "plan")
+    return dict(zip(("token_tile", "splits", "sk_tiles", "max_contrib", "grid"), list(out)))

@@ -85,22 +85,55 @@ bool layout_of(const qgemm_wdesc* d, Layout* L) {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // ---------------------------------------------------------------- dispatch
-// Token tile and split-K factor from a cost model of one call on a persistent grid:
-//   time ~ T0 + ceil(units / SMs) * (ceil(k_blocks / splits) * stage(tile) + unit(tile)
-//                                   + [splits > 1] splits * tile * reduce)
-// where units = m_tiles * n_tiles * splits; the last term is the last-arriving split's
-// sum over the splits' partial tiles.  The constants were fitted (least squares on log
-// time) to event-timed calls of every tile and split count on one GB300, over the INT4 and
-// MXFP4 shapes N x K = 28672 x 8192, 8192 x 28672, 4096 x 7168, 7168 x 2048 and
-// M = 1 ... 2048; the model's choice was within 0.5% of the fastest measured one on
-// average (13% in the worst case).
+// Token tile and schedule from a cost model of one call on a persistent grid of P CTAs.
+// Schedules (T = m_tiles * n_tiles tiles of k_blocks 128-K records each):
+//   uniform  every tile cut into s equal K parts (s = 1: plain data-parallel), unit u on
+//            CTA u % P: time ~ T0 + ceil(T s / P) (ceil(k_blocks / s) stage + unit
+//                                                  + [s > 1] s tile reduce)
+//   stream-K the records of the T mod P leftover tiles (all T when T < P) are dealt out
+//            evenly over the P CTAs, which then take the remaining whole tiles:
+//            time ~ T0 + (records per CTA) stage + (units per CTA) unit
+//                       + [no whole tiles] contributors tile reduce
+// (stream-K, after "Stream-K: Work-centric Parallel Decomposition for Dense Matrix-Matrix
+// Multiplication on the GPU", Osama et al., 2023: the cut pieces run first, so their
+// reduction overlaps the whole tiles that follow).
 namespace {
 constexpr int kTiles[5] = {16, 32, 64, 128, 256};
 constexpr double kStageUs[5] = {0.326, 0.330, 0.353, 0.401, 0.657};  // per 128-K block
 constexpr double kUnitUs[5] = {3.08, 6.11, 7.88, 10.05, 17.59};      // per unit
 constexpr double kReduceUsPerSplitRow = 0.0716;
 constexpr double kCallUs = 6.44;
+constexpr int kMaxContrib = 8;       // stream-K (unforced): at most this many CTAs per tile
 }  // namespace
+
+// The CTA whose stream-K range holds record x of S (same formula as the kernel).
+int64_t sk_cta_of(int64_t x, int64_t S, int64_t P) { return ((x + 1) * P - 1) / S; }
+
+struct SkShape {
+  int sk_tiles = 0, max_contrib = 0, max_units = 0;
+  int64_t max_records = 0;
+};
+
+// Stream-K over the leftover tiles for T tiles of kb records on P CTAs.
+SkShape sk_shape(int64_t T, int64_t kb, int64_t P) {
+  SkShape r;
+  const int64_t q = T / P;
+  r.sk_tiles = int(q == 0 ? T : T % P);
+  if (r.sk_tiles == 0) return r;
+  const int64_t S = int64_t(r.sk_tiles) * kb;
+  for (int64_t t = 0; t < r.sk_tiles; ++t) {
+    const int64_t c = sk_cta_of((t + 1) * kb - 1, S, P) - sk_cta_of(t * kb, S, P) + 1;
+    r.max_contrib = std::max<int>(r.max_contrib, int(c));
+  }
+  for (int64_t i = 0; i < P; ++i) {
+    const int64_t lo = i * S / P, hi = (i + 1) * S / P;
+    const int64_t pieces = hi > lo ? (hi - 1) / kb - lo / kb + 1 : 0;
+    r.max_units = std::max<int>(r.max_units, int(q + pieces));
+    r.max_records = std::max<int64_t>(r.max_records, q * kb + (hi - lo));
+  }
+  if (r.max_contrib <= 1) r.max_contrib = 0;      // nothing is cut
+  return r;
+}
 
 double plan_cost_us(const Layout& L, int64_t M, int ti, int splits, int sms) {
   const int64_t tt = kTiles[ti];
@@ -113,44 +146,76 @@ double plan_cost_us(const Layout& L, int64_t M, int ti, int splits, int sms) {
   return kCallUs + double(per_cta) * unit;
 }
 
+double sk_cost_us(const Layout& L, int64_t M, int ti, int sms, SkShape* out) {
+  const int64_t tt = kTiles[ti];
+  const int64_t T = (M + tt - 1) / tt * L.n_tiles;
+  const SkShape sh = sk_shape(T, L.k_blocks, sms);
+  *out = sh;
+  if (sh.sk_tiles == 0 || (sh.max_contrib > kMaxContrib && g_force_splits >= 0)) return 1e300;
+  double c = kCallUs + double(sh.max_records) * kStageUs[ti] + double(sh.max_units) * kUnitUs[ti];
+  if (T < sms) c += double(sh.max_contrib) * double(tt) * kReduceUsPerSplitRow;
+  return c;
+}
+
 GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
   GemmPlan p;
   p.token_tile = 16;
   p.splits = 1;
+  p.sk_tiles = 0;
+  p.max_contrib = 0;
   double best = 1e300;
   for (int ti = 0; ti < 5; ++ti) {
     const int tt = kTiles[ti];
     if (g_force_tile ? tt != g_force_tile : (tt > 16 && tt > 2 * M)) continue;
-    for (int s : {1, 2, 3, 4, 6, 8}) {
-      if (g_force_splits) {
-        if (s != 1) break;
-        s = int(std::min<int64_t>(g_force_splits, L.k_blocks));
-      } else if (s > 1 && (M > kSplitMaxM || L.k_blocks / s < 2)) {
-        break;
+    if (g_force_splits >= 0) {
+      for (int s : {1, 2, 3, 4, 6, 8}) {
+        if (g_force_splits > 0) {
+          if (s != 1) break;
+          s = int(std::min<int64_t>(g_force_splits, L.k_blocks));
+        } else if (s > 1 && (M > kSplitMaxM || L.k_blocks / s < 2)) {
+          break;
+        }
+        const double c = plan_cost_us(L, M, ti, s, sms);
+        if (c < best) {
+          best = c;
+          p.token_tile = tt;
+          p.splits = s;
+          p.sk_tiles = 0;
+          p.max_contrib = s > 1 ? s : 0;
+        }
+        if (g_force_splits > 0) break;
       }
-      const double c = plan_cost_us(L, M, ti, s, sms);
-      if (c < best) { best = c; p.token_tile = tt; p.splits = s; }
-      if (g_force_splits) break;
+    }
+    if (g_force_splits <= 0 && M <= kSplitMaxM) {
+      SkShape sh;
+      const double c = sk_cost_us(L, M, ti, sms, &sh);
+      if (c < best) {
+        best = c;
+        p.token_tile = tt;
+        p.splits = 1;
+        p.sk_tiles = sh.sk_tiles;
+        p.max_contrib = sh.max_contrib;
+      }
     }
   }
   if (g_force_tile) p.token_tile = g_force_tile;
-  const int64_t units = (M + p.token_tile - 1) / p.token_tile * L.n_tiles * p.splits;
-  p.grid = int(std::min<int64_t>(units, sms));
+  const int64_t tiles = (M + p.token_tile - 1) / p.token_tile * L.n_tiles;
+  p.grid = p.sk_tiles > 0 ? sms : int(std::min<int64_t>(tiles * p.splits, sms));
   return p;
 }
 
-// Split-K workspace: one FP32 partial-sum slice per split (plain stores, no atomics), then
-// one arrival counter per output tile.
-int64_t split_slice_floats(const Layout& L, int64_t M, const GemmPlan& p) {
-  const int64_t m_tiles = (M + p.token_tile - 1) / p.token_tile;
-  return round_up(m_tiles * p.token_tile * L.N_pad, 64);
+// Partial-sum slots and arrival counters of the cut tiles: uniform cuts cut every tile,
+// stream-K the sk_tiles leftover tiles.
+int64_t cut_tiles(const Layout& L, int64_t M, const GemmPlan& p) {
+  if (p.max_contrib == 0) return 0;
+  if (p.sk_tiles > 0) return p.sk_tiles;
+  return (M + p.token_tile - 1) / p.token_tile * L.n_tiles;
 }
 
 int64_t split_ws_bytes(const Layout& L, int64_t M, const GemmPlan& p) {
-  if (p.splits <= 1) return 0;
-  const int64_t m_tiles = (M + p.token_tile - 1) / p.token_tile;
-  const int64_t partial = int64_t(p.splits) * split_slice_floats(L, M, p) * 4;
-  return partial + round_up(m_tiles * L.n_tiles * 4, 256);
+  const int64_t n = cut_tiles(L, M, p);
+  if (n == 0) return 0;
+  return n * p.max_contrib * int64_t(kTileN) * p.token_tile * 4 + round_up(n * 4, 256);
 }
 
 typedef PFN_cuTensorMapEncodeTiled_v12000 EncodeFn;
@@ -250,7 +315,9 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   a.M = M;
   a.m_tiles = int((M + plan.token_tile - 1) / plan.token_tile);
   a.splits = plan.splits;
-  a.num_units = int(int64_t(a.m_tiles) * L.n_tiles * plan.splits);
+  a.num_units = plan.sk_tiles > 0 ? plan.grid : int(int64_t(a.m_tiles) * L.n_tiles * plan.splits);
+  a.sk_tiles = plan.sk_tiles;
+  a.sk_records = int64_t(plan.sk_tiles) * L.k_blocks;
   // Token tiles per rasterization group: as many as keep the group's activation rows
   // within about half of L2, so that they are read from DRAM once.
   {
@@ -264,10 +331,10 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   a.ldy = ldy;
   if (need > 0) {
     a.ws = static_cast<float*>(ws);
-    a.ws_ld = L.N_pad;
-    a.ws_slice = split_slice_floats(L, M, plan);
-    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
-                                            int64_t(plan.splits) * a.ws_slice * 4);
+    a.max_contrib = plan.max_contrib;
+    a.counters = reinterpret_cast<int32_t*>(
+        static_cast<uint8_t*>(ws) +
+        cut_tiles(L, M, plan) * plan.max_contrib * int64_t(kTileN) * plan.token_tile * 4);
   }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
@@ -389,6 +456,8 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   if (g_force_tile) tt = g_force_tile;
   plan.token_tile = tt;
   plan.splits = 1;
+  plan.sk_tiles = 0;
+  plan.max_contrib = 0;
   plan.grid = dev->sms;
   CUtensorMap tmap;
   int x3d = 0;
@@ -439,11 +508,23 @@ qgemm_status qgemm_device_status(int32_t clear) {
   return static_cast<qgemm_status>(v);
 }
 
+qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]) {
+  Layout L;
+  if (!layout_of(desc, &L) || M <= 0 || out == nullptr) return QGEMM_ERR_INVALID_ARG;
+  const GemmPlan p = plan_dense(L, M, sms_or_default());
+  out[0] = p.token_tile;
+  out[1] = p.splits;
+  out[2] = p.sk_tiles;
+  out[3] = p.max_contrib;
+  out[4] = p.grid;
+  return QGEMM_OK;
+}
+
 qgemm_status qgemm_force_config(int32_t token_tile, int32_t splits) {
   if (token_tile != 0 && token_tile != 16 && token_tile != 32 && token_tile != 64 &&
       token_tile != 128 && token_tile != 256)
     return QGEMM_ERR_INVALID_ARG;
-  if (splits < 0 || splits > 64) return QGEMM_ERR_INVALID_ARG;
+  if (splits < -1 || splits > 64) return QGEMM_ERR_INVALID_ARG;
   g_force_tile = token_tile;
   g_force_splits = splits;
   return QGEMM_OK;

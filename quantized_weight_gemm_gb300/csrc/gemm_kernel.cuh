@@ -154,34 +154,46 @@ struct GemmCfg {
 };
 
 struct Unit {
-  int nt, mt, split, expert;
+  int nt, mt, expert;
   int kb0, kb1;            // record range [kb0, kb1)
   int64_t row0, row_end;
+  // Cut tiles only (ncontrib > 1): partial-sum slot tile_id * max_contrib + contrib, and
+  // the number of contributors whose arrivals complete the tile.
+  int tile_id, contrib, ncontrib;
 };
 
-__device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& a, int bnt, const int* prefix,
-                                            const int* offs) {
-  Unit w;
+// Token tile and weight tile of dense tile `tile` in rasterization order: groups of
+// group_m token tiles, the token tile changing fastest inside a group, so the CTAs running
+// at one time share a few weight tiles and the group's activation rows, which stay in L2.
+__device__ __forceinline__ void dense_tile_coords(int tile, const GemmArgs& a, Unit& w) {
   const int n_tiles = int(a.L.n_tiles);
+  const int per_group = a.group_m * n_tiles;
+  const int first_mt = (tile / per_group) * a.group_m;
+  const int gm = min(a.group_m, a.m_tiles - first_mt);
+  const int in = tile - (tile / per_group) * per_group;
+  w.mt = first_mt + in % gm;
+  w.nt = in / gm;
+}
+
+// The CTA whose stream-K record range holds record x of the S = sk_records: the largest i
+// with floor(i S / P) <= x.
+__device__ __forceinline__ int sk_cta_of(int64_t x, int64_t S, int P) {
+  return int(((x + 1) * P - 1) / S);
+}
+
+// Unit j (0, 1, ...) of this CTA; false once the CTA has no more.  Every warp role walks
+// the same sequence.
+__device__ __forceinline__ bool unit_at(int j, const GemmArgs& a, int bnt, int num_units,
+                                        const int* prefix, const int* offs, Unit& w) {
   const int k_blocks = int(a.L.k_blocks);
-  if (a.offsets == nullptr) {
-    // Splits of a tile are consecutive units.  Tiles run in groups of group_m token tiles:
-    // inside a group the token tile changes fastest, so the CTAs running at one time share
-    // a few weight tiles and the group's activation rows, which stay in L2.
-    w.split = u % a.splits;
-    const int tile = u / a.splits;
-    const int per_group = a.group_m * n_tiles;
-    const int first_mt = (tile / per_group) * a.group_m;
-    const int gm = min(a.group_m, a.m_tiles - first_mt);
-    const int in = tile - (tile / per_group) * per_group;
-    w.mt = first_mt + in % gm;
-    w.nt = in / gm;
-    w.expert = 0;
-    w.row0 = int64_t(w.mt) * bnt;
-    w.row_end = a.M;
-    w.kb0 = int(int64_t(w.split) * k_blocks / a.splits);
-    w.kb1 = int(int64_t(w.split + 1) * k_blocks / a.splits);
-  } else {
+  const int P = int(gridDim.x), cta = int(blockIdx.x);
+  w.tile_id = 0;
+  w.contrib = 0;
+  w.ncontrib = 1;
+  if (a.offsets != nullptr) {
+    const int u = cta + j * P;
+    if (u >= num_units) return false;
+    const int n_tiles = int(a.L.n_tiles);
     w.nt = u % n_tiles;
     const int gmt = u / n_tiles;
     int lo = 0, hi = a.E;                    // largest e with prefix[e] <= gmt
@@ -191,13 +203,56 @@ __device__ __forceinline__ Unit decode_unit(int u, const GemmArgs& a, int bnt, c
     }
     w.expert = lo;
     w.mt = gmt - prefix[lo];
-    w.split = 0;
     w.row0 = int64_t(offs[lo]) + int64_t(w.mt) * bnt;
     w.row_end = offs[lo + 1];
     w.kb0 = 0;
     w.kb1 = k_blocks;
+    return true;
   }
-  return w;
+  w.expert = 0;
+  int tile;
+  if (a.sk_tiles == 0) {
+    // (tile, split) units; the splits of a tile are consecutive units
+    const int u = cta + j * P;
+    if (u >= num_units) return false;
+    const int split = u % a.splits;
+    tile = u / a.splits;
+    w.kb0 = int(int64_t(split) * k_blocks / a.splits);
+    w.kb1 = int(int64_t(split + 1) * k_blocks / a.splits);
+    if (a.splits > 1) {
+      w.tile_id = tile;
+      w.contrib = split;
+      w.ncontrib = a.splits;
+    }
+  } else {
+    const int64_t S = a.sk_records;
+    const int64_t lo = int64_t(cta) * S / P, hi = int64_t(cta + 1) * S / P;
+    const int n_sk = hi > lo ? int((hi - 1) / k_blocks - lo / k_blocks + 1) : 0;
+    if (j < n_sk) {
+      // piece j of this CTA's record range: a part of stream-K tile t
+      const int t = int(lo / k_blocks) + j;
+      const int64_t t0 = int64_t(t) * k_blocks;
+      w.kb0 = j == 0 ? int(lo - t0) : 0;
+      w.kb1 = int(min(hi, t0 + k_blocks) - t0);
+      const int first = sk_cta_of(t0, S, P);
+      const int last = sk_cta_of(t0 + k_blocks - 1, S, P);
+      tile = t;
+      if (last > first) {
+        w.tile_id = t;
+        w.contrib = cta - first;
+        w.ncontrib = last - first + 1;
+      }
+    } else {
+      tile = a.sk_tiles + cta + (j - n_sk) * P;
+      if (tile >= a.m_tiles * int(a.L.n_tiles)) return false;
+      w.kb0 = 0;
+      w.kb1 = k_blocks;
+    }
+  }
+  dense_tile_coords(tile, a, w);
+  w.row0 = int64_t(w.mt) * bnt;
+  w.row_end = a.M;
+  return true;
 }
 
 __device__ __forceinline__ bool warp_all(bool v) { return __all_sync(0xffffffffu, v); }
@@ -433,8 +488,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       uint32_t pending = 0, pending_parity = 0;   // copies in flight, for the wind-down
       uint32_t g = 0;                             // stage counter of this CTA
       bool alive = true;
-      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
-        const Unit w = decode_unit(u, a, BNT, prefix, offs);
+      Unit w;
+      for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
         const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
                              (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
         for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
@@ -472,8 +527,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       Ring rx;
       uint32_t pending = 0, pending_parity = 0;
       bool alive = true;
-      for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
-        const Unit w = decode_unit(u, a, BNT, prefix, offs);
+      Unit w;
+      for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
         const int32_t row0 = int32_t(w.row0);
         const int nst = (w.kb1 - w.kb0) * kSub;
         for (int i0 = 0; i0 < nst; i0 += XQ) {
@@ -514,8 +569,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     uint32_t g0 = 0;                      // CTA stage counter at the unit start
     bool alive = true;
     const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
-    for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x, ++ui) {
-      const Unit w = decode_unit(u, a, BNT, prefix, offs);
+    Unit w;
+    for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       if (!warp_all(ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma))) break;
@@ -582,8 +637,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const int zoff = L.off_zeros - L.off_scales;
     uint32_t g0 = 0;                                       // CTA stage counter at the unit start
     bool alive = true;
-    for (int u = blockIdx.x; u < num_units && alive; u += gridDim.x) {
-      const Unit w = decode_unit(u, a, BNT, prefix, offs);
+    Unit w;
+    for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
       const int nst = (w.kb1 - w.kb0) * kSub;
       // Visit only this warpgroup's stages; ring slots and phases follow from the stage
       // counter (the ring depths are compile-time constants).
@@ -687,8 +742,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     };
     int ui = 0;
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
-    for (int u = blockIdx.x; u < num_units; u += gridDim.x, ++ui) {
-      const Unit w = decode_unit(u, a, BNT, prefix, offs);
+    Unit w;
+    for (int uj = 0; unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       const int nst = (w.kb1 - w.kb0) * kSub;
@@ -698,7 +753,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       ptx::tc_fence_after();
       const int64_t n = int64_t(w.nt) * kTileN + r;
       const bool n_ok = n < L.N;
-      const bool split = a.splits > 1;
+      const bool split = w.ncontrib > 1;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
       // Partial accumulators of the issuers that had a stage in this unit: the unit's
       // stages g0, g0 + 1, ... went to issuers (g0 + d) % kIssuers.
@@ -767,7 +822,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         }
         continue;
       }
-      // Split-K: store this split's FP32 partial tile into its slice of the workspace.
+      // Cut tile: store this contributor's FP32 partial tile into its slot of the
+      // workspace (row r of the slot is kTileN-major: BNT contiguous floats per weight row).
+      const int64_t slot_floats = int64_t(kTileN) * BNT;
+      float* my_row = a.ws + (int64_t(w.tile_id) * a.max_contrib + w.contrib) * slot_floats +
+                      int64_t(r) * BNT + eh * kCols;
 #pragma unroll 1
       for (int c = 0; c < kCols / kChunk; ++c) {
         uint32_t v[32];
@@ -776,48 +835,52 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           ptx::tc_fence_before();
           warp_arrive(&accempty[acc], lane);
         }
-        if (n_ok) {
 #pragma unroll
-          for (int j = 0; j < kChunk; ++j) {
-            const int64_t m = m_first + c * kChunk + j;
-            if (m < w.row_end)
-              __stcg(a.ws + int64_t(w.split) * a.ws_slice + m * a.ws_ld + n, __uint_as_float(v[j]));
-          }
-        }
+        for (int j = 0; j < kChunk; j += 4)
+          __stcg(reinterpret_cast<float4*>(my_row + c * kChunk + j),
+                 make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                             __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3])));
       }
-      // The last of the tile's splits to arrive sums the slices and converts.
+      // The last contributor to arrive sums the slots and converts.
       __threadfence();
       if (!epi_sync()) break;
       if (r == 0 && eh == 0) {
-        const int tile = w.mt * int(L.n_tiles) + w.nt;
-        const int prev = atomicAdd(&a.counters[tile], 1);
-        misc[4] = (prev == a.splits - 1) ? 1 : 0;
-        if (prev == a.splits - 1) a.counters[tile] = 0;
+        const int prev = atomicAdd(&a.counters[w.tile_id], 1);
+        misc[4] = (prev == w.ncontrib - 1) ? 1 : 0;
+        if (prev == w.ncontrib - 1) a.counters[w.tile_id] = 0;
       }
       if (!epi_sync()) break;
       if (misc[4]) {
-        // Sum the slices in split order (a fixed order: the result does not depend on
-        // which split arrived last), scale, convert.
+        // Sum in contributor order (fixed by the schedule, not by the arrival order), two
+        // contributors' loads in flight at a time, 16 columns per pass.
         __threadfence();
-        if (n_ok) {
-          const float cs2 = a.chan_scale != nullptr ? a.chan_scale[n] : 1.0f;
-          const int64_t m_lim = m_first + kCols < w.row_end ? m_first + kCols : w.row_end;
-          // 8 independent loads in flight per thread; rows of one warp are coalesced.
-          for (int64_t m0 = m_first; m0 < m_lim; m0 += 8) {
-            float v[8];
+        const float* row0p = a.ws + int64_t(w.tile_id) * a.max_contrib * slot_floats +
+                             int64_t(r) * BNT + eh * kCols;
+        const float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+        constexpr int kPass = kCols < 16 ? kCols : 16;
+#pragma unroll 1
+        for (int c0 = 0; c0 < kCols; c0 += kPass) {
+          float sum[kPass];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0.0f;
-            for (int sl = 0; sl < a.splits; ++sl) {
-              const float* src = a.ws + int64_t(sl) * a.ws_slice + n;
+          for (int j = 0; j < kPass; ++j) sum[j] = 0.0f;
+#pragma unroll 2
+          for (int q = 0; q < w.ncontrib; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(row0p + q * slot_floats + c0);
 #pragma unroll
-              for (int j = 0; j < 8; ++j)
-                if (m0 + j < m_lim) v[j] += __ldcg(src + (m0 + j) * a.ws_ld);
+            for (int j = 0; j < kPass / 4; ++j) {
+              const float4 x = __ldcg(src + j);
+              sum[4 * j] += x.x;
+              sum[4 * j + 1] += x.y;
+              sum[4 * j + 2] += x.z;
+              sum[4 * j + 3] += x.w;
             }
+          }
+          if (n_ok) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const int64_t m = m0 + j;
-              if (m < m_lim) {
-                float y = v[j] * cs2;
+            for (int j = 0; j < kPass; ++j) {
+              const int64_t m = m_first + c0 + j;
+              if (m < w.row_end) {
+                float y = sum[j] * cs2;
                 if (A8) y *= a.tok_scale[m];
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }

@@ -25,16 +25,27 @@ struct GemmArgs {
   const int32_t* offsets;      // MoE: device int32 [E+1]; nullptr for dense
   int32_t E;
   int64_t M;                   // dense rows (M) or MoE rows (R)
-  int32_t m_tiles, splits, num_units;   // dense schedule
-  int32_t group_m;             // dense: token tiles per rasterization group (>= 1)
+  // Dense schedule.  Tiles are numbered in rasterization order (groups of group_m token
+  // tiles, the token tile changing fastest inside a group).
+  //  - sk_tiles == 0: units = (tile, split) pairs, unit u on CTA u % grid; splits == 1 is
+  //    plain data-parallel, splits > 1 cuts every tile's K range into `splits` equal parts.
+  //  - sk_tiles > 0 ("stream-K"): the records of tiles [0, sk_tiles) are dealt out evenly
+  //    as contiguous ranges, CTA i taking records [i S / grid, (i + 1) S / grid) of the
+  //    S = sk_tiles * k_blocks; after its range a CTA takes the whole tiles
+  //    sk_tiles + i, sk_tiles + i + grid, ...
+  int32_t m_tiles, splits, num_units;
+  int32_t group_m;             // token tiles per rasterization group (>= 1)
+  int32_t sk_tiles;
+  int64_t sk_records;          // sk_tiles * k_blocks
   const float* chan_scale;     // [N] or nullptr
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
-  float* ws;                   // split-K partial sums [splits][m_tiles * tile_m][ws_ld]
-  int32_t* counters;           // split-K arrival counters [m_tiles * n_tiles]
-  int64_t ws_ld;
-  int64_t ws_slice;            // floats per split slice of ws
+  // Partial sums of the tiles whose K range is cut: slot (tile_id * max_contrib + j) holds
+  // contributor j's FP32 tile [128 weight rows][token_tile], row-major.
+  float* ws;
+  int32_t* counters;           // arrival counter per cut tile (zero between calls)
+  int32_t max_contrib;
   int* status;
   uint64_t timeout_ns;
   int32_t x_3d;                // X map is 3-D (a box covers several stages); else 2-D
@@ -42,7 +53,9 @@ struct GemmArgs {
 
 struct GemmPlan {
   int token_tile;              // MMA N: 16, 32, 64, 128 or 256 rows of X per tile
-  int splits;                  // split-K factor (dense)
+  int splits;                  // split-K factor (dense, uniform cut; 1 = none)
+  int sk_tiles;                // > 0: stream-K over the first sk_tiles tiles (splits == 1)
+  int max_contrib;             // partial-sum slots per cut tile (0 when nothing is cut)
   int grid;                    // persistent CTAs
 };
 

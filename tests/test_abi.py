@@ -95,6 +95,7 @@ def test_argument_errors_before_any_launch(L):
     # FP8 entry point with a BF16-activation descriptor
     assert L.qgemm_w4a8(ctypes.byref(d), P(256), P(256), 4, 512, P(256), None, P(256), 256, None, 0, None) == 1
     assert L.qgemm_force_config(48, 0) == 1
+    assert L.qgemm_force_config(0, -2) == 1
     assert L.qgemm_force_config(0, 0) == 0
 
 
@@ -105,3 +106,54 @@ def test_product_package_does_not_import_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert "oracle" not in text.replace("the oracle", ""), f
+
+
+def _sk_contributors(T, kb, P):
+    """Stream-K as the header defines it, walked record by record: CTA i takes records
+    [floor(i S / P), floor((i + 1) S / P)) of the S = T kb records of the cut tiles."""
+    S = T * kb
+    owners = [set() for _ in range(T)]
+    covered = 0
+    for i in range(P):
+        lo, hi = i * S // P, (i + 1) * S // P
+        for x in range(lo, hi):
+            owners[x // kb].add(i)
+        covered += hi - lo
+    assert covered == S
+    return max(len(o) for o in owners)
+
+
+@pytest.mark.parametrize("N,K,M", [(28672, 1152, 16), (28672, 8192, 100), (8192, 28672, 16),
+                                   (4096, 7168, 1), (384, 1024, 100), (7168, 2048, 48)])
+def test_stream_k_plan(L, N, K, M):
+    """The forced stream-K plan of the dense path: leftover tiles = T mod P (all T when
+    T < P), and partial-sum slots = the most CTAs whose record ranges meet one tile."""
+    d = qg.WeightDesc("uint4_zp", N, K, 128)
+    P = 152
+    qg.force_config(16, -1)
+    try:
+        p = qg.plan(d, M)
+        ws = qg.workspace_bytes(d, M)
+    finally:
+        qg.force_config(0, 0)
+    T = -(-M // 16) * -(-N // 128)
+    kb = -(-K // 128)
+    sk = T if T < P else T % P
+    assert p["token_tile"] == 16 and p["splits"] == 1 and p["grid"] == P
+    assert p["sk_tiles"] == sk
+    c = _sk_contributors(sk, kb, P)
+    assert p["max_contrib"] == (c if c > 1 else 0)
+    if c > 1:
+        assert ws >= sk * c * 128 * 16 * 4 + 4 * sk
+
+
+def test_plan_defaults_are_valid(L):
+    for (N, K) in [(28672, 8192), (8192, 28672), (4096, 7168), (7168, 2048)]:
+        d = qg.WeightDesc("uint4_zp", N, K, 128)
+        for M in (1, 16, 64, 256, 1024, 8192):
+            p = qg.plan(d, M)
+            assert p["token_tile"] in (16, 32, 64, 128, 256)
+            assert p["splits"] >= 1 and 0 < p["grid"] <= 152
+            assert p["sk_tiles"] == 0 or p["splits"] == 1
+            assert (p["max_contrib"] > 0) == (p["splits"] > 1 or p["sk_tiles"] > 0)
+            assert qg.workspace_bytes(d, M) >= (4 if p["max_contrib"] else 0)

@@ -129,9 +129,10 @@ def test_one_hot_columns_exact(wfmt, group):
 
 
 @pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
-@pytest.mark.parametrize("splits", [1, 2, 3, 7])
+@pytest.mark.parametrize("splits", [1, 2, 3, 7, -1])
 def test_every_dispatch_entry(tile, splits):
-    """Each (token tile, split-K) configuration the dispatcher can pick, forced."""
+    """Each (token tile, schedule) configuration the dispatcher can pick, forced: uniform K
+    cuts and stream-K (-1; here every tile is shared by up to eight CTAs)."""
     qg = _qg()
     r = WL.rng(25)
     M, N, K = 100, 384, 1024
@@ -150,14 +151,16 @@ def test_every_dispatch_entry(tile, splits):
 
 # ------------------------------------------------------------------------------- W4A8
 
-@pytest.mark.parametrize("splits", [2, 3, 5])
-def test_many_units_with_odd_stage_counts(splits):
+@pytest.mark.parametrize("M,splits", [(16, 2), (16, 3), (16, 5), (16, -1), (100, -1)])
+def test_many_units_with_odd_stage_counts(M, splits):
     """Many units per CTA whose stage counts are odd or differ between units: the stage
     to warp assignment runs on across unit boundaries and must keep every ring slot with
-    fixed owners (a slot shared by two waiters lets one of them pass a wait a phase early)."""
+    fixed owners (a slot shared by two waiters lets one of them pass a wait a phase early).
+    Stream-K (-1) here cuts the 72 (M = 16) or 48 (M = 100, seven token tiles) leftover
+    tiles into pieces of a few K blocks, then runs whole tiles."""
     qg = _qg()
     r = WL.rng(30)
-    M, N, K = 16, 28672, 1152                         # 224 weight tiles x 9 K-blocks
+    N, K = 28672, 1152                                # 224 weight tiles x 9 K-blocks
     x = WL.gen_x(r, M, K)
     w = WL.gen_weights(r, "uint4_zp", N, K)
     ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)

@@ -372,7 +372,8 @@ def sweep_moe(device, flush, peaks):
                 X = torch.from_numpy(ins[name].view(np.int16)).view(torch.bfloat16).to(device)
                 Y = torch.empty(R, N, dtype=torch.bfloat16, device=device)
                 d, p = descs[name], packs[name]
-                ms = time_one(lambda: qg.moe_grouped(d, p, E, X, off, out=Y), flush)
+                wsp = qg.moe_workspace(d, E, R, device=device)
+                ms = time_one(lambda: qg.moe_grouped(d, p, E, X, off, out=Y, ws=wsp), flush)
                 wb = active * mx_weight_bytes(N, K)
                 r[name + "_us"] = round(ms * 1e3, 2)
                 tot_ms += ms

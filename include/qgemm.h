@@ -170,6 +170,12 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
  *   X              : device [R, ldx] sorted rows; padding rows should be zero
  *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
  *   Y              : device BF16 [R, ldy]; rows of every expert are written
+ *   ws, ws_bytes   : optional device workspace, 256-byte aligned and zero-filled before
+ *                    its first use (calls leave it reusable, as for qgemm_w4a16).  With
+ *                    ws_bytes >= qgemm_moe_workspace_bytes(desc, E, R) the kernel may cut
+ *                    the K range of the tiles left over after whole rounds of tiles over
+ *                    several CTAs (stream-K), which evens out the work when few tiles
+ *                    exist; with NULL (or less) every CTA runs whole tiles.
  * "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths; tokens are
  * distributed over experts and the work per expert varies with the load).
  */
@@ -177,6 +183,13 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
                                int32_t afmt, const void* X, int64_t R, int64_t ldx,
                                const float* tok_scale, const int32_t* expert_offsets,
                                void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes that let qgemm_moe_grouped use stream-K for E experts and R sorted rows
+ * (token tile from R / E): FP32 partial-sum slots for twice the SM count plus one arrival
+ * counter per SM.  0 for an invalid descriptor, E < 1 or R <= 0.
+ */
+size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R);
 
 /*
  * Test hook: unpack a packed matrix back to BF16 W[n, k] = RNE_bf16(dequant) through the

@@ -14,7 +14,7 @@ import torch
 __all__ = [
     "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
-    "force_config", "plan", "check_desc", "WFMT", "AFMT", "EXPORTS",
+    "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "check_desc", "WFMT", "AFMT", "EXPORTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -25,7 +25,8 @@ AFMT = {"bf16": 0, "fp8": 1}
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
-           "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan")
+           "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
+           "qgemm_moe_workspace_bytes")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -94,6 +95,7 @@ def lib():
         "qgemm_force_config": (ctypes.c_int, [I32, I32]),
         "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
+        "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -225,9 +227,19 @@ def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None):
     return out
 
 
-def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None):
+def moe_workspace_bytes(desc, E, R):
+    d = desc.c()
+    return int(lib().qgemm_moe_workspace_bytes(ctypes.byref(d), int(E), int(R)))
+
+
+def moe_workspace(desc, E, R, device="cuda"):
+    """A zero-filled workspace that lets qgemm_moe_grouped use stream-K (reusable)."""
+    return torch.zeros(max(moe_workspace_bytes(desc, E, R), 256), dtype=torch.uint8, device=device)
+
+
+def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None):
     """MoE grouped GEMM over expert-sorted rows X [R, K] (BF16, or uint8 e4m3 with
-    tok_scale); offsets: int32 [E+1] on the device."""
+    tok_scale); offsets: int32 [E+1] on the device; ws: optional moe_workspace()."""
     fp8 = X.dtype == torch.uint8
     _need(offsets, "offsets", torch.int32)
     _row_major(X, "X")
@@ -235,9 +247,10 @@ def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None):
     if out is None:
         out = torch.empty(R, desc.N, dtype=torch.bfloat16, device=X.device)
     d = desc.c()
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().qgemm_moe_grouped(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
                                    _ptr(X), R, X.stride(0), _ptr(tok_scale), _ptr(offsets),
-                                   _ptr(out), out.stride(0), None, 0, _stream()), "moe_grouped")
+                                   _ptr(out), out.stride(0), _ptr(ws), wsb, _stream()), "moe_grouped")
     return out
 
 

@@ -146,7 +146,15 @@ double plan_cost_us(const Layout& L, int64_t M, int ti, int splits, int sms) {
   return kCallUs + double(per_cta) * unit;
 }
 
+// The kernel's stream-K arithmetic is 32-bit: (record + 1) * SMs must stay below 2^32 for
+// the fewer than SMs cut tiles (a limit far above practical K).
+bool sk_fits(const Layout& L, int sms) {
+  return uint64_t(sms) * uint64_t(sms) * uint64_t(L.k_blocks) < (uint64_t(1) << 32);
+}
+
 double sk_cost_us(const Layout& L, int64_t M, int ti, int sms, SkShape* out) {
+  *out = SkShape();
+  if (!sk_fits(L, sms)) return 1e300;
   const int64_t tt = kTiles[ti];
   const int64_t T = (M + tt - 1) / tt * L.n_tiles;
   const SkShape sh = sk_shape(T, L.k_blocks, sms);
@@ -204,18 +212,40 @@ GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
   return p;
 }
 
-// Partial-sum slots and arrival counters of the cut tiles: uniform cuts cut every tile,
-// stream-K the sk_tiles leftover tiles.
-int64_t cut_tiles(const Layout& L, int64_t M, const GemmPlan& p) {
-  if (p.max_contrib == 0) return 0;
-  if (p.sk_tiles > 0) return p.sk_tiles;
-  return (M + p.token_tile - 1) / p.token_tile * L.n_tiles;
+// Partial-sum slots and arrival counters of the cut tiles: a uniform cut of s parts needs
+// s slots per tile, stream-K fewer than sk_tiles + grid slots (see the kernel's unit_at).
+void cut_sizes(const Layout& L, int64_t M, const GemmPlan& p, int64_t* slots, int64_t* counters) {
+  *slots = *counters = 0;
+  if (p.sk_tiles > 0) {
+    if (p.max_contrib == 0) return;
+    *slots = p.sk_tiles + p.grid;
+    *counters = p.sk_tiles;
+  } else if (p.splits > 1) {
+    *counters = (M + p.token_tile - 1) / p.token_tile * L.n_tiles;
+    *slots = *counters * p.splits;
+  }
 }
 
+int64_t slot_bytes(int token_tile) { return int64_t(kTileN) * token_tile * 4; }
+
 int64_t split_ws_bytes(const Layout& L, int64_t M, const GemmPlan& p) {
-  const int64_t n = cut_tiles(L, M, p);
-  if (n == 0) return 0;
-  return n * p.max_contrib * int64_t(kTileN) * p.token_tile * 4 + round_up(n * 4, 256);
+  int64_t slots, counters;
+  cut_sizes(L, M, p, &slots, &counters);
+  if (slots == 0) return 0;
+  return slots * slot_bytes(p.token_tile) + round_up(counters * 4, 256);
+}
+
+// MoE: the token tile from the average rows per expert; the stream-K workspace holds
+// 2 * SMs slots and SMs counters.
+int moe_token_tile(int64_t R, int32_t E) {
+  const int64_t avg = R / E;
+  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  if (g_force_tile) tt = g_force_tile;
+  return tt;
+}
+
+int64_t moe_ws_bytes(int tt, int sms) {
+  return 2 * int64_t(sms) * slot_bytes(tt) + round_up(int64_t(sms) * 4, 256);
 }
 
 typedef PFN_cuTensorMapEncodeTiled_v12000 EncodeFn;
@@ -317,7 +347,6 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   a.splits = plan.splits;
   a.num_units = plan.sk_tiles > 0 ? plan.grid : int(int64_t(a.m_tiles) * L.n_tiles * plan.splits);
   a.sk_tiles = plan.sk_tiles;
-  a.sk_records = int64_t(plan.sk_tiles) * L.k_blocks;
   // Token tiles per rasterization group: as many as keep the group's activation rows
   // within about half of L2, so that they are read from DRAM once.
   {
@@ -330,11 +359,11 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   a.Y = Y;
   a.ldy = ldy;
   if (need > 0) {
+    int64_t slots, counters;
+    cut_sizes(L, M, plan, &slots, &counters);
     a.ws = static_cast<float*>(ws);
-    a.max_contrib = plan.max_contrib;
-    a.counters = reinterpret_cast<int32_t*>(
-        static_cast<uint8_t*>(ws) +
-        cut_tiles(L, M, plan) * plan.max_contrib * int64_t(kTileN) * plan.token_tile * 4);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
+                                            slots * slot_bytes(plan.token_tile));
   }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
@@ -433,8 +462,6 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
                                int32_t afmt, const void* X, int64_t R, int64_t ldx,
                                const float* tok_scale, const int32_t* expert_offsets,
                                void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws;
-  (void)ws_bytes;
   Layout L;
   if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
   const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
@@ -451,9 +478,7 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
   GemmPlan plan;
-  const int64_t avg = R / E;
-  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
-  if (g_force_tile) tt = g_force_tile;
+  const int tt = moe_token_tile(R, E);
   plan.token_tile = tt;
   plan.splits = 1;
   plan.sk_tiles = 0;
@@ -475,10 +500,24 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   a.tok_scale = tok_scale;
   a.Y = Y;
   a.ldy = ldy;
+  // Stream-K needs the whole bound; a smaller (or no) workspace keeps whole tiles.
+  if (ws != nullptr && g_force_splits != 1 && sk_fits(L, plan.grid) &&
+      int64_t(ws_bytes) >= moe_ws_bytes(tt, plan.grid)) {
+    if (!aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+    a.ws = static_cast<float*>(ws);
+    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
+                                            2 * int64_t(plan.grid) * slot_bytes(tt));
+  }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
   cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
+}
+
+size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R) {
+  Layout L;
+  if (!layout_of(desc, &L) || E < 1 || R <= 0) return 0;
+  return size_t(moe_ws_bytes(moe_token_tile(R, E), sms_or_default()));
 }
 
 qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,

@@ -157,101 +157,135 @@ struct Unit {
   int nt, mt, expert;
   int kb0, kb1;            // record range [kb0, kb1)
   int64_t row0, row_end;
-  // Cut tiles only (ncontrib > 1): partial-sum slot tile_id * max_contrib + contrib, and
-  // the number of contributors whose arrivals complete the tile.
-  int tile_id, contrib, ncontrib;
+  // Cut tiles only (ncontrib > 1): arrival counter tile_id; contributor j of the tile
+  // keeps its partial sums in workspace slot slot0 + j, j = contrib.
+  int tile_id, slot0, contrib, ncontrib;
 };
 
-// Token tile and weight tile of dense tile `tile` in rasterization order: groups of
-// group_m token tiles, the token tile changing fastest inside a group, so the CTAs running
-// at one time share a few weight tiles and the group's activation rows, which stay in L2.
-__device__ __forceinline__ void dense_tile_coords(int tile, const GemmArgs& a, Unit& w) {
+// The schedule of one launch (the same in every CTA; MoE: from the expert offsets) and
+// this CTA's part of it, computed once.  Stream-K record counts stay below 2^31 / SMs
+// (fewer than SMs tiles of at most 2^16 K blocks), so 32-bit arithmetic is exact.
+struct Sched {                 // 7 words: fits misc[8..14] of the kernel's shared memory
+  int num_units;           // uniform schedule: units dealt round-robin
+  int tiles;               // output tiles
+  int sk_tiles;            // > 0: stream-K over tiles [0, sk_tiles), then whole tiles
+  uint32_t S;              // stream-K records, sk_tiles * k_blocks
+  int lo, hi;              // this CTA's stream-K records [lo, hi)
+  int n_sk;                // ... and the pieces (tiles) they fall into
+};
+
+static_assert(sizeof(Sched) <= 8 * sizeof(int), "schedule must fit misc[8..15]");
+
+__device__ __forceinline__ Sched make_sched(int num_units, int tiles, int sk_tiles, int k_blocks) {
+  Sched sc;
+  sc.num_units = num_units;
+  sc.tiles = tiles;
+  sc.sk_tiles = sk_tiles;
+  sc.S = uint32_t(sk_tiles) * uint32_t(k_blocks);
+  const uint32_t P = gridDim.x, cta = blockIdx.x;
+  sc.lo = int(cta * sc.S / P);
+  sc.hi = int((cta + 1) * sc.S / P);
+  sc.n_sk = sc.hi > sc.lo ? (sc.hi - 1) / k_blocks - sc.lo / k_blocks + 1 : 0;
+  return sc;
+}
+
+// Coordinates of output tile `tile`.  Dense: rasterization order, groups of group_m token
+// tiles with the token tile changing fastest, so the CTAs running at one time share a few
+// weight tiles and the group's activation rows, which stay in L2.  MoE: m-tiles of the
+// experts in order, each with its n_tiles weight tiles; `e_hint` is the expert of this
+// role's previous tile (tiles only grow along a role's sequence), -1 at the start.
+__device__ __forceinline__ void tile_coords(int tile, const GemmArgs& a, int bnt,
+                                            const int* prefix, const int* offs, int& e_hint,
+                                            Unit& w) {
   const int n_tiles = int(a.L.n_tiles);
-  const int per_group = a.group_m * n_tiles;
-  const int first_mt = (tile / per_group) * a.group_m;
-  const int gm = min(a.group_m, a.m_tiles - first_mt);
-  const int in = tile - (tile / per_group) * per_group;
-  w.mt = first_mt + in % gm;
-  w.nt = in / gm;
-}
-
-// The CTA whose stream-K record range holds record x of the S = sk_records: the largest i
-// with floor(i S / P) <= x.
-__device__ __forceinline__ int sk_cta_of(int64_t x, int64_t S, int P) {
-  return int(((x + 1) * P - 1) / S);
-}
-
-// Unit j (0, 1, ...) of this CTA; false once the CTA has no more.  Every warp role walks
-// the same sequence.
-__device__ __forceinline__ bool unit_at(int j, const GemmArgs& a, int bnt, int num_units,
-                                        const int* prefix, const int* offs, Unit& w) {
-  const int k_blocks = int(a.L.k_blocks);
-  const int P = int(gridDim.x), cta = int(blockIdx.x);
-  w.tile_id = 0;
-  w.contrib = 0;
-  w.ncontrib = 1;
-  if (a.offsets != nullptr) {
-    const int u = cta + j * P;
-    if (u >= num_units) return false;
-    const int n_tiles = int(a.L.n_tiles);
-    w.nt = u % n_tiles;
-    const int gmt = u / n_tiles;
-    int lo = 0, hi = a.E;                    // largest e with prefix[e] <= gmt
+  if (a.offsets == nullptr) {
+    const int per_group = a.group_m * n_tiles;
+    const int first_mt = (tile / per_group) * a.group_m;
+    const int gm = min(a.group_m, a.m_tiles - first_mt);
+    const int in = tile - (tile / per_group) * per_group;
+    w.mt = first_mt + in % gm;
+    w.nt = in / gm;
+    w.expert = 0;
+    w.row0 = int64_t(w.mt) * bnt;
+    w.row_end = a.M;
+  } else {
+    w.nt = tile % n_tiles;
+    const int gmt = tile / n_tiles;
+    // the largest e < E with prefix[e] <= gmt (empty experts have prefix[e] == prefix[e+1]);
+    // binary search above the previous answer (many empty experts may lie in between)
+    int lo = e_hint > 0 ? e_hint : 0, hi = a.E;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (prefix[mid] <= gmt) lo = mid; else hi = mid;
     }
-    w.expert = lo;
-    w.mt = gmt - prefix[lo];
-    w.row0 = int64_t(offs[lo]) + int64_t(w.mt) * bnt;
-    w.row_end = offs[lo + 1];
-    w.kb0 = 0;
-    w.kb1 = k_blocks;
-    return true;
+    const int e = lo;
+    e_hint = e;
+    w.expert = e;
+    w.mt = gmt - prefix[e];
+    w.row0 = int64_t(offs[e]) + int64_t(w.mt) * bnt;
+    w.row_end = offs[e + 1];
   }
-  w.expert = 0;
+}
+
+// The CTA whose stream-K record range holds record x of the S: the largest i with
+// floor(i S / P) <= x.
+__device__ __forceinline__ int sk_cta_of(uint32_t x, uint32_t S) {
+  return int(((x + 1) * gridDim.x - 1) / S);
+}
+
+// Unit j (0, 1, ...) of this CTA; false once the CTA has no more.  Every warp role walks
+// the same sequence.
+//  - uniform: unit u = cta + j P; dense units are (tile, split) pairs, a tile's splits
+//    consecutive, splits == 1 meaning whole tiles; MoE units are whole tiles.
+//  - stream-K: CTA i first takes records [i S / P, (i + 1) S / P) of the S records of
+//    tiles [0, sk_tiles) (pieces of at most two or three tiles), then the whole tiles
+//    sk_tiles + i, sk_tiles + i + P, ...  The contributors of a cut tile t are the CTAs
+//    first(t) .. last(t) whose ranges meet it; their slots t + first(t) + j never overlap
+//    those of another tile, so sk_tiles + P slots hold them all.
+__device__ __forceinline__ bool unit_at(int j, const GemmArgs& a, const Sched& sc, int bnt,
+                                        const int* prefix, const int* offs, int& e_hint,
+                                        Unit& w) {
+  const int k_blocks = int(a.L.k_blocks);
+  const int P = int(gridDim.x), cta = int(blockIdx.x);
+  w.tile_id = 0;
+  w.slot0 = 0;
+  w.contrib = 0;
+  w.ncontrib = 1;
+  w.kb0 = 0;
+  w.kb1 = k_blocks;
   int tile;
-  if (a.sk_tiles == 0) {
-    // (tile, split) units; the splits of a tile are consecutive units
+  if (sc.sk_tiles == 0) {
     const int u = cta + j * P;
-    if (u >= num_units) return false;
-    const int split = u % a.splits;
-    tile = u / a.splits;
-    w.kb0 = int(int64_t(split) * k_blocks / a.splits);
-    w.kb1 = int(int64_t(split + 1) * k_blocks / a.splits);
-    if (a.splits > 1) {
+    if (u >= sc.num_units) return false;
+    tile = u;
+    if (a.offsets == nullptr && a.splits > 1) {
+      const int split = u % a.splits;
+      tile = u / a.splits;
+      w.kb0 = split * k_blocks / a.splits;
+      w.kb1 = (split + 1) * k_blocks / a.splits;
       w.tile_id = tile;
+      w.slot0 = tile * a.splits;
       w.contrib = split;
       w.ncontrib = a.splits;
     }
-  } else {
-    const int64_t S = a.sk_records;
-    const int64_t lo = int64_t(cta) * S / P, hi = int64_t(cta + 1) * S / P;
-    const int n_sk = hi > lo ? int((hi - 1) / k_blocks - lo / k_blocks + 1) : 0;
-    if (j < n_sk) {
-      // piece j of this CTA's record range: a part of stream-K tile t
-      const int t = int(lo / k_blocks) + j;
-      const int64_t t0 = int64_t(t) * k_blocks;
-      w.kb0 = j == 0 ? int(lo - t0) : 0;
-      w.kb1 = int(min(hi, t0 + k_blocks) - t0);
-      const int first = sk_cta_of(t0, S, P);
-      const int last = sk_cta_of(t0 + k_blocks - 1, S, P);
-      tile = t;
-      if (last > first) {
-        w.tile_id = t;
-        w.contrib = cta - first;
-        w.ncontrib = last - first + 1;
-      }
-    } else {
-      tile = a.sk_tiles + cta + (j - n_sk) * P;
-      if (tile >= a.m_tiles * int(a.L.n_tiles)) return false;
-      w.kb0 = 0;
-      w.kb1 = k_blocks;
+  } else if (j < sc.n_sk) {
+    tile = sc.lo / k_blocks + j;
+    const int t0 = tile * k_blocks;
+    w.kb0 = j == 0 ? sc.lo - t0 : 0;
+    w.kb1 = min(sc.hi, t0 + k_blocks) - t0;
+    const int first = sk_cta_of(uint32_t(t0), sc.S);
+    const int last = sk_cta_of(uint32_t(t0 + k_blocks - 1), sc.S);
+    if (last > first) {
+      w.tile_id = tile;
+      w.slot0 = tile + first;
+      w.contrib = cta - first;
+      w.ncontrib = last - first + 1;
     }
+  } else {
+    tile = sc.sk_tiles + cta + (j - sc.n_sk) * P;
+    if (tile >= sc.tiles) return false;
   }
-  dense_tile_coords(tile, a, w);
-  w.row0 = int64_t(w.mt) * bnt;
-  w.row_end = a.M;
+  tile_coords(tile, a, bnt, prefix, offs, e_hint, w);
   return true;
 }
 
@@ -355,7 +389,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   uint64_t* accempty = accfull + C::kNumAcc;
   uint64_t* drain = accempty + C::kNumAcc;
   uint64_t* epibar = drain + 1;                          // epilogue rendezvous (split-K)
-  int* misc = reinterpret_cast<int*>(epibar + 1);        // [0] tmem [1] abort [2] ok [3] units [4] last
+  // misc: [0] tmem [1] abort [2] ok [3] units [4] last arriver [8..14] schedule (Sched)
+  int* misc = reinterpret_cast<int*>(epibar + 1);
+                                                         // [8..14] schedule (Sched)
   int* prefix = misc + 16;                               // MoE: m-tiles before expert e
   int* offs = prefix + (kMaxExperts + 1);                // MoE: row offsets
 
@@ -455,12 +491,25 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (a.offsets != nullptr) num_units = misc[3] * int(L.n_tiles);
+  int tiles = a.m_tiles * int(L.n_tiles), sk_tiles = a.sk_tiles;
+  if (a.offsets != nullptr) {
+    // MoE: the tile count is known only now.  With a workspace, stream-K over the leftover
+    // tiles when every CTA's share is at least 16 K blocks (shorter pieces cost more in
+    // partial sums than the better balance saves).
+    num_units = tiles = misc[3] * int(L.n_tiles);
+    const int P = int(gridDim.x);
+    const int left = tiles < P ? tiles : tiles % P;
+    sk_tiles = (a.ws != nullptr && int64_t(left) * L.k_blocks >= 16 * int64_t(P)) ? left : 0;
+  }
   const uint32_t tbase = static_cast<uint32_t>(misc[0]);
-  if (!misc[2] || int(blockIdx.x) >= num_units) {           // nothing to do: give TMEM back
+  if (!misc[2] || (sk_tiles == 0 && int(blockIdx.x) >= num_units)) {   // nothing to do
     if (warp == kEpiWarp0) ptx::tmem_dealloc(tbase, C::kTmemCols);
     return;
   }
+  // The schedule lives in shared memory (written once, read once per unit) rather than in
+  // registers of every role.
+  Sched* sched = reinterpret_cast<Sched*>(misc + 8);
+  if (threadIdx.x == 0) *sched = make_sched(num_units, tiles, sk_tiles, int(L.k_blocks));
   volatile int* abort_flag = &misc[1];
   const uint64_t T = a.timeout_ns;
 
@@ -475,6 +524,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   }
   __syncthreads();
   ptx::tc_fence_after();
+  const Sched& sc = *sched;
 
   if (warp >= RO::kRecProducerWarp0) {
     // ---------------------------------------------------------------- record producers
@@ -489,7 +539,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       uint32_t g = 0;                             // stage counter of this CTA
       bool alive = true;
       Unit w;
-      for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
+      int e_hint = -1;
+      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
         const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
                              (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
         for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
@@ -528,7 +579,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       uint32_t pending = 0, pending_parity = 0;
       bool alive = true;
       Unit w;
-      for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
+      int e_hint = -1;
+      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
         const int32_t row0 = int32_t(w.row0);
         const int nst = (w.kb1 - w.kb0) * kSub;
         for (int i0 = 0; i0 < nst; i0 += XQ) {
@@ -570,7 +622,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     bool alive = true;
     const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
     Unit w;
-    for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj, ++ui) {
+    int e_hint = -1;
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       if (!warp_all(ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma))) break;
@@ -638,7 +691,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     uint32_t g0 = 0;                                       // CTA stage counter at the unit start
     bool alive = true;
     Unit w;
-    for (int uj = 0; alive && unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj) {
+    int e_hint = -1;
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
       const int nst = (w.kb1 - w.kb0) * kSub;
       // Visit only this warpgroup's stages; ring slots and phases follow from the stage
       // counter (the ring depths are compile-time constants).
@@ -743,7 +797,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     int ui = 0;
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
     Unit w;
-    for (int uj = 0; unit_at(uj, a, BNT, num_units, prefix, offs, w); ++uj, ++ui) {
+    int e_hint = -1;
+    for (int uj = 0; unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       const int nst = (w.kb1 - w.kb0) * kSub;
@@ -825,8 +880,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       // Cut tile: store this contributor's FP32 partial tile into its slot of the
       // workspace (row r of the slot is kTileN-major: BNT contiguous floats per weight row).
       const int64_t slot_floats = int64_t(kTileN) * BNT;
-      float* my_row = a.ws + (int64_t(w.tile_id) * a.max_contrib + w.contrib) * slot_floats +
-                      int64_t(r) * BNT + eh * kCols;
+      float* my_row = a.ws + int64_t(w.slot0 + w.contrib) * slot_floats + int64_t(r) * BNT +
+                      eh * kCols;
 #pragma unroll 1
       for (int c = 0; c < kCols / kChunk; ++c) {
         uint32_t v[32];
@@ -854,8 +909,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         // Sum in contributor order (fixed by the schedule, not by the arrival order), two
         // contributors' loads in flight at a time, 16 columns per pass.
         __threadfence();
-        const float* row0p = a.ws + int64_t(w.tile_id) * a.max_contrib * slot_floats +
-                             int64_t(r) * BNT + eh * kCols;
+        const float* row0p = a.ws + int64_t(w.slot0) * slot_floats + int64_t(r) * BNT +
+                             eh * kCols;
         const float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
         constexpr int kPass = kCols < 16 ? kCols : 16;
 #pragma unroll 1

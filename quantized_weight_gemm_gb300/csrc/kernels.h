@@ -32,20 +32,20 @@ struct GemmArgs {
   //  - sk_tiles > 0 ("stream-K"): the records of tiles [0, sk_tiles) are dealt out evenly
   //    as contiguous ranges, CTA i taking records [i S / grid, (i + 1) S / grid) of the
   //    S = sk_tiles * k_blocks; after its range a CTA takes the whole tiles
-  //    sk_tiles + i, sk_tiles + i + grid, ...
+  //    sk_tiles + i, sk_tiles + i + grid, ...  (MoE: decided in the kernel.)
   int32_t m_tiles, splits, num_units;
   int32_t group_m;             // token tiles per rasterization group (>= 1)
   int32_t sk_tiles;
-  int64_t sk_records;          // sk_tiles * k_blocks
   const float* chan_scale;     // [N] or nullptr
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
-  // Partial sums of the tiles whose K range is cut: slot (tile_id * max_contrib + j) holds
-  // contributor j's FP32 tile [128 weight rows][token_tile], row-major.
+  // Partial sums of the tiles whose K range is cut over several CTAs: one slot per
+  // contributor, an FP32 tile [128 weight rows][token_tile], row-major (uniform cuts: slot
+  // tile * splits + split; stream-K: slot t + first(t) + j, fewer than sk_tiles + grid).
+  // MoE: optional; when given, the kernel may run stream-K (2 * grid slots).
   float* ws;
   int32_t* counters;           // arrival counter per cut tile (zero between calls)
-  int32_t max_contrib;
   int* status;
   uint64_t timeout_ns;
   int32_t x_3d;                // X map is 3-D (a box covers several stages); else 2-D

@@ -120,6 +120,9 @@ def _sk_contributors(T, kb, P):
             owners[x // kb].add(i)
         covered += hi - lo
     assert covered == S
+    # partial-sum slots: contributor j of tile t uses slot t + min(owners) + j
+    top = max(t + min(o) + len(o) - 1 for t, o in enumerate(owners))
+    assert top < T + P
     return max(len(o) for o in owners)
 
 
@@ -144,7 +147,7 @@ def test_stream_k_plan(L, N, K, M):
     c = _sk_contributors(sk, kb, P)
     assert p["max_contrib"] == (c if c > 1 else 0)
     if c > 1:
-        assert ws >= sk * c * 128 * 16 * 4 + 4 * sk
+        assert ws >= (sk + P) * 128 * 16 * 4 + 4 * sk
 
 
 def test_plan_defaults_are_valid(L):
@@ -157,3 +160,11 @@ def test_plan_defaults_are_valid(L):
             assert p["sk_tiles"] == 0 or p["splits"] == 1
             assert (p["max_contrib"] > 0) == (p["splits"] > 1 or p["sk_tiles"] > 0)
             assert qg.workspace_bytes(d, M) >= (4 if p["max_contrib"] else 0)
+
+
+def test_moe_workspace_bytes(L):
+    d = qg.WeightDesc("mxfp4", 4096, 7168, 32)
+    assert qg.moe_workspace_bytes(d, 256, 8) == 2 * 152 * 128 * 16 * 4 + 768   # 16-row tiles, counters rounded up to 256 B
+    assert qg.moe_workspace_bytes(d, 8, 8 * 200) == 2 * 152 * 128 * 256 * 4 + 768
+    assert qg.moe_workspace_bytes(d, 0, 8) == 0
+    assert qg.moe_workspace_bytes(d, 8, 0) == 0

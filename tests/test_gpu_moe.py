@@ -58,24 +58,29 @@ def _experts_exact(ws):
     return [oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros) for w in ws]
 
 
-def _run_moe(ws, x_bits, offsets, afmt="bf16", tok_scale=None, out_fill=None):
+def _run_moe(ws, x_bits, offsets, afmt="bf16", tok_scale=None, out_fill=None, stream_k=False,
+             calls=1):
+    """stream_k: pass the MoE workspace, which lets the kernel cut leftover tiles over CTAs
+    (it does so when the leftover tiles hold at least 16 K blocks per SM)."""
     from tests import gpu_util as G
     import quantized_weight_gemm_gb300 as qg
     d, packed = _pack_experts(ws, afmt)
     off = torch.tensor(np.asarray(offsets, dtype=np.int32), device="cuda")
     R = x_bits.shape[0]
+    wsp = qg.moe_workspace(d, len(ws), R) if stream_k else None
     out = torch.empty(R, ws[0].N, dtype=torch.bfloat16, device="cuda")
-    if out_fill is not None:
-        out.fill_(out_fill)
-    if afmt == "bf16":
-        X = G.bf16_tensor(x_bits)
-        y = qg.moe_grouped(d, packed, len(ws), X, off, out=out)
-    else:
-        X = G.u8_tensor(x_bits)
-        ts = torch.from_numpy(np.asarray(tok_scale, dtype=np.float32)).cuda()
-        y = qg.moe_grouped(d, packed, len(ws), X, off, tok_scale=ts, out=out)
-    torch.cuda.synchronize()
-    assert qg.device_status(clear=True) == 0
+    for _ in range(calls):            # later calls check that the workspace came back clean
+        if out_fill is not None:
+            out.fill_(out_fill)
+        if afmt == "bf16":
+            X = G.bf16_tensor(x_bits)
+            y = qg.moe_grouped(d, packed, len(ws), X, off, out=out, ws=wsp)
+        else:
+            X = G.u8_tensor(x_bits)
+            ts = torch.from_numpy(np.asarray(tok_scale, dtype=np.float32)).cuda()
+            y = qg.moe_grouped(d, packed, len(ws), X, off, tok_scale=ts, out=out, ws=wsp)
+        torch.cuda.synchronize()
+        assert qg.device_status(clear=True) == 0
     return G.to_f64(y)
 
 
@@ -90,25 +95,51 @@ def _offsets(counts):
     return np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
 
 
+@pytest.mark.parametrize("stream_k", [False, True])
 @pytest.mark.parametrize("wfmt,counts,N,K", [
     ("mxfp4", [5, 0, 37, 16, 0, 1, 130, 8], 256, 512),
     ("mxfp4", [0, 0, 0, 64], 384, 1024),
     ("uint4_zp", [17, 300, 0, 3], 300, 768),
     ("int4_sym", [1, 1, 1, 1, 1, 1, 1, 1, 1, 1], 128, 256),
 ])
-def test_moe_a16_parity(wfmt, counts, N, K):
+def test_moe_a16_parity(wfmt, counts, N, K, stream_k):
     r = WL.rng(41)
     off = _offsets(counts)
     R = int(off[-1])
     x = WL.gen_x(r, R, K)
     ws = [WL.gen_weights(r, wfmt, N, K) for _ in counts]
     ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
-    _assert_close(_run_moe(ws, x, off), ref, TOL_A16)
+    _assert_close(_run_moe(ws, x, off, stream_k=stream_k, calls=2), ref, TOL_A16)
 
 
 def F_bits(x_bits):
     from oracle import formats as F
     return F.bf16_bits_to_float(x_bits)
+
+
+@pytest.mark.parametrize("afmt,counts,N,K", [
+    ("bf16", [1, 1, 2, 1, 1, 1, 1, 1], 7168, 3072),     # 448 tiles: two whole rounds, 144 cut
+    ("bf16", [1, 1, 1, 1, 1, 1, 1, 1], 2048, 2560),     # 128 tiles, all cut (20 K blocks each)
+    ("bf16", [40, 3, 0, 17, 9, 1, 0, 22], 1536, 2688),  # several m-tiles per expert
+    ("fp8", [12, 0, 41, 200, 1], 2048, 3584),           # 64-row tiles, FP8 activations
+])
+def test_moe_stream_k(afmt, counts, N, K):
+    """MoE calls whose leftover tiles hold at least 16 K blocks per SM, so that the kernel
+    cuts them over several CTAs (given the workspace); two calls on one workspace."""
+    r = WL.rng(46)
+    off = _offsets(counts)
+    R = int(off[-1])
+    x = WL.gen_x(r, R, K, outliers=afmt == "fp8")
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    if afmt == "bf16":
+        ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+        _assert_close(_run_moe(ws, x, off, stream_k=True, calls=2), ref, TOL_A16)
+    else:
+        from oracle import formats as F
+        xq, sc = oracle.quant_act_fp8(x)
+        ref = oracle.moe_grouped(F.e4m3_to_float(xq), off, _experts_exact(ws), tok_scale=sc)
+        _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=sc, stream_k=True, calls=2),
+                      ref, TOL_A8)
 
 
 @pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
@@ -125,9 +156,11 @@ def test_moe_every_token_tile(tile):
     qg.force_config(tile, 0)
     try:
         y = _run_moe(ws, x, off)
+        y2 = _run_moe(ws, x, off, stream_k=True)
     finally:
         qg.force_config(0, 0)
     _assert_close(y, ref, TOL_A16)
+    _assert_close(y2, ref, TOL_A16)
 
 
 def test_moe_single_expert_equals_dense():
@@ -163,7 +196,8 @@ def test_moe_rows_outside_groups_untouched():
     _assert_close(y[5:int(off[-1])], ref, TOL_A16)
 
 
-def test_moe_a8_parity():
+@pytest.mark.parametrize("stream_k", [False, True])
+def test_moe_a8_parity(stream_k):
     r = WL.rng(45)
     counts = [12, 0, 41, 200, 1]
     off = _offsets(counts)
@@ -174,22 +208,24 @@ def test_moe_a8_parity():
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     from oracle import formats as F
     ref = oracle.moe_grouped(F.e4m3_to_float(xq), off, _experts_exact(ws), tok_scale=s)
-    _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=s), ref, TOL_A8)
+    _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=s, stream_k=stream_k, calls=2),
+                  ref, TOL_A8)
 
 
-def test_moe_router_workload_sampled():
+@pytest.mark.parametrize("T", [1, 128])
+def test_moe_router_workload_sampled(T):
     """The DeepSeek-V3-like layer's gate_up GEMM (E = 256 MXFP4 experts of 4096 x 7168)
-    at T = 128 tokens routed top-8 with the skewed logits, in the default launch
-    configuration: 32 sampled rows (each against its own expert) plus every row of the two
-    largest experts."""
+    at T tokens routed top-8 with the skewed logits, in the launch configuration the
+    benchmark times (with the MoE workspace): up to 32 sampled rows (each against its own
+    expert) plus every row of the two largest experts."""
     from tests import gpu_util as G
     import quantized_weight_gemm_gb300 as qg
-    case = WL.moe_case(128, seed=0, skewed=True)
+    case = WL.moe_case(T, seed=0, skewed=True)
     E, N, K = WL.MOE_E, 2 * WL.MOE_INTER, WL.MOE_HIDDEN
     off = np.asarray(case.offsets, dtype=np.int64)
     R = int(off[-1])
     r = WL.rng(46)
-    rows = set(int(v) for v in r.choice(R, size=32, replace=False))
+    rows = set(int(v) for v in r.choice(R, size=min(32, R), replace=False))
     for e in np.argsort(-np.diff(off), kind="stable")[:2]:
         rows.update(range(int(off[e]), int(off[e + 1])))
     rows = sorted(rows)
@@ -207,7 +243,8 @@ def test_moe_router_workload_sampled():
             W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales)
             ref[mine] = oracle.gemm(xf[[rows[i] for i in mine]], W)
     X = G.bf16_tensor(case.x_bits)
-    y = qg.moe_grouped(d, packed, E, X, torch.tensor(off.astype(np.int32), device="cuda"))
+    y = qg.moe_grouped(d, packed, E, X, torch.tensor(off.astype(np.int32), device="cuda"),
+                       ws=qg.moe_workspace(d, E, R))
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     y = G.to_f64(y)

@@ -67,8 +67,8 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "2f73d0df699b2345d5aef126f4b0295efea10e0cdf86cdeb11e93ccaaf3ecdee",
-    "launches": {"28672,8192,8192": 3095267000 + 887767808},
+    "csrc_sha256": "da525c1656239b89bd2ca8819dfc95bb0df262ad8a78f09afb62f72705b9ba0a",
+    "launches": {"28672,8192,8192": 3155723000 + 938716160},
 }
 
 

@@ -61,12 +61,6 @@ namespace qgemm {
 #ifndef QGEMM_ISSUERS_NARROW
 #define QGEMM_ISSUERS_NARROW 4
 #endif
-#ifndef QGEMM_SA_256
-#define QGEMM_SA_256 5
-#endif
-#ifndef QGEMM_SX_256
-#define QGEMM_SX_256 5
-#endif
 // Warp roles, in this order: the dequant warpgroups, the four epilogue warps, the MMA
 // issuers, the activation producer and the two record producers.  Groups of four start at a
 // multiple of 4, so `warp & 3` is the tensor-memory lane quarter a warp may access.  Every
@@ -118,7 +112,7 @@ struct GemmCfg {
   static constexpr int kATmemMax = (512 - kAccCols - (A8 ? 8 : 0)) / (kACols + kSfCols);
   static constexpr int kAStagesMax =
       A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
-         : (BNT >= 256 ? QGEMM_SA_256 : (kATmemMax < 7 ? kATmemMax : 7));
+         : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
   // Stage g of the CTA goes to dequant warpgroup g % kDeqWGs and to issuer g % kIssuers.
   // A ring slot must always have the same two owners: a waiter that is not the slot's only
   // consumer could run two uses ahead, where a one-bit mbarrier phase parity cannot tell
@@ -128,10 +122,7 @@ struct GemmCfg {
   static constexpr int kAStages = kAStagesMax / kALcm * kALcm;
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
   static constexpr int kXChunk = BNT <= 32 ? 4 : BNT == 64 ? 2 : 1;
-  // One stage per slot otherwise: as deep as the A ring, up to what shared memory holds
-  // next to the record ring (the rings are independent: a stage waits for both its slots).
-  static constexpr int kXSlotsMax = (!A8 && BNT >= 256) ? QGEMM_SX_256 : kAStages;
-  static constexpr int kXSlots = kXChunk > 1 ? 3 : (kAStages < kXSlotsMax ? kAStages : kXSlotsMax);
+  static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
   static constexpr int kXSlotBytes = kXChunk * kXBytes;
   static constexpr int kXBoxSlabs = kXChunk * kSlabs;
   static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4;

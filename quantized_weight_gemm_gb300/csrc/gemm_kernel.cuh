@@ -4,7 +4,7 @@
 // unit (a 128-row weight tile x a token tile, over a range of K); the 256-token BF16 variant
 // uses half stages (64 K) so that its 32 KB activation tiles fit.  Warp roles, in order:
 //
-//   dequant     W warpgroups (4 for 16-token tiles, else 2) taking the CTA's stages
+//   dequant     W warpgroups (4 for token tiles up to 64, else 2) taking the CTA's stages
 //               round-robin: thread r owns weight row r (= tensor-memory lane r), decodes
 //               its row's codes from the record ring in registers (dequant.cuh), releases
 //               the record slot, and writes the weights with tcgen05.st into the stage's
@@ -68,7 +68,7 @@ namespace qgemm {
 // leave fewer registers per thread.
 template <int BNT>
 struct Roles {
-  static constexpr int kDeqWGs = BNT <= 16 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
+  static constexpr int kDeqWGs = BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
   static constexpr int kIssuers = BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
@@ -102,6 +102,7 @@ struct GemmCfg {
   static constexpr int kXBytes = kSlabs * kSlabBytes;
   static constexpr int kACols = A8 ? 32 : kChunks * 16;          // A-operand columns / stage
   static constexpr int kMmaPerStage = A8 ? kChunks : 2 * kChunks;
+  static_assert(A8 || kMmaPerStage % 4 == 0, "BF16 stages issue their MMAs in groups of four");
   static constexpr int kIssuers = Roles<BNT>::kIssuers;
   static constexpr int kNumSub = kIssuers;                       // partial accumulators
   static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
@@ -650,20 +651,24 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           ptx::tc_fence_after();
           const uint64_t bdesc = desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
           const uint32_t a_tmem = tbase + uint32_t(C::kACol0 + cur.slot * C::kACols);
+          if constexpr (A8) {
 #pragma unroll
-          for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
-            const uint32_t accum = kk > 0 ? 1u : (first ^ 1u);
-            if constexpr (A8) {
+            for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
+              const uint32_t accum = kk > 0 ? 1u : (first ^ 1u);
               ptx::mma_mxf8f6f4_ts_elect(d_tmem, a_tmem + kk * 8, bdesc + uint64_t(kk * 2),
                                          ptx::idesc_mxf8_e4m3(128, BNT, kk, 0),
                                          tbase + uint32_t(C::kSfaCol0 + 4 * cur.slot),
                                          tbase + uint32_t(C::kSfbCol0), accum);
-            } else {
-              // slab kk / 4, 32-byte K step kk % 4 inside the 128-byte swizzled row
-              ptx::mma_f16_ts_elect(d_tmem, a_tmem + kk * 8,
-                                    bdesc + uint64_t(((kk >> 2) * C::kSlabBytes) >> 4) +
-                                        uint64_t((kk & 3) * 2),
-                                    ptx::idesc_bf16(128, BNT), accum);
+            }
+          } else {
+            // one 128-byte slab (64 K) per group of four: 32-byte K steps inside its swizzled
+            // rows, the four MMAs issued under one election
+#pragma unroll
+            for (int q = 0; q < C::kMmaPerStage / 4; ++q) {
+              const uint64_t b = bdesc + uint64_t((q * C::kSlabBytes) >> 4);
+              const uint32_t a = a_tmem + uint32_t(q * 32);
+              ptx::mma4_f16_ts_elect(d_tmem, a, a + 8u, a + 16u, a + 24u, b, b + 2u, b + 4u, b + 6u,
+                                     ptx::idesc_bf16(128, BNT), q > 0 ? 1u : (first ^ 1u));
             }
           }
           first = 0;
@@ -763,36 +768,28 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       epi_phase ^= 1u;
       return warp_all(ok);
     };
-    // This warp's accumulator chunk c (kChunk columns), partial accumulators summed.
+    // This warp's accumulator chunk c (kChunk columns), partial accumulators summed in the
+    // order sub0, sub0 + 1, ... (16 columns at a time, so that few registers are live).
     auto load_chunk = [&](int acc, int sub0, int active, int c, uint32_t (&v)[32]) {
       const uint32_t col = t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * kChunk);
-      if constexpr (kChunk == 32) {
-        ptx::tmem_ld32(col + uint32_t(sub0 * BNT), v);
-      } else {
-        uint32_t v16[16];
-        ptx::tmem_ld16(col + uint32_t(sub0 * BNT), v16);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) v[j] = v16[j];
-      }
-#pragma unroll
-      for (int d = 1; d < C::kNumSub; ++d) {
-        if (d >= active) break;
-        const int sub = (sub0 + d) % C::kNumSub;
-        uint32_t p[32];
-        if constexpr (kChunk == 32) {
-          ptx::tmem_ld32(col + uint32_t(sub * BNT), p);
-        } else {
-          uint32_t p16[16];
-          ptx::tmem_ld16(col + uint32_t(sub * BNT), p16);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) p[j] = p16[j];
-        }
+      for (int h = 0; h < kChunk / 16; ++h) {
+        uint32_t p16[16];
+        ptx::tmem_ld16(col + uint32_t(sub0 * BNT + h * 16), p16);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < kChunk; ++j)
-          v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(p[j]));
+        for (int j = 0; j < 16; ++j) v[h * 16 + j] = p16[j];
+#pragma unroll
+        for (int d = 1; d < C::kNumSub; ++d) {
+          if (d >= active) break;
+          const int sub = (sub0 + d) % C::kNumSub;
+          ptx::tmem_ld16(col + uint32_t(sub * BNT + h * 16), p16);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            v[h * 16 + j] = __float_as_uint(__uint_as_float(v[h * 16 + j]) + __uint_as_float(p16[j]));
+        }
       }
-      ptx::tmem_wait_ld();
     };
     int ui = 0;
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start

@@ -194,6 +194,23 @@ __device__ __forceinline__ void mma_f16_ts_elect(uint32_t d_tmem, uint32_t a_tme
       :: "r"(d_tmem), "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate) : "memory");
 }
 
+// Four kind::f16 MMAs into one accumulator under a single election (the first accumulates
+// when `accumulate` is non-zero, the other three always): one elect.sync instead of four.
+__device__ __forceinline__ void mma4_f16_ts_elect(uint32_t d_tmem, uint32_t a0, uint32_t a1,
+                                                  uint32_t a2, uint32_t a3, uint64_t b0,
+                                                  uint64_t b1, uint64_t b2, uint64_t b3,
+                                                  uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P, Q, E;\n setp.ne.b32 P, %10, 0;\n setp.eq.b32 Q, %10, %10;\n"
+      " elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %5, %9, P;\n"
+      " @E tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %6, %9, Q;\n"
+      " @E tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %7, %9, Q;\n"
+      " @E tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %9, Q;\n}\n"
+      :: "r"(d_tmem), "r"(a0), "r"(a1), "r"(a2), "r"(a3), "l"(b0), "l"(b1), "l"(b2), "l"(b3),
+         "r"(idesc), "r"(accumulate) : "memory");
+}
+
 __device__ __forceinline__ void mma_mxf8f6f4_ts_elect(uint32_t d_tmem, uint32_t a_tmem,
                                                       uint64_t b_desc, uint32_t idesc,
                                                       uint32_t sfa_tmem, uint32_t sfb_tmem,

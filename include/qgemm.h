@@ -139,6 +139,41 @@ qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void
                          size_t ws_bytes, void* stream);
 
 /*
+ * Device staging bytes that qgemm_w4a16_host needs for any M <= M_max: two buffers of a
+ * chunk's X rows and two of its Y rows (a chunk is all M rows up to 512, else M / 16
+ * rounded up to a multiple of 256 and at least 512).  0 for an invalid descriptor or
+ * M_max <= 0.
+ */
+size_t qgemm_host_staging_bytes(const qgemm_wdesc* desc, int64_t M_max);
+
+/*
+ * Dense W4A16 with X and Y in host memory: Y_host = qgemm_w4a16(X_host) with the copies
+ * overlapped.  The rows are cut into chunks (see qgemm_host_staging_bytes); chunk i is
+ * copied in on a library-owned stream, multiplied on `stream` into `staging`, and copied out
+ * on a second library-owned stream while chunk i + 1 is multiplied (a single chunk runs all
+ * three steps on `stream`).  Returns once the work is enqueued; work ordered after the call
+ * on `stream` sees Y_host complete.
+ *   X_host  : host BF16 [M, ldx] (ldx >= K); page-locked memory (cudaHostAlloc /
+ *             cudaHostRegister) lets the copies run asynchronously and at full speed
+ *   Y_host  : host BF16 [M, ldy] (ldy >= N), same advice
+ *   staging : device buffer of qgemm_host_staging_bytes(desc, M) bytes, 256-byte aligned,
+ *             owned by the caller and busy until `stream` reaches the end of the call
+ *   ws, chan_scale, stream : as for qgemm_w4a16 (the chunks run one after another on
+ *             `stream`, so they share one workspace)
+ * Errors: QGEMM_ERR_INVALID_ARG (descriptor, null pointers, ld too small, FP8 descriptor),
+ * QGEMM_ERR_WORKSPACE (staging missing or too small), QGEMM_ERR_ALIGNMENT, any status of
+ * qgemm_w4a16, QGEMM_ERR_CUDA when a copy or an event could not be enqueued (chunks already
+ * enqueued then still run).  Calls from several host threads are serialized while they
+ * enqueue (the library streams and events are shared per device).
+ * The pages time the GEMM kernels alone; this entry point is a library convenience that
+ * the end-to-end measurement uses.
+ */
+qgemm_status qgemm_w4a16_host(const qgemm_wdesc* desc, const void* packed, const void* X_host,
+                              int64_t M, int64_t ldx, const float* chan_scale, void* Y_host,
+                              int64_t ldy, void* staging, size_t staging_bytes, void* ws,
+                              size_t ws_bytes, void* stream);
+
+/*
  * Tokenwise FP8 activation quantization (the input of W4A8): per row m,
  * s[m] = max_k |X[m, k]| / 448 (1 when the row is zero) and Xq[m, k] = e4m3 code of
  * X[m, k] / s[m], rounded to nearest even with saturation, all in float32.

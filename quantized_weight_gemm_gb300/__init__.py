@@ -14,7 +14,8 @@ import torch
 __all__ = [
     "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
-    "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "check_desc", "WFMT", "AFMT", "EXPORTS",
+    "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "host_staging_bytes",
+    "host_staging", "w4a16_host", "check_desc", "WFMT", "AFMT", "EXPORTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,7 @@ EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packe
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
-           "qgemm_moe_workspace_bytes")
+           "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -96,6 +97,8 @@ def lib():
         "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
+        "qgemm_host_staging_bytes": (SZ, [D, I64]),
+        "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -224,6 +227,37 @@ def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None):
     _check(lib().qgemm_w4a8(ctypes.byref(d), _ptr(packed), _ptr(Xq), M, Xq.stride(0),
                             _ptr(tok_scale), _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(ws),
                             ws.numel() * ws.element_size(), _stream()), "w4a8")
+    return out
+
+
+def host_staging_bytes(desc, M_max):
+    d = desc.c()
+    return int(lib().qgemm_host_staging_bytes(ctypes.byref(d), int(M_max)))
+
+
+def host_staging(desc, M_max, device="cuda"):
+    """Device staging for w4a16_host calls with M <= M_max (reusable on one stream)."""
+    return torch.empty(max(host_staging_bytes(desc, M_max), 256), dtype=torch.uint8, device=device)
+
+
+def w4a16_host(desc, packed, X_host, out=None, staging=None, ws=None, chan_scale=None):
+    """Dense W4A16 with X [M, K] and Y [M, N] in host memory (BF16, pin them for speed):
+    the copies in and out overlap the GEMM chunk by chunk.  Asynchronous on the current
+    stream: synchronize before reading `out`."""
+    _row_major(X_host, "X_host")
+    if X_host.is_cuda:
+        raise QGemmError("w4a16_host takes a host X; use w4a16 for device tensors")
+    M = X_host.shape[0]
+    if out is None:
+        out = torch.empty(M, desc.N, dtype=torch.bfloat16, pin_memory=True)
+    if staging is None:
+        staging = host_staging(desc, M, device=packed.device)
+    if ws is None:
+        ws = workspace(desc, M, device=packed.device)
+    d = desc.c()
+    _check(lib().qgemm_w4a16_host(ctypes.byref(d), _ptr(packed), _ptr(X_host), M, X_host.stride(0),
+                                  _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(staging),
+                                  staging.numel(), _ptr(ws), ws.numel(), _stream()), "w4a16_host")
     return out
 
 

@@ -3,6 +3,8 @@
 Bar: |y - y_ref| <= 8e-3 * max(|y_ref|, rms(y_ref)) for BF16 activations and 2e-2 for
 FP8 activations, element by element; exact equality where the arithmetic is exact
 (integer-valued inputs with power-of-two scales, one-hot activations)."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -237,3 +239,59 @@ def test_a8_dispatch_entries(tile, splits):
     finally:
         qg.force_config(0, 0)
     _assert_close(y, ref, TOL_A8)
+
+
+# ------------------------------------------------------------------- host buffers
+
+@pytest.mark.parametrize("M,ldx_pad,ldy_pad", [(1, 0, 0), (300, 0, 0), (1500, 8, 16),
+                                               (2049, 0, 8), (5000, 0, 0)])
+def test_w4a16_host_buffers(M, ldx_pad, ldy_pad):
+    """X and Y in page-locked host memory: one chunk (M <= 512) or several (chunks of at
+    least 512 rows, the last one ragged: 1500 = 2 x 512 + 476, 5000 = 9 x 512 + 392), leading dimensions wider than K and N;
+    the padding columns of Y stay untouched, and a second call on the same staging buffer
+    gives the same bits."""
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(34)
+    N, K = 1024, 512
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    d, packed = G.pack(w)
+    xh = torch.zeros(M, K + ldx_pad, dtype=torch.bfloat16).pin_memory()
+    xh[:, :K] = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16)
+    yh = torch.full((M, N + ldy_pad), 7.0, dtype=torch.bfloat16).pin_memory()
+    staging = qg.host_staging(d, M)
+    ws = qg.workspace(d, M)
+    qg.w4a16_host(d, packed, xh[:, :K], out=yh[:, :N], staging=staging, ws=ws)
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    y1 = yh[:, :N].float().numpy().astype(np.float64)
+    _assert_close(y1, ref, TOL_A16)
+    if ldy_pad:
+        assert torch.all(yh[:, N:] == 7.0)
+    qg.w4a16_host(d, packed, xh[:, :K], out=yh[:, :N], staging=staging, ws=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(yh[:, :N].float().numpy().astype(np.float64), y1)
+
+
+def test_w4a16_host_argument_errors():
+    from tests import gpu_util as G
+    qg = _qg()
+    w = WL.gen_weights(WL.rng(35), "int4_sym", 256, 512)
+    d, packed = G.pack(w)
+    L = qg.lib()
+    cd = d.c()
+    P = ctypes.c_void_p
+    xh = torch.zeros(600, 512, dtype=torch.bfloat16).pin_memory()
+    yh = torch.zeros(600, 256, dtype=torch.bfloat16).pin_memory()
+    need = qg.host_staging_bytes(d, 600)
+    assert need == 2 * (512 * 512 * 2 + 256 * 512 * 2)          # chunks of 512 rows
+    st = torch.empty(need, dtype=torch.uint8, device="cuda")
+    args = lambda stg, n: (ctypes.byref(cd), P(packed.data_ptr()), P(xh.data_ptr()), 600, 512, None,
+                           P(yh.data_ptr()), 256, stg, n, None, 0, None)
+    assert L.qgemm_w4a16_host(*args(None, 0)) == 4                    # no staging
+    assert L.qgemm_w4a16_host(*args(P(st.data_ptr()), need - 1)) == 4  # too small
+    assert L.qgemm_w4a16_host(*args(P(st.data_ptr() + 16), need)) == 3  # misaligned
+    assert L.qgemm_w4a16_host(ctypes.byref(cd), P(packed.data_ptr()), None, 600, 512, None,
+                              P(yh.data_ptr()), 256, P(st.data_ptr()), need, None, 0, None) == 1

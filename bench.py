@@ -68,8 +68,8 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "da525c1656239b89bd2ca8819dfc95bb0df262ad8a78f09afb62f72705b9ba0a",
-    "launches": {"28672,8192,8192": 3155723000 + 938716160},
+    "csrc_sha256": "de9b40d1519fdb188eb5ad82dcd2937d29a0bf3688e8340e586a26a5b060bd29",
+    "launches": {"28672,8192,8192": 3025148000 + 930310144},
 }
 
 

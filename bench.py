@@ -68,7 +68,7 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "de9b40d1519fdb188eb5ad82dcd2937d29a0bf3688e8340e586a26a5b060bd29",
+    "csrc_sha256": "7f03174a95235a3a6c5c7a1f0d59edb534349d17ca9afceff4a2f6706a8d931e",
     "launches": {"28672,8192,8192": 3025148000 + 930310144},
 }
 
@@ -80,16 +80,26 @@ GEMM_SOURCES = ("api.cu", "dequant.cuh", "gemm_a16_any.cu", "gemm_a16_mxfp4.cu",
                 "kernels.h", "ptx.cuh", "qgemm_internal.h")
 
 
+def _code_only(text):
+    """Source text without comments and blank space, so that comment edits keep the digest."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def csrc_digest():
+    """sha256 over the code (comments and white space dropped) of the GEMM sources and the
+    public header."""
     import hashlib
     h = hashlib.sha256()
     d = os.path.join(ROOT, "quantized_weight_gemm_gb300", "csrc")
     for f in sorted(os.listdir(d)):
         if f in GEMM_SOURCES:
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
-    with open(os.path.join(ROOT, "include", "qgemm.h"), "rb") as fh:
-        h.update(fh.read())
+            with open(os.path.join(d, f), encoding="utf-8") as fh:
+                h.update(f.encode() + b"\0" + _code_only(fh.read()).encode())
+    with open(os.path.join(ROOT, "include", "qgemm.h"), encoding="utf-8") as fh:
+        h.update(_code_only(fh.read()).encode())
     return h.hexdigest()
 
 

@@ -9,10 +9,12 @@
 //               its row's codes from the record ring in registers (dequant.cuh), releases
 //               the record slot, and writes the weights with tcgen05.st into the stage's
 //               A-operand columns of tensor memory.  The weights never touch shared memory.
-//   epilogue    4 warps: tcgen05.ld of the accumulator(s), fused per-channel / per-token
-//               scaling, BF16 store of Y; or, under split-K, a store of the FP32 partial
-//               tile into the split's slice of the workspace, after which the last of the
-//               tile's splits to arrive sums the slices in split order and converts.
+//   epilogue    4 warps (8 for 128- and 256-token tiles): tcgen05.ld of the accumulator(s),
+//               fused per-channel / per-token scaling, BF16 store of Y; or, for a tile whose
+//               K range is cut over several CTAs (split-K or stream-K, see unit_at), a store
+//               of the FP32 partial tile into the contributor's workspace slot, after which
+//               the last contributor to arrive sums the slots in contributor order and
+//               converts.
 //   MMA issuers I warps (4 for token tiles up to 64, else 1), each a converged warp whose
 //               elected lane issues tcgen05.mma with A = weights in tensor memory (M = 128
 //               weight rows) and B = the X tile (N = token_tile rows of X), FP32
@@ -31,6 +33,8 @@
 //               slots) so that many weight bytes are in flight: small batches are bound by
 //               HBM.
 //
+// Every role walks the CTA's units in the same order (unit_at); the schedule is computed
+// once into shared memory after the prologue.
 // Stage g of a CTA (counted over all its units) belongs to dequant warpgroup g % W and to
 // issuer g % I, and every ring's depth is a multiple of the number of its owners, so each
 // slot is always written and read by the same warps.  A waiter that shared a slot with

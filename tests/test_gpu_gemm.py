@@ -295,3 +295,21 @@ def test_w4a16_host_argument_errors():
     assert L.qgemm_w4a16_host(*args(P(st.data_ptr() + 16), need)) == 3  # misaligned
     assert L.qgemm_w4a16_host(ctypes.byref(cd), P(packed.data_ptr()), None, 600, 512, None,
                               P(yh.data_ptr()), 256, P(st.data_ptr()), need, None, 0, None) == 1
+
+
+def test_w4a16_host_channel_scale():
+    """The host-buffer call forwards the per-channel scale to every chunk (3 chunks)."""
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(36)
+    M, N, K = 1300, 768, 640
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    chan = r.uniform(0.25, 4.0, size=N).astype(np.float32)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros, chan_scale=chan)
+    d, packed = G.pack(w)
+    xh = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y = qg.w4a16_host(d, packed, xh, chan_scale=torch.from_numpy(chan).cuda())
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    _assert_close(y.float().numpy().astype(np.float64), ref, TOL_A16)

@@ -152,6 +152,33 @@ def moe_grouped(x_rows, offsets, experts, tok_scale=None, chan_scales=None):
     return y
 
 
+def moe_indexed(x, offsets, row_index, experts, tok_scale=None):
+    """MoE GEMM over rows gathered by index (the pages' "Indexed" MoE path, "Humming wird
+    angekündigt", section "WnA16": the kernel reads each token's row where it lies instead
+    of a copy sorted by expert).
+
+    x: activation values [T, K] in token order; offsets: int [E+1] over the R sorted
+    positions; row_index: int [R], the row of x that sorted position r takes, or a negative
+    value for a padding position; experts: E exact weights [N, K]; tok_scale: float [T] per
+    row of x (FP8 activations) or None.  Output row r (sorted order) is x[row_index[r]] times
+    expert e's weights for the e whose block holds r, scaled by tok_scale[row_index[r]];
+    padding positions give zero rows.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    row_index = np.asarray(row_index, dtype=np.int64)
+    n = experts[0].shape[0]
+    y = np.zeros((row_index.shape[0], n), dtype=np.float64)
+    for e, w in enumerate(experts):
+        for r in range(int(offsets[e]), int(offsets[e + 1])):
+            t = int(row_index[r])
+            if t < 0:
+                continue
+            ts = None if tok_scale is None else np.asarray(tok_scale)[t:t + 1]
+            y[r:r + 1] = gemm(x[t:t + 1], w, tok_scale=ts)
+    return y
+
+
 def tolerance_ok(y, y_ref, rel):
     """The parity bar: |y - y_ref| <= rel * max(|y_ref|, rms(y_ref)) elementwise.
 

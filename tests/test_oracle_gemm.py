@@ -239,6 +239,32 @@ def test_moe_decomposition():
     np.testing.assert_array_equal(y1, oracle.gemm(x, Ws[0]))
 
 
+def test_moe_indexed():
+    """Gathering rows by index: equals the grouped GEMM on the rows sorted beforehand
+    (including padding rows, which index -1 and give zeros), and does not depend on where
+    the token rows lie (a permutation of x with the index remapped gives the same Y)."""
+    case = WL.moe_case(T=9, seed=3, E=4, topk=2, hidden=64, inter=32)
+    ws = [WL.gen_weights(np.random.Generator(np.random.PCG64(10 + e)), "int4_sym", 40, 64, group=32)
+          for e in range(4)]
+    Ws = [oracle.dequant(w.wfmt, w.group, w.codes, w.scales) for w in ws]
+    x_tok = F.bf16_bits_to_float(case.x_tok_bits)
+    x_sorted = F.bf16_bits_to_float(case.x_bits)
+    y = oracle.moe_indexed(x_tok, case.offsets, case.token_of_row, Ws)
+    ref = oracle.moe_grouped(x_sorted, case.offsets, Ws)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+    assert np.all(y[case.token_of_row < 0] == 0) and np.any(case.token_of_row < 0)
+    perm = np.random.Generator(np.random.PCG64(4)).permutation(case.T)
+    inv = np.argsort(perm)                          # x_tok[t] now sits at row inv[t]
+    idx = np.where(case.token_of_row >= 0, inv[np.maximum(case.token_of_row, 0)], -1)
+    np.testing.assert_array_equal(oracle.moe_indexed(x_tok[perm], case.offsets, idx, Ws), y)
+    # per-row token scales follow the gathered row
+    s = np.linspace(0.5, 2.0, case.T)
+    ys = oracle.moe_indexed(x_tok, case.offsets, case.token_of_row, Ws, tok_scale=s)
+    rows = case.token_of_row >= 0
+    np.testing.assert_allclose(ys[rows], y[rows] * s[case.token_of_row[rows]][:, None],
+                               rtol=1e-12, atol=1e-12)
+
+
 def test_routing_layout():
     case = WL.moe_case(T=50, seed=2, E=16, topk=4, hidden=32, inter=32)
     assert case.counts.sum() == 50 * 4

@@ -43,6 +43,7 @@ class MoECase:
     token_of_row: np.ndarray   # int64 [R] source token of each row (-1 for padding)
     x_bits: np.ndarray = field(default=None)        # uint16 [R, K] gate_up input, sorted
     down_bits: np.ndarray = field(default=None)     # uint16 [R, inter] down input
+    x_tok_bits: np.ndarray = field(default=None)    # uint16 [T, K] gate_up input, token order
 
 
 def rng(seed):
@@ -169,7 +170,7 @@ def moe_case(T, seed=0, skewed=False, E=MOE_E, topk=MOE_TOPK, hidden=MOE_HIDDEN,
         xs[valid] = x_tok[tor[valid]]
         down = gen_x(r, R, inter)
         down[~valid] = 0
-        case.x_bits, case.down_bits = xs, down
+        case.x_bits, case.down_bits, case.x_tok_bits = xs, down, x_tok
     return case
 
 

@@ -220,9 +220,32 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
                                void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 
 /*
- * Workspace bytes that let qgemm_moe_grouped use stream-K for E experts and R sorted rows
- * (token tile from R / E): FP32 partial-sum slots for twice the SM count plus one arrival
- * counter per SM.  0 for an invalid descriptor, E < 1 or R <= 0.
+ * MoE GEMM over rows gathered by index (the "Indexed" MoE path): sorted position r of
+ * expert e's block [expert_offsets[e], expert_offsets[e+1]) takes X row row_index[r], so
+ * the caller needs no copy of X sorted by expert.
+ *   Y[r, :] = X[row_index[r], :] * W_e^T   (times tok_scale[row_index[r]] for FP8 X)
+ * and a padding position (row_index[r] < 0) gives a zero row.
+ *   X              : device [T, ldx] rows in token order (BF16, or e4m3 with tok_scale [T])
+ *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
+ *   row_index      : device int32 [R], values in [0, T) or negative; 4-byte aligned
+ *   Y              : device BF16 [R, ldy] in sorted order
+ *   ws, ws_bytes   : as for qgemm_moe_grouped (qgemm_moe_workspace_bytes covers both)
+ * Rows are gathered with TMA four at a time; a gathered tile holds half a token tile of
+ * rows (token tiles up to 64: 8, 16 or 32 rows per tile, from R / E), which suits the
+ * few rows per expert of decode-sized routing; the grouped call is the faster choice for
+ * large batches.  QGEMM_ERR_UNSUPPORTED when qgemm_force_config forces a token tile above
+ * 64.  "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths).
+ */
+qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
+                               int32_t afmt, const void* X, int64_t T, int64_t ldx,
+                               const float* tok_scale, const int32_t* expert_offsets,
+                               const int32_t* row_index, int64_t R, void* Y, int64_t ldy,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Workspace bytes that let qgemm_moe_grouped or qgemm_moe_indexed use stream-K for E
+ * experts and R sorted rows (token tile from R / E): FP32 partial-sum slots for twice the
+ * SM count plus one arrival counter per SM.  0 for an invalid descriptor, E < 1 or R <= 0.
  */
 size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R);
 

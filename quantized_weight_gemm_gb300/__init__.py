@@ -15,7 +15,7 @@ __all__ = [
     "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
     "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "host_staging_bytes",
-    "host_staging", "w4a16_host", "check_desc", "WFMT", "AFMT", "EXPORTS",
+    "host_staging", "w4a16_host", "moe_indexed", "check_desc", "WFMT", "AFMT", "EXPORTS",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -27,7 +27,8 @@ EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packe
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
-           "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host")
+           "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host",
+           "qgemm_moe_indexed")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -98,6 +99,7 @@ def lib():
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
         "qgemm_host_staging_bytes": (SZ, [D, I64]),
+        "qgemm_moe_indexed": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, I64, P, I64, P, SZ, P]),
         "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
@@ -285,6 +287,26 @@ def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None):
     _check(lib().qgemm_moe_grouped(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
                                    _ptr(X), R, X.stride(0), _ptr(tok_scale), _ptr(offsets),
                                    _ptr(out), out.stride(0), _ptr(ws), wsb, _stream()), "moe_grouped")
+    return out
+
+
+def moe_indexed(desc, packed, E, X, offsets, row_index, tok_scale=None, out=None, ws=None):
+    """MoE GEMM over rows gathered by index: X [T, K] in token order (BF16, or uint8 e4m3
+    with tok_scale [T]); offsets int32 [E+1] and row_index int32 [R] on the device
+    (row_index[r] < 0: padding).  Returns Y [R, N] in sorted order."""
+    fp8 = X.dtype == torch.uint8
+    _need(offsets, "offsets", torch.int32)
+    _need(row_index, "row_index", torch.int32)
+    _row_major(X, "X")
+    R = row_index.numel()
+    if out is None:
+        out = torch.empty(R, desc.N, dtype=torch.bfloat16, device=X.device)
+    d = desc.c()
+    wsb = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib().qgemm_moe_indexed(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
+                                   _ptr(X), X.shape[0], X.stride(0), _ptr(tok_scale), _ptr(offsets),
+                                   _ptr(row_index), R, _ptr(out), out.stride(0), _ptr(ws), wsb,
+                                   _stream()), "moe_indexed")
     return out
 
 

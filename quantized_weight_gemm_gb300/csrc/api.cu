@@ -244,6 +244,14 @@ int moe_token_tile(int64_t R, int32_t E) {
   return tt;
 }
 
+// Indexed (gathered) MoE: tiles of token_tile / 2 rows, token tiles up to 64.
+int moe_indexed_token_tile(int64_t R, int32_t E) {
+  const int64_t avg = R / E;
+  int tt = avg <= 8 ? 16 : avg <= 16 ? 32 : 64;
+  if (g_force_tile) tt = g_force_tile;
+  return tt;
+}
+
 int64_t moe_ws_bytes(int tt, int sms) {
   return 2 * int64_t(sms) * slot_bytes(tt) + round_up(int64_t(sms) * 4, 256);
 }
@@ -297,6 +305,23 @@ bool make_x_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   *is_3d = 0;
   return r == CUDA_SUCCESS;
+}
+
+// X rows gathered four at a time (tile::gather4): a 2-D map whose box is one 128-byte slab
+// of one row, 128-byte swizzle (the gathered rows land in the MMA's swizzled tile).
+bool make_x_gather_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K,
+                       int64_t ldx) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  const int esize = fp8 ? 1 : 2;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ldx) * esize};
+  cuuint32_t box[2] = {cuuint32_t(128 / esize), 1};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 qgemm_status check_x(const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx) {
@@ -458,19 +483,27 @@ qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ld
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }
 
-qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
-                               int32_t afmt, const void* X, int64_t R, int64_t ldx,
-                               const float* tok_scale, const int32_t* expert_offsets,
-                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// The grouped and the indexed MoE call: X has x_rows rows; row_index == nullptr means the
+// rows are already sorted by expert (sorted position r is X row r).
+qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int32_t afmt,
+                     const void* X, int64_t x_rows, int64_t ldx, const float* tok_scale,
+                     const int32_t* expert_offsets, const int32_t* row_index, int64_t R,
+                     void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
   Layout L;
   if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
   const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
   if (afmt != QGEMM_A_BF16 && !fp8) return QGEMM_ERR_INVALID_ARG;
   if (L.afmt != afmt) return QGEMM_ERR_INVALID_ARG;
-  if (E < 1 || E > 1024 || packed == nullptr || expert_offsets == nullptr || R < 0)
+  if (E < 1 || E > 1024 || packed == nullptr || expert_offsets == nullptr || R < 0 || x_rows < 0)
     return QGEMM_ERR_INVALID_ARG;
-  if (!aligned(packed, 256) || !aligned(expert_offsets, 4)) return QGEMM_ERR_ALIGNMENT;
-  qgemm_status s = check_x(X, fp8, R, L.K, ldx);
+  if (row_index != nullptr && R > 0 && x_rows == 0) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(expert_offsets, 4) || !aligned(row_index, 4))
+    return QGEMM_ERR_ALIGNMENT;
+  qgemm_status s = check_x(X, fp8, x_rows, L.K, ldx);
   if (s != QGEMM_OK) return s;
   if ((s = check_y(Y, L.N, ldy)) != QGEMM_OK) return s;
   if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
@@ -478,7 +511,8 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
   GemmPlan plan;
-  const int tt = moe_token_tile(R, E);
+  const int tt = row_index != nullptr ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
+  if (row_index != nullptr && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathered tiles: <= 64
   plan.token_tile = tt;
   plan.splits = 1;
   plan.sk_tiles = 0;
@@ -486,7 +520,11 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   plan.grid = dev->sms;
   CUtensorMap tmap;
   int x3d = 0;
-  if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d)) return QGEMM_ERR_CUDA;
+  if (row_index != nullptr) {
+    if (!make_x_gather_map(&tmap, X, fp8, x_rows, L.K, ldx)) return QGEMM_ERR_CUDA;
+  } else if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d)) {
+    return QGEMM_ERR_CUDA;
+  }
   GemmArgs a;
   memset(&a, 0, sizeof(a));
   a.x_3d = x3d;
@@ -494,6 +532,7 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   a.packed = static_cast<const uint8_t*>(packed);
   a.expert_stride = L.total_bytes;
   a.offsets = expert_offsets;
+  a.row_index = row_index;
   a.E = E;
   a.M = R;
   a.splits = 1;
@@ -514,10 +553,33 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
+                               int32_t afmt, const void* X, int64_t R, int64_t ldx,
+                               const float* tok_scale, const int32_t* expert_offsets,
+                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  return run_moe(desc, packed, E, afmt, X, R, ldx, tok_scale, expert_offsets, nullptr, R, Y, ldy,
+                 ws, ws_bytes, stream);
+}
+
+qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
+                               int32_t afmt, const void* X, int64_t T, int64_t ldx,
+                               const float* tok_scale, const int32_t* expert_offsets,
+                               const int32_t* row_index, int64_t R, void* Y, int64_t ldy,
+                               void* ws, size_t ws_bytes, void* stream) {
+  if (row_index == nullptr && R > 0) return QGEMM_ERR_INVALID_ARG;
+  return run_moe(desc, packed, E, afmt, X, T, ldx, tok_scale, expert_offsets, row_index, R, Y,
+                 ldy, ws, ws_bytes, stream);
+}
+
 size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R) {
   Layout L;
   if (!layout_of(desc, &L) || E < 1 || R <= 0) return 0;
-  return size_t(moe_ws_bytes(moe_token_tile(R, E), sms_or_default()));
+  const int tt = std::max(moe_token_tile(R, E), std::min(moe_indexed_token_tile(R, E), 64));
+  return size_t(moe_ws_bytes(tt, sms_or_default()));
 }
 
 qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,

@@ -130,7 +130,7 @@ struct GemmCfg {
   static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
   static constexpr int kXSlotBytes = kXChunk * kXBytes;
   static constexpr int kXBoxSlabs = kXChunk * kSlabs;
-  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4;
+  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4 + (BNT / 2) * 4;
   static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
   static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
                                 kAStages * kBarBytesPerA + kMiscBytes + 64;
@@ -364,9 +364,10 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
   }
 }
 
-template <int BNT, bool A8, int DM>
+template <int BNT, bool A8, int DM, bool GATHER>
 __global__ void __launch_bounds__(Roles<BNT>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
+  static_assert(!GATHER || BNT <= 64, "gathered tiles exist for token tiles up to 64");
   using C = GemmCfg<BNT, A8>;
   using RO = Roles<BNT>;
   constexpr int kEpiWarp0 = RO::kEpiWarp0;
@@ -399,10 +400,14 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
                                                          // [8..14] schedule (Sched)
   int* prefix = misc + 16;                               // MoE: m-tiles before expert e
   int* offs = prefix + (kMaxExperts + 1);                // MoE: row offsets
+  int* idx_s = offs + (kMaxExperts + 1);                 // indexed MoE: the unit's X rows
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Layout& L = a.L;
+  // Output rows per tile: the token tile, or half of it for gathered (indexed MoE) tiles,
+  // whose rows fill the first four rows of every eight of the activation tile.
+  constexpr int tile_rows = GATHER ? BNT / 2 : BNT;
 
   // ------------------------------------------------------------------ prologue
   // The header loads are issued first and checked after the barrier set-up, and tensor
@@ -442,6 +447,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     // MoE: the last expert's header as well
     ok = ok && hl_magic == kPackedMagic && hl_N == L.N && hl_K == L.K && hl_afmt == L.afmt;
     if (!ok) atomicCAS(a.status, 0, kStatusBadPacked);
+    // the gathering variant runs exactly the indexed calls
+    if (ok && (a.row_index != nullptr) != GATHER) {
+      atomicCAS(a.status, 0, kStatusBadValue);
+      ok = false;
+    }
     misc[2] = ok ? 1 : 0;
   }
   if (warp == kEpiWarp0) {
@@ -476,7 +486,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (e < a.E) {
         const int o = offs[e], o1 = offs[e + 1];
         if (o1 < o || o < 0 || o1 > a.M) bad = true;
-        t = (o1 > o) ? (o1 - o + BNT - 1) / BNT : 0;
+        t = (o1 > o) ? (o1 - o + tile_rows - 1) / tile_rows : 0;
       }
       int incl = t;
 #pragma unroll
@@ -545,7 +555,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       bool alive = true;
       Unit w;
       int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
         const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
                              (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
         for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
@@ -577,7 +587,52 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     }
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer
-    if (lane == 0) {
+    if constexpr (GATHER) {
+      // Gathered (indexed MoE) tiles: the whole warp stages the unit's row indices in shared
+      // memory, then one thread loads four rows at a time (tile::gather4) into the first
+      // half of each 8-row swizzle atom, so that every load starts on a 1024-byte boundary.
+      const uint64_t pol_x = ptx::policy_evict_last();
+      Ring rx;
+      uint32_t pending = 0, pending_parity = 0;
+      bool alive = true;
+      Unit w;
+      int e_hint = -1;
+      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
+        // rows past the expert's block are padding (index -1: the load reads zeros)
+        for (int i = lane; i < tile_rows; i += 32) {
+          const int64_t r = w.row0 + i;
+          idx_s[i] = r < w.row_end ? __ldg(a.row_index + r) : -1;
+        }
+        __syncwarp();
+        if (lane == 0) {
+          const int nst = (w.kb1 - w.kb0) * kSub;
+          for (int i0 = 0; i0 < nst; i0 += XQ) {
+            if (!ptx::mbar_wait(&xempty[rx.slot], rx.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
+            uint8_t* sx = s_x + rx.slot * C::kXSlotBytes;
+            const int k0 = w.kb0 * kStageK + i0 * (kStageK / kSub);
+            ptx::mbar_arrive_expect_tx(&xfull[rx.slot], uint32_t(C::kXSlotBytes / 2));
+#pragma unroll 1
+            for (int sl = 0; sl < C::kXBoxSlabs; ++sl)
+#pragma unroll 1
+              for (int at = 0; at < BNT / 8; ++at)
+                ptx::tma_gather4(sx + sl * C::kSlabBytes + at * 1024, &tmap_x,
+                                 k0 + sl * (A8 ? 128 : 64), idx_s[4 * at], idx_s[4 * at + 1],
+                                 idx_s[4 * at + 2], idx_s[4 * at + 3], &xfull[rx.slot], pol_x);
+            pending |= 1u << rx.slot;
+            pending_parity = (pending_parity & ~(1u << rx.slot)) | (rx.phase << rx.slot);
+            rx.next(SX);
+          }
+        }
+        // the warp moves on together (the index cache is rewritten next unit)
+        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
+      }
+      if (lane == 0 && !alive) {
+        volatile int no_abort = 0;
+        for (int s = 0; s < SX; ++s)
+          if (pending & (1u << s))
+            ptx::mbar_wait(&xfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
+      }
+    } else if (lane == 0) {
       // every X tile is read by all weight tiles of its group: keep it in L2
       const uint64_t pol_x = ptx::policy_evict_last();
       Ring rx;
@@ -585,7 +640,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       bool alive = true;
       Unit w;
       int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
         const int32_t row0 = int32_t(w.row0);
         const int nst = (w.kb1 - w.kb0) * kSub;
         for (int i0 = 0; i0 < nst; i0 += XQ) {
@@ -628,7 +683,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
     Unit w;
     int e_hint = -1;
-    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
+    for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       if (!warp_all(ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma))) break;
@@ -701,7 +756,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     bool alive = true;
     Unit w;
     int e_hint = -1;
-    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+    for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
       const int nst = (w.kb1 - w.kb0) * kSub;
       // Visit only this warpgroup's stages; ring slots and phases follow from the stage
       // counter (the ring depths are compile-time constants).
@@ -799,7 +854,27 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
     Unit w;
     int e_hint = -1;
-    for (int uj = 0; unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
+    // Output row of accumulator column `col` of the current unit, or -1.  Gathered (indexed
+    // MoE) tiles hold their rows in the first four columns of every eight.
+    auto row_of = [&](int col) -> int64_t {
+      int64_t m;
+      if constexpr (GATHER) {
+        if (col & 4) return -1;
+        m = w.row0 + ((col >> 3) << 2) + (col & 3);
+      } else {
+        m = w.row0 + col;
+      }
+      return m < w.row_end ? m : -1;
+    };
+    // Per-token activation scale of output row m (indexed: of the row it was gathered from).
+    auto tok_scale_of = [&](int64_t m) -> float {
+      if constexpr (GATHER) {
+        const int t = __ldg(a.row_index + m);
+        return t >= 0 ? a.tok_scale[t] : 0.0f;
+      }
+      return a.tok_scale[m];
+    };
+    for (int uj = 0; unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       const int nst = (w.kb1 - w.kb0) * kSub;
@@ -815,7 +890,6 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       // stages g0, g0 + 1, ... went to issuers (g0 + d) % kIssuers.
       const int active = min(C::kNumSub, nst);
       const int sub0 = int(g0 % uint32_t(C::kNumSub));
-      const int64_t m_first = w.row0 + int64_t(eh) * kCols;   // first row of this warp
       if constexpr (kHalves > 1) {
         if (!split) {
           // Wide tiles: scale and round every column of this warp to BF16 in registers,
@@ -838,7 +912,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             uint16_t* Yh = reinterpret_cast<uint16_t*>(Y) + n;
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
-              const int64_t m = m_first + j;
+              const int64_t m = w.row0 + int64_t(eh) * kCols + j;   // (never a gathered tile)
               if (m < w.row_end) {
                 uint16_t h = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
                 if (A8) {
@@ -867,10 +941,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           if (n_ok) {
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) {
-              const int64_t m = m_first + c * kChunk + j;
-              if (m < w.row_end) {
+              const int64_t m = GATHER ? row_of(eh * kCols + c * kChunk + j)
+                                       : w.row0 + int64_t(eh) * kCols + c * kChunk + j;
+              if (GATHER ? m >= 0 : m < w.row_end) {
                 float y = __uint_as_float(v[j]) * cs;
-                if (A8) y *= a.tok_scale[m];
+                if (A8) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }
             }
@@ -934,10 +1009,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           if (n_ok) {
 #pragma unroll
             for (int j = 0; j < kPass; ++j) {
-              const int64_t m = m_first + c0 + j;
-              if (m < w.row_end) {
+              const int64_t m = GATHER ? row_of(eh * kCols + c0 + j)
+                                       : w.row0 + int64_t(eh) * kCols + c0 + j;
+              if (GATHER ? m >= 0 : m < w.row_end) {
                 float y = sum[j] * cs2;
-                if (A8) y *= a.tok_scale[m];
+                if (A8) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }
             }
@@ -956,7 +1032,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   if (warp == kEpiWarp0) ptx::tmem_dealloc(tbase, C::kTmemCols);
 }
 
-template <int BNT, bool A8, int DM>
+template <int BNT, bool A8, int DM, bool GATHER>
 cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                            cudaStream_t st) {
   using C = GemmCfg<BNT, A8>;
@@ -965,24 +1041,32 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
   constexpr int kSmem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<BNT, A8, DM>,
+    cudaError_t e = cudaFuncSetAttribute(qgemm_tc_kernel<BNT, A8, DM, GATHER>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  qgemm_tc_kernel<BNT, A8, DM><<<plan.grid, Roles<BNT>::kThreads, kSmem, st>>>(tmap, args);
+  qgemm_tc_kernel<BNT, A8, DM, GATHER><<<plan.grid, Roles<BNT>::kThreads, kSmem, st>>>(tmap, args);
   return cudaGetLastError();
 }
 
 template <bool A8, int DM>
 cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                              cudaStream_t st) {
+  if (args.row_index != nullptr) {          // gathered (indexed MoE) tiles: up to 64 tokens
+    switch (plan.token_tile) {
+      case 16: return launch_variant<16, A8, DM, true>(plan, tmap, args, st);
+      case 32: return launch_variant<32, A8, DM, true>(plan, tmap, args, st);
+      case 64: return launch_variant<64, A8, DM, true>(plan, tmap, args, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (plan.token_tile) {
-    case 16: return launch_variant<16, A8, DM>(plan, tmap, args, st);
-    case 32: return launch_variant<32, A8, DM>(plan, tmap, args, st);
-    case 64: return launch_variant<64, A8, DM>(plan, tmap, args, st);
-    case 128: return launch_variant<128, A8, DM>(plan, tmap, args, st);
-    case 256: return launch_variant<256, A8, DM>(plan, tmap, args, st);
+    case 16: return launch_variant<16, A8, DM, false>(plan, tmap, args, st);
+    case 32: return launch_variant<32, A8, DM, false>(plan, tmap, args, st);
+    case 64: return launch_variant<64, A8, DM, false>(plan, tmap, args, st);
+    case 128: return launch_variant<128, A8, DM, false>(plan, tmap, args, st);
+    case 256: return launch_variant<256, A8, DM, false>(plan, tmap, args, st);
     default: return cudaErrorInvalidValue;
   }
 }

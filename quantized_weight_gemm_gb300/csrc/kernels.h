@@ -23,6 +23,9 @@ struct GemmArgs {
   const uint8_t* packed;       // expert 0
   int64_t expert_stride;       // bytes between experts (MoE), 0 for dense
   const int32_t* offsets;      // MoE: device int32 [E+1]; nullptr for dense
+  // Indexed MoE: device int32 [R], the X row of sorted position r (negative: padding);
+  // nullptr otherwise.  Gathered tiles hold token_tile / 2 rows (see the kernel).
+  const int32_t* row_index;
   int32_t E;
   int64_t M;                   // dense rows (M) or MoE rows (R)
   // Dense schedule.  Tiles are numbered in rasterization order (groups of group_m token

@@ -100,6 +100,19 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
 }
 
+// Four rows of a 2-D tensor (rows r0..r3, elements c0.. of the box width) into consecutive
+// rows at dst; the tensor map's box is one row high.  Negative or out-of-range rows read
+// the fill value (zero).
+__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t c0, int32_t r0,
+                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
+      :: "r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+         "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
 // 2-D tiled tensor copy global -> shared (coordinates: c0 innermost, in elements).
 __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t c0, int32_t c1,
                                             uint64_t* bar, uint64_t policy) {

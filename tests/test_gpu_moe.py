@@ -249,3 +249,97 @@ def test_moe_router_workload_sampled(T):
     assert qg.device_status(clear=True) == 0
     y = G.to_f64(y)
     _assert_close(y[rows], ref, TOL_A16)
+
+
+# ------------------------------------------------------------------------- indexed
+
+def _run_moe_indexed(ws, x_bits, offsets, row_index, afmt="bf16", tok_scale=None, stream_k=False):
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    d, packed = _pack_experts(ws, afmt)
+    off = torch.tensor(np.asarray(offsets, dtype=np.int32), device="cuda")
+    idx = torch.tensor(np.asarray(row_index, dtype=np.int32), device="cuda")
+    R = idx.numel()
+    wsp = qg.moe_workspace(d, len(ws), R) if stream_k else None
+    out = torch.full((R, ws[0].N), 5.0, dtype=torch.bfloat16, device="cuda")
+    for _ in range(2):              # the second call checks that the workspace came back clean
+        if afmt == "bf16":
+            y = qg.moe_indexed(d, packed, len(ws), G.bf16_tensor(x_bits), off, idx, out=out, ws=wsp)
+        else:
+            ts = torch.from_numpy(np.asarray(tok_scale, dtype=np.float32)).cuda()
+            y = qg.moe_indexed(d, packed, len(ws), G.u8_tensor(x_bits), off, idx, tok_scale=ts,
+                               out=out, ws=wsp)
+        torch.cuda.synchronize()
+        assert qg.device_status(clear=True) == 0
+    return G.to_f64(y)
+
+
+@pytest.mark.parametrize("stream_k", [False, True])
+@pytest.mark.parametrize("afmt", ["bf16", "fp8"])
+def test_moe_indexed_router(afmt, stream_k):
+    """Routed tokens gathered from X in token order (padding positions index -1), against
+    the oracle; FP8 rows take the scale of the row they come from."""
+    case = WL.moe_case(T=40, seed=5, E=8, topk=2, hidden=256, inter=64)
+    r = WL.rng(47)
+    ws = [WL.gen_weights(r, "mxfp4", 256, 256) for _ in range(8)]
+    idx = case.token_of_row.astype(np.int32)
+    if afmt == "bf16":
+        x = case.x_tok_bits
+        ref = oracle.moe_indexed(F_bits(x), case.offsets, idx, _experts_bf16(ws))
+        _assert_close(_run_moe_indexed(ws, x, case.offsets, idx, stream_k=stream_k), ref, TOL_A16)
+    else:
+        from oracle import formats as F
+        xq, s = oracle.quant_act_fp8(WL.gen_x(WL.rng(48), case.T, 256, outliers=True))
+        ref = oracle.moe_indexed(F.e4m3_to_float(xq), case.offsets, idx, _experts_exact(ws),
+                                 tok_scale=s)
+        y = _run_moe_indexed(ws, xq, case.offsets, idx, afmt="fp8", tok_scale=s, stream_k=stream_k)
+        _assert_close(y, ref, TOL_A8)
+
+
+@pytest.mark.parametrize("tile", [16, 32, 64])
+def test_moe_indexed_every_tile(tile):
+    """Arbitrary gathers: repeated rows, rows in any order, padding, empty experts and
+    blocks longer than one tile, for each token tile a gathered tile can have."""
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(49)
+    T, N, K = 37, 384, 512
+    counts = [0, 9, 1, 40, 0, 3, 17, 2]
+    off = _offsets(counts)
+    R = int(off[-1])
+    idx = r.integers(-1, T, size=R).astype(np.int32)          # includes -1 (padding)
+    x = WL.gen_x(r, T, K)
+    ws = [WL.gen_weights(r, "uint4_zp", N, K) for _ in counts]
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    qg.force_config(tile, 0)
+    try:
+        y = _run_moe_indexed(ws, x, off, idx)
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A16)
+    assert np.all(y[idx < 0] == 0)
+
+
+def test_moe_indexed_stream_k():
+    """Enough leftover tiles for the kernel to cut them over several CTAs (448 gathered
+    tiles of 8 rows: two whole rounds and 144 tiles of 24 K blocks cut)."""
+    r = WL.rng(50)
+    T, N, K = 12, 7168, 3072
+    counts = [1, 1, 2, 1, 1, 1, 1, 1]
+    off = _offsets(counts)
+    idx = r.permutation(T)[:int(off[-1])].astype(np.int32)
+    x = WL.gen_x(r, T, K)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    _assert_close(_run_moe_indexed(ws, x, off, idx, stream_k=True), ref, TOL_A16)
+
+
+def test_moe_indexed_refuses_wide_tiles():
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(51)
+    ws = [WL.gen_weights(r, "mxfp4", 256, 256) for _ in range(2)]
+    qg.force_config(128, 0)
+    try:
+        with pytest.raises(qg.QGemmError):
+            _run_moe_indexed(ws, WL.gen_x(r, 4, 256), [0, 2, 4], [0, 1, 2, 3])
+    finally:
+        qg.force_config(0, 0)

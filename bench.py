@@ -354,7 +354,9 @@ def sweep_mxfp4(device, flush, peaks, fp8):
 def sweep_moe(device, flush, peaks):
     """The MoE layer (E = 256 MXFP4 experts, top-8, hidden 7168, intermediate 2048):
     gate_up [4096 x 7168] and down [7168 x 2048] grouped GEMMs over expert-sorted rows,
-    T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone."""
+    T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone.  For
+    T <= 1024 the gate_up GEMM is also timed on the indexed path (token-order X gathered by
+    index), reported as gate_up_indexed_us beside the grouped time."""
     import numpy as np
     import torch
     import workloads as WL
@@ -395,6 +397,17 @@ def sweep_moe(device, flush, peaks):
                 tot_flops += 2.0 * valid * N * K
                 tot_w += wb
                 tot_b += wb + valid * K * 2 + valid * N * 2
+            # the same gate_up GEMM on the indexed path: X in token order [T, hidden], rows
+            # gathered by index (padding positions -1), no sorted copy of X
+            if T <= 1024:
+                N, K, _ = shapes["gate_up"]
+                Xt = torch.from_numpy(case.x_tok_bits.view(np.int16)).view(torch.bfloat16).to(device)
+                idx = torch.from_numpy(case.token_of_row.astype(np.int32)).to(device)
+                Y = torch.empty(R, N, dtype=torch.bfloat16, device=device)
+                d, p = descs["gate_up"], packs["gate_up"]
+                wsp = qg.moe_workspace(d, E, R, device=device)
+                ms = time_one(lambda: qg.moe_indexed(d, p, E, Xt, off, idx, out=Y, ws=wsp), flush)
+                r["gate_up_indexed_us"] = round(ms * 1e3, 2)
             r.update({"us": round(tot_ms * 1e3, 2),
                       "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 2),
                       "weight_gbs": round(tot_w / (tot_ms * 1e-3) / 1e9, 1),

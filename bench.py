@@ -68,8 +68,8 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "7f03174a95235a3a6c5c7a1f0d59edb534349d17ca9afceff4a2f6706a8d931e",
-    "launches": {"28672,8192,8192": 3025148000 + 930310144},
+    "csrc_sha256": "f9f54a13ef8c9651b97c190df9de2ca7d39f6bd3b28c4ccc0811da8b3a45e984",
+    "launches": {"28672,8192,8192": 2728057000 + 898700544},
 }
 
 
@@ -235,6 +235,37 @@ def run_step(cases, flush, e2e=False):
             out.append((c["N"], c["K"], M, e0, e1))
     torch.cuda.synchronize()
     return [(N, K, M, e0.elapsed_time(e1)) for (N, K, M, e0, e1) in out]
+
+
+def host_copy_rates(device, nbytes=256 << 20, reps=3):
+    """Pinned host <-> device copy rates of this machine in GB/s (best of `reps`), each direction
+    alone and both at once on two streams: the ceiling that the e2e leg's copies work under."""
+    import torch
+    h = [torch.empty(nbytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    d = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    s = [torch.cuda.Stream(device=device) for _ in range(2)]
+
+    def timed(fn):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def both():
+        with torch.cuda.stream(s[0]):
+            d[0].copy_(h[0], non_blocking=True)
+        with torch.cuda.stream(s[1]):
+            h[1].copy_(d[1], non_blocking=True)
+
+    t_h2d = timed(lambda: d[0].copy_(h[0], non_blocking=True))
+    t_d2h = timed(lambda: h[1].copy_(d[1], non_blocking=True))
+    t_both = timed(both)
+    return {"h2d": round(nbytes / t_h2d / 1e9, 1), "d2h": round(nbytes / t_d2h / 1e9, 1),
+            "both": round(2 * nbytes / t_both / 1e9, 1), "bytes_per_copy": nbytes}
 
 
 def cpu_sample(seconds=12.0, threads=1):
@@ -455,6 +486,7 @@ def bench_ours(args):
         run_step(cases, flush, e2e=True)
     e2e_steps = [run_step(cases, flush, e2e=True) for _ in range(max(1, args.steps))]
     torch.cuda.synchronize()
+    copy_gbs = host_copy_rates(device)
     extra = None
     if not args.no_extra:
         del cases
@@ -530,7 +562,8 @@ def bench_ours(args):
         "sweep": sweep,
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(M * K * 2 for (N, K) in SHAPES for M in M_SWEEP),
-                "d2h_bytes_per_step": sum(M * N * 2 for (N, K) in SHAPES for M in M_SWEEP)},
+                "d2h_bytes_per_step": sum(M * N * 2 for (N, K) in SHAPES for M in M_SWEEP),
+                "host_copy_gbs": copy_gbs},
         "gpu_launches": len(SHAPES) * len(M_SWEEP) * args.steps,
         "clocks": clocks,
     }

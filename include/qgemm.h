@@ -53,7 +53,8 @@ typedef enum {
                                   4 s, or QGEMM_TIMEOUT_MS milliseconds from the env)  */
   QGEMM_ERR_NO_DEVICE = 8,     /* no sm_103 device is current                          */
   QGEMM_ERR_BAD_VALUE = 9      /* (device status) repack met an E8M0 of 255, a non-finite
-                                  BF16 scale or a zero point above 15                  */
+                                  BF16 scale or a zero point above 15; a MoE call met
+                                  invalid offsets or a row index past the end of X     */
 } qgemm_status;
 
 typedef enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2 } qgemm_wfmt;
@@ -230,11 +231,13 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
  *   row_index      : device int32 [R], values in [0, T) or negative; 4-byte aligned
  *   Y              : device BF16 [R, ldy] in sorted order
  *   ws, ws_bytes   : as for qgemm_moe_grouped (qgemm_moe_workspace_bytes covers both)
- * Rows are gathered with TMA four at a time; a gathered tile holds half a token tile of
- * rows (token tiles up to 64: 8, 16 or 32 rows per tile, from R / E), which suits the
- * few rows per expert of decode-sized routing; the grouped call is the faster choice for
- * large batches.  QGEMM_ERR_UNSUPPORTED when qgemm_force_config forces a token tile above
- * 64.  "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths).
+ * The kernel copies the indexed rows into its activation tiles itself (token tiles of 16,
+ * 32 or 64 rows, from R / E), which suits the few rows per expert of decode-sized routing;
+ * for large batches the grouped call's wider tiles are faster.  An index >= T is an error
+ * (QGEMM_ERR_BAD_VALUE in the device status word, see qgemm_device_status) and that row
+ * reads as zeros.  QGEMM_ERR_UNSUPPORTED when qgemm_force_config forces a token tile
+ * above 64.
+ * "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths).
  */
 qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
                                int32_t afmt, const void* X, int64_t T, int64_t ldx,

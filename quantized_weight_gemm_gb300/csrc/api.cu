@@ -244,10 +244,10 @@ int moe_token_tile(int64_t R, int32_t E) {
   return tt;
 }
 
-// Indexed (gathered) MoE: tiles of token_tile / 2 rows, token tiles up to 64.
+// Indexed (gathered) MoE: the grouped rule, token tiles up to 64.
 int moe_indexed_token_tile(int64_t R, int32_t E) {
   const int64_t avg = R / E;
-  int tt = avg <= 8 ? 16 : avg <= 16 ? 32 : 64;
+  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : 64;
   if (g_force_tile) tt = g_force_tile;
   return tt;
 }
@@ -305,23 +305,6 @@ bool make_x_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   *is_3d = 0;
   return r == CUDA_SUCCESS;
-}
-
-// X rows gathered four at a time (tile::gather4): a 2-D map whose box is one 128-byte slab
-// of one row, 128-byte swizzle (the gathered rows land in the MMA's swizzled tile).
-bool make_x_gather_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K,
-                       int64_t ldx) {
-  EncodeFn enc = encode_fn();
-  if (enc == nullptr) return false;
-  const int esize = fp8 ? 1 : 2;
-  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  cuuint64_t dims[2] = {cuuint64_t(K), cuuint64_t(rows)};
-  cuuint64_t strides[1] = {cuuint64_t(ldx) * esize};
-  cuuint32_t box[2] = {cuuint32_t(128 / esize), 1};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 qgemm_status check_x(const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx) {
@@ -512,21 +495,25 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
   GemmPlan plan;
   const int tt = row_index != nullptr ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
-  if (row_index != nullptr && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathered tiles: <= 64
+  if (row_index != nullptr && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathering kernels: <= 64
   plan.token_tile = tt;
   plan.splits = 1;
   plan.sk_tiles = 0;
   plan.max_contrib = 0;
   plan.grid = dev->sms;
+  // the gathering kernel copies X rows itself and never reads a tensor map
   CUtensorMap tmap;
+  memset(&tmap, 0, sizeof(tmap));
   int x3d = 0;
-  if (row_index != nullptr) {
-    if (!make_x_gather_map(&tmap, X, fp8, x_rows, L.K, ldx)) return QGEMM_ERR_CUDA;
-  } else if (!make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d)) {
+  if (row_index == nullptr && !make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d))
     return QGEMM_ERR_CUDA;
-  }
   GemmArgs a;
   memset(&a, 0, sizeof(a));
+  if (row_index != nullptr) {
+    a.x = static_cast<const uint8_t*>(X);
+    a.ldx_bytes = ldx * (fp8 ? 1 : 2);
+    a.x_rows = x_rows;
+  }
   a.x_3d = x3d;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);

@@ -1,4 +1,4 @@
-// The tcgen05 quantized-weight GEMM kernel (dense and MoE grouped), sm_103a.
+// The tcgen05 quantized-weight GEMM kernel (dense, MoE grouped and MoE indexed), sm_103a.
 //
 // One persistent CTA per SM, warp-specialised.  A "stage" is 128 K-elements of one work
 // unit (a 128-row weight tile x a token tile, over a range of K); the 256-token BF16 variant
@@ -26,7 +26,9 @@
 //               weight scales as scale factors.
 //   activation  1 warp (one thread): TMA tiles of X (token_tile rows x 128 bytes per 64-K
 //   producer    slab, 128-byte swizzle) into the X ring; for narrow token tiles one 3-D load
-//               brings several stages at once.
+//               brings several stages at once.  Indexed MoE (the GATHER instantiations,
+//               token tiles up to 64): the whole warp copies the rows that the row index
+//               names with cp.async, 16 bytes per lane, into the same swizzled layout.
 //   record      2 warps (one thread each, alternate stages): one bulk copy per stage of the
 //   producers   packed weight record (codes, scales and zero points of 128 weight rows x
 //               128 K, see qgemm_internal.h) into the record ring, which is deep (up to 16
@@ -130,7 +132,7 @@ struct GemmCfg {
   static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
   static constexpr int kXSlotBytes = kXChunk * kXBytes;
   static constexpr int kXBoxSlabs = kXChunk * kSlabs;
-  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4 + (BNT / 2) * 4;
+  static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4 + BNT * 8;
   static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
   static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
                                 kAStages * kBarBytesPerA + kMiscBytes + 64;
@@ -364,6 +366,16 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
   }
 }
 
+// One gathered row of an activation slot: 16 bytes at src + s * 128 into dst + s * SLAB for
+// the S slabs s (src and dst already include the lane's piece).
+template <int S, int SLAB, int I = 0>
+__device__ __forceinline__ void gather_row(uint32_t dst, const uint8_t* src, uint64_t pol) {
+  if constexpr (I < S) {
+    ptx::cp_async_16_at<I * SLAB, I * 128>(dst, src, pol);
+    gather_row<S, SLAB, I + 1>(dst, src, pol);
+  }
+}
+
 template <int BNT, bool A8, int DM, bool GATHER>
 __global__ void __launch_bounds__(Roles<BNT>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
@@ -400,14 +412,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
                                                          // [8..14] schedule (Sched)
   int* prefix = misc + 16;                               // MoE: m-tiles before expert e
   int* offs = prefix + (kMaxExperts + 1);                // MoE: row offsets
-  int* idx_s = offs + (kMaxExperts + 1);                 // indexed MoE: the unit's X rows
+  int* idx_s = offs + (kMaxExperts + 1);                 // indexed MoE: X row offsets (int64)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const Layout& L = a.L;
-  // Output rows per tile: the token tile, or half of it for gathered (indexed MoE) tiles,
-  // whose rows fill the first four rows of every eight of the activation tile.
-  constexpr int tile_rows = GATHER ? BNT / 2 : BNT;
 
   // ------------------------------------------------------------------ prologue
   // The header loads are issued first and checked after the barrier set-up, and tensor
@@ -426,7 +435,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       ptx::mbar_init(&rempty[s], 4);     // one arrival per dequant warp
     }
     for (int s = 0; s < SX; ++s) {
-      ptx::mbar_init(&xfull[s], 1);
+      ptx::mbar_init(&xfull[s], GATHER ? 32 : 1);   // gathered slots: one arrival per lane
       ptx::mbar_init(&xempty[s], C::kIssuers);
     }
     for (int s = 0; s < SA; ++s) {
@@ -458,7 +467,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     ptx::tmem_alloc(reinterpret_cast<uint32_t*>(&misc[0]), C::kTmemCols);
     ptx::tmem_relinquish();
   }
-  if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
+  if constexpr (!GATHER)
+    if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
   int num_units = a.num_units;
   if (a.offsets != nullptr && warp == 0) {
     // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).  All offsets
@@ -486,7 +496,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (e < a.E) {
         const int o = offs[e], o1 = offs[e + 1];
         if (o1 < o || o < 0 || o1 > a.M) bad = true;
-        t = (o1 > o) ? (o1 - o + tile_rows - 1) / tile_rows : 0;
+        t = (o1 > o) ? (o1 - o + BNT - 1) / BNT : 0;
       }
       int incl = t;
 #pragma unroll
@@ -555,7 +565,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       bool alive = true;
       Unit w;
       int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
+      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
         const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
                              (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
         for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
@@ -588,50 +598,67 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer
     if constexpr (GATHER) {
-      // Gathered (indexed MoE) tiles: the whole warp stages the unit's row indices in shared
-      // memory, then one thread loads four rows at a time (tile::gather4) into the first
-      // half of each 8-row swizzle atom, so that every load starts on a 1024-byte boundary.
+      // Gathered (indexed MoE) tiles: the warp copies each unit's rows out of X in token
+      // order, 16 bytes per lane and copy (cp.async), straight into the 128-byte-swizzled
+      // layout that the MMA reads (16-byte piece j of tile row i sits at piece j xor (i mod 8)
+      // of the row's 128 bytes).  The eight lanes of a group cover one 128-byte line, so each
+      // instruction reads four whole lines, and a lane keeps its row's source offset over
+      // the slabs.  Rows past the end of the expert's block are not copied: their
+      // accumulator columns are never stored, and MMA column n reads activation row n only.
+      // Each lane hands its copies of a slot to the slot's barrier (32 arrivals,
+      // each made by the hardware once that lane's copies have landed), so the warp never
+      // waits for its own copies and runs up to the ring's depth ahead.  The copies land in
+      // the generic proxy: the MMA issuers fence them for the tensor cores after their wait.
+      // Negative indices and columns past K are zero-filled; an index past the end of X
+      // sets the error status and reads zeros.
+      constexpr int kEsz = A8 ? 1 : 2;
       const uint64_t pol_x = ptx::policy_evict_last();
+      int64_t* xoff_s = reinterpret_cast<int64_t*>(idx_s);
+      const int grp = lane >> 3, ch = lane & 7;
       Ring rx;
-      uint32_t pending = 0, pending_parity = 0;
       bool alive = true;
       Unit w;
       int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
-        // rows past the expert's block are padding (index -1: the load reads zeros)
-        for (int i = lane; i < tile_rows; i += 32) {
-          const int64_t r = w.row0 + i;
-          idx_s[i] = r < w.row_end ? __ldg(a.row_index + r) : -1;
+      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+        __syncwarp();                     // every lane is done with the previous unit's rows
+        const int nrows = w.row_end - w.row0 < BNT ? int(w.row_end - w.row0) : BNT;
+        for (int i = lane; i < nrows; i += 32) {
+          const int32_t t = __ldg(a.row_index + w.row0 + i);
+          if (t >= a.x_rows) atomicCAS(a.status, 0, kStatusBadValue);
+          xoff_s[i] = t >= 0 && t < a.x_rows ? int64_t(t) * a.ldx_bytes : -1;
         }
         __syncwarp();
-        if (lane == 0) {
-          const int nst = (w.kb1 - w.kb0) * kSub;
-          for (int i0 = 0; i0 < nst; i0 += XQ) {
-            if (!ptx::mbar_wait(&xempty[rx.slot], rx.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
-            uint8_t* sx = s_x + rx.slot * C::kXSlotBytes;
-            const int k0 = w.kb0 * kStageK + i0 * (kStageK / kSub);
-            ptx::mbar_arrive_expect_tx(&xfull[rx.slot], uint32_t(C::kXSlotBytes / 2));
-#pragma unroll 1
-            for (int sl = 0; sl < C::kXBoxSlabs; ++sl)
-#pragma unroll 1
-              for (int at = 0; at < BNT / 8; ++at)
-                ptx::tma_gather4(sx + sl * C::kSlabBytes + at * 1024, &tmap_x,
-                                 k0 + sl * (A8 ? 128 : 64), idx_s[4 * at], idx_s[4 * at + 1],
-                                 idx_s[4 * at + 2], idx_s[4 * at + 3], &xfull[rx.slot], pol_x);
-            pending |= 1u << rx.slot;
-            pending_parity = (pending_parity & ~(1u << rx.slot)) | (rx.phase << rx.slot);
-            rx.next(SX);
+        const int nst = (w.kb1 - w.kb0) * kSub;
+        for (int i0 = 0; i0 < nst; i0 += XQ) {
+          if (!warp_all(ptx::mbar_wait(&xempty[rx.slot], rx.phase ^ 1u, abort_flag, T, kSleepProducer))) { alive = false; break; }
+          const uint32_t sx = ptx::smem_u32(s_x + rx.slot * C::kXSlotBytes);
+          // first column (elements) of this lane's piece in the slot's first slab, and the
+          // number of the slot's slabs in which that piece lies before K (K is a multiple of
+          // 32, so a piece is wholly inside K or wholly past it)
+          const int64_t c0 = int64_t(w.kb0) * kStageK + i0 * (kStageK / kSub) + ch * (16 / kEsz);
+          const int64_t left = (L.K - c0 + 128 / kEsz - 1) / (128 / kEsz);
+          const int n_in = left <= 0 ? 0 : left < C::kXBoxSlabs ? int(left) : C::kXBoxSlabs;
+          const uint8_t* xk = a.x + c0 * kEsz;
+#pragma unroll 2
+          for (int i = grp; i < nrows; i += 4) {
+            const int64_t off = xoff_s[i];
+            const uint32_t dst = sx + uint32_t(i * 128 + ((ch ^ (i & 7)) << 4));
+            if (off >= 0 && n_in == C::kXBoxSlabs) {
+              gather_row<C::kXBoxSlabs, C::kSlabBytes>(dst, xk + off, pol_x);
+            } else {
+#pragma unroll
+              for (int sl = 0; sl < C::kXBoxSlabs; ++sl) {
+                const bool in = off >= 0 && sl < n_in;
+                ptx::cp_async_16(dst + sl * C::kSlabBytes, in ? xk + off + sl * 128 : a.x,
+                                 in ? 16u : 0u, pol_x);
+              }
+            }
           }
+          ptx::cp_async_arrive_noinc(&xfull[rx.slot]);
+          rx.next(SX);
         }
-        // the warp moves on together (the index cache is rewritten next unit)
-        alive = __shfl_sync(0xffffffffu, alive ? 1 : 0, 0) != 0;
       }
-      if (lane == 0 && !alive) {
-        volatile int no_abort = 0;
-        for (int s = 0; s < SX; ++s)
-          if (pending & (1u << s))
-            ptx::mbar_wait(&xfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
-      }
+      ptx::cp_async_wait_all();           // nothing of this warp is left in flight at exit
     } else if (lane == 0) {
       // every X tile is read by all weight tiles of its group: keep it in L2
       const uint64_t pol_x = ptx::policy_evict_last();
@@ -640,7 +667,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       bool alive = true;
       Unit w;
       int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
+      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
         const int32_t row0 = int32_t(w.row0);
         const int nst = (w.kb1 - w.kb0) * kSub;
         for (int i0 = 0; i0 < nst; i0 += XQ) {
@@ -683,7 +710,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
     Unit w;
     int e_hint = -1;
-    for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj, ++ui) {
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       if (!warp_all(ptx::mbar_wait(&accempty[acc], acc_par ^ 1u, abort_flag, T, kSleepMma))) break;
@@ -695,6 +722,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         // Every issuer waits for every X slot, even one without a stage of its own: its
         // release of the slot below must count towards this fill of the slot, not the next.
         if (!warp_all(ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepMma))) { alive = false; break; }
+        // gathered slots were written by cp.async (generic proxy): order them before the
+        // tensor cores read them
+        if constexpr (GATHER) ptx::fence_proxy_async_smem();
         const int x1 = x0 + XQ < nst ? x0 + XQ : nst;
         // this issuer's stages in [x0, x1): CTA stage g0 + i with (g0 + i) % kIssuers == issuer
         const uint32_t gx = g0 + uint32_t(x0);
@@ -756,7 +786,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     bool alive = true;
     Unit w;
     int e_hint = -1;
-    for (int uj = 0; alive && unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj) {
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
       const int nst = (w.kb1 - w.kb0) * kSub;
       // Visit only this warpgroup's stages; ring slots and phases follow from the stage
       // counter (the ring depths are compile-time constants).
@@ -854,27 +884,15 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
     Unit w;
     int e_hint = -1;
-    // Output row of accumulator column `col` of the current unit, or -1.  Gathered (indexed
-    // MoE) tiles hold their rows in the first four columns of every eight.
-    auto row_of = [&](int col) -> int64_t {
-      int64_t m;
-      if constexpr (GATHER) {
-        if (col & 4) return -1;
-        m = w.row0 + ((col >> 3) << 2) + (col & 3);
-      } else {
-        m = w.row0 + col;
-      }
-      return m < w.row_end ? m : -1;
-    };
     // Per-token activation scale of output row m (indexed: of the row it was gathered from).
     auto tok_scale_of = [&](int64_t m) -> float {
       if constexpr (GATHER) {
         const int t = __ldg(a.row_index + m);
-        return t >= 0 ? a.tok_scale[t] : 0.0f;
+        return t >= 0 && t < a.x_rows ? a.tok_scale[t] : 0.0f;
       }
       return a.tok_scale[m];
     };
-    for (int uj = 0; unit_at(uj, a, sc, tile_rows, prefix, offs, e_hint, w); ++uj, ++ui) {
+    for (int uj = 0; unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
       const int nst = (w.kb1 - w.kb0) * kSub;
@@ -941,9 +959,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           if (n_ok) {
 #pragma unroll
             for (int j = 0; j < kChunk; ++j) {
-              const int64_t m = GATHER ? row_of(eh * kCols + c * kChunk + j)
-                                       : w.row0 + int64_t(eh) * kCols + c * kChunk + j;
-              if (GATHER ? m >= 0 : m < w.row_end) {
+              const int64_t m = w.row0 + int64_t(eh) * kCols + c * kChunk + j;
+              if (m < w.row_end) {
                 float y = __uint_as_float(v[j]) * cs;
                 if (A8) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
@@ -1009,9 +1026,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           if (n_ok) {
 #pragma unroll
             for (int j = 0; j < kPass; ++j) {
-              const int64_t m = GATHER ? row_of(eh * kCols + c0 + j)
-                                       : w.row0 + int64_t(eh) * kCols + c0 + j;
-              if (GATHER ? m >= 0 : m < w.row_end) {
+              const int64_t m = w.row0 + int64_t(eh) * kCols + c0 + j;
+              if (m < w.row_end) {
                 float y = sum[j] * cs2;
                 if (A8) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);

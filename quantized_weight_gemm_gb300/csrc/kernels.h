@@ -24,8 +24,11 @@ struct GemmArgs {
   int64_t expert_stride;       // bytes between experts (MoE), 0 for dense
   const int32_t* offsets;      // MoE: device int32 [E+1]; nullptr for dense
   // Indexed MoE: device int32 [R], the X row of sorted position r (negative: padding);
-  // nullptr otherwise.  Gathered tiles hold token_tile / 2 rows (see the kernel).
+  // nullptr otherwise.  The gathering kernel copies those rows from x itself (no tensor map).
   const int32_t* row_index;
+  const uint8_t* x;            // indexed MoE: X in token order, x_rows rows of ldx_bytes
+  int64_t ldx_bytes;
+  int64_t x_rows;
   int32_t E;
   int64_t M;                   // dense rows (M) or MoE rows (R)
   // Dense schedule.  Tiles are numbered in rasterization order (groups of group_m token

@@ -100,17 +100,31 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       :: "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
 }
 
-// Four rows of a 2-D tensor (rows r0..r3, elements c0.. of the box width) into consecutive
-// rows at dst; the tensor map's box is one row high.  Negative or out-of-range rows read
-// the fill value (zero).
-__device__ __forceinline__ void tma_gather4(void* dst, const void* tmap, int32_t c0, int32_t r0,
-                                            int32_t r1, int32_t r2, int32_t r3, uint64_t* bar,
+// 16 bytes global -> shared through L2 only (cp.async.cg): the first src_bytes (0 or 16)
+// come from src and the rest is zero-filled.  The bytes land in the generic proxy.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes,
                                             uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;"
-      :: "r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-         "r"(smem_u32(bar)), "l"(policy) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;"
+               :: "r"(dst), "l"(src), "r"(src_bytes), "l"(policy) : "memory");
+}
+
+// The same with the shared and global addresses offset by compile-time byte counts (folded
+// into the instruction), all 16 bytes from src.
+template <int DOFF, int SOFF>
+__device__ __forceinline__ void cp_async_16_at(uint32_t dst, const void* src, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0+%3], [%1+%4], 16, %2;"
+               :: "r"(dst), "l"(src), "l"(policy), "n"(DOFF), "n"(SOFF) : "memory");
+}
+
+// Wait for every cp.async this thread has issued, committed or not.
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Arrive on bar once every cp.async this thread has issued so far has completed; the
+// barrier's expected count includes this arrival (noinc).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
 }
 
 // 2-D tiled tensor copy global -> shared (coordinates: c0 innermost, in elements).

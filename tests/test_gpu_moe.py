@@ -321,7 +321,7 @@ def test_moe_indexed_every_tile(tile):
 
 def test_moe_indexed_stream_k():
     """Enough leftover tiles for the kernel to cut them over several CTAs (448 gathered
-    tiles of 8 rows: two whole rounds and 144 tiles of 24 K blocks cut)."""
+    tiles of 16 rows: two whole rounds and 144 tiles of 24 K blocks cut)."""
     r = WL.rng(50)
     T, N, K = 12, 7168, 3072
     counts = [1, 1, 2, 1, 1, 1, 1, 1]
@@ -331,6 +331,64 @@ def test_moe_indexed_stream_k():
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
     _assert_close(_run_moe_indexed(ws, x, off, idx, stream_k=True), ref, TOL_A16)
+
+
+@pytest.mark.parametrize("tile", [16, 64])
+def test_moe_indexed_ragged_k_and_stride(tile):
+    """K = 608 ends inside an activation slot (512 K for 16-row tiles, 256 for 64), and X is a
+    view into wider rows whose extra columns hold NaN: the gathered copies must stop at K
+    and zero-fill the rest of the slot."""
+    import quantized_weight_gemm_gb300 as qg
+    from tests import gpu_util as G
+    r = WL.rng(52)
+    T, N, K = 29, 256, 608
+    counts = [5, 0, 30, 11]
+    off = _offsets(counts)
+    idx = r.integers(-1, T, size=int(off[-1])).astype(np.int32)
+    x = WL.gen_x(r, T, K)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    wide = torch.full((T, K + 64), float("nan"), dtype=torch.bfloat16, device="cuda")
+    wide[:, :K] = G.bf16_tensor(x)
+    d, packed = _pack_experts(ws)
+    qg.force_config(tile, 0)
+    try:
+        y = qg.moe_indexed(d, packed, len(ws), wide[:, :K],
+                           torch.tensor(off, dtype=torch.int32, device="cuda"),
+                           torch.tensor(idx, device="cuda"))
+        torch.cuda.synchronize()
+        assert qg.device_status(clear=True) == 0
+    finally:
+        qg.force_config(0, 0)
+    y = G.to_f64(y)
+    assert np.all(np.isfinite(y))
+    _assert_close(y, ref, TOL_A16)
+
+
+def test_moe_indexed_index_past_end():
+    """A row index at or past T is reported in the device status word (BAD_VALUE) and its
+    row reads as zeros; the other rows are unaffected."""
+    import quantized_weight_gemm_gb300 as qg
+    from tests import gpu_util as G
+    r = WL.rng(53)
+    T, N, K = 10, 256, 256
+    counts = [3, 4]
+    off = _offsets(counts)
+    idx = np.array([0, 9, T, 2, T + 1000, -1, 5], dtype=np.int32)
+    x = WL.gen_x(r, T, K)
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
+    ok_idx = np.where(idx < T, idx, -1).astype(np.int32)
+    ref = oracle.moe_indexed(F_bits(x), off, ok_idx, _experts_bf16(ws))
+    d, packed = _pack_experts(ws)
+    qg.device_status(clear=True)
+    y = qg.moe_indexed(d, packed, len(ws), G.bf16_tensor(x),
+                       torch.tensor(off, dtype=torch.int32, device="cuda"),
+                       torch.tensor(idx, device="cuda"))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 9          # QGEMM_ERR_BAD_VALUE
+    y = G.to_f64(y)
+    assert np.all(y[idx >= T] == 0)
+    _assert_close(y, ref, TOL_A16)
 
 
 def test_moe_indexed_refuses_wide_tiles():

@@ -24,6 +24,13 @@ Readings where the pages are silent (each is listed in the design notes):
   * INT4 symmetric: the nibble is a two's-complement q in [-8, 7], w = q * s[n, k//g];
   * INT4 with zero point: q, z in [0, 15], w = (q - z) * s[n, k//g] (no "+1" offset);
   * MXFP4: w = e2m1(q) * 2^(e[n, k//32] - 127);
+  * MXINT4 (named beside NVFP4 for the B300 MoE results of the German page, section
+    "WnA16"): the nibble is a two's-complement q in [-8, 7] with one E8M0 per 32 K,
+    w = q * 2^(e[n, k//32] - 127) (no implicit fixed-point factor; one would only shift e);
+  * NVFP4 (same place): w = e2m1(q) * e4m3(s[n, k//16]) * g with a float32 per-tensor g.
+    The 16-bit operand is e2m1(q) * e4m3(s), which BF16 holds exactly, and g is a
+    per-tensor secondary scale that multiplies the output (the output stage, as for the
+    per-channel scale);
   * secondary scale: optional float32 c[n] multiplying output column n;
   * FP8 activation quantization: per row m, s_m = amax_m / 448 in float32 (1.0 when the row
     is all zero), codes = e4m3 round-to-nearest-even with saturation of x / s_m computed in
@@ -37,7 +44,7 @@ import numpy as np
 
 from . import formats as F
 
-WFMTS = ("int4_sym", "uint4_zp", "mxfp4")
+WFMTS = ("int4_sym", "uint4_zp", "mxfp4", "mxint4", "nvfp4")
 
 
 def unpack_nibbles(codes):
@@ -51,18 +58,23 @@ def unpack_nibbles(codes):
 
 
 def scale_values(wfmt, scales):
-    """Per-group scale values as float64: BF16 bit patterns, or E8M0 exponents for MXFP4."""
-    if wfmt == "mxfp4":
+    """Per-group scale values as float64: BF16 bit patterns, E8M0 exponents (MXFP4, MXINT4)
+    or E4M3 codes (NVFP4)."""
+    if wfmt in ("mxfp4", "mxint4"):
         return F.e8m0_to_float(scales)
+    if wfmt == "nvfp4":
+        return F.e4m3_to_float(scales)
     return F.bf16_bits_to_float(scales)
 
 
-def dequant(wfmt, group, codes, scales, zeros=None):
+def dequant(wfmt, group, codes, scales, zeros=None, global_scale=1.0):
     """Exact dequantized weights W [N, K] in float64.
 
-    wfmt: "int4_sym" | "uint4_zp" | "mxfp4"; group: K-elements per scale (32 for mxfp4);
-    codes: uint8 [N, K/2]; scales: uint16 bf16 bits [N, K/group] (uint8 E8M0 for mxfp4);
-    zeros: uint8 [N, K/group] in [0, 15] for "uint4_zp", else None.
+    wfmt: "int4_sym" | "uint4_zp" | "mxfp4" | "mxint4" | "nvfp4"; group: K-elements per
+    scale (32 for mxfp4 and mxint4, 16 for nvfp4); codes: uint8 [N, K/2]; scales: uint16
+    bf16 bits [N, K/group], uint8 E8M0 (mxfp4, mxint4) or uint8 E4M3 (nvfp4); zeros: uint8
+    [N, K/group] in [0, 15] for "uint4_zp", else None; global_scale: the per-tensor float32
+    factor (NVFP4's second-level scale; 1 for the other formats).
     """
     if wfmt not in WFMTS:
         raise ValueError(wfmt)
@@ -72,16 +84,18 @@ def dequant(wfmt, group, codes, scales, zeros=None):
         raise ValueError("K must be a multiple of the group size")
     gidx = np.arange(k) // group                       # group of each K position
     s = scale_values(wfmt, scales)[:, gidx]            # [N, K]
-    if wfmt == "int4_sym":
-        return F.int4_signed(q).astype(np.float64) * s
+    g = np.float64(np.float32(global_scale))
+    if wfmt in ("int4_sym", "mxint4"):
+        return F.int4_signed(q).astype(np.float64) * s * g
     if wfmt == "uint4_zp":
         z = np.asarray(zeros).astype(np.int64)[:, gidx]
-        return (q.astype(np.int64) - z).astype(np.float64) * s
-    return F.e2m1_to_float(q) * s
+        return (q.astype(np.int64) - z).astype(np.float64) * s * g
+    return F.e2m1_to_float(q) * s * g
 
 
 def dequant_bf16(wfmt, group, codes, scales, zeros=None):
-    """The weights as a kernel must feed them to a BF16 tensor core: RNE_bf16(W_exact)."""
+    """The weights as a kernel must feed them to a BF16 tensor core: RNE_bf16(W_exact),
+    without the per-tensor scale (that one multiplies the output)."""
     return F.round_to_bf16(dequant(wfmt, group, codes, scales, zeros))
 
 
@@ -98,15 +112,17 @@ def gemm(x, w, chan_scale=None, tok_scale=None):
     return y
 
 
-def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None, global_scale=1.0):
     """Dense W4A16: BF16 activations (bit patterns [M, K]) times the dequantized weights.
 
     W4A16 computes on 16-bit tensor cores ("Humming wird angekündigt", section "WnA16":
     low-bit weights combined with FP16/BF16 activations, using the widely available 16-bit
     compute), so the dequantized weight is the BF16 value RNE_bf16(W_exact) -- the same
-    weights the dequantization must reproduce bit for bit.  The sum runs in float64."""
+    weights the dequantization must reproduce bit for bit.  The sum runs in float64; the
+    per-tensor scale (NVFP4) then multiplies the output like the per-channel one."""
     x = F.bf16_bits_to_float(x_bits)
-    return gemm(x, dequant_bf16(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+    y = gemm(x, dequant_bf16(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+    return y * np.float64(np.float32(global_scale))
 
 
 def quant_act_fp8(x_bits):

@@ -72,7 +72,15 @@ def _e2m1_table():
     return {int(k): Fraction(v[0][0]) for k, v in g.items()}
 
 
-def _brute_force(wfmt, group, codes, scales_val, zeros, x_int):
+def _e4m3_fraction(code):
+    """E4M3 (OCP "fn") code -> exact rational, from the format definition: exponent field
+    e (bias 7), mantissa m, value (1 + m/8) 2^(e-7), or m/8 2^-6 when e == 0."""
+    e, m = (code >> 3) & 15, code & 7
+    v = Fraction(m, 8) * Fraction(1, 64) if e == 0 else (1 + Fraction(m, 8)) * Fraction(2) ** (e - 7)
+    return -v if code & 0x80 else v
+
+
+def _brute_force(wfmt, group, codes, scales_val, zeros, x_int, g=Fraction(1)):
     """y[m][n] with Python rationals: nibble k from byte k//2 (low nibble for even k)."""
     tab = _e2m1_table()
     N, Kh = codes.shape
@@ -84,29 +92,39 @@ def _brute_force(wfmt, group, codes, scales_val, zeros, x_int):
             byte = int(codes[n, k // 2])
             nib = (byte >> 4) if (k % 2) else (byte & 15)
             s = scales_val[n][k // group]
-            if wfmt == "int4_sym":
+            if wfmt in ("int4_sym", "mxint4"):
                 w = (nib - 16 if nib >= 8 else nib) * s
             elif wfmt == "uint4_zp":
                 w = (nib - int(zeros[n, k // group])) * s
             else:
                 w = tab[nib] * s
             for m in range(M):
-                y[m][n] += x_int[m][k] * w
+                y[m][n] += x_int[m][k] * w * g
     return y
 
 
-@pytest.mark.parametrize("wfmt,group", [("int4_sym", 32), ("uint4_zp", 64), ("mxfp4", 32)])
+@pytest.mark.parametrize("wfmt,group", [("int4_sym", 32), ("uint4_zp", 64), ("mxfp4", 32),
+                                        ("mxint4", 32), ("nvfp4", 16)])
 def test_integer_brute_force(wfmt, group):
     r = np.random.Generator(np.random.PCG64(7))
     M, N, K = 3, 5, 128
     x_int = r.integers(-4, 5, size=(M, K))
     codes = r.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
     G = K // group
-    if wfmt == "mxfp4":
+    g, gf = 1.0, Fraction(1)
+    if wfmt in ("mxfp4", "mxint4"):
         exps = r.integers(124, 131, size=(N, G), dtype=np.uint8)
         scales = exps
         scales_val = [[Fraction(2) ** (int(e) - 127) for e in row] for row in exps]
         zeros = None
+    elif wfmt == "nvfp4":
+        # every E4M3 code but NaN, subnormals included, either sign; a float32 global scale
+        scales = r.integers(0, 256, size=(N, G), dtype=np.uint8)
+        scales[(scales & 0x7F) == 0x7F] = 0x38
+        scales_val = [[_e4m3_fraction(int(c)) for c in row] for row in scales]
+        zeros = None
+        g = float(np.float32(0.3))
+        gf = Fraction(g)
     else:
         p = r.integers(-3, 3, size=(N, G))
         sv = np.ldexp(1.0, p)
@@ -114,8 +132,8 @@ def test_integer_brute_force(wfmt, group):
         scales_val = [[Fraction(2) ** int(e) for e in row] for row in p]
         zeros = r.integers(0, 16, size=(N, G), dtype=np.uint8) if wfmt == "uint4_zp" else None
     xb = F.float_to_bf16_bits(x_int.astype(np.float64))
-    Y = oracle.w4a16(xb, wfmt, group, codes, scales, zeros)
-    ref = _brute_force(wfmt, group, codes, scales_val, zeros, x_int.tolist())
+    Y = oracle.w4a16(xb, wfmt, group, codes, scales, zeros, global_scale=g)
+    ref = _brute_force(wfmt, group, codes, scales_val, zeros, x_int.tolist(), gf)
     for m in range(M):
         for n in range(N):
             assert Fraction(Y[m, n]) == ref[m][n], (m, n)
@@ -166,16 +184,22 @@ def test_scale_linearity():
     np.testing.assert_array_equal(y2, 2 * y1)
 
 
-@pytest.mark.parametrize("wfmt,group", [("uint4_zp", 128), ("mxfp4", 32)])
+@pytest.mark.parametrize("wfmt,group", [("uint4_zp", 128), ("mxfp4", 32), ("mxint4", 32),
+                                        ("nvfp4", 16)])
 def test_group_boundary_selects_next_scale(wfmt, group):
     r = np.random.Generator(np.random.PCG64(6))
     N, K = 8, 4 * group
     nib = np.full((N, K), 2, np.uint8)                    # int 2 / e2m1 1.0 everywhere
     codes = WL.pack_nibbles(nib)
-    if wfmt == "mxfp4":
+    if wfmt in ("mxfp4", "mxint4"):
         scales = r.integers(100, 140, size=(N, K // group), dtype=np.uint8)
         zeros = None
         sv = np.ldexp(1.0, scales.astype(np.int64) - 127)
+        unit = 1.0 if wfmt == "mxfp4" else 2.0
+    elif wfmt == "nvfp4":
+        scales = r.integers(0x08, 0x78, size=(N, K // group), dtype=np.uint8)   # normals
+        zeros = None
+        sv = np.array([[float(_e4m3_fraction(int(c))) for c in row] for row in scales])
         unit = 1.0
     else:
         scales = WL.to_bf16_bits(r.uniform(0.5, 2, size=(N, K // group)).astype(np.float32))
@@ -186,6 +210,43 @@ def test_group_boundary_selects_next_scale(wfmt, group):
     for j in range(K // group):
         np.testing.assert_array_equal(W[:, j * group], unit * sv[:, j])
         np.testing.assert_array_equal(W[:, j * group + group - 1], unit * sv[:, j])
+
+
+def test_worked_mxint4_and_nvfp4_values():
+    """Hand-worked weights from the format definitions.  MXINT4, E8M0 129 (x4): nibbles
+    8, 7, 15, 1 are -8, 7, -1, 1 -> -32, 28, -4, 4.  NVFP4 with per-tensor scale 0.5:
+    e2m1 7 (6.0) x E4M3 0x38 (1.0) -> 3.0; e2m1 11 (-1.5) x 0x01 (the smallest subnormal,
+    2^-9) -> -1.5 * 2^-10; e2m1 1 (0.5) x 0x7E (448) -> 112; e2m1 8 (-0) x 0x50 (4.0) -> -0."""
+    codes = np.array([[0x78, 0x1F] + [0] * 14], dtype=np.uint8)        # 32 elements
+    W = oracle.dequant("mxint4", 32, codes, np.array([[129]], dtype=np.uint8))
+    np.testing.assert_array_equal(W[0, :4], [-32.0, 28.0, -4.0, 4.0])
+    for j, (c, sc, want) in enumerate([(7, 0x38, 3.0), (11, 0x01, -1.5 * 2.0 ** -10),
+                                       (1, 0x7E, 112.0), (8, 0x50, -0.0)]):
+        cd = np.zeros((1, 8), np.uint8)                                  # 16 elements
+        cd[0, 0] = c
+        w = oracle.dequant("nvfp4", 16, cd, np.array([[sc]], dtype=np.uint8), global_scale=0.5)
+        assert w[0, 0] == want and np.signbit(w[0, 0]) == np.signbit(want), (j, w[0, 0])
+
+
+def test_nvfp4_global_scale_multiplies_the_output():
+    """The per-tensor scale multiplies the output, after the BF16 operand e2m1 x E4M3
+    (exact): a one-hot row reproduces g x e2m1 x s without a BF16 rounding of the product
+    with g, and y(g) = g y(1)."""
+    r = np.random.Generator(np.random.PCG64(11))
+    w = WL.gen_weights(r, "nvfp4", 6, 64)
+    g = float(np.float32(0.1234567))
+    exact = oracle.dequant("nvfp4", 16, w.codes, w.scales, global_scale=g)
+    assert np.any(F.round_to_bf16(exact) != exact)           # g makes the product inexact
+    for k in (0, 15, 16, 63):
+        onehot = np.zeros((1, 64))
+        onehot[0, k] = 1.0
+        y = oracle.w4a16(F.float_to_bf16_bits(onehot), "nvfp4", 16, w.codes, w.scales,
+                         global_scale=g)
+        np.testing.assert_array_equal(y[0], exact[:, k])
+    x = WL.gen_x(r, 3, 64)
+    y1 = oracle.w4a16(x, "nvfp4", 16, w.codes, w.scales)
+    yg = oracle.w4a16(x, "nvfp4", 16, w.codes, w.scales, global_scale=g)
+    np.testing.assert_array_equal(yg, y1 * g)
 
 
 def test_fp8_activation_worked_example():

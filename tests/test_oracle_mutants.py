@@ -28,6 +28,10 @@ PINS = [
     lambda: TG.test_group_boundary_selects_next_scale("mxfp4", 32),
     TG.test_fp8_activation_worked_example, TG.test_fp8_activation_invariants,
     TG.test_w4a8_equals_dense_on_dequantized_activations, TG.test_moe_decomposition,
+    lambda: TG.test_integer_brute_force("mxint4", 32),
+    lambda: TG.test_integer_brute_force("nvfp4", 16),
+    lambda: TG.test_group_boundary_selects_next_scale("nvfp4", 16),
+    TG.test_worked_mxint4_and_nvfp4_values, TG.test_nvfp4_global_scale_multiplies_the_output,
 ]
 
 
@@ -92,9 +96,11 @@ def _gemm_transposed(x, w, chan_scale=None, tok_scale=None):
     return y
 
 
-def _w4a16_exact_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+def _w4a16_exact_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None,
+                         global_scale=1.0):
     x = F.bf16_bits_to_float(x_bits)
-    return Q.gemm(x, Q.dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+    return Q.gemm(x, Q.dequant(wfmt, group, codes, scales, zeros, global_scale),
+                  chan_scale=chan_scale)
 
 
 def _gemm_drop_tok_scale(x, w, chan_scale=None, tok_scale=None):
@@ -109,8 +115,32 @@ def _quant_no_zero_guard(x_bits):
     return F.e4m3_encode(F.round_to_e4m3_satfinite(v.astype(np.float64))), s
 
 
+def _scale_values_nvfp4_as_e8m0(wfmt, scales):
+    if wfmt == "nvfp4":
+        return F.e8m0_to_float(scales)
+    return _orig_scale_values(wfmt, scales)
+
+
+def _dequant_mxint4_as_e2m1(wfmt, group, codes, scales, zeros=None, global_scale=1.0):
+    if wfmt == "mxint4":
+        wfmt = "mxfp4"
+    return _orig_dequant(wfmt, group, codes, scales, zeros, global_scale)
+
+
+def _dequant_global_dropped(wfmt, group, codes, scales, zeros=None, global_scale=1.0):
+    return _orig_dequant(wfmt, group, codes, scales, zeros)
+
+
+def _w4a16_global_inside_bf16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None,
+                              global_scale=1.0):
+    x = F.bf16_bits_to_float(x_bits)
+    w = F.round_to_bf16(_orig_dequant(wfmt, group, codes, scales, zeros, global_scale))
+    return Q.gemm(x, w, chan_scale=chan_scale)
+
+
 _orig_dequant = Q.dequant
 _orig_gemm = Q.gemm
+_orig_scale_values = Q.scale_values
 
 MUTANTS = {
     "nibble order swapped": (Q, "unpack_nibbles", _unpack_swapped),
@@ -123,6 +153,10 @@ MUTANTS = {
     "token scale dropped": (Q, "gemm", _gemm_drop_tok_scale),
     "w4a16 without bf16 weights": (Q, "w4a16", _w4a16_exact_weights),
     "zero row not guarded": (Q, "quant_act_fp8", _quant_no_zero_guard),
+    "nvfp4 scale read as e8m0": (Q, "scale_values", _scale_values_nvfp4_as_e8m0),
+    "mxint4 read as e2m1": (Q, "dequant", _dequant_mxint4_as_e2m1),
+    "global scale dropped": (Q, "dequant", _dequant_global_dropped),
+    "global scale before bf16 rounding": (Q, "w4a16", _w4a16_global_inside_bf16),
 }
 
 

@@ -23,13 +23,14 @@ M_SWEEP = tuple(2 ** i for i in range(14))            # 1 .. 8192
 
 @dataclass
 class WeightCase:
-    wfmt: str                  # "int4_sym" | "uint4_zp" | "mxfp4"
+    wfmt: str                  # "int4_sym" | "uint4_zp" | "mxfp4" | "mxint4" | "nvfp4"
     group: int
     N: int
     K: int
     codes: np.ndarray          # uint8 [N, K/2], even k in the low nibble
-    scales: np.ndarray         # uint16 bf16 bits [N, K/g]  or uint8 E8M0 [N, K/32]
+    scales: np.ndarray         # uint16 bf16 bits [N, K/g], uint8 E8M0 [N, K/32] or E4M3 [N, K/16]
     zeros: Optional[np.ndarray] = None   # uint8 [N, K/g] for uint4_zp
+    global_scale: float = 1.0  # float32 per-tensor scale (nvfp4)
 
 
 @dataclass
@@ -71,13 +72,26 @@ def gen_x(r, M, K, outliers=False):
 
 
 def gen_weights(r, wfmt, N, K, group=None, scale_lo=0.005, scale_hi=0.02, zp_lo=6, zp_hi=9,
-                e8m0_lo=118, e8m0_hi=126):
-    """Draw codes, then scales, then zero points (in that order)."""
-    if wfmt == "mxfp4":
+                e8m0_lo=118, e8m0_hi=126, e4m3_exp_lo=5, e4m3_exp_hi=9, global_lo=0.002,
+                global_hi=0.004):
+    """Draw codes, then scales, then zero points or the per-tensor scale (in that order).
+
+    mxfp4 / mxint4: all 16 codes, E8M0 exponents in [e8m0_lo, e8m0_hi] per 32.  nvfp4: all
+    16 e2m1 codes, positive E4M3 scales with exponent field in [e4m3_exp_lo, e4m3_exp_hi]
+    and any mantissa per 16, and a float32 per-tensor scale in [global_lo, global_hi)."""
+    if wfmt in ("mxfp4", "mxint4"):
         group = 32 if group is None else group
-        nib = r.integers(0, 16, size=(N, K), dtype=np.uint8)          # all 16 e2m1 codes
+        nib = r.integers(0, 16, size=(N, K), dtype=np.uint8)          # all 16 codes
         scales = r.integers(e8m0_lo, e8m0_hi + 1, size=(N, K // group), dtype=np.uint8)
         return WeightCase(wfmt, group, N, K, pack_nibbles(nib), scales)
+    if wfmt == "nvfp4":
+        group = 16 if group is None else group
+        nib = r.integers(0, 16, size=(N, K), dtype=np.uint8)
+        ex = r.integers(e4m3_exp_lo, e4m3_exp_hi + 1, size=(N, K // group))
+        man = r.integers(0, 8, size=(N, K // group))
+        scales = ((ex << 3) | man).astype(np.uint8)
+        g = float(np.float32(r.uniform(global_lo, global_hi)))
+        return WeightCase(wfmt, group, N, K, pack_nibbles(nib), scales, None, g)
     group = 128 if group is None else group
     if wfmt == "int4_sym":
         q = r.integers(-8, 8, size=(N, K), dtype=np.int64)             # signed codes

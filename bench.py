@@ -382,6 +382,41 @@ def sweep_mxfp4(device, flush, peaks, fp8):
     return rows
 
 
+FMT_M = (1, 16, 128, 1024, 8192)
+
+
+def sweep_w4a16_fmt(device, flush, peaks, wfmt):
+    """Dense W4A16 on the MXINT4 (E8M0 per 32) or NVFP4 (E4M3 per 16 and a per-tensor
+    scale) weight formats, N x K in {4096 x 7168, 7168 x 2048}, M in FMT_M."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import quantized_weight_gemm_gb300 as qg
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12
+    rows = []
+    Mmax = max(FMT_M)
+    for (N, K) in MX_SHAPES:
+        r = WL.rng(0)
+        x = WL.gen_x(r, Mmax, K)
+        w = WL.gen_weights(r, wfmt, N, K)
+        d = qg.WeightDesc(wfmt, N, K, w.group)
+        packed = qg.repack(d, torch.from_numpy(w.codes).to(device),
+                           torch.from_numpy(w.scales).to(device), global_scale=w.global_scale)
+        X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        Y = torch.empty(Mmax, N, dtype=torch.bfloat16, device=device)
+        ws = qg.workspace(d, Mmax, device)
+        wb = N * K // 2 + N * (K // w.group)
+        for M in FMT_M:
+            ms = time_one(lambda: qg.w4a16(d, packed, X[:M], out=Y[:M], ws=ws), flush)
+            rows.append(_row(N, K, M, ms, wb, wb + M * K * 2 + M * N * 2, 2.0 * M * N * K, bw, tc))
+        del packed, X, Y, ws
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError(f"a {wfmt} GEMM reported a device error")
+    return rows
+
+
 def sweep_moe(device, flush, peaks):
     """The MoE layer (E = 256 MXFP4 experts, top-8, hidden 7168, intermediate 2048):
     gate_up [4096 x 7168] and down [7168 x 2048] grouped GEMMs over expert-sorted rows,
@@ -493,6 +528,8 @@ def bench_ours(args):
         torch.cuda.empty_cache()
         extra = {"mxfp4_a16": sweep_mxfp4(device, flush, peaks, fp8=False),
                  "mxfp4_a8": sweep_mxfp4(device, flush, peaks, fp8=True),
+                 "mxint4_a16": sweep_w4a16_fmt(device, flush, peaks, "mxint4"),
+                 "nvfp4_a16": sweep_w4a16_fmt(device, flush, peaks, "nvfp4"),
                  "moe": sweep_moe(device, flush, peaks)}
     if qg.device_status(clear=True) != 0:
         raise RuntimeError("a GEMM reported a device error")
@@ -577,6 +614,12 @@ def bench_ours(args):
                                       "same shapes; quant_act_us = the separate quantization call; "
                                       "roofline tensor peak = 2 x measured bf16"),
                          "sweep": extra["mxfp4_a8"]},
+            "mxint4_a16": {"workload": ("dense W4A16 MXINT4 (two's-complement nibbles, E8M0 per "
+                                        "32), same shapes"),
+                           "sweep": extra["mxint4_a16"]},
+            "nvfp4_a16": {"workload": ("dense W4A16 NVFP4 (e2m1, E4M3 per 16, float32 "
+                                       "per-tensor scale), same shapes"),
+                          "sweep": extra["nvfp4_a16"]},
             "moe": {"workload": ("MoE grouped W4A16 MXFP4, E=256 top-8, gate_up 4096 x 7168 + "
                                  "down 7168 x 2048, expert-sorted rows padded to 8; flops and "
                                  "bytes on routed (unpadded) rows and active experts"),

@@ -57,8 +57,11 @@ typedef enum {
                                   invalid offsets or a row index past the end of X     */
 } qgemm_status;
 
-typedef enum { QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2 } qgemm_wfmt;
-typedef enum { QGEMM_SCALE_BF16 = 0, QGEMM_SCALE_E8M0 = 1 } qgemm_sdtype;
+typedef enum {
+  QGEMM_W_INT4_SYM = 0, QGEMM_W_UINT4_ZP = 1, QGEMM_W_MXFP4 = 2, QGEMM_W_MXINT4 = 3,
+  QGEMM_W_NVFP4 = 4
+} qgemm_wfmt;
+typedef enum { QGEMM_SCALE_BF16 = 0, QGEMM_SCALE_E8M0 = 1, QGEMM_SCALE_E4M3 = 2 } qgemm_sdtype;
 typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1 } qgemm_afmt;
 
 /*
@@ -67,7 +70,13 @@ typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1 } qgemm_afmt;
  *   wfmt INT4_SYM : sdtype BF16, has_zp 0, group_size 32 or a multiple of 64, K % group == 0
  *   wfmt UINT4_ZP : sdtype BF16, has_zp 1, group_size as above
  *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32
+ *   wfmt MXINT4   : sdtype E8M0, has_zp 0, group_size 32, afmt BF16
+ *                   (w = q * 2^(e - 127), q the two's-complement nibble)
+ *   wfmt NVFP4    : sdtype E4M3, has_zp 0, group_size 16, afmt BF16
+ *                   (w = e2m1(q) * s * g, g the per-tensor scale of qgemm_repack_scaled)
  * K must be a multiple of 32; N >= 1 is arbitrary (the packed form pads it).
+ * MXINT4 and NVFP4 are the formats of the B300 MoE results in "Humming wird
+ * angekündigt", section "WnA16".
  * afmt names the activation format the packed weights will be multiplied with.
  */
 typedef struct {
@@ -102,16 +111,30 @@ size_t qgemm_packed_bytes(const qgemm_wdesc* desc);
  * JIT-Kompilierung für jeden Workload": validate parameters, pad dimensions, repack into
  * the kernel layout).  Reads the canonical weight tensors and writes the packed form.
  *   codes  : device uint8 [N, K/2]; element k of row n is in byte k/2, even k in the low
- *            nibble.  INT4_SYM nibbles are two's complement; UINT4_ZP nibbles are 0..15;
- *            MXFP4 nibbles are e2m1 codes (bit 3 sign).
- *   scales : device [N, K/group] row-major: uint16 BF16 bit patterns, or uint8 E8M0.
+ *            nibble.  INT4_SYM and MXINT4 nibbles are two's complement; UINT4_ZP nibbles
+ *            are 0..15; MXFP4 and NVFP4 nibbles are e2m1 codes (bit 3 sign).
+ *   scales : device [N, K/group] row-major: uint16 BF16 bit patterns, or uint8 E8M0, or
+ *            uint8 E4M3 (OCP "fn": bit 7 sign, exponent bias 7, S.1111.111 NaN).
  *   zeros  : device uint8 [N, K/group] with values 0..15 (UINT4_ZP), else NULL.
  *   packed : device buffer of qgemm_packed_bytes(desc) bytes, 256-byte aligned.
- * Values the format forbids (E8M0 = 255, a NaN/Inf BF16 scale, a zero point > 15) set
- * QGEMM_ERR_BAD_VALUE in the device status word.
+ * Values the format forbids (E8M0 = 255, a NaN/Inf BF16 scale, a NaN E4M3 scale, a zero
+ * point > 15) set QGEMM_ERR_BAD_VALUE in the device status word.  An NVFP4 matrix packed
+ * here has per-tensor scale 1.
  */
 qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const void* scales,
                           const uint8_t* zeros, void* packed, void* stream);
+
+/*
+ * qgemm_repack, recording NVFP4's per-tensor (second-level) scale g in the packed header:
+ * every GEMM on these weights multiplies its output by g (in FP32, with the per-channel
+ * scale, before the BF16 rounding of Y), so an MoE layer has one g per expert.  g must be
+ * finite (QGEMM_ERR_INVALID_ARG) and 1 for the other formats (QGEMM_ERR_UNSUPPORTED).
+ * "Humming wird angekündigt", section "Eine einheitliche Quantisierungsdarstellung"
+ * (secondary scales are a parameter of the weight description).
+ */
+qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
+                                 const void* scales, const uint8_t* zeros, float global_scale,
+                                 void* packed, void* stream);
 
 /*
  * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max: the FP32 partial

@@ -21,14 +21,15 @@ __all__ = [
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libqgemm.so")
 
-WFMT = {"int4_sym": 0, "uint4_zp": 1, "mxfp4": 2}
+WFMT = {"int4_sym": 0, "uint4_zp": 1, "mxfp4": 2, "mxint4": 3, "nvfp4": 4}
+SDTYPE = {"int4_sym": 0, "uint4_zp": 0, "mxfp4": 1, "mxint4": 1, "nvfp4": 2}   # BF16, E8M0, E4M3
 AFMT = {"bf16": 0, "fp8": 1}
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
            "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host",
-           "qgemm_moe_indexed")
+           "qgemm_moe_indexed", "qgemm_repack_scaled")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -58,7 +59,7 @@ class WeightDesc:
 
     def c(self):
         w = WFMT[self.wfmt]
-        return _WDesc(w, 1 if self.wfmt == "mxfp4" else 0, self.group,
+        return _WDesc(w, SDTYPE[self.wfmt], self.group,
                       1 if self.wfmt == "uint4_zp" else 0, AFMT[self.afmt], 0, self.N, self.K)
 
 
@@ -87,6 +88,7 @@ def lib():
         "qgemm_check_desc": (ctypes.c_int, [D]),
         "qgemm_packed_bytes": (SZ, [D]),
         "qgemm_repack": (ctypes.c_int, [D, P, P, P, P, P]),
+        "qgemm_repack_scaled": (ctypes.c_int, [D, P, P, P, ctypes.c_float, P, P]),
         "qgemm_workspace_bytes": (SZ, [D, I64]),
         "qgemm_w4a16": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P]),
         "qgemm_w4a8": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P]),
@@ -150,10 +152,11 @@ def packed_bytes(desc):
     return int(n)
 
 
-def repack(desc, codes, scales, zeros=None, out=None, num_experts=1):
-    """Canonical (codes uint8 [N, K/2], scales bf16-bits/E8M0 [N, K/g], zeros) -> packed.
+def repack(desc, codes, scales, zeros=None, out=None, num_experts=1, global_scale=None):
+    """Canonical (codes uint8 [N, K/2], scales bf16-bits/E8M0/E4M3 [N, K/g], zeros) -> packed.
 
-    For an MoE layer pass tensors with a leading expert dimension and num_experts=E."""
+    For an MoE layer pass tensors with a leading expert dimension and num_experts=E.
+    global_scale: NVFP4's per-tensor scale, a float or one per expert (default 1)."""
     nb = packed_bytes(desc)
     if out is None:
         out = torch.empty(nb * num_experts, dtype=torch.uint8, device=codes.device)
@@ -165,8 +168,11 @@ def repack(desc, codes, scales, zeros=None, out=None, num_experts=1):
         z = None if zeros is None else (zeros[e] if num_experts > 1 else zeros)
         c, s = c.contiguous(), s.contiguous()
         z = None if z is None else z.contiguous()
-        _check(L.qgemm_repack(ctypes.byref(d), _ptr(c), _ptr(s), _ptr(z),
-                              ctypes.c_void_p(out.data_ptr() + e * nb), _stream()), "repack")
+        g = 1.0 if global_scale is None else global_scale
+        g = float(g[e]) if isinstance(g, (list, tuple)) else float(g)
+        _check(L.qgemm_repack_scaled(ctypes.byref(d), _ptr(c), _ptr(s), _ptr(z), g,
+                                     ctypes.c_void_p(out.data_ptr() + e * nb), _stream()),
+               "repack")
     return out
 
 

@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <mutex>
 
@@ -121,8 +122,11 @@ SkShape sk_shape(int64_t T, int64_t kb, int64_t P) {
   r.sk_tiles = int(q == 0 ? T : T % P);
   if (r.sk_tiles == 0) return r;
   const int64_t S = int64_t(r.sk_tiles) * kb;
+  // CTAs holding a record of tile t: first..last when every CTA holds one (S >= P); with
+  // fewer records than CTAs each CTA holds at most one, so a tile has kb contributors.
   for (int64_t t = 0; t < r.sk_tiles; ++t) {
-    const int64_t c = sk_cta_of((t + 1) * kb - 1, S, P) - sk_cta_of(t * kb, S, P) + 1;
+    const int64_t c = S >= P ? sk_cta_of((t + 1) * kb - 1, S, P) - sk_cta_of(t * kb, S, P) + 1
+                             : kb;
     r.max_contrib = std::max<int>(r.max_contrib, int(c));
   }
   for (int64_t i = 0; i < P; ++i) {
@@ -414,15 +418,26 @@ size_t qgemm_packed_bytes(const qgemm_wdesc* desc) {
 
 qgemm_status qgemm_repack(const qgemm_wdesc* desc, const uint8_t* codes, const void* scales,
                           const uint8_t* zeros, void* packed, void* stream) {
+  return qgemm_repack_scaled(desc, codes, scales, zeros, 1.0f, packed, stream);
+}
+
+qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
+                                 const void* scales, const uint8_t* zeros, float global_scale,
+                                 void* packed, void* stream) {
   Layout L;
   if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
+  // NVFP4's decode leaves the weights 2^8 smaller (e2m1 x s x 2^-8, exact in BF16): the
+  // accumulators take 2^8 back with the per-tensor scale.  Other formats have none.
+  const float acc_scale = L.wfmt == W_NVFP4 ? global_scale * 256.0f : global_scale;
+  if (!std::isfinite(acc_scale)) return QGEMM_ERR_INVALID_ARG;
+  if (L.wfmt != W_NVFP4 && global_scale != 1.0f) return QGEMM_ERR_UNSUPPORTED;
   if (codes == nullptr || scales == nullptr || packed == nullptr) return QGEMM_ERR_INVALID_ARG;
   if (L.has_zp && zeros == nullptr) return QGEMM_ERR_INVALID_ARG;
   if (!aligned(codes, 4) || !aligned(scales, L.scale_bytes) || !aligned(packed, 256))
     return QGEMM_ERR_ALIGNMENT;
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
-  cudaError_t e = launch_repack(L, codes, scales, L.has_zp ? zeros : nullptr, packed,
+  cudaError_t e = launch_repack(L, codes, scales, L.has_zp ? zeros : nullptr, acc_scale, packed,
                                 static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }

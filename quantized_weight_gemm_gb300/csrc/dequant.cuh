@@ -15,6 +15,12 @@
 //   bit 15, which is the bf16 number e2m1(q) * 2^-126 (a subnormal for e = 0); multiplying
 //   by 2^(E-1) (or by 2^127 and then 2^(E-128) when E > 128) gives e2m1(q) * 2^(E-127),
 //   exact unless it overflows bf16.
+//   MXINT4: the INT4 decode with z = 8 and the scale 2^(E-127) as a BF16 factor (the
+//   subnormal 2^-127 for E = 0): q * 2^(E-127), exact unless it overflows bf16.
+//   NVFP4: the MXFP4 bit move, then one multiply by the E4M3 group scale s times 2^118,
+//   giving e2m1(q) * s * 2^-8 -- exact, since e2m1 and E4M3 significands have 2 and 4 bits
+//   and the result stays in the normal range; the GEMM multiplies its FP32 accumulators by
+//   2^8 and the per-tensor scale.
 //
 // FP8 activations (tensor-core operand E4M3 with block scales): a word holds K-elements
 // 8j..8j+7 with nibbles [e0, e4, e1, e5, e2, e6, e3, e7], so masking low nibbles gives
@@ -60,6 +66,23 @@ __device__ __forceinline__ void mxfp4_factors(uint32_t E, uint32_t& sa, uint32_t
   const uint32_t b = big ? ((E - 1u) << 7) : 0x3F80u;        // 2^(E-128) or 1
   sa = a | (a << 16);
   sb = b | (b << 16);
+}
+
+// bf16x2 of 2^(E-127) for an E8M0 exponent E < 255 (E = 0: the bf16 subnormal 2^-127).
+__device__ __forceinline__ uint32_t e8m0_bf16x2(uint32_t E) {
+  return (E != 0u ? (E << 7) : 0x0040u) * 0x00010001u;
+}
+
+// bf16x2 of (E4M3 value of byte b) * 2^118, exact: the significand (8 + m for a normal,
+// m for a subnormal) shifted by the exponent is an integer below 2^18, and the value
+// 2^(e-1) (8 + m) 2^109 = (1 + m/8) 2^(e-7) 2^118 has at most 4 significant bits.  NaN
+// codes never get here (the repack refuses them).
+__device__ __forceinline__ uint32_t e4m3_bf16x2_p118(uint32_t b) {
+  const uint32_t e = (b >> 3) & 0xFu, m = b & 7u;
+  const uint32_t sig = e != 0u ? ((8u | m) << (e - 1u)) : m;
+  const float v = __uint2float_rn(sig) * 0x1p109f;
+  const uint32_t h = (__float_as_uint(v) >> 16) | ((b & 0x80u) << 8);
+  return h * 0x00010001u;
 }
 
 // MXFP4 word (FP8 nibble order) -> two 32-bit words of four e4m3 bytes each.

@@ -284,9 +284,19 @@ __device__ __forceinline__ bool unit_at(int j, const GemmArgs& a, const Sched& s
     const int last = sk_cta_of(uint32_t(t0 + k_blocks - 1), sc.S);
     if (last > first) {
       w.tile_id = tile;
-      w.slot0 = tile + first;
-      w.contrib = cta - first;
-      w.ncontrib = last - first + 1;
+      if (sc.S >= uint32_t(P)) {
+        // every CTA holds a record, so the tile's contributors are CTAs first..last
+        w.slot0 = tile + first;
+        w.contrib = cta - first;
+        w.ncontrib = last - first + 1;
+      } else {
+        // fewer records than CTAs: each CTA holds at most one, and some none, so the
+        // contributors are the owners of the tile's k_blocks records, in record order
+        // (slot = the record's index, below S)
+        w.slot0 = t0;
+        w.contrib = sc.lo - t0;
+        w.ncontrib = k_blocks;
+      }
     }
   } else {
     tile = sc.sk_tiles + cta + (j - sc.n_sk) * P;
@@ -317,7 +327,9 @@ struct Ring {
 // Decode modes: the kernel is compiled per weight format so that the decode loop holds
 // only the code it runs.  "G1": one scale (and zero point) per row per record, i.e. a
 // group of 128 K or longer, so they are read once per record.
-enum DecodeMode : int { DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3 };
+enum DecodeMode : int {
+  DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5
+};
 
 // Decode two 32-K chunks of weight row r into 32 bf16x2 registers (pair order).  The codes
 // come from slot chunks `slot0`, `slot0 + 1` of the staged record; their scales and zero
@@ -352,6 +364,17 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
         const bool two = __any_sync(0xffffffffu, big);
 #pragma unroll
         for (int j = 0; j < 4; ++j) decode_mxfp4_word(wd[j], sa, sb, two, &regs[16 * c + 4 * j]);
+      } else if constexpr (DM == DM_MXINT4) {
+        const uint32_t s2 = e8m0_bf16x2(rec[tail + r * 4 + rchunk0 + c]);   // one E8M0 per 32 K
+#pragma unroll
+        for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], 0x43084308u, s2, &regs[16 * c + 4 * j]);
+      } else if constexpr (DM == DM_NVFP4) {
+        // one E4M3 scale per 16 K: words 0, 1 of the chunk take the first, words 2, 3 the second
+        const uint32_t sp = reinterpret_cast<const uint16_t*>(rec + tail)[r * 4 + rchunk0 + c];
+        const uint32_t s0 = e4m3_bf16x2_p118(sp & 0xFFu), s1 = e4m3_bf16x2_p118(sp >> 8);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          decode_mxfp4_word(wd[j], j < 2 ? s0 : s1, 0u, false, &regs[16 * c + 4 * j]);
       } else {
         const int ent = r * G + ((rchunk0 + c) * G) / 4;      // scale entry of this chunk
         const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[ent];
@@ -904,6 +927,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const bool n_ok = n < L.N;
       const bool split = w.ncontrib > 1;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
+      // NVFP4: the accumulator scale of the unit's expert, from its packed header
+      float acc_s = 1.0f;
+      if constexpr (DM == DM_NVFP4)
+        acc_s = __ldg(&reinterpret_cast<const PackedHeader*>(
+                          a.packed + int64_t(w.expert) * a.expert_stride)->acc_scale);
       // Partial accumulators of the issuers that had a stage in this unit: the unit's
       // stages g0, g0 + 1, ... went to issuers (g0 + d) % kIssuers.
       const int active = min(C::kNumSub, nst);
@@ -912,7 +940,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         if (!split) {
           // Wide tiles: scale and round every column of this warp to BF16 in registers,
           // hand the accumulator back to the MMA at once, then store.
-          const float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+          float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+          if constexpr (DM == DM_NVFP4) cs *= acc_s;
           uint32_t packed[kCols / 2];
 #pragma unroll
           for (int c = 0; c < kCols / 16; ++c) {
@@ -947,7 +976,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       if (!split) {
         // Narrow tiles (double-buffered accumulators): convert and store chunk by chunk.
-        const float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+        float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+        if constexpr (DM == DM_NVFP4) cs *= acc_s;
 #pragma unroll 1
         for (int c = 0; c < kCols / kChunk; ++c) {
           uint32_t v[32];
@@ -1004,7 +1034,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         __threadfence();
         const float* row0p = a.ws + int64_t(w.slot0) * slot_floats + int64_t(r) * BNT +
                              eh * kCols;
-        const float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+        float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
+        if constexpr (DM == DM_NVFP4) cs2 *= acc_s;
         constexpr int kPass = kCols < 16 ? kCols : 16;
 #pragma unroll 1
         for (int c0 = 0; c0 < kCols; c0 += kPass) {
@@ -1090,6 +1121,8 @@ cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, cons
 // Decode mode of a packed layout (BF16 activations).
 inline int decode_mode(const Layout& L) {
   if (L.wfmt == W_MXFP4) return DM_MXFP4;
+  if (L.wfmt == W_MXINT4) return DM_MXINT4;
+  if (L.wfmt == W_NVFP4) return DM_NVFP4;
   if (L.groups_per_record == 1) return L.has_zp ? DM_INT4_ZP_G1 : DM_INT4_SYM_G1;
   return DM_INT4_ANY;
 }

@@ -11,8 +11,9 @@ namespace qgemm {
 
 int* device_status_ptr();
 
+// acc_scale: the factor the GEMM applies to its accumulators, stored in the header.
 cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* scales,
-                          const uint8_t* zeros, void* packed, cudaStream_t st);
+                          const uint8_t* zeros, float acc_scale, void* packed, cudaStream_t st);
 cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, cudaStream_t st);
 cudaError_t launch_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
                                  int64_t ldq, float* s, cudaStream_t st);
@@ -48,7 +49,8 @@ struct GemmArgs {
   int64_t ldy;
   // Partial sums of the tiles whose K range is cut over several CTAs: one slot per
   // contributor, an FP32 tile [128 weight rows][token_tile], row-major (uniform cuts: slot
-  // tile * splits + split; stream-K: slot t + first(t) + j, fewer than sk_tiles + grid).
+  // tile * splits + split; stream-K: slot t + first(t) + j, fewer than sk_tiles + grid, or
+  // with fewer records S than CTAs the record's own index, below S).
   // MoE: optional; when given, the kernel may run stream-K (2 * grid slots).
   float* ws;
   int32_t* counters;           // arrival counter per cut tile (zero between calls)

@@ -50,7 +50,7 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         uint32_t nib = pad ? 0u : (src >> (4 * e)) & 0xFu;   // even k in the low nibble
-        if (L.wfmt == W_INT4_SYM) nib ^= 8u;                 // two's complement -> q + 8
+        if (L.wfmt == W_INT4_SYM || L.wfmt == W_MXINT4) nib ^= 8u;   // two's complement -> q + 8
         const int pos = (L.afmt == A_FP8) ? nibble_pos_a8(e) : nibble_pos_a16(e);
         w |= nib << (4 * pos);
       }
@@ -92,11 +92,18 @@ __global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
         if ((v & 0x7F80u) == 0x7F80u) set_status(kStatusBadValue);   // NaN / Inf
       }
       reinterpret_cast<uint16_t*>(dst)[r * G + j] = v;
-    } else {
-      uint8_t v = 127;
+    } else if (L.sdtype == 1) {
+      uint8_t v = 127;                                                 // E8M0 1.0
       if (valid) {
         v = static_cast<const uint8_t*>(scales)[n * ngroups + grp];
         if (v == 255) set_status(kStatusBadValue);
+      }
+      dst[r * G + j] = v;
+    } else {
+      uint8_t v = 0x38;                                                // E4M3 1.0
+      if (valid) {
+        v = static_cast<const uint8_t*>(scales)[n * ngroups + grp];
+        if ((v & 0x7Fu) == 0x7Fu) set_status(kStatusBadValue);       // NaN
       }
       dst[r * G + j] = v;
     }
@@ -134,7 +141,7 @@ __global__ void repack_zeros_kernel(Layout L, const uint8_t* __restrict__ zeros,
   }
 }
 
-__global__ void write_header_kernel(Layout L, uint8_t* packed) {
+__global__ void write_header_kernel(Layout L, float acc_scale, uint8_t* packed) {
   PackedHeader h;
   h.magic = kPackedMagic;
   h.version = kPackedVersion;
@@ -143,6 +150,7 @@ __global__ void write_header_kernel(Layout L, uint8_t* packed) {
   h.N = L.N; h.K = L.K;
   h.n_tiles = L.n_tiles; h.k_blocks = L.k_blocks; h.record_bytes = L.record_bytes;
   h.off_scales = L.off_scales; h.off_zeros = L.off_zeros; h.total_bytes = L.total_bytes;
+  h.acc_scale = acc_scale;
   *reinterpret_cast<PackedHeader*>(packed) = h;
 }
 
@@ -152,9 +160,9 @@ static int grid_for(int64_t n) {
 }
 
 cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* scales,
-                          const uint8_t* zeros, void* packed, cudaStream_t st) {
+                          const uint8_t* zeros, float acc_scale, void* packed, cudaStream_t st) {
   uint8_t* p = static_cast<uint8_t*>(packed);
-  write_header_kernel<<<1, 1, 0, st>>>(L, p);
+  write_header_kernel<<<1, 1, 0, st>>>(L, acc_scale, p);
   repack_codes_kernel<<<grid_for(L.n_tiles * L.k_blocks * 4 * kTileN), 256, 0, st>>>(L, codes, p);
   repack_scales_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record), 256, 0,
                          st>>>(L, scales, p);
@@ -219,12 +227,26 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
       continue;
     }
     uint32_t out[4];
+    if (L.wfmt == W_NVFP4) {
+      // the GEMM's decode (e2m1 x s x 2^-8, exact), then the accumulator factor (2^8 times
+      // the per-tensor scale) in double and one rounding to BF16
+      const uint32_t s = e4m3_bf16x2_p118(rec[L.off_scales + r * G + c * 2 + j / 2]);
+      decode_mxfp4_word(w, s, 0u, false, out);
+      const double f = double(reinterpret_cast<const PackedHeader*>(packed)->acc_scale);
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t hb = (out[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;
+        dst[e] = __double2bfloat16(double(__uint_as_float(hb << 16)) * f);
+      }
+      continue;
+    }
     if (L.wfmt == W_MXFP4) {
       const uint32_t E = rec[L.off_scales + ent];
       uint32_t sa, sb;
       bool big;
       mxfp4_factors(E, sa, sb, big);
       decode_mxfp4_word(w, sa, sb, big, out);
+    } else if (L.wfmt == W_MXINT4) {
+      decode_int4_word(w, 0x43084308u, e8m0_bf16x2(rec[L.off_scales + ent]), out);
     } else {
       const uint32_t s = reinterpret_cast<const uint16_t*>(rec + L.off_scales)[ent];
       uint32_t z = 8;

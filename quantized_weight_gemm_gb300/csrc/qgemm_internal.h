@@ -13,7 +13,7 @@
 //            of that row as four 32-bit words of 8 nibbles, the nibbles interleaved so one
 //            mask yields two decoded lanes (dequant.cuh);
 //   scales : [128 rows][G] entries of S bytes, G = max(1, 128 / group) groups per record,
-//            S = 2 (BF16) or 1 (E8M0); a group longer than 128 repeats in each record;
+//            S = 2 (BF16) or 1 (E8M0, E4M3); a group longer than 128 repeats in each record;
 //   zeros  : (INT4 with zero points only) [128 rows x G] nibbles, entry (r, j) in nibble
 //            (r*G + j) & 1 of byte (r*G + j) / 2.
 // Records are multiples of 16 bytes and the first starts 256 bytes in, so every record is
@@ -25,13 +25,13 @@
 namespace qgemm {
 
 constexpr uint32_t kPackedMagic = 0x32575147u;   // "GQW2"
-constexpr uint32_t kPackedVersion = 2;
+constexpr uint32_t kPackedVersion = 3;
 constexpr int kTileN = 128;                      // weight rows per tile (MMA M)
 constexpr int kStageK = 128;                     // K-elements per pipeline stage
 constexpr int kCodeBytes = kTileN * kStageK / 2; // 8192
 constexpr int kHeaderBytes = 256;
 
-enum WFmt : int32_t { W_INT4_SYM = 0, W_UINT4_ZP = 1, W_MXFP4 = 2 };
+enum WFmt : int32_t { W_INT4_SYM = 0, W_UINT4_ZP = 1, W_MXFP4 = 2, W_MXINT4 = 3, W_NVFP4 = 4 };
 enum AFmt : int32_t { A_BF16 = 0, A_FP8 = 1 };
 
 struct PackedHeader {
@@ -41,6 +41,9 @@ struct PackedHeader {
   int64_t N, K;
   int64_t n_tiles, k_blocks, record_bytes;
   int64_t off_scales, off_zeros, total_bytes;    // offsets inside a record / total size
+  // Factor the GEMM applies to its FP32 accumulators (NVFP4: the per-tensor scale times
+  // 2^8, the decode having left the weights 2^8 smaller; 1 for the other formats).
+  float acc_scale;
 };
 static_assert(sizeof(PackedHeader) <= kHeaderBytes, "header too large");
 
@@ -65,6 +68,11 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
   if (afmt != A_BF16 && afmt != A_FP8) return false;
   if (wfmt == W_MXFP4) {
     if (sdtype != 1 || group != 32 || has_zp != 0) return false;
+  } else if (wfmt == W_MXINT4 || wfmt == W_NVFP4) {
+    // BF16 activations only
+    if (wfmt == W_MXINT4 && (sdtype != 1 || group != 32)) return false;
+    if (wfmt == W_NVFP4 && (sdtype != 2 || group != 16)) return false;
+    if (has_zp != 0 || afmt != A_BF16) return false;
   } else if (wfmt == W_INT4_SYM || wfmt == W_UINT4_ZP) {
     if (sdtype != 0 || has_zp != (wfmt == W_UINT4_ZP ? 1 : 0)) return false;
     if (!(group == 32 || (group >= 64 && group % 64 == 0))) return false;

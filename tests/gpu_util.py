@@ -37,4 +37,4 @@ def desc_of(w, afmt="bf16"):
 def pack(w, afmt="bf16"):
     d = desc_of(w, afmt)
     z = None if w.zeros is None else u8_tensor(w.zeros)
-    return d, qg.repack(d, u8_tensor(w.codes), scales_tensor(w), z)
+    return d, qg.repack(d, u8_tensor(w.codes), scales_tensor(w), z, global_scale=w.global_scale)

@@ -44,6 +44,9 @@ def test_status_strings(L):
     ("mxfp4", 32, "bf16", True), ("mxfp4", 32, "fp8", True),
     ("int4_sym", 48, "bf16", False), ("mxfp4", 64, "bf16", False),
     ("int4_sym", 128, "fp8", False),
+    ("mxint4", 32, "bf16", True), ("nvfp4", 16, "bf16", True),
+    ("mxint4", 64, "bf16", False), ("nvfp4", 32, "bf16", False),
+    ("mxint4", 32, "fp8", False), ("nvfp4", 16, "fp8", False),
 ])
 def test_check_desc(L, wfmt, group, afmt, ok):
     d = qg.WeightDesc(wfmt, 256, 512, group, afmt)
@@ -64,6 +67,23 @@ def test_packed_bytes_accounting(L):
     # ragged N and K pad to the tile
     d = qg.WeightDesc("int4_sym", 130, 96, 32)
     assert qg.packed_bytes(d) >= 256 * 128 // 2
+    # MXINT4 packs like MXFP4; NVFP4: codes + one E4M3 byte per 16
+    assert qg.packed_bytes(qg.WeightDesc("mxint4", 4096, 7168, 32)) == \
+        qg.packed_bytes(qg.WeightDesc("mxfp4", 4096, 7168, 32))
+    n = qg.packed_bytes(qg.WeightDesc("nvfp4", 4096, 7168, 16))
+    assert 0 <= n - (4096 * 7168 // 2 + 4096 * 7168 // 16) < 4096
+
+
+def test_repack_scaled_argument_errors(L):
+    """The per-tensor scale belongs to NVFP4 and must be finite; checked before any launch."""
+    P = ctypes.c_void_p
+    buf = P(1 << 20)                       # never dereferenced: the calls fail first
+    for wfmt, group, g, want in [("mxfp4", 32, 2.0, 2), ("int4_sym", 128, 0.5, 2),
+                                 ("nvfp4", 16, float("nan"), 1), ("nvfp4", 16, float("inf"), 1),
+                                 ("nvfp4", 16, 3.0e38, 1)]:
+        d = qg.WeightDesc(wfmt, 256, 512, group).c()
+        st = L.qgemm_repack_scaled(ctypes.byref(d), buf, buf, None, ctypes.c_float(g), buf, None)
+        assert st == want, (wfmt, g, st)
 
 
 def test_bad_descriptors_give_zero(L):
@@ -120,34 +140,45 @@ def _sk_contributors(T, kb, P):
             owners[x // kb].add(i)
         covered += hi - lo
     assert covered == S
-    # partial-sum slots: contributor j of tile t uses slot t + min(owners) + j
-    top = max(t + min(o) + len(o) - 1 for t, o in enumerate(owners))
-    assert top < T + P
+    if S >= P:
+        # every CTA holds a record: a tile's owners are consecutive CTAs, and contributor j
+        # of tile t uses partial-sum slot t + min(owners) + j
+        for o in owners:
+            assert o == set(range(min(o), max(o) + 1))
+        top = max(t + min(o) + len(o) - 1 for t, o in enumerate(owners))
+        assert top < T + P
+    else:
+        # at most one record per CTA: kb owners per tile, a record's slot is its index (< S)
+        assert all(len(o) == kb for o in owners)
     return max(len(o) for o in owners)
 
 
-@pytest.mark.parametrize("N,K,M", [(28672, 1152, 16), (28672, 8192, 100), (8192, 28672, 16),
-                                   (4096, 7168, 1), (384, 1024, 100), (7168, 2048, 48)])
-def test_stream_k_plan(L, N, K, M):
+@pytest.mark.parametrize("N,K,M,tt", [(28672, 1152, 16, 16), (28672, 8192, 100, 16),
+                                      (8192, 28672, 16, 16), (4096, 7168, 1, 16),
+                                      (384, 1024, 100, 16), (7168, 2048, 48, 16),
+                                      (384, 1024, 100, 32), (384, 1024, 150, 32),
+                                      (6400, 256, 16, 16), (19968, 512, 16, 16)])
+def test_stream_k_plan(L, N, K, M, tt):
     """The forced stream-K plan of the dense path: leftover tiles = T mod P (all T when
-    T < P), and partial-sum slots = the most CTAs whose record ranges meet one tile."""
+    T < P), and partial-sum slots = the most CTAs whose record ranges meet one tile (also
+    when the cut tiles hold fewer records than there are CTAs)."""
     d = qg.WeightDesc("uint4_zp", N, K, 128)
     P = 152
-    qg.force_config(16, -1)
+    qg.force_config(tt, -1)
     try:
         p = qg.plan(d, M)
         ws = qg.workspace_bytes(d, M)
     finally:
         qg.force_config(0, 0)
-    T = -(-M // 16) * -(-N // 128)
+    T = -(-M // tt) * -(-N // 128)
     kb = -(-K // 128)
     sk = T if T < P else T % P
-    assert p["token_tile"] == 16 and p["splits"] == 1 and p["grid"] == P
+    assert p["token_tile"] == tt and p["splits"] == 1 and p["grid"] == P
     assert p["sk_tiles"] == sk
     c = _sk_contributors(sk, kb, P)
     assert p["max_contrib"] == (c if c > 1 else 0)
     if c > 1:
-        assert ws >= (sk + P) * 128 * 16 * 4 + 4 * sk
+        assert ws >= (sk + P) * 128 * tt * 4 + 4 * sk
 
 
 def test_plan_defaults_are_valid(L):

@@ -42,7 +42,9 @@ def _run_a16(x_bits, w, chan=None):
     d, packed = G.pack(w)
     X = G.bf16_tensor(x_bits)
     cs = None if chan is None else torch.from_numpy(chan.astype(np.float32)).cuda()
-    y = qg.w4a16(d, packed, X, chan_scale=cs)
+    # NaN-filled output: an element the kernel does not write cannot pass for a result
+    out = torch.full((X.shape[0], w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = qg.w4a16(d, packed, X, chan_scale=cs, out=out)
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     return G.to_f64(y)
@@ -82,12 +84,18 @@ def test_tiny_dense_workload():
     ("mxfp4", 32, 17, 1024, 1024),
     ("mxfp4", 32, 260, 256, 416),
     ("mxfp4", 32, 600, 384, 640),
+    ("mxint4", 32, 5, 520, 2048),
+    ("mxint4", 32, 260, 256, 416),
+    ("nvfp4", 16, 1, 512, 7168),
+    ("nvfp4", 16, 17, 1024, 1024),
+    ("nvfp4", 16, 600, 384, 640),
 ])
 def test_dense_a16_parity(wfmt, group, M, N, K):
     r = WL.rng(21)
     x = WL.gen_x(r, M, K)
     w = WL.gen_weights(r, wfmt, N, K, group=group)
-    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros,
+                       global_scale=w.global_scale)
     _assert_close(_run_a16(x, w), ref, TOL_A16)
 
 
@@ -100,7 +108,19 @@ def test_chan_scale():
     _assert_close(_run_a16(x, w, chan), ref, TOL_A16)
 
 
-@pytest.mark.parametrize("wfmt,group", [("int4_sym", 128), ("uint4_zp", 64), ("mxfp4", 32)])
+def test_nvfp4_chan_and_global_scale():
+    """The per-channel and the per-tensor scale multiply the same output."""
+    r = WL.rng(25)
+    x = WL.gen_x(r, 48, 512)
+    w = WL.gen_weights(r, "nvfp4", 200, 512)
+    chan = r.uniform(0.5, 2.0, 200).astype(np.float32)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, chan_scale=chan,
+                       global_scale=w.global_scale)
+    _assert_close(_run_a16(x, w, chan), ref, TOL_A16)
+
+
+@pytest.mark.parametrize("wfmt,group", [("int4_sym", 128), ("uint4_zp", 64), ("mxfp4", 32),
+                                        ("mxint4", 32), ("nvfp4", 16)])
 def test_integer_inputs_exact(wfmt, group):
     """Integer X and power-of-two scales: every partial sum is exact in fp32, so the
     output must be exactly RNE_bf16 of the oracle's exact result."""
@@ -108,26 +128,53 @@ def test_integer_inputs_exact(wfmt, group):
     M, N, K = 8, 256, 256
     x = WL.to_bf16_bits(r.integers(-4, 5, size=(M, K)).astype(np.float32))
     w = WL.gen_weights(r, wfmt, N, K, group=group)
-    if wfmt == "mxfp4":
+    if wfmt in ("mxfp4", "mxint4"):
         w.scales[:] = r.integers(124, 130, size=w.scales.shape, dtype=np.uint8)
+    elif wfmt == "nvfp4":
+        w.scales[:] = (r.integers(4, 10, size=w.scales.shape) << 3).astype(np.uint8)  # 2^-3..2^2
+        w.global_scale = 0.25
     else:
         w.scales[:] = F.float_to_bf16_bits(np.ldexp(1.0, r.integers(-3, 3, size=w.scales.shape)))
-    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros,
+                       global_scale=w.global_scale)
     y = _run_a16(x, w)
     np.testing.assert_array_equal(y, F.round_to_bf16(ref))
 
 
-@pytest.mark.parametrize("wfmt,group", [("uint4_zp", 128), ("mxfp4", 32)])
+@pytest.mark.parametrize("wfmt,group", [("uint4_zp", 128), ("mxfp4", 32), ("mxint4", 32),
+                                        ("nvfp4", 16)])
 def test_one_hot_columns_exact(wfmt, group):
     r = WL.rng(24)
     N, K = 384, 512
     w = WL.gen_weights(r, wfmt, N, K, group=group)
+    w.global_scale = 0.125 if wfmt == "nvfp4" else 1.0      # a power of two: one rounding
     ks = np.array([0, 1, 31, 32, 63, 64, 127, 128, 255, 511])
     x = np.zeros((len(ks), K), dtype=np.float32)
     x[np.arange(len(ks)), ks] = 1.0
     y = _run_a16(WL.to_bf16_bits(x), w)
-    W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    W = F.round_to_bf16(oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros,
+                                       w.global_scale))
     np.testing.assert_array_equal(y, W[:, ks].T)
+
+
+@pytest.mark.parametrize("wfmt", ["mxint4", "nvfp4"])
+@pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 3, -1])
+def test_new_formats_every_tile(wfmt, tile, splits):
+    """Each token tile (wide, narrow and cut-tile epilogues) and K cut, for the formats whose
+    decode (and, for NVFP4, output factor) the kernels compile separately."""
+    qg = _qg()
+    r = WL.rng(26)
+    M, N, K = 150, 384, 1024
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, wfmt, N, K)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, global_scale=w.global_scale)
+    qg.force_config(tile, splits)
+    try:
+        y = _run_a16(x, w)
+    finally:
+        qg.force_config(0, 0)
+    _assert_close(y, ref, TOL_A16)
 
 
 @pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
@@ -194,7 +241,8 @@ def _run_a8(xq, s, w, chan=None):
     qg = _qg()
     d, packed = G.pack(w, afmt="fp8")
     cs = None if chan is None else torch.from_numpy(chan.astype(np.float32)).cuda()
-    y = qg.w4a8(d, packed, G.u8_tensor(xq), torch.from_numpy(s).cuda(), chan_scale=cs)
+    out = torch.full((xq.shape[0], w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y = qg.w4a8(d, packed, G.u8_tensor(xq), torch.from_numpy(s).cuda(), chan_scale=cs, out=out)
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     return G.to_f64(y)

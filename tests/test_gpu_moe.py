@@ -47,19 +47,23 @@ def _pack_experts(ws, afmt="bf16"):
     sc = torch.from_numpy(sc.view(np.int16) if sc.dtype == np.uint16 else sc).cuda()
     z = _stack(ws, "zeros")
     z = None if z is None else G.u8_tensor(z)
-    return d, qg.repack(d, codes, sc, z, num_experts=len(ws))
+    return d, qg.repack(d, codes, sc, z, num_experts=len(ws),
+                        global_scale=[w.global_scale for w in ws])
 
 
 def _experts_bf16(ws):
-    return [oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros) for w in ws]
+    """The BF16 operands, times each expert's per-tensor scale (which multiplies its output,
+    so it may as well scale its weights: the oracle sums exactly)."""
+    return [oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros) *
+            np.float64(np.float32(w.global_scale)) for w in ws]
 
 
 def _experts_exact(ws):
     return [oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros) for w in ws]
 
 
-def _run_moe(ws, x_bits, offsets, afmt="bf16", tok_scale=None, out_fill=None, stream_k=False,
-             calls=1):
+def _run_moe(ws, x_bits, offsets, afmt="bf16", tok_scale=None, out_fill=float("nan"),
+             stream_k=False, calls=1):
     """stream_k: pass the MoE workspace, which lets the kernel cut leftover tiles over CTAs
     (it does so when the leftover tiles hold at least 16 K blocks per SM)."""
     from tests import gpu_util as G
@@ -101,6 +105,8 @@ def _offsets(counts):
     ("mxfp4", [0, 0, 0, 64], 384, 1024),
     ("uint4_zp", [17, 300, 0, 3], 300, 768),
     ("int4_sym", [1, 1, 1, 1, 1, 1, 1, 1, 1, 1], 128, 256),
+    ("mxint4", [9, 0, 70, 2], 256, 512),
+    ("nvfp4", [5, 0, 37, 16, 0, 1, 130, 8], 256, 512),
 ])
 def test_moe_a16_parity(wfmt, counts, N, K, stream_k):
     r = WL.rng(41)
@@ -294,6 +300,22 @@ def test_moe_indexed_router(afmt, stream_k):
                                  tok_scale=s)
         y = _run_moe_indexed(ws, xq, case.offsets, idx, afmt="fp8", tok_scale=s, stream_k=stream_k)
         _assert_close(y, ref, TOL_A8)
+
+
+def test_moe_indexed_nvfp4():
+    """Indexed rows with NVFP4 experts, each with its own per-tensor scale, with and without
+    stream-K (K blocks enough to cut the leftover tiles)."""
+    r = WL.rng(54)
+    T, N, K = 9, 7168, 3072
+    counts = [1, 1, 2, 1, 1, 1, 1, 1]
+    off = _offsets(counts)
+    idx = r.permutation(T)[:int(off[-1])].astype(np.int32)
+    x = WL.gen_x(r, T, K)
+    ws = [WL.gen_weights(r, "nvfp4", N, K) for _ in counts]
+    assert len(set(w.global_scale for w in ws)) == len(ws)
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    for sk in (False, True):
+        _assert_close(_run_moe_indexed(ws, x, off, idx, stream_k=sk), ref, TOL_A16)
 
 
 @pytest.mark.parametrize("tile", [16, 32, 64])

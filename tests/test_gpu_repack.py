@@ -8,6 +8,7 @@ import pytest
 import torch
 
 import oracle
+from oracle import formats as F
 import workloads as WL
 
 pytestmark = pytest.mark.gpu
@@ -28,7 +29,8 @@ def _check(w, afmt="bf16"):
     import quantized_weight_gemm_gb300 as qg
     d, packed = G.pack(w, afmt)
     got = G.to_f64(qg.dequant_debug(d, packed))
-    ref = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    ref = F.round_to_bf16(oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros,
+                                         w.global_scale))
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     same = (got == ref) | (np.isnan(got) & np.isnan(ref))
@@ -39,7 +41,7 @@ def _check(w, afmt="bf16"):
 
 @pytest.mark.parametrize("wfmt,group", [("int4_sym", 128), ("uint4_zp", 128), ("int4_sym", 32),
                                         ("uint4_zp", 32), ("uint4_zp", 64), ("uint4_zp", 256),
-                                        ("mxfp4", 32)])
+                                        ("mxfp4", 32), ("mxint4", 32), ("nvfp4", 16)])
 @pytest.mark.parametrize("N,K", [(256, 512), (300, 768), (1, 256), (130, 96)])
 def test_repack_roundtrip_bitexact(wfmt, group, N, K):
     if K % group:
@@ -65,6 +67,27 @@ def test_mxfp4_all_exponents():
     _check(w, afmt="fp8")
 
 
+def test_mxint4_all_exponents():
+    """Every E8M0 exponent 0..254: the subnormal factor 2^-127 at 0, overflow to infinity
+    at the top, exactly as RNE_bf16 of the exact weight."""
+    r = WL.rng(16)
+    w = WL.gen_weights(r, "mxint4", 255, 64)
+    w.scales[:] = np.arange(255, dtype=np.uint8)[:, None]
+    _check(w)
+
+
+@pytest.mark.parametrize("g", [1.0, 0.37, 2.0 ** -20])
+def test_nvfp4_all_scales(g):
+    """Every E4M3 scale code but NaN (either sign, subnormals included) with every e2m1
+    code, times a per-tensor scale: one rounding of the exact product."""
+    r = WL.rng(17)
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    w = WL.gen_weights(r, "nvfp4", len(codes), 64)
+    w.scales[:] = codes[:, None]
+    w.global_scale = float(np.float32(g))
+    _check(w)
+
+
 def test_int4_scale_extremes():
     r = WL.rng(14)
     w = WL.gen_weights(r, "uint4_zp", 128, 256, group=128, zp_lo=0, zp_hi=15)
@@ -86,3 +109,8 @@ def test_repack_rejects_bad_values():
     w.zeros[0, 0] = 16
     G.pack(w)
     assert qg.device_status(clear=True) == 9
+    for nan in (0x7F, 0xFF):                                # E4M3 NaN scales
+        w = WL.gen_weights(WL.rng(15), "nvfp4", 128, 64)
+        w.scales[5, 2] = nan
+        G.pack(w)
+        assert qg.device_status(clear=True) == 9

@@ -68,8 +68,8 @@ def alg_bytes(M, N, K):
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
     # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch)
-    "csrc_sha256": "f9f54a13ef8c9651b97c190df9de2ca7d39f6bd3b28c4ccc0811da8b3a45e984",
-    "launches": {"28672,8192,8192": 2728057000 + 898700544},
+    "csrc_sha256": "beff4503d87f1db9a3b4654d02e2a88db523d524f1495779f0d8b4893717c831",
+    "launches": {"28672,8192,8192": 2983337000 + 926694656},
 }
 
 
@@ -546,11 +546,14 @@ def bench_ours(args):
     value = ws * flops_step / (local_ms * 1e-3) / 1e12
     e2e_value = ws * flops_step / (local_e2e * 1e-3) / 1e12
 
-    # per-call table (median over steps)
-    per = {}
+    # per-call table (median over steps), with each call's end-to-end time beside it
+    per, per_e2e = {}, {}
     for s in steps:
         for (N, K, M, ms) in s:
             per.setdefault((N, K, M), []).append(ms)
+    for s in e2e_steps:
+        for (N, K, M, ms) in s:
+            per_e2e.setdefault((N, K, M), []).append(ms)
     bw = peaks["hbm_gbs"] * 1e9
     tc = peaks["bf16_tflops"] * 1e12
     sweep = []
@@ -561,7 +564,8 @@ def bench_ours(args):
                       "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2),
                       "weight_gbs": round(weight_bytes(N, K) / (ms * 1e-3) / 1e9, 1),
                       "roofline_frac": round(rt / (ms * 1e-3), 3),
-                      "bound": "hbm" if alg_bytes(M, N, K) / bw > 2.0 * M * N * K / tc else "tensor"})
+                      "bound": "hbm" if alg_bytes(M, N, K) / bw > 2.0 * M * N * K / tc else "tensor",
+                      "e2e_us": round(statistics.median(per_e2e[(N, K, M)]) * 1e3, 2)})
     # dominant launch: the call with the largest share of the step's time
     dom = max(sweep, key=lambda r: r["us"])
     dom_flops = 2.0 * dom["M"] * dom["N"] * dom["K"]

@@ -118,7 +118,8 @@ def dist_env():
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi samples (200 ms) of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi samples (every PERIOD_MS) of SM clock and throttle reasons during the
+    timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -604,7 +605,10 @@ def bench_ours(args):
         "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": sum(M * K * 2 for (N, K) in SHAPES for M in M_SWEEP),
                 "d2h_bytes_per_step": sum(M * N * 2 for (N, K) in SHAPES for M in M_SWEEP),
-                "host_copy_gbs": copy_gbs},
+                "host_copy_gbs": copy_gbs,
+                # value is the mean over steps; the steps themselves show any outliers
+                "step_ms": [round(v, 3) for v in e2e_ms],
+                "median_step_ms": round(statistics.median(e2e_ms), 3)},
         "gpu_launches": len(SHAPES) * len(M_SWEEP) * args.steps,
         "clocks": clocks,
     }

@@ -78,14 +78,26 @@ typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1 } qgemm_afmt;
  * MXINT4 and NVFP4 are the formats of the B300 MoE results in "Humming wird
  * angekündigt", section "WnA16".
  * afmt names the activation format the packed weights will be multiplied with.
+ * flags: QGEMM_FLAG_BATCH_INVARIANT (below) or 0; other bits are invalid.  The packed form
+ * does not depend on flags.
  */
+/*
+ * Batch invariance ("Humming wird angekündigt", section "Tuning und JIT-Kompilierung für
+ * jeden Workload": a Compute Config option).  Calls on a descriptor with this flag run one
+ * schedule for every M: 128-token tiles with one MMA issuer, no K cut and no stream-K.  Each
+ * output row is then computed with the same operations in the same order whatever the
+ * batch: the same bits for X row m at any M, and in an MoE grouped call whatever the other
+ * experts' rows.  Small M runs slower than with the default schedules (a full 128-token
+ * MMA per stage); qgemm_moe_indexed refuses the flag (QGEMM_ERR_UNSUPPORTED).
+ */
+#define QGEMM_FLAG_BATCH_INVARIANT 1
 typedef struct {
   int32_t wfmt;        /* qgemm_wfmt   */
   int32_t sdtype;      /* qgemm_sdtype */
   int32_t group_size;  /* K elements per scale */
   int32_t has_zp;      /* 1 iff wfmt == QGEMM_W_UINT4_ZP */
   int32_t afmt;        /* qgemm_afmt   */
-  int32_t reserved;    /* must be 0    */
+  int32_t flags;       /* 0 or QGEMM_FLAG_BATCH_INVARIANT */
   int64_t N;
   int64_t K;
 } qgemm_wdesc;

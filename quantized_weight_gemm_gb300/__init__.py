@@ -44,23 +44,26 @@ class QGemmError(RuntimeError):
 class _WDesc(ctypes.Structure):
     _fields_ = [("wfmt", ctypes.c_int32), ("sdtype", ctypes.c_int32),
                 ("group_size", ctypes.c_int32), ("has_zp", ctypes.c_int32),
-                ("afmt", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("afmt", ctypes.c_int32), ("flags", ctypes.c_int32),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
 @dataclass(frozen=True)
 class WeightDesc:
-    """One quantized weight matrix [N, K]: format, group size and activation format."""
+    """One quantized weight matrix [N, K]: format, group size and activation format.
+    batch_invariant: every call runs one schedule for all M (QGEMM_FLAG_BATCH_INVARIANT)."""
     wfmt: str
     N: int
     K: int
     group: int = 128
     afmt: str = "bf16"
+    batch_invariant: bool = False
 
     def c(self):
         w = WFMT[self.wfmt]
         return _WDesc(w, SDTYPE[self.wfmt], self.group,
-                      1 if self.wfmt == "uint4_zp" else 0, AFMT[self.afmt], 0, self.N, self.K)
+                      1 if self.wfmt == "uint4_zp" else 0, AFMT[self.afmt],
+                      1 if self.batch_invariant else 0, self.N, self.K)
 
 
 _lib = None

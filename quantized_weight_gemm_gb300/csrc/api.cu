@@ -79,7 +79,7 @@ int sms_or_default() {
 }
 
 bool layout_of(const qgemm_wdesc* d, Layout* L) {
-  if (d == nullptr || d->reserved != 0) return false;
+  if (d == nullptr || (d->flags & ~QGEMM_FLAG_BATCH_INVARIANT) != 0) return false;
   return make_layout(d->wfmt, d->sdtype, d->group_size, d->has_zp, d->afmt, d->N, d->K, L);
 }
 
@@ -169,12 +169,23 @@ double sk_cost_us(const Layout& L, int64_t M, int ti, int sms, SkShape* out) {
   return c;
 }
 
-GemmPlan plan_dense(const Layout& L, int64_t M, int sms) {
+bool batch_invariant(const qgemm_wdesc* d) { return (d->flags & QGEMM_FLAG_BATCH_INVARIANT) != 0; }
+
+// The one schedule of batch-invariant calls: 128-token tiles (one MMA issuer, so a tile's
+// stages accumulate in K order into one accumulator), no cut, no stream-K.
+constexpr int kInvariantTile = 128;
+
+GemmPlan plan_dense(const Layout& L, int64_t M, int sms, bool invariant = false) {
   GemmPlan p;
   p.token_tile = 16;
   p.splits = 1;
   p.sk_tiles = 0;
   p.max_contrib = 0;
+  if (invariant) {
+    p.token_tile = kInvariantTile;
+    p.grid = int(std::min<int64_t>((M + kInvariantTile - 1) / kInvariantTile * L.n_tiles, sms));
+    return p;
+  }
   double best = 1e300;
   for (int ti = 0; ti < 5; ++ti) {
     const int tt = kTiles[ti];
@@ -342,7 +353,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   if (M == 0) return QGEMM_OK;
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
-  const GemmPlan plan = plan_dense(L, M, dev->sms);
+  const GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
   const int64_t need = split_ws_bytes(L, M, plan);
   if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need)) return QGEMM_ERR_WORKSPACE;
   if (need > 0 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
@@ -448,8 +459,10 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
   const int sms = sms_or_default();
   int64_t best = 0;
   const int64_t top = std::min<int64_t>(M_max, kSplitMaxM);
-  for (int64_t M = 1; M <= top; ++M) best = std::max(best, split_ws_bytes(L, M, plan_dense(L, M, sms)));
-  best = std::max(best, split_ws_bytes(L, M_max, plan_dense(L, M_max, sms)));
+  const bool inv = batch_invariant(desc);
+  for (int64_t M = 1; M <= top; ++M)
+    best = std::max(best, split_ws_bytes(L, M, plan_dense(L, M, sms, inv)));
+  best = std::max(best, split_ws_bytes(L, M_max, plan_dense(L, M_max, sms, inv)));
   return size_t(best);
 }
 
@@ -509,7 +522,10 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
   GemmPlan plan;
-  const int tt = row_index != nullptr ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
+  const bool inv = batch_invariant(desc);
+  if (inv && row_index != nullptr) return QGEMM_ERR_UNSUPPORTED;
+  const int tt = inv ? kInvariantTile
+                     : row_index != nullptr ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
   if (row_index != nullptr && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathering kernels: <= 64
   plan.token_tile = tt;
   plan.splits = 1;
@@ -542,7 +558,7 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   a.Y = Y;
   a.ldy = ldy;
   // Stream-K needs the whole bound; a smaller (or no) workspace keeps whole tiles.
-  if (ws != nullptr && g_force_splits != 1 && sk_fits(L, plan.grid) &&
+  if (ws != nullptr && !inv && g_force_splits != 1 && sk_fits(L, plan.grid) &&
       int64_t(ws_bytes) >= moe_ws_bytes(tt, plan.grid)) {
     if (!aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
     a.ws = static_cast<float*>(ws);
@@ -614,7 +630,7 @@ qgemm_status qgemm_device_status(int32_t clear) {
 qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]) {
   Layout L;
   if (!layout_of(desc, &L) || M <= 0 || out == nullptr) return QGEMM_ERR_INVALID_ARG;
-  const GemmPlan p = plan_dense(L, M, sms_or_default());
+  const GemmPlan p = plan_dense(L, M, sms_or_default(), batch_invariant(desc));
   out[0] = p.token_tile;
   out[1] = p.splits;
   out[2] = p.sk_tiles;

@@ -74,6 +74,22 @@ def test_packed_bytes_accounting(L):
     assert 0 <= n - (4096 * 7168 // 2 + 4096 * 7168 // 16) < 4096
 
 
+def test_batch_invariant_plan(L):
+    """QGEMM_FLAG_BATCH_INVARIANT: one schedule for every M (128-token tiles, no cut, no
+    stream-K, so no workspace); other flag bits are invalid."""
+    d = qg.WeightDesc("uint4_zp", 28672, 8192, 128, batch_invariant=True)
+    assert qg.check_desc(d) == 0
+    for M in (1, 16, 100, 1000, 8192):
+        p = qg.plan(d, M)
+        assert (p["token_tile"], p["splits"], p["sk_tiles"], p["max_contrib"]) == (128, 1, 0, 0)
+        assert p["grid"] == min(-(-M // 128) * 224, 152)
+    assert qg.workspace_bytes(d, 8192) == 0
+    raw = qg.WeightDesc("uint4_zp", 256, 512, 128).c()
+    raw.flags = 2
+    assert L.qgemm_check_desc(ctypes.byref(raw)) != 0
+    assert L.qgemm_packed_bytes(ctypes.byref(raw)) == 0
+
+
 def test_repack_scaled_argument_errors(L):
     """The per-tensor scale belongs to NVFP4 and must be finite; checked before any launch."""
     P = ctypes.c_void_p

@@ -177,6 +177,61 @@ def test_new_formats_every_tile(wfmt, tile, splits):
     _assert_close(y, ref, TOL_A16)
 
 
+@pytest.mark.parametrize("wfmt,afmt", [("uint4_zp", "bf16"), ("mxfp4", "bf16"),
+                                       ("nvfp4", "bf16"), ("mxfp4", "fp8")])
+def test_batch_invariant_rows(wfmt, afmt):
+    """With the batch-invariant flag, row m of Y is the same bits for every M (the default
+    schedules change token tile and K cuts with M), and the largest call matches the oracle."""
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(27)
+    Mmax, N, K = 1000, 384, 1536
+    x = WL.gen_x(r, Mmax, K, outliers=(afmt == "fp8"))
+    w = WL.gen_weights(r, wfmt, N, K)
+    d = qg.WeightDesc(wfmt, N, K, w.group, afmt, batch_invariant=True)
+    z = None if w.zeros is None else G.u8_tensor(w.zeros)
+    packed = qg.repack(d, G.u8_tensor(w.codes), G.scales_tensor(w), z, global_scale=w.global_scale)
+    X = G.bf16_tensor(x)
+    if afmt == "fp8":
+        Xq, ts = qg.quant_act_fp8(X)
+        run = lambda M: qg.w4a8(d, packed, Xq[:M], ts[:M])
+    else:
+        run = lambda M: qg.w4a16(d, packed, X[:M])
+    full = G.bf16_bits_of(run(Mmax))
+    for M in (1, 5, 64, 129, 700):
+        np.testing.assert_array_equal(G.bf16_bits_of(run(M)), full[:M])
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    y = F.bf16_bits_to_float(full)
+    if afmt == "fp8":
+        xq, s = oracle.quant_act_fp8(x)
+        ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
+        _assert_close(y, ref, TOL_A8)
+    else:
+        ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros,
+                           global_scale=w.global_scale)
+        _assert_close(y, ref, TOL_A16)
+
+
+def test_batch_invariant_host_chunks():
+    """The host-buffer call cuts M into chunks; with the flag every chunk's rows are the same
+    bits as the device call on all rows."""
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(28)
+    M, N, K = 1500, 256, 1024
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    d = qg.WeightDesc("uint4_zp", N, K, 128, batch_invariant=True)
+    packed = qg.repack(d, G.u8_tensor(w.codes), G.scales_tensor(w), G.u8_tensor(w.zeros))
+    X = G.bf16_tensor(x)
+    dev = G.bf16_bits_of(qg.w4a16(d, packed, X))
+    xh = X.cpu().pin_memory()
+    yh = qg.w4a16_host(d, packed, xh)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16), dev)
+
+
 @pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, -1])
 def test_every_dispatch_entry(tile, splits):

@@ -413,6 +413,40 @@ def test_moe_indexed_index_past_end():
     _assert_close(y, ref, TOL_A16)
 
 
+def test_moe_batch_invariant():
+    """With the flag, expert 0's rows are the same bits whatever the other experts' loads
+    (the default token tile and stream-K follow R / E), and the indexed call refuses it."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(55)
+    N, K = 256, 2048
+    ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in range(4)]
+    x0 = WL.gen_x(r, 40, K)
+    codes = G.u8_tensor(_stack(ws, "codes"))
+    sc = G.u8_tensor(_stack(ws, "scales"))
+    d = qg.WeightDesc("mxfp4", N, K, 32, batch_invariant=True)
+    packed = qg.repack(d, codes, sc, None, num_experts=4)
+    outs = []
+    for counts in ([40, 0, 0, 0], [40, 300, 7, 900], [40, 1, 1, 1]):
+        off = _offsets(counts)
+        R = int(off[-1])
+        xr = np.concatenate([x0, WL.gen_x(r, R - 40, K)]) if R > 40 else x0
+        wsp = qg.moe_workspace(d, 4, R)
+        y = qg.moe_grouped(d, packed, 4, G.bf16_tensor(xr),
+                           torch.tensor(off, dtype=torch.int32, device="cuda"), ws=wsp)
+        outs.append(G.bf16_bits_of(y)[:40])
+        ref = oracle.moe_grouped(F_bits(xr), off, _experts_bf16(ws))
+        _assert_close(G.to_f64(y), ref, TOL_A16)
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[0], outs[2])
+    with pytest.raises(qg.QGemmError):
+        qg.moe_indexed(d, packed, 4, G.bf16_tensor(x0),
+                       torch.tensor([0, 40, 40, 40, 40], dtype=torch.int32, device="cuda"),
+                       torch.arange(40, dtype=torch.int32, device="cuda"))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+
+
 def test_moe_indexed_refuses_wide_tiles():
     import quantized_weight_gemm_gb300 as qg
     r = WL.rng(51)

@@ -109,6 +109,23 @@ def captured_traffic(N, K, M):
     return CAPTURED_TRAFFIC["launches"].get(f"{N},{K},{M}")
 
 
+def job_times(local, dist=None, device="cpu"):
+    """The job's times: each entry of `local` as its slowest rank saw it (one MAX all_reduce;
+    a job ends when its last rank does), or `local` itself on one rank."""
+    if dist is None:
+        return [float(v) for v in local]
+    import torch
+    t = torch.tensor([float(v) for v in local], device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def job_value(ws, flops_step, ms):
+    """Whole-job TFLOP/s: each of the ws ranks does flops_step per step (weak scaling) in the
+    slowest rank's ms."""
+    return ws * flops_step / (ms * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -540,12 +557,9 @@ def bench_ours(args):
     e2e_ms = [sum(r[3] for r in s) for s in e2e_steps]
     local_ms = statistics.mean(step_ms)
     local_e2e = statistics.mean(e2e_ms)
-    if dist is not None:
-        t = torch.tensor([local_ms, local_e2e], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        local_ms, local_e2e = float(t[0]), float(t[1])
-    value = ws * flops_step / (local_ms * 1e-3) / 1e12
-    e2e_value = ws * flops_step / (local_e2e * 1e-3) / 1e12
+    local_ms, local_e2e = job_times([local_ms, local_e2e], dist, device)
+    value = job_value(ws, flops_step, local_ms)
+    e2e_value = job_value(ws, flops_step, local_e2e)
 
     # per-call table (median over steps), with each call's end-to-end time beside it
     per, per_e2e = {}, {}

@@ -10,13 +10,15 @@ wird angekündigt" (vLLM blog, German edition), section "Leistung".
 value   = sum of 2*M*N*K over the step / sum of the event-timed call durations (TFLOP/s)
 e2e     = the same calls through the public host-buffer entry point (qgemm_w4a16_host): X
           copied in from pinned host memory and Y copied back to pinned host memory inside the
-          timed region, the copies overlapped with the GEMM chunk by chunk
+          timed region, the copies overlapped with the GEMM chunk by chunk (mean over steps;
+          the per-step times and each call's median sit beside it)
 roofline: the dominant launch (the call with the largest share of the step time, a
           tensor-bound M = 8192 call): 2*M*N*K / its event time against the measured bf16
           peak; the HBM-bound small-M calls (M <= 16: weight + X + Y bytes / time against
           the measured copy bandwidth) are reported beside it
-other_workloads: the MXFP4 W4A16, MXFP4 W4A8 and MoE grouped sweeps, measured once after
-          the timed region (--no-extra skips them)
+other_workloads: the MXFP4 W4A16, MXFP4 W4A8, MXINT4 W4A16 and NVFP4 W4A16 sweeps and the
+          MoE sweep (grouped, and indexed gate_up up to 1024 tokens), measured once after the
+          timed region (--no-extra skips them)
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 

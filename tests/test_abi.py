@@ -135,6 +135,32 @@ def test_argument_errors_before_any_launch(L):
     assert L.qgemm_force_config(0, 0) == 0
 
 
+def test_host_staging_bytes(L):
+    """Staging of the host-buffer call: two X and two Y chunk buffers; chunks are all rows up
+    to 512, else M/16 rounded up to 256 rows (at least 512), so the size never shrinks as M
+    grows (a buffer sized for M_max serves every smaller M)."""
+    d = qg.WeightDesc("uint4_zp", 8192, 28672, 128)
+    K, N = 28672, 8192
+
+    def rows(M):
+        if M <= 512:
+            return M
+        return max(512, -(-(-(-M // 16)) // 256) * 256)
+
+    def rup(v):
+        return -(-v // 256) * 256
+
+    prev = 0
+    for M in (1, 2, 100, 511, 512, 513, 1000, 4096, 8191, 8192, 8193, 20000):
+        n = qg.host_staging_bytes(d, M)
+        r = rows(M)
+        assert n == 2 * (rup(r * K * 2) + rup(r * N * 2)), M
+        assert n >= prev
+        prev = n
+    assert qg.host_staging_bytes(d, 0) == 0
+    assert qg.host_staging_bytes(qg.WeightDesc("int4_sym", 0, 512), 16) == 0
+
+
 def test_product_package_does_not_import_oracle():
     pkg = os.path.join(ROOT, "quantized_weight_gemm_gb300")
     for dirpath, _, files in os.walk(pkg):

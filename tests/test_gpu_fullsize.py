@@ -42,6 +42,11 @@ def _rows(w, ns):
     return w.codes[ns], w.scales[ns], z
 
 
+def _nan_out(M, N):
+    """An output buffer whose every element the call must overwrite."""
+    return torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+
+
 @pytest.mark.parametrize("N,K,M", [(28672, 8192, 1), (28672, 8192, 16), (8192, 28672, 16),
                                    (28672, 8192, 256), (8192, 28672, 8192)])
 def test_int4_zp_bench_shapes(N, K, M):
@@ -49,7 +54,7 @@ def test_int4_zp_bench_shapes(N, K, M):
     import quantized_weight_gemm_gb300 as qg
     x, w = WL.int4_asym_shape(N, K, M, seed=0)
     d, packed = G.pack(w)
-    y = qg.w4a16(d, packed, G.bf16_tensor(x))
+    y = qg.w4a16(d, packed, G.bf16_tensor(x), out=_nan_out(M, N))
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(50), N, M)
@@ -66,7 +71,7 @@ def test_mxfp4_bench_shapes(N, K, M):
     import quantized_weight_gemm_gb300 as qg
     x, w = WL.mxfp4_shape(N, K, M, seed=0)
     d, packed = G.pack(w)
-    y = qg.w4a16(d, packed, G.bf16_tensor(x))
+    y = qg.w4a16(d, packed, G.bf16_tensor(x), out=_nan_out(M, N))
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(51), N, M)
@@ -87,7 +92,7 @@ def test_w4a8_bench_shapes(N, K, M):
     x, w = WL.mxfp4_shape(N, K, M, seed=0, outliers=True)
     d, packed = G.pack(w, afmt="fp8")
     Xq, ts = qg.quant_act_fp8(G.bf16_tensor(x))
-    y = qg.w4a8(d, packed, Xq, ts)
+    y = qg.w4a8(d, packed, Xq, ts, out=_nan_out(M, N))
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(52), N, M)

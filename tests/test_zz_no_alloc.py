@@ -54,7 +54,7 @@ def test_noalloc_matches_workspace_entry_point(qg, wfmt, M, N, K):
     cd = d.c()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     for _ in range(2):                            # the scratch is reused by the second call
-        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        y = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         st = L.qgemm_w4a16_noalloc(ctypes.byref(cd), ctypes.c_void_p(packed.data_ptr()),
                                    ctypes.c_void_p(X.data_ptr()), M, X.stride(0), None,
                                    ctypes.c_void_p(y.data_ptr()), y.stride(0), stream)

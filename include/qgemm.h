@@ -160,7 +160,8 @@ qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
 size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);
 
 /*
- * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k]   (c = 1 when chan_scale == NULL)
+ * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k]   (c = 1 when chan_scale == NULL;
+ *               for NVFP4, W includes the per-tensor scale g, applied to the FP32 sum)
  *   packed     : device, from qgemm_repack with desc->afmt == QGEMM_A_BF16
  *   X          : device BF16 [M, ldx], 16-byte aligned, ldx % 8 == 0, ldx >= K
  *   chan_scale : device float32 [N] secondary per-channel scale, or NULL

@@ -291,6 +291,7 @@ size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R);
 /*
  * Test hook: unpack a packed matrix back to BF16 W[n, k] = RNE_bf16(dequant) through the
  * same register decode the GEMM kernels use.  W_out: device BF16 [N, K] (row stride K).
+ * NVFP4: the decoded e2m1 * s (exact) times the per-tensor scale g, rounded to BF16 once.
  */
 qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,
                                  void* stream);

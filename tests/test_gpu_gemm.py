@@ -232,6 +232,19 @@ def test_batch_invariant_host_chunks():
     np.testing.assert_array_equal(yh.view(torch.int16).numpy().view(np.uint16), dev)
 
 
+@pytest.mark.parametrize("N,K,M", [(19968, 512, 16), (6400, 256, 16), (19968, 512, 1)])
+def test_default_plan_small_k(N, K, M):
+    """Small-K shapes with the planner's own choice.  On 152 SMs, 19968 x 512 at M = 16 is
+    one whole round of tiles plus four leftover tiles of four records each, cut over
+    stream-K with fewer records than CTAs."""
+    qg = _qg()
+    r = WL.rng(29)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "uint4_zp", N, K)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    _assert_close(_run_a16(x, w), ref, TOL_A16)
+
+
 @pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
 @pytest.mark.parametrize("splits", [1, 2, 3, 7, -1])
 def test_every_dispatch_entry(tile, splits):

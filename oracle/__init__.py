@@ -5,8 +5,9 @@ bench.py, never by the product package.  See qgemm_oracle.py for what it compute
 """
 from . import formats
 from .qgemm_oracle import (WFMTS, unpack_nibbles, scale_values, dequant, dequant_bf16, gemm,
-                           w4a16, quant_act_fp8, w4a8, moe_grouped, moe_indexed, tolerance_ok)
+                           w4a16, quant_act_fp8, w4a8, moe_grouped, moe_indexed, tolerance_ok,
+                           quant_act_mxfp4, dequant_act_mxfp4, w4a4)
 
 __all__ = ["formats", "WFMTS", "unpack_nibbles", "scale_values", "dequant", "dequant_bf16",
            "gemm", "w4a16", "quant_act_fp8", "w4a8", "moe_grouped", "moe_indexed",
-           "tolerance_ok"]
+           "tolerance_ok", "quant_act_mxfp4", "dequant_act_mxfp4", "w4a4"]

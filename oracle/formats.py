@@ -22,11 +22,12 @@ import numpy as np
 __all__ = [
     "int4_signed", "e2m1_to_float", "e8m0_to_float", "e4m3_to_float", "bf16_bits_to_float",
     "round_to_bf16", "round_to_e4m3_satfinite", "e4m3_encode", "float_to_bf16_bits",
-    "BF16_MAX", "E4M3_MAX",
+    "round_to_e2m1_satfinite", "e2m1_encode", "BF16_MAX", "E4M3_MAX", "E2M1_MAX",
 ]
 
 BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127
 E4M3_MAX = 448.0
+E2M1_MAX = 6.0
 
 
 def int4_signed(nibbles):
@@ -99,6 +100,27 @@ def round_to_e4m3_satfinite(x):
     results beyond the largest finite value (448) to +-448 ("satfinite")."""
     r = _round_binary(x, 4, -6)
     return np.clip(r, -E4M3_MAX, E4M3_MAX)
+
+
+def round_to_e2m1_satfinite(x):
+    """Round-to-nearest-even to FP4 e2m1 (2 significant bits, emin 0, so spacing 0.5 below
+    1), then clamp beyond the largest finite value (6) to +-6."""
+    r = _round_binary(x, 2, 0)
+    return np.clip(r, -E2M1_MAX, E2M1_MAX)
+
+
+_E2M1_POS = e2m1_to_float(np.arange(8))          # codes 0..7, strictly increasing
+
+
+def e2m1_encode(v):
+    """Codes (0..15) of values already on the e2m1 grid (|v| <= 6); the sign bit (bit 3)
+    follows the sign of v, so -0.0 encodes as 8."""
+    v = np.asarray(v, dtype=np.float64)
+    mag = np.abs(v)
+    code = np.searchsorted(_E2M1_POS, mag).astype(np.int64)
+    if not np.all(_E2M1_POS[np.minimum(code, 7)] == mag):
+        raise ValueError("e2m1_encode: value not on the e2m1 grid")
+    return (code | (np.signbit(v).astype(np.int64) << 3)).astype(np.uint8)
 
 
 _E4M3_POS = e4m3_to_float(np.arange(0x7F))      # codes 0x00..0x7E, strictly increasing

@@ -35,6 +35,12 @@ Readings where the pages are silent (each is listed in the design notes):
   * FP8 activation quantization: per row m, s_m = amax_m / 448 in float32 (1.0 when the row
     is all zero), codes = e4m3 round-to-nearest-even with saturation of x / s_m computed in
     float32.
+  * MXFP4 activation quantization (for W4A4, section "W8A8 / W4A8 / W4A4": MX formats on
+    Blackwell's tensor cores): the OCP Microscaling conversion restated -- per block of 32
+    K-elements of a row, the shared exponent is floor(log2(amax)) minus e2m1's largest
+    exponent (2), stored as E8M0 (clamped to 0..254; 127, i.e. 1, for an all-zero block),
+    and each element is x / 2^(E-127) rounded to nearest even on the e2m1 grid with
+    saturation at 6.
 
 The matmul accumulates in float64; W4A16 uses the dequantized weights as BF16 values (the
 operand of a 16-bit tensor core), W4A8 the exact e2m1 x E8M0 values (exact in FP8 with a
@@ -137,6 +143,37 @@ def quant_act_fp8(x_bits):
     s = np.where(amax == 0, np.float32(1.0), s).astype(np.float32)
     v = (x / s[:, None]).astype(np.float32)            # IEEE float32 quotient
     return F.e4m3_encode(F.round_to_e4m3_satfinite(v.astype(np.float64))), s
+
+
+def quant_act_mxfp4(x_bits, block=32):
+    """MXFP4 activations: BF16 X [M, K] (bit patterns, K % block == 0) -> (codes uint8
+    [M, K/2] in the canonical nibble order, E8M0 exponents uint8 [M, K/block])."""
+    x = F.bf16_bits_to_float(x_bits)
+    m, k = x.shape
+    if k % block:
+        raise ValueError("K must be a multiple of the block")
+    xb = x.reshape(m, k // block, block)
+    amax = np.max(np.abs(xb), axis=2)
+    _, e2 = np.frexp(amax)                        # amax = f 2^e2 with 0.5 <= f < 1
+    e = np.where(amax > 0, (e2 - 1) - 2 + 127, 127)   # floor(log2 amax) - 2, biased
+    e = np.clip(e, 0, 254).astype(np.int64)
+    q = F.round_to_e2m1_satfinite(xb / np.ldexp(1.0, e - 127)[..., None])
+    nib = F.e2m1_encode(q).reshape(m, k)
+    codes = (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)   # even k in the low nibble
+    return codes, e.astype(np.uint8)
+
+
+def dequant_act_mxfp4(codes, exps, block=32):
+    """The exact values of MXFP4 activations: e2m1(code) * 2^(E - 127) per block."""
+    q = unpack_nibbles(codes)
+    return F.e2m1_to_float(q) * F.e8m0_to_float(exps)[:, np.arange(q.shape[1]) // block]
+
+
+def w4a4(xq, x_exps, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+    """W4A4: y = sum_k dequant_act(xq)[m, k] * W[n, k] with exact weights (both operands are
+    MX values a block-scaled FP4 MMA multiplies exactly), times c[n] if given."""
+    return gemm(dequant_act_mxfp4(xq, x_exps), dequant(wfmt, group, codes, scales, zeros),
+                chan_scale=chan_scale)
 
 
 def w4a8(xq, tok_scale, wfmt, group, codes, scales, zeros=None, chan_scale=None):

@@ -11,6 +11,7 @@ from oracle import formats as F
 from oracle import qgemm_oracle as Q
 from tests import test_oracle_formats as TF
 from tests import test_oracle_gemm as TG
+from tests import test_oracle_w4a4 as TW
 
 PINS = [
     TF.test_e2m1_matches_printed_grid, TF.test_e8m0_matches_torch,
@@ -32,6 +33,9 @@ PINS = [
     lambda: TG.test_integer_brute_force("nvfp4", 16),
     lambda: TG.test_group_boundary_selects_next_scale("nvfp4", 16),
     TG.test_worked_mxint4_and_nvfp4_values, TG.test_nvfp4_global_scale_multiplies_the_output,
+    TW.test_e2m1_rounding_matches_nearest_search, TW.test_mxfp4_quant_worked_blocks,
+    TW.test_mxfp4_quant_power_of_two_invariance, TW.test_mxfp4_quant_error_bound,
+    TW.test_w4a4_rational_brute_force,
 ]
 
 
@@ -138,6 +142,33 @@ def _w4a16_global_inside_bf16(x_bits, wfmt, group, codes, scales, zeros=None, ch
     return Q.gemm(x, w, chan_scale=chan_scale)
 
 
+def _e2m1_ties_away(x):
+    x = np.asarray(x, dtype=np.float64)
+    _, e = np.frexp(x)
+    q = np.ldexp(1.0, np.maximum(e, 1) - 2)
+    r = np.sign(x) * np.floor(np.abs(x) / q + 0.5) * q
+    return np.clip(r, -6.0, 6.0)
+
+
+def _quant_act_mxfp4_exp_minus_one(x_bits, block=32):
+    x = F.bf16_bits_to_float(x_bits)
+    m, k = x.shape
+    xb = x.reshape(m, k // block, block)
+    amax = np.max(np.abs(xb), axis=2)
+    _, e2 = np.frexp(amax)
+    e = np.clip(np.where(amax > 0, (e2 - 1) - 1 + 127, 127), 0, 254).astype(np.int64)
+    q = F.round_to_e2m1_satfinite(xb / np.ldexp(1.0, e - 127)[..., None])
+    nib = F.e2m1_encode(q).reshape(m, k)
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8), e.astype(np.uint8)
+
+
+def _dequant_act_block_shifted(codes, exps, block=32):
+    q = Q.unpack_nibbles(codes)
+    k = q.shape[1]
+    g = np.minimum((np.arange(k) + 1) // block, k // block - 1)
+    return F.e2m1_to_float(q) * F.e8m0_to_float(exps)[:, g]
+
+
 _orig_dequant = Q.dequant
 _orig_gemm = Q.gemm
 _orig_scale_values = Q.scale_values
@@ -157,6 +188,9 @@ MUTANTS = {
     "mxint4 read as e2m1": (Q, "dequant", _dequant_mxint4_as_e2m1),
     "global scale dropped": (Q, "dequant", _dequant_global_dropped),
     "global scale before bf16 rounding": (Q, "w4a16", _w4a16_global_inside_bf16),
+    "e2m1 ties away from zero": (F, "round_to_e2m1_satfinite", _e2m1_ties_away),
+    "mxfp4 act exponent minus one": (Q, "quant_act_mxfp4", _quant_act_mxfp4_exp_minus_one),
+    "act block index shifted": (Q, "dequant_act_mxfp4", _dequant_act_block_shifted),
 }
 
 

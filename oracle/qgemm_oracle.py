@@ -105,16 +105,20 @@ def dequant_bf16(wfmt, group, codes, scales, zeros=None):
     return F.round_to_bf16(dequant(wfmt, group, codes, scales, zeros))
 
 
-def gemm(x, w, chan_scale=None, tok_scale=None):
-    """y[m, n] = tok_scale[m] * chan_scale[n] * sum_k x[m, k] * w[n, k], in float64.
+def gemm(x, w, chan_scale=None, tok_scale=None, bias=None):
+    """y[m, n] = tok_scale[m] * chan_scale[n] * sum_k x[m, k] * w[n, k] + bias[n], in float64.
 
     x: activation values [M, K] (any real dtype, used exactly); w: exact weights [N, K].
+    The bias is added after every scale ("Humming wird angekündigt", section "Gemeinsam
+    genutzte CUDA-Komponenten": scaling and bias addition fused into the output stage).
     """
     y = np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
     if tok_scale is not None:
         y = y * np.asarray(tok_scale, dtype=np.float64)[:, None]
     if chan_scale is not None:
         y = y * np.asarray(chan_scale, dtype=np.float64)[None, :]
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)[None, :]
     return y
 
 

@@ -249,6 +249,21 @@ def test_nvfp4_global_scale_multiplies_the_output():
     np.testing.assert_array_equal(yg, y1 * g)
 
 
+def test_bias_is_added_after_the_scales():
+    """Integer X, power-of-two weights, a dyadic bias: every step is exact, so the bias
+    shows up unscaled on top of the scaled sum, once per output column."""
+    r = np.random.Generator(np.random.PCG64(12))
+    x = r.integers(-3, 4, size=(3, 64)).astype(np.float64)
+    w = np.ldexp(1.0, r.integers(-2, 2, size=(5, 64)))
+    c = np.array([0.5, 2.0, 1.0, 4.0, 0.25])
+    t = np.array([2.0, 0.5, 1.0])
+    b = np.array([0.125, -3.0, 0.0, 7.5, -0.25])
+    y = oracle.gemm(x, w, chan_scale=c, tok_scale=t, bias=b)
+    base = (x @ w.T) * t[:, None] * c[None, :]
+    np.testing.assert_array_equal(y - base, np.broadcast_to(b, y.shape))
+    np.testing.assert_array_equal(oracle.gemm(x, w, bias=b) - x @ w.T, np.broadcast_to(b, y.shape))
+
+
 def test_fp8_activation_worked_example():
     g = load_golden("worked_fp8_act.txt")
     X = np.array(g["X"], dtype=np.float64)

@@ -35,7 +35,7 @@ PINS = [
     TG.test_worked_mxint4_and_nvfp4_values, TG.test_nvfp4_global_scale_multiplies_the_output,
     TW.test_e2m1_rounding_matches_nearest_search, TW.test_mxfp4_quant_worked_blocks,
     TW.test_mxfp4_quant_power_of_two_invariance, TW.test_mxfp4_quant_error_bound,
-    TW.test_w4a4_rational_brute_force,
+    TW.test_w4a4_rational_brute_force, TG.test_bias_is_added_after_the_scales,
 ]
 
 
@@ -91,7 +91,7 @@ def _dequant_group_shift(wfmt, group, codes, scales, zeros=None):
     return F.e2m1_to_float(q) * s
 
 
-def _gemm_transposed(x, w, chan_scale=None, tok_scale=None):
+def _gemm_transposed(x, w, chan_scale=None, tok_scale=None, bias=None):
     x = np.asarray(x, dtype=np.float64)
     w = np.asarray(w, dtype=np.float64)
     y = x @ w.T[:, ::-1] if w.shape[0] > 1 else x @ w.T        # columns in reverse order
@@ -107,8 +107,8 @@ def _w4a16_exact_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_sc
                   chan_scale=chan_scale)
 
 
-def _gemm_drop_tok_scale(x, w, chan_scale=None, tok_scale=None):
-    return _orig_gemm(x, w, chan_scale=chan_scale, tok_scale=None)
+def _gemm_drop_tok_scale(x, w, chan_scale=None, tok_scale=None, bias=None):
+    return _orig_gemm(x, w, chan_scale=chan_scale, tok_scale=None, bias=bias)
 
 
 def _quant_no_zero_guard(x_bits):
@@ -169,6 +169,17 @@ def _dequant_act_block_shifted(codes, exps, block=32):
     return F.e2m1_to_float(q) * F.e8m0_to_float(exps)[:, g]
 
 
+def _gemm_bias_scaled(x, w, chan_scale=None, tok_scale=None, bias=None):
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w, dtype=np.float64).T
+    if bias is not None:
+        y = y + np.asarray(bias, dtype=np.float64)[None, :]
+    if tok_scale is not None:
+        y = y * np.asarray(tok_scale, dtype=np.float64)[:, None]
+    if chan_scale is not None:
+        y = y * np.asarray(chan_scale, dtype=np.float64)[None, :]
+    return y
+
+
 _orig_dequant = Q.dequant
 _orig_gemm = Q.gemm
 _orig_scale_values = Q.scale_values
@@ -191,6 +202,7 @@ MUTANTS = {
     "e2m1 ties away from zero": (F, "round_to_e2m1_satfinite", _e2m1_ties_away),
     "mxfp4 act exponent minus one": (Q, "quant_act_mxfp4", _quant_act_mxfp4_exp_minus_one),
     "act block index shifted": (Q, "dequant_act_mxfp4", _dequant_act_block_shifted),
+    "bias added before the scales": (Q, "gemm", _gemm_bias_scaled),
 }
 
 

@@ -201,8 +201,8 @@ size_t qgemm_host_staging_bytes(const qgemm_wdesc* desc, int64_t M_max);
  * QGEMM_ERR_WORKSPACE (staging missing or too small), QGEMM_ERR_ALIGNMENT, any status of
  * qgemm_w4a16, QGEMM_ERR_CUDA when a copy or an event could not be enqueued (chunks already
  * enqueued then still run, and `stream` is not ordered after them: synchronize the device
- * before reusing staging or reading Y_host).  Calls from several host threads are serialized while they
- * enqueue (the library streams and events are shared per device).
+ * before reusing staging or reading Y_host).  Calls from several host threads are
+ * serialized while they enqueue (the library streams and events are shared per device).
  * The pages time the GEMM kernels alone; this entry point is a library convenience that
  * the end-to-end measurement uses.
  */

@@ -223,6 +223,34 @@ def test_stream_k_plan(L, N, K, M, tt):
         assert ws >= (sk + P) * 128 * tt * 4 + 4 * sk
 
 
+def test_default_plans_match_the_contributor_model(L):
+    """Over a grid of shapes, every default plan that cuts tiles agrees with the record-walk
+    model of stream-K (leftover tiles, contributors per tile, at most 8 unforced), uniform
+    cuts keep at least two K blocks per part, and a workspace sized for M covers the plan."""
+    P = 152
+    for N in (128, 384, 4096, 19968, 28672):
+        for K in (128, 256, 512, 1024, 8192):
+            d = qg.WeightDesc("uint4_zp", N, K, 128)
+            kb = -(-K // 128)
+            for M in (1, 2, 7, 16, 33, 100, 300, 1024):
+                p = qg.plan(d, M)
+                tt = p["token_tile"]
+                T = -(-M // tt) * -(-N // 128)
+                assert 1 <= p["grid"] <= P
+                if p["sk_tiles"] > 0:
+                    assert p["splits"] == 1
+                    assert p["sk_tiles"] == (T if T < P else T % P), (N, K, M, p)
+                    c = _sk_contributors(p["sk_tiles"], kb, P)
+                    assert p["max_contrib"] == (c if c > 1 else 0), (N, K, M, p, c)
+                    assert c <= 8
+                    if c > 1:
+                        need = (p["sk_tiles"] + p["grid"]) * 128 * tt * 4
+                        assert qg.workspace_bytes(d, M) >= need
+                elif p["splits"] > 1:
+                    assert kb // p["splits"] >= 2
+                    assert qg.workspace_bytes(d, M) >= T * p["splits"] * 128 * tt * 4
+
+
 def test_plan_defaults_are_valid(L):
     for (N, K) in [(28672, 8192), (8192, 28672), (4096, 7168), (7168, 2048)]:
         d = qg.WeightDesc("uint4_zp", N, K, 128)

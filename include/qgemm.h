@@ -108,13 +108,18 @@ int32_t qgemm_version(void);
 /* Human-readable name of a status code (static string, never NULL). */
 const char* qgemm_status_str(qgemm_status s);
 
-/* Validate a descriptor without touching any device (QGEMM_OK if supported). */
+/*
+ * Validate a descriptor without touching any device (QGEMM_OK if supported).
+ * ("Humming wird angekündigt", section "Tuning und JIT-Kompilierung für jeden Workload":
+ * the preprocessing validates the parameters.)
+ */
 qgemm_status qgemm_check_desc(const qgemm_wdesc* desc);
 
 /*
  * Size in bytes of the packed (repacked) form of one weight matrix, or 0 if `desc` is
  * invalid.  For an MoE layer, expert e's packed weights start at e * qgemm_packed_bytes().
- * The size is a multiple of 256.
+ * The size is a multiple of 256.  (Same section: the preprocessing pads the dimensions
+ * and repacks into the kernel layout.)
  */
 size_t qgemm_packed_bytes(const qgemm_wdesc* desc);
 
@@ -156,6 +161,8 @@ qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
  * 256-byte aligned and zero-filled before its first use; every successful call leaves the
  * counters zero again (the partial sums are overwritten by every call), so one
  * zero-filled buffer can be reused by consecutive calls on one stream.
+ * The K cuts are the pages' Stream-K planning ("Humming wird angekündigt", section
+ * "Leistungsoptimierung basierend auf Geräteparametern").
  */
 size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);
 
@@ -333,6 +340,9 @@ qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, co
  * SMs assumed when no device is visible): out[0] token tile, out[1] uniform K cut (1 = none),
  * out[2] stream-K tiles (0 = none), out[3] partial-sum slots per cut tile, out[4] CTAs.
  * Host-only (launches nothing); honours qgemm_force_config.
+ * The choice is the pages' Tuning Config (tile shape, Stream-K planning; "Humming wird
+ * angekündigt", sections "Tuning und JIT-Kompilierung für jeden Workload" and
+ * "Leistungsoptimierung basierend auf Geräteparametern"), made by a cost model here.
  */
 qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]);
 

@@ -161,6 +161,38 @@ def test_host_staging_bytes(L):
     assert qg.host_staging_bytes(qg.WeightDesc("int4_sym", 0, 512), 16) == 0
 
 
+def test_moe_argument_errors_before_any_launch(L):
+    """The MoE calls check their arguments on the host, before any device is touched."""
+    P = ctypes.c_void_p
+    d = qg.WeightDesc("mxfp4", 256, 512, 32).c()
+    bf16, fp8 = 0, 1
+    buf, off = P(1 << 20), P(1 << 21)
+
+    def grouped(E=4, afmt=bf16, X=buf, R=8, ldx=512, ts=None, offs=off, Y=buf, ldy=256, packed=buf):
+        return L.qgemm_moe_grouped(ctypes.byref(d), packed, E, afmt, X, R, ldx, ts, offs, Y, ldy,
+                                   None, 0, None)
+
+    def indexed(T=8, R=8, idx=P(1 << 22), E=4):
+        return L.qgemm_moe_indexed(ctypes.byref(d), buf, E, bf16, buf, T, 512, None, off, idx, R,
+                                   buf, 256, None, 0, None)
+
+    assert grouped(E=0) == 1 and grouped(E=1025) == 1           # expert count
+    assert grouped(afmt=fp8) == 1                                # descriptor is BF16
+    assert grouped(R=-1) == 1 and grouped(offs=None) == 1 and grouped(packed=None) == 1
+    assert grouped(packed=P((1 << 20) + 16)) == 3                # packed not 256-byte aligned
+    assert grouped(offs=P((1 << 21) + 2)) == 3                   # offsets not 4-byte aligned
+    assert grouped(ldx=256) == 1                                 # ldx < K
+    assert grouped(X=P((1 << 20) + 2)) == 3                      # X not 16-byte aligned
+    assert grouped(ldy=128) == 1                                 # ldy < N
+    assert grouped(R=0) == 0                                     # empty: a no-op
+    assert indexed(T=0) == 1                                     # rows to gather from none
+    assert indexed(idx=P((1 << 22) + 2)) == 3                    # index not 4-byte aligned
+    assert indexed(R=0) == 0
+    d8 = qg.WeightDesc("mxfp4", 256, 512, 32, "fp8").c()
+    assert L.qgemm_moe_grouped(ctypes.byref(d8), buf, 4, fp8, buf, 8, 512, None, off, buf, 256,
+                               None, 0, None) == 1               # FP8 without token scales
+
+
 def test_product_package_does_not_import_oracle():
     pkg = os.path.join(ROOT, "quantized_weight_gemm_gb300")
     for dirpath, _, files in os.walk(pkg):

@@ -628,7 +628,8 @@ def bench_ours(args):
                 # value is the mean over steps; the steps themselves show any outliers
                 "step_ms": [round(v, 3) for v in e2e_ms],
                 "median_step_ms": round(statistics.median(e2e_ms), 3)},
-        "gpu_launches": len(SHAPES) * len(M_SWEEP) * args.steps,
+        # each call: the FP16 activation pre-pass and the GEMM
+        "gpu_launches": 2 * len(SHAPES) * len(M_SWEEP) * args.steps,
         "clocks": clocks,
     }
     if extra is not None:

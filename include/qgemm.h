@@ -154,17 +154,34 @@ qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
                                  void* packed, void* stream);
 
 /*
- * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max: the FP32 partial
- * sums of the output tiles whose K range the schedule cuts over several CTAs (split-K or
- * stream-K; one 128 x token-tile slot per contributing CTA) and one arrival counter per
- * cut tile; 0 when no M <= M_max cuts a tile.  The workspace must be
- * 256-byte aligned and zero-filled before its first use; every successful call leaves the
- * counters zero again (the partial sums are overwritten by every call), so one
+ * Workspace bytes that qgemm_w4a16 / qgemm_w4a8 need for any M <= M_max.  In this order:
+ *   - INT4 weights with BF16 scales only: an FP16 copy of X, [M][K] FP16 plus one FP32 row
+ *     scale per row (qgemm_act_copy_bytes).  These layouts run the tensor cores on FP16
+ *     operands: a dequantized weight (q - z) * s needs up to 12 significant bits, BF16
+ *     holds 8 and FP16 11, so the kernel rounds it to FP16; X is converted exactly (each
+ *     row times a power of two, 2^-e_m, into FP16's range) by a pre-pass launched before
+ *     the GEMM, and the epilogue takes the powers of two back;
+ *   - the FP32 partial sums of the output tiles whose K range the schedule cuts over
+ *     several CTAs (split-K or stream-K; one 128 x token-tile slot per contributing CTA)
+ *     and one arrival counter per cut tile.
+ * 0 when neither applies to any M <= M_max.  The workspace must be 256-byte aligned and
+ * zero-filled before its first use; every successful call leaves the counters zero again
+ * (the partial sums and the activation copy are overwritten by every call), so one
  * zero-filled buffer can be reused by consecutive calls on one stream.
  * The K cuts are the pages' Stream-K planning ("Humming wird angekündigt", section
- * "Leistungsoptimierung basierend auf Geräteparametern").
+ * "Leistungsoptimierung basierend auf Geräteparametern"); FP16 and BF16 are both 16-bit
+ * activation types of the W4A16 path (same page, section "WnA16").
  */
 size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);
+
+/*
+ * Bytes of the FP16 activation copy that the GEMMs on INT4 weights with BF16 scales keep
+ * at the head of their workspace for x_rows rows of X (see qgemm_workspace_bytes): the
+ * smallest workspace the MoE calls accept for such weights (x_rows = R for
+ * qgemm_moe_grouped, T for qgemm_moe_indexed).  0 for every other layout, an invalid
+ * descriptor or x_rows <= 0.
+ */
+size_t qgemm_act_copy_bytes(const qgemm_wdesc* desc, int64_t x_rows);
 
 /*
  * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k]   (c = 1 when chan_scale == NULL;
@@ -250,12 +267,15 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
  *   X              : device [R, ldx] sorted rows; padding rows should be zero
  *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
  *   Y              : device BF16 [R, ldy]; rows of every expert are written
- *   ws, ws_bytes   : optional device workspace, 256-byte aligned and zero-filled before
- *                    its first use (calls leave it reusable, as for qgemm_w4a16).  With
- *                    ws_bytes >= qgemm_moe_workspace_bytes(desc, E, R) the kernel may cut
- *                    the K range of the tiles left over after whole rounds of tiles over
- *                    several CTAs (stream-K), which evens out the work when few tiles
- *                    exist; with NULL (or less) every CTA runs whole tiles.
+ *   ws, ws_bytes   : device workspace, 256-byte aligned and zero-filled before its first
+ *                    use (calls leave it reusable, as for qgemm_w4a16).  Required for INT4
+ *                    weights with BF16 scales: at least qgemm_act_copy_bytes(desc, R), the
+ *                    FP16 activation copy (QGEMM_ERR_WORKSPACE otherwise); optional (NULL)
+ *                    for the other formats.  With ws_bytes >=
+ *                    qgemm_moe_workspace_bytes(desc, E, R) the kernel may cut the K range
+ *                    of the tiles left over after whole rounds of tiles over several CTAs
+ *                    (stream-K), which evens out the work when few tiles exist; with less
+ *                    every CTA runs whole tiles.
  * "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths; tokens are
  * distributed over experts and the work per expert varies with the load).
  */
@@ -274,7 +294,10 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
  *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
  *   row_index      : device int32 [R], values in [0, T) or negative; 4-byte aligned
  *   Y              : device BF16 [R, ldy] in sorted order
- *   ws, ws_bytes   : as for qgemm_moe_grouped (qgemm_moe_workspace_bytes covers both)
+ *   ws, ws_bytes   : as for qgemm_moe_grouped, with the activation copy for the T rows
+ *                    of X: qgemm_act_copy_bytes(desc, T) at least for INT4 weights with
+ *                    BF16 scales, and qgemm_moe_workspace_bytes(desc, E, max(R, T)) for
+ *                    stream-K
  * The kernel copies the indexed rows into its activation tiles itself (token tiles of 16,
  * 32 or 64 rows, from R / E), which suits the few rows per expert of decode-sized routing;
  * for large batches the grouped call's wider tiles are faster.  An index >= T is an error
@@ -291,8 +314,10 @@ qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int3
 
 /*
  * Workspace bytes that let qgemm_moe_grouped or qgemm_moe_indexed use stream-K for E
- * experts and R sorted rows (token tile from R / E): FP32 partial-sum slots for twice the
- * SM count plus one arrival counter per SM.  0 for an invalid descriptor, E < 1 or R <= 0.
+ * experts and R sorted rows (token tile from R / E): the FP16 activation copy of R rows
+ * for INT4 weights with BF16 scales (qgemm_act_copy_bytes), then FP32 partial-sum slots
+ * for twice the SM count plus one arrival counter per SM.  0 for an invalid descriptor,
+ * E < 1 or R <= 0.
  */
 size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R);
 
@@ -322,12 +347,17 @@ qgemm_status qgemm_device_status(int32_t clear);
  * device synchronization.  The pages have no counterpart; this is a library convenience.
  * Same arguments and result as qgemm_w4a16 without `ws`/`ws_bytes`: the split-K scratch
  * is a fixed QGEMM_NOALLOC_SCRATCH_BYTES device array inside the library, held by every
- * GPU that loads it until the process exits.  Calls whose plan needs more scratch than
- * that return QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a workspace for them.
+ * GPU that loads it until the process exits.  A call needs only what its own schedule for
+ * this M uses (qgemm_plan): the partial sums of the tiles it cuts (none above M = 1024 by
+ * default), after the FP16 activation copy for INT4 weights with BF16 scales
+ * (qgemm_act_copy_bytes).  A call that needs more than the array returns
+ * QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a workspace for it.  Arguments are
+ * checked as qgemm_w4a16 checks them, before anything is enqueued.
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library routine.  The first
- * call on a device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture.  Each call zeroes the
- * part of the array it uses, on `stream`.  All calls share the one array, so calls that
+ * call on a device that needs scratch looks up the array's device address (once per
+ * device, with that device current); make that first call before any stream capture.
+ * Such a call zeroes the arrival counters of its schedule inside the array, on `stream`
+ * (the partial sums are written before they are read).  All calls share the one array, so calls that
  * may overlap on the GPU (different streams, or different host threads) race and give
  * wrong results; serialize them on one stream.
  */
@@ -354,6 +384,22 @@ qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]);
  * apply); 0 restores the built-in heuristic for that part.  Process-wide, not thread-safe.
  */
 qgemm_status qgemm_force_config(int32_t token_tile, int32_t splits);
+
+/*
+ * Test aid for the kernels' bounded waits (off by default).  With skip_first_x = 1 the
+ * dense calls' activation producer never issues the first activation load of each CTA,
+ * so the MMA issuers' wait for it, and after it every other role's, runs into the time
+ * limit: the kernel then winds down (it waits for every copy it did issue), sets
+ * QGEMM_ERR_TIMEOUT in the status word (qgemm_device_status) and returns, and the context
+ * stays usable.  Nothing is left in flight and no wait is removed.  timeout_ms > 0
+ * replaces the wait limit (QGEMM_TIMEOUT_MS, default 4000 ms) for the following calls;
+ * 0 restores it.  Process-wide, not thread-safe.  The pages' counterpart is the
+ * isolation of failures so that inference survives them (the Chinese release notes,
+ * v0.1.1: kernel compilation in a separate process).
+ * Returns QGEMM_ERR_INVALID_ARG for skip_first_x outside {0, 1} or timeout_ms outside
+ * 0..60000.
+ */
+qgemm_status qgemm_debug_stall(int32_t skip_first_x, int32_t timeout_ms);
 
 #ifdef __cplusplus
 }

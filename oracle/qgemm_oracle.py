@@ -42,9 +42,9 @@ Readings where the pages are silent (each is listed in the design notes):
     and each element is x / 2^(E-127) rounded to nearest even on the e2m1 grid with
     saturation at 6.
 
-The matmul accumulates in float64; W4A16 uses the dequantized weights as BF16 values (the
-operand of a 16-bit tensor core), W4A8 the exact e2m1 x E8M0 values (exact in FP8 with a
-block scale).  Nothing is blocked, fused or reordered beyond the plain definition.
+The matmul accumulates in float64 over the exact dequantized weights, for W4A16 and W4A8
+alike; dequant_bf16 (the weights rounded to BF16) is what the bit-exact dequantization
+check compares.  Nothing is blocked, fused or reordered beyond the plain definition.
 """
 import numpy as np
 
@@ -100,8 +100,9 @@ def dequant(wfmt, group, codes, scales, zeros=None, global_scale=1.0):
 
 
 def dequant_bf16(wfmt, group, codes, scales, zeros=None):
-    """The weights as a kernel must feed them to a BF16 tensor core: RNE_bf16(W_exact),
-    without the per-tensor scale (that one multiplies the output)."""
+    """The dequantized weights as BF16 numbers: RNE_bf16(W_exact), without the per-tensor
+    scale (that one multiplies the output).  This is what a dequantization to BF16 must
+    reproduce bit for bit; the GEMM's reference uses the exact weights."""
     return F.round_to_bf16(dequant(wfmt, group, codes, scales, zeros))
 
 
@@ -123,15 +124,16 @@ def gemm(x, w, chan_scale=None, tok_scale=None, bias=None):
 
 
 def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None, global_scale=1.0):
-    """Dense W4A16: BF16 activations (bit patterns [M, K]) times the dequantized weights.
+    """Dense W4A16: BF16 activations (bit patterns [M, K]) times the exact dequantized weights.
 
-    W4A16 computes on 16-bit tensor cores ("Humming wird angekündigt", section "WnA16":
-    low-bit weights combined with FP16/BF16 activations, using the widely available 16-bit
-    compute), so the dequantized weight is the BF16 value RNE_bf16(W_exact) -- the same
-    weights the dequantization must reproduce bit for bit.  The sum runs in float64; the
-    per-tensor scale (NVFP4) then multiplies the output like the per-channel one."""
+    The plain definition: unpack the codes, dequantize exactly in float64 and multiply with
+    float64 accumulation.  A kernel on a BF16 tensor core meets it by keeping the weights
+    exact there and applying the group scale to its FP32 accumulators (the Chinese release
+    notes, v0.1.3: the "apply scale on C" path); a BF16-rounded weight is what the
+    dequantization check compares (dequant_bf16), not what the product uses.  The per-tensor
+    scale (NVFP4) then multiplies the output like the per-channel one."""
     x = F.bf16_bits_to_float(x_bits)
-    y = gemm(x, dequant_bf16(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
+    y = gemm(x, dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
     return y * np.float64(np.float32(global_scale))
 
 

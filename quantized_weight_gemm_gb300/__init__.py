@@ -16,6 +16,7 @@ __all__ = [
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
     "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "host_staging_bytes",
     "host_staging", "w4a16_host", "moe_indexed", "check_desc", "WFMT", "AFMT", "EXPORTS",
+    "debug_stall", "act_copy_bytes",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -29,7 +30,8 @@ EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packe
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
            "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host",
-           "qgemm_moe_indexed", "qgemm_repack_scaled")
+           "qgemm_moe_indexed", "qgemm_repack_scaled", "qgemm_debug_stall",
+           "qgemm_act_copy_bytes")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -100,9 +102,11 @@ def lib():
         "qgemm_dequant_debug": (ctypes.c_int, [D, P, P, P]),
         "qgemm_device_status": (ctypes.c_int, [I32]),
         "qgemm_force_config": (ctypes.c_int, [I32, I32]),
+        "qgemm_debug_stall": (ctypes.c_int, [I32, I32]),
         "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
+        "qgemm_act_copy_bytes": (SZ, [D, I64]),
         "qgemm_host_staging_bytes": (SZ, [D, I64]),
         "qgemm_moe_indexed": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, I64, P, I64, P, SZ, P]),
         "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P, SZ, P]),
@@ -282,15 +286,30 @@ def moe_workspace(desc, E, R, device="cuda"):
     return torch.zeros(max(moe_workspace_bytes(desc, E, R), 256), dtype=torch.uint8, device=device)
 
 
+def act_copy_bytes(desc, x_rows):
+    """Bytes of the FP16 activation copy (INT4 with BF16 scales; 0 for other formats)."""
+    d = desc.c()
+    return int(lib().qgemm_act_copy_bytes(ctypes.byref(d), int(x_rows)))
+
+
+def _moe_min_ws(desc, x_rows, device):
+    """The smallest workspace the MoE calls accept: the activation copy, or None."""
+    n = act_copy_bytes(desc, x_rows)
+    return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
+
+
 def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None):
     """MoE grouped GEMM over expert-sorted rows X [R, K] (BF16, or uint8 e4m3 with
-    tok_scale); offsets: int32 [E+1] on the device; ws: optional moe_workspace()."""
+    tok_scale); offsets: int32 [E+1] on the device; ws: optional moe_workspace() (without
+    one, whole tiles, and for INT4 with BF16 scales just the activation copy)."""
     fp8 = X.dtype == torch.uint8
     _need(offsets, "offsets", torch.int32)
     _row_major(X, "X")
     R = X.shape[0]
     if out is None:
         out = torch.empty(R, desc.N, dtype=torch.bfloat16, device=X.device)
+    if ws is None:
+        ws = _moe_min_ws(desc, R, X.device)
     d = desc.c()
     wsb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().qgemm_moe_grouped(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
@@ -310,6 +329,8 @@ def moe_indexed(desc, packed, E, X, offsets, row_index, tok_scale=None, out=None
     R = row_index.numel()
     if out is None:
         out = torch.empty(R, desc.N, dtype=torch.bfloat16, device=X.device)
+    if ws is None:
+        ws = _moe_min_ws(desc, X.shape[0], X.device)
     d = desc.c()
     wsb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().qgemm_moe_indexed(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
@@ -336,6 +357,11 @@ def device_status(clear=True):
 def force_config(token_tile=0, splits=0):
     """splits: >= 1 uniform K cut, -1 stream-K, 0 heuristic (see qgemm_force_config)."""
     _check(lib().qgemm_force_config(int(token_tile), int(splits)), "force_config")
+
+
+def debug_stall(skip_first_x=0, timeout_ms=0):
+    """Test aid for the bounded waits (see qgemm_debug_stall); (0, 0) restores the default."""
+    _check(lib().qgemm_debug_stall(int(skip_first_x), int(timeout_ms)), "debug_stall")
 
 
 def plan(desc, M):

@@ -22,9 +22,14 @@ constexpr int kMaxDevices = 64;
 constexpr int64_t kSplitMaxM = 1024;          // split-K is considered only up to this M
 constexpr uint64_t kTimeoutNs = 4000000000ull;     // default limit of one device wait
 
+int g_debug_skip_first_x = 0;
+uint64_t g_debug_timeout_ns = 0;
+
 // Limit of every bounded wait inside a kernel: QGEMM_TIMEOUT_MS in the environment (read
-// once; a profiler that replays each launch many times needs a longer limit), else 4 s.
+// once; a profiler that replays each launch many times needs a longer limit), else 4 s;
+// qgemm_debug_stall may override it.
 uint64_t timeout_ns() {
+  if (g_debug_timeout_ns != 0) return g_debug_timeout_ns;
   static const uint64_t v = []() -> uint64_t {
     const char* e = std::getenv("QGEMM_TIMEOUT_MS");
     if (e != nullptr) {
@@ -291,13 +296,18 @@ EncodeFn encode_fn() {
 // 3-D tensor [K / slab][rows][slab] so that one load brings several slabs (several
 // pipeline stages for narrow token tiles); otherwise as a 2-D tensor [rows][K] loaded one
 // slab at a time.  Sets *is_3d accordingly.
-bool make_x_map(CUtensorMap* m, const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx,
+enum XType { X_BF16 = 0, X_F16 = 1, X_FP8 = 2 };
+
+bool make_x_map(CUtensorMap* m, const void* X, XType xt, int64_t rows, int64_t K, int64_t ldx,
                 int box_rows, int* is_3d) {
   EncodeFn enc = encode_fn();
   if (enc == nullptr) return false;
+  const bool fp8 = xt == X_FP8;
   const int esize = fp8 ? 1 : 2;
   const int64_t slab = 128 / esize;                        // elements per 128-byte slab
-  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : xt == X_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                               : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   const int box_slabs = gemm_x_box_slabs(fp8, box_rows);
   if (K % slab == 0 && box_slabs > 0) {
     cuuint64_t dims[3] = {cuuint64_t(slab), cuuint64_t(rows), cuuint64_t(K / slab)};
@@ -334,32 +344,60 @@ qgemm_status check_y(const void* Y, int64_t N, int64_t ldy) {
   return QGEMM_OK;
 }
 
+// Every argument check of the dense calls that needs no device.
+qgemm_status check_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
+                         int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
+                         const void* Y, int64_t ldy, Layout* L) {
+  if (!layout_of(desc, L)) return QGEMM_ERR_INVALID_ARG;
+  if ((L->afmt == A_FP8) != fp8) return QGEMM_ERR_INVALID_ARG;
+  if (fp8 && L->wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
+  if (M < 0) return QGEMM_ERR_INVALID_ARG;
+  if (packed == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(packed, 256)) return QGEMM_ERR_ALIGNMENT;
+  qgemm_status s = check_x(X, fp8, M, L->K, ldx);
+  if (s != QGEMM_OK) return s;
+  if ((s = check_y(Y, L->N, ldy)) != QGEMM_OK) return s;
+  if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
+  if ((chan_scale && !aligned(chan_scale, 4)) || (tok_scale && !aligned(tok_scale, 4)))
+    return QGEMM_ERR_ALIGNMENT;
+  return QGEMM_OK;
+}
+
 qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
                        int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
                        void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
   Layout L;
-  if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
-  if ((L.afmt == A_FP8) != fp8) return QGEMM_ERR_INVALID_ARG;
-  if (fp8 && L.wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
-  if (M < 0) return QGEMM_ERR_INVALID_ARG;
-  if (packed == nullptr) return QGEMM_ERR_INVALID_ARG;
-  if (!aligned(packed, 256)) return QGEMM_ERR_ALIGNMENT;
-  qgemm_status s = check_x(X, fp8, M, L.K, ldx);
+  const qgemm_status s = check_dense(desc, fp8, packed, X, M, ldx, tok_scale, chan_scale, Y,
+                                     ldy, &L);
   if (s != QGEMM_OK) return s;
-  if ((s = check_y(Y, L.N, ldy)) != QGEMM_OK) return s;
-  if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
-  if ((chan_scale && !aligned(chan_scale, 4)) || (tok_scale && !aligned(tok_scale, 4)))
-    return QGEMM_ERR_ALIGNMENT;
   if (M == 0) return QGEMM_OK;
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
-  const GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
-  const int64_t need = split_ws_bytes(L, M, plan);
+  GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
+  // FP16 operands: the pre-pass's FP16 rows and row scales lead the workspace
+  const bool f16 = f16_operands(L);
+  const int64_t prep = f16 ? prep_x_f16_bytes(M, L.K) : 0;
+  const int64_t need = prep + split_ws_bytes(L, M, plan);
   if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need)) return QGEMM_ERR_WORKSPACE;
   if (need > 0 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void* xg = X;                                    // what the GEMM reads as X
+  int64_t ldg = ldx;
+  float* rowscale = nullptr;
+  if (f16) {
+    rowscale = reinterpret_cast<float*>(wsb + round_up(M * L.K * 2, 256));
+    if (launch_prep_x_f16(X, M, L.K, ldx, wsb, rowscale, static_cast<cudaStream_t>(stream)) !=
+        cudaSuccess)
+      return QGEMM_ERR_CUDA;
+    xg = wsb;
+    ldg = L.K;
+    plan.pdl = 1;
+  }
   CUtensorMap tmap;
   int x3d = 0;
-  if (!make_x_map(&tmap, X, fp8, M, L.K, ldx, plan.token_tile, &x3d)) return QGEMM_ERR_CUDA;
+  if (!make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, M, L.K, ldg, plan.token_tile,
+                  &x3d))
+    return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
   a.x_3d = x3d;
@@ -378,23 +416,51 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
     a.group_m = int(std::min<int64_t>(gm, a.m_tiles));
   }
   a.chan_scale = chan_scale;
-  a.tok_scale = tok_scale;
+  a.tok_scale = f16 ? rowscale : tok_scale;
   a.Y = Y;
   a.ldy = ldy;
-  if (need > 0) {
+  if (need > prep) {
     int64_t slots, counters;
     cut_sizes(L, M, plan, &slots, &counters);
-    a.ws = static_cast<float*>(ws);
-    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
-                                            slots * slot_bytes(plan.token_tile));
+    a.ws = reinterpret_cast<float*>(wsb + prep);
+    a.counters = reinterpret_cast<int32_t*>(wsb + prep + slots * slot_bytes(plan.token_tile));
   }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
+  a.debug_skip_first_x = g_debug_skip_first_x;
   cudaError_t e = launch_gemm(fp8, plan, tmap, a, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace qgemm {
+
+qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, const void* X,
+                               int64_t M, int64_t ldx, const float* chan_scale, const void* Y,
+                               int64_t ldy, int64_t* need, int64_t* counter_off,
+                               int64_t* counter_bytes) {
+  *need = *counter_off = *counter_bytes = 0;
+  Layout L;
+  const qgemm_status s = check_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, Y,
+                                     ldy, &L);
+  if (s != QGEMM_OK || M == 0) return s;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  const GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
+  int64_t slots, counters;
+  cut_sizes(L, M, plan, &slots, &counters);
+  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(M, L.K) : 0;
+  const int64_t split = split_ws_bytes(L, M, plan);
+  *need = prep + split;
+  if (split > 0) {
+    *counter_off = prep + slots * slot_bytes(plan.token_tile);
+    *counter_bytes = split - slots * slot_bytes(plan.token_tile);
+  }
+  return QGEMM_OK;
+}
+
+}  // namespace qgemm
 
 extern "C" {
 
@@ -463,6 +529,8 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
   for (int64_t M = 1; M <= top; ++M)
     best = std::max(best, split_ws_bytes(L, M, plan_dense(L, M, sms, inv)));
   best = std::max(best, split_ws_bytes(L, M_max, plan_dense(L, M_max, sms, inv)));
+  // FP16 operands: the activation copy, largest at M_max
+  if (f16_operands(L)) best += prep_x_f16_bytes(M_max, L.K);
   return size_t(best);
 }
 
@@ -532,17 +600,37 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   plan.sk_tiles = 0;
   plan.max_contrib = 0;
   plan.grid = dev->sms;
+  // FP16 operands: the pre-pass's FP16 copy of the x_rows rows of X and their row scales
+  // lead the workspace, which is then required
+  const bool f16 = f16_operands(L);
+  const int64_t prep = f16 ? prep_x_f16_bytes(x_rows, L.K) : 0;
+  if (f16 && (ws == nullptr || int64_t(ws_bytes) < prep)) return QGEMM_ERR_WORKSPACE;
+  if (f16 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const void* xg = X;
+  int64_t ldg = ldx;
+  float* rowscale = nullptr;
+  if (f16) {
+    rowscale = reinterpret_cast<float*>(wsb + round_up(x_rows * L.K * 2, 256));
+    if (launch_prep_x_f16(X, x_rows, L.K, ldx, wsb, rowscale,
+                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return QGEMM_ERR_CUDA;
+    xg = wsb;
+    ldg = L.K;
+    plan.pdl = 1;
+  }
   // the gathering kernel copies X rows itself and never reads a tensor map
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   int x3d = 0;
-  if (row_index == nullptr && !make_x_map(&tmap, X, fp8, R, L.K, ldx, tt, &x3d))
+  if (row_index == nullptr &&
+      !make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, R, L.K, ldg, tt, &x3d))
     return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
   if (row_index != nullptr) {
-    a.x = static_cast<const uint8_t*>(X);
-    a.ldx_bytes = ldx * (fp8 ? 1 : 2);
+    a.x = static_cast<const uint8_t*>(xg);
+    a.ldx_bytes = ldg * (fp8 ? 1 : 2);
     a.x_rows = x_rows;
   }
   a.x_3d = x3d;
@@ -554,16 +642,16 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   a.E = E;
   a.M = R;
   a.splits = 1;
-  a.tok_scale = tok_scale;
+  a.tok_scale = f16 ? rowscale : tok_scale;
   a.Y = Y;
   a.ldy = ldy;
-  // Stream-K needs the whole bound; a smaller (or no) workspace keeps whole tiles.
+  // Stream-K needs the whole bound after the activation copy; a smaller (or no) workspace
+  // keeps whole tiles.
   if (ws != nullptr && !inv && g_force_splits != 1 && sk_fits(L, plan.grid) &&
-      int64_t(ws_bytes) >= moe_ws_bytes(tt, plan.grid)) {
+      int64_t(ws_bytes) >= prep + moe_ws_bytes(tt, plan.grid)) {
     if (!aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
-    a.ws = static_cast<float*>(ws);
-    a.counters = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) +
-                                            2 * int64_t(plan.grid) * slot_bytes(tt));
+    a.ws = reinterpret_cast<float*>(wsb + prep);
+    a.counters = reinterpret_cast<int32_t*>(wsb + prep + 2 * int64_t(plan.grid) * slot_bytes(tt));
   }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
@@ -593,11 +681,18 @@ qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int3
                  ldy, ws, ws_bytes, stream);
 }
 
+size_t qgemm_act_copy_bytes(const qgemm_wdesc* desc, int64_t x_rows) {
+  Layout L;
+  if (!layout_of(desc, &L) || x_rows <= 0 || !f16_operands(L)) return 0;
+  return size_t(prep_x_f16_bytes(x_rows, L.K));
+}
+
 size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R) {
   Layout L;
   if (!layout_of(desc, &L) || E < 1 || R <= 0) return 0;
   const int tt = std::max(moe_token_tile(R, E), std::min(moe_indexed_token_tile(R, E), 64));
-  return size_t(moe_ws_bytes(tt, sms_or_default()));
+  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(R, L.K) : 0;
+  return size_t(prep + moe_ws_bytes(tt, sms_or_default()));
 }
 
 qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,
@@ -636,6 +731,14 @@ qgemm_status qgemm_plan(const qgemm_wdesc* desc, int64_t M, int32_t out[5]) {
   out[2] = p.sk_tiles;
   out[3] = p.max_contrib;
   out[4] = p.grid;
+  return QGEMM_OK;
+}
+
+qgemm_status qgemm_debug_stall(int32_t skip_first_x, int32_t timeout_ms) {
+  if (skip_first_x < 0 || skip_first_x > 1 || timeout_ms < 0 || timeout_ms > 60000)
+    return QGEMM_ERR_INVALID_ARG;
+  g_debug_skip_first_x = skip_first_x;
+  g_debug_timeout_ns = uint64_t(timeout_ms) * 1000000ull;
   return QGEMM_OK;
 }
 

@@ -11,6 +11,10 @@
 //   Symmetric INT4 is stored as u = q + 8 and decoded with z = 8 (the "magic number"
 //   construction of Kim et al., "Who Says Elephants Can't Run?", 2022, restated from the
 //   bfloat16 format definition).
+//   INT4 with BF16 scales runs on FP16 operands instead (the same construction in FP16:
+//   1024.0 = 0x6400 has a unit last place, so 0x6400 | u is 1024 + u): one FP16 multiply
+//   by s * 2^k rounds (u - z) * s * 2^k to 11 significant bits, where BF16 would keep 8
+//   of the up to 12 that the product has.
 //   MXFP4: the e2m1 magnitude bits (e1 e0 m) are moved to bf16 bits 8..6 and the sign to
 //   bit 15, which is the bf16 number e2m1(q) * 2^-126 (a subnormal for e = 0); multiplying
 //   by 2^(E-1) (or by 2^127 and then 2^(E-128) when E > 128) gives e2m1(q) * 2^(E-127),
@@ -43,6 +47,22 @@ __device__ __forceinline__ void decode_int4_word(uint32_t w, uint32_t zz, uint32
     const uint32_t t = ptx::lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x43004300u);
     out[i] = ptx::bf16x2_mul(ptx::bf16x2_sub(t, zz), s2);
   }
+}
+
+// INT4 word -> 4 f16x2 (pairs 0..3).  zz = f16x2(1024 + z), s2 = f16x2(scale * 2^k).
+__device__ __forceinline__ void decode_int4_word_f16(uint32_t w, uint32_t zz, uint32_t s2,
+                                                     uint32_t* out) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ptx::lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x64006400u);
+    out[i] = ptx::f16x2_mul(ptx::f16x2_sub(t, zz), s2);
+  }
+}
+
+// f16x2 of a BF16 scale (bits) times the power of two p, rounded once to FP16.
+__device__ __forceinline__ uint32_t scale_f16x2(uint32_t s_bf16, float p) {
+  const float v = __uint_as_float(s_bf16 << 16) * p;
+  return ptx::cvt_f16x2_f32(v, v);
 }
 
 // MXFP4 word -> 4 bf16x2.  sa, sb: bf16x2 factors (sb == 0 means single multiply).

@@ -315,6 +315,16 @@ __device__ __forceinline__ void warp_arrive(uint64_t* bar, int lane) {
   if (lane == 0) ptx::mbar_arrive(bar);
 }
 
+// Release a shared-memory slot that this warp read with ordinary loads to a producer that
+// refills it with bulk copies: every lane orders its reads before the copies (which write
+// through the async proxy) with a proxy fence, then one arrival is made.  Without the
+// fence the refill could overwrite the slot before all reads of it were performed, which
+// showed as a lane quarter of a tile decoded from the next record.
+__device__ __forceinline__ void release_to_async(uint64_t* bar, int lane) {
+  ptx::fence_proxy_async_smem();
+  warp_arrive(bar, lane);
+}
+
 // Position in a ring of `n` slots: slot index and the parity of its current use.
 struct Ring {
   int slot = 0;
@@ -331,25 +341,31 @@ enum DecodeMode : int {
   DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5
 };
 
-// Decode two 32-K chunks of weight row r into 32 bf16x2 registers (pair order).  The codes
-// come from slot chunks `slot0`, `slot0 + 1` of the staged record; their scales and zero
-// points are the record's entries for record chunks `rchunk0`, `rchunk0 + 1`.
+// INT4 with BF16 scales (every group size): FP16 tensor-core operands, see f16_operands().
+template <bool A8, int DM>
+constexpr bool kF16Operands =
+    !A8 && (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1 || DM == DM_INT4_ANY);
+
+// Decode two 32-K chunks of weight row r into 32 registers of 16-bit pairs (pair order):
+// FP16 for INT4 with BF16 scales (the scale times w_pre = 2^k), BF16 for the other formats.
+// The codes come from slot chunks `slot0`, `slot0 + 1` of the staged record; their scales
+// and zero points are the record's entries for record chunks `rchunk0`, `rchunk0 + 1`.
 template <int DM>
 __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int tail, int slot0,
                                                       int rchunk0, int r, int has_zp, int G,
-                                                      int zoff, uint32_t (&regs)[32]) {
+                                                      int zoff, float w_pre, uint32_t (&regs)[32]) {
   if constexpr (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1) {
     const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[r];
     uint32_t z = 8;
     if constexpr (DM == DM_INT4_ZP_G1) z = (rec[tail + zoff + (r >> 1)] >> (4 * (r & 1))) & 0xFu;
-    const uint32_t zz = (0x4300u | z) * 0x00010001u;
-    const uint32_t s2 = s * 0x00010001u;
+    const uint32_t zz = (0x6400u | z) * 0x00010001u;
+    const uint32_t s2 = scale_f16x2(s, w_pre);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const uint4 q = *reinterpret_cast<const uint4*>(rec + (slot0 + c) * (kTileN * 16) + r * 16);
       const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+      for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, s2, &regs[16 * c + 4 * j]);
     }
   } else {
 #pragma unroll
@@ -380,10 +396,10 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
         const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[ent];
         uint32_t z = 8;
         if (has_zp) z = (rec[tail + zoff + (ent >> 1)] >> (4 * (ent & 1))) & 0xFu;
-        const uint32_t zz = (0x4300u | z) * 0x00010001u;
-        const uint32_t s2 = s * 0x00010001u;
+        const uint32_t zz = (0x6400u | z) * 0x00010001u;
+        const uint32_t s2 = scale_f16x2(s, w_pre);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) decode_int4_word(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+        for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, s2, &regs[16 * c + 4 * j]);
       }
     }
   }
@@ -403,6 +419,9 @@ template <int BNT, bool A8, int DM, bool GATHER>
 __global__ void __launch_bounds__(Roles<BNT>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   static_assert(!GATHER || BNT <= 64, "gathered tiles exist for token tiles up to 64");
+  constexpr bool F16 = kF16Operands<A8, DM>;
+  // per-token (per-row) output scale: FP8's token scale, or the FP16 copy's row scale
+  constexpr bool kTokScale = A8 || F16;
   using C = GemmCfg<BNT, A8>;
   using RO = Roles<BNT>;
   constexpr int kEpiWarp0 = RO::kEpiWarp0;
@@ -620,6 +639,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     }
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer
+    // FP16 operands: the activations come from the pre-pass launched just before
+    if constexpr (F16) ptx::grid_dependency_wait();
     if constexpr (GATHER) {
       // Gathered (indexed MoE) tiles: the warp copies each unit's rows out of X in token
       // order, 16 bytes per lane and copy (cp.async), straight into the 128-byte-swizzled
@@ -695,6 +716,10 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         const int nst = (w.kb1 - w.kb0) * kSub;
         for (int i0 = 0; i0 < nst; i0 += XQ) {
           if (!ptx::mbar_wait(&xempty[rx.slot], rx.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
+          if (a.debug_skip_first_x && uj == 0 && i0 == 0) {   // test aid: issue nothing
+            rx.next(SX);
+            continue;
+          }
           uint8_t* sx = s_x + rx.slot * C::kXSlotBytes;
           // K offset (elements) of the chunk's first stage: records kb0.., sub-stage h
           const int k0 = w.kb0 * kStageK + i0 * (kStageK / kSub);
@@ -780,7 +805,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               const uint64_t b = bdesc + uint64_t((q * C::kSlabBytes) >> 4);
               const uint32_t a = a_tmem + uint32_t(q * 32);
               ptx::mma4_f16_ts_elect(d_tmem, a, a + 8u, a + 16u, a + 24u, b, b + 2u, b + 4u, b + 6u,
-                                     ptx::idesc_bf16(128, BNT), q > 0 ? 1u : (first ^ 1u));
+                                     F16 ? ptx::idesc_f16(128, BNT) : ptx::idesc_bf16(128, BNT),
+                                     q > 0 ? 1u : (first ^ 1u));
             }
           }
           first = 0;
@@ -811,6 +837,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     int e_hint = -1;
     for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
       const int nst = (w.kb1 - w.kb0) * kSub;
+      // FP16 operands: the unit's expert's scale factor 2^k, from its packed header
+      float w_pre = 1.0f;
+      if constexpr (F16)
+        w_pre = __ldg(&reinterpret_cast<const PackedHeader*>(
+                          a.packed + int64_t(w.expert) * a.expert_stride)->w_prescale);
       // Visit only this warpgroup's stages; ring slots and phases follow from the stage
       // counter (the ring depths are compile-time constants).
       const uint32_t g1 = g0 + uint32_t(nst);
@@ -837,7 +868,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               decode_e2m1_to_e4m3_word(wd[j], regs[8 * c + 2 * j], regs[8 * c + 2 * j + 1]);
           }
           const uint32_t sf = *reinterpret_cast<const uint32_t*>(rec + kTail + r * 4);
-          warp_arrive(&rempty[cr.slot], lane);           // record consumed
+          release_to_async(&rempty[cr.slot], lane);           // record consumed
           if (!warp_all(ptx::mbar_wait(&aempty[ca.slot], ca.phase ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
           ptx::tc_fence_after();
           ptx::tmem_st4(t_lane + uint32_t(C::kSfaCol0 + 4 * ca.slot), sf, sf, sf, sf);
@@ -846,14 +877,14 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           // A half record holds record chunks 2h, 2h + 1 (h = i % 2) in slot chunks 0, 1.
           const int rbase = (CH == 4) ? 0 : 2 * (i & 1);
           uint32_t regs[32];
-          decode_two_chunks_a16<DM>(rec, kTail, 0, rbase, r, L.has_zp, G, zoff, regs);
-          if (CH == 2) warp_arrive(&rempty[cr.slot], lane);
+          decode_two_chunks_a16<DM>(rec, kTail, 0, rbase, r, L.has_zp, G, zoff, w_pre, regs);
+          if (CH == 2) release_to_async(&rempty[cr.slot], lane);
           if (!warp_all(ptx::mbar_wait(&aempty[ca.slot], ca.phase ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
           ptx::tc_fence_after();
           ptx::tmem_st32(a_col, regs);
           if (CH == 4) {
-            decode_two_chunks_a16<DM>(rec, kTail, 2, 2, r, L.has_zp, G, zoff, regs);
-            warp_arrive(&rempty[cr.slot], lane);
+            decode_two_chunks_a16<DM>(rec, kTail, 2, 2, r, L.has_zp, G, zoff, w_pre, regs);
+            release_to_async(&rempty[cr.slot], lane);
             ptx::tmem_st32(a_col + 32u, regs);
           }
         }
@@ -915,6 +946,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       }
       return a.tok_scale[m];
     };
+    if constexpr (F16) ptx::grid_dependency_wait();   // the row scales come from the pre-pass
     for (int uj = 0; unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
       const int acc = ui % C::kNumAcc;
       const uint32_t acc_par = uint32_t((ui / C::kNumAcc) & 1);
@@ -927,9 +959,10 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       const bool n_ok = n < L.N;
       const bool split = w.ncontrib > 1;
       __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(a.Y);
-      // NVFP4: the accumulator scale of the unit's expert, from its packed header
+      // NVFP4 and the FP16 operands: the accumulator scale of the unit's expert, from its
+      // packed header
       float acc_s = 1.0f;
-      if constexpr (DM == DM_NVFP4)
+      if constexpr (DM == DM_NVFP4 || F16)
         acc_s = __ldg(&reinterpret_cast<const PackedHeader*>(
                           a.packed + int64_t(w.expert) * a.expert_stride)->acc_scale);
       // Partial accumulators of the issuers that had a stage in this unit: the unit's
@@ -941,7 +974,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           // Wide tiles: scale and round every column of this warp to BF16 in registers,
           // hand the accumulator back to the MMA at once, then store.
           float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
-          if constexpr (DM == DM_NVFP4) cs *= acc_s;
+          if constexpr (DM == DM_NVFP4 || F16) cs *= acc_s;
           uint32_t packed[kCols / 2];
 #pragma unroll
           for (int c = 0; c < kCols / 16; ++c) {
@@ -962,8 +995,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               const int64_t m = w.row0 + int64_t(eh) * kCols + j;   // (never a gathered tile)
               if (m < w.row_end) {
                 uint16_t h = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
-                if (A8) {
-                  // per-token scale after the rounding above would round twice: redo it
+                if (kTokScale) {
+                  // the per-token scale after the rounding above: FP8's rounds twice (within
+                  // its tolerance); the FP16 copy's is a power of two and commutes with it
                   const float y = __uint_as_float(uint32_t(h) << 16);
                   h = uint16_t(ptx::pack_bf16x2(y * a.tok_scale[m], 0.0f) & 0xFFFFu);
                 }
@@ -977,7 +1011,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if (!split) {
         // Narrow tiles (double-buffered accumulators): convert and store chunk by chunk.
         float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
-        if constexpr (DM == DM_NVFP4) cs *= acc_s;
+        if constexpr (DM == DM_NVFP4 || F16) cs *= acc_s;
 #pragma unroll 1
         for (int c = 0; c < kCols / kChunk; ++c) {
           uint32_t v[32];
@@ -992,7 +1026,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               const int64_t m = w.row0 + int64_t(eh) * kCols + c * kChunk + j;
               if (m < w.row_end) {
                 float y = __uint_as_float(v[j]) * cs;
-                if (A8) y *= tok_scale_of(m);
+                if (kTokScale) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }
             }
@@ -1035,7 +1069,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         const float* row0p = a.ws + int64_t(w.slot0) * slot_floats + int64_t(r) * BNT +
                              eh * kCols;
         float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
-        if constexpr (DM == DM_NVFP4) cs2 *= acc_s;
+        if constexpr (DM == DM_NVFP4 || F16) cs2 *= acc_s;
         constexpr int kPass = kCols < 16 ? kCols : 16;
 #pragma unroll 1
         for (int c0 = 0; c0 < kCols; c0 += kPass) {
@@ -1060,7 +1094,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               const int64_t m = w.row0 + int64_t(eh) * kCols + c0 + j;
               if (m < w.row_end) {
                 float y = sum[j] * cs2;
-                if (A8) y *= tok_scale_of(m);
+                if (kTokScale) y *= tok_scale_of(m);
                 Y[m * a.ldy + n] = __float2bfloat16_rn(y);
               }
             }
@@ -1072,10 +1106,12 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   }
 
   // ------------------------------------------------------------------ teardown
-  if (threadIdx.x == 0 && *abort_flag) atomicCAS(a.status, 0, kStatusTimeout);
+  // (the abort flag is read after the barrier: a role that finished early must not miss
+  // a wait that gave up later in another role)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
+  if (threadIdx.x == 0 && *abort_flag) atomicCAS(a.status, 0, kStatusTimeout);
   if (warp == kEpiWarp0) ptx::tmem_dealloc(tbase, C::kTmemCols);
 }
 
@@ -1093,8 +1129,17 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  qgemm_tc_kernel<BNT, A8, DM, GATHER><<<plan.grid, Roles<BNT>::kThreads, kSmem, st>>>(tmap, args);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(plan.grid));
+  cfg.blockDim = dim3(Roles<BNT>::kThreads);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = plan.pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, qgemm_tc_kernel<BNT, A8, DM, GATHER>, tmap, args);
 }
 
 template <bool A8, int DM>

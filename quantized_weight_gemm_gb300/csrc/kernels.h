@@ -5,9 +5,20 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "qgemm.h"
 #include "qgemm_internal.h"
 
 namespace qgemm {
+
+// The scratch that the dense W4A16 call would use for these arguments under its own plan
+// for M: *need bytes in all (0 when the plan cuts no tile's K range), of which the arrival
+// counters, [*counter_off, *counter_off + *counter_bytes), must be zero at launch.  Checks
+// every argument as qgemm_w4a16 does and returns its error, if any, before looking at the
+// device.
+qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, const void* X,
+                               int64_t M, int64_t ldx, const float* chan_scale, const void* Y,
+                               int64_t ldy, int64_t* need, int64_t* counter_off,
+                               int64_t* counter_bytes);
 
 int* device_status_ptr();
 
@@ -15,6 +26,12 @@ int* device_status_ptr();
 cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* scales,
                           const uint8_t* zeros, float acc_scale, void* packed, cudaStream_t st);
 cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, cudaStream_t st);
+// The FP16 copy of BF16 activations for the FP16-operand GEMM: for each row m,
+// e_m = floor(log2(amax_m)) - 14 (0 for an all-zero row), X16[m][k] = X[m][k] * 2^-e_m
+// rounded to FP16 (exact unless |x| < 2^-31 amax_m, below FP16's subnormal grid),
+// rowscale[m] = 2^e_m.  X16 is [rows][K] with leading dimension K.
+cudaError_t launch_prep_x_f16(const void* X, int64_t rows, int64_t K, int64_t ldx, void* X16,
+                              float* rowscale, cudaStream_t st);
 cudaError_t launch_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
                                  int64_t ldq, float* s, cudaStream_t st);
 
@@ -57,6 +74,9 @@ struct GemmArgs {
   int* status;
   uint64_t timeout_ns;
   int32_t x_3d;                // X map is 3-D (a box covers several stages); else 2-D
+  // Test aid (qgemm_debug_stall): the activation producer of each CTA never issues its
+  // first load, so the waits on it run into their time limit; nothing is left in flight.
+  int32_t debug_skip_first_x;
 };
 
 struct GemmPlan {
@@ -65,6 +85,10 @@ struct GemmPlan {
   int sk_tiles;                // > 0: stream-K over the first sk_tiles tiles (splits == 1)
   int max_contrib;             // partial-sum slots per cut tile (0 when nothing is cut)
   int grid;                    // persistent CTAs
+  // Launched as a programmatic dependent of the kernel before it on the stream (the FP16
+  // activation pre-pass): its prologue and weight stream start early, and its reads of the
+  // pre-pass's output wait for that kernel (griddepcontrol.wait).
+  int pdl = 0;
 };
 
 // Launch the tcgen05 GEMM for the given plan.  tmap describes X (BF16 or E4M3, K-major,

@@ -92,6 +92,12 @@ __global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
         if ((v & 0x7F80u) == 0x7F80u) set_status(kStatusBadValue);   // NaN / Inf
       }
       reinterpret_cast<uint16_t*>(dst)[r * G + j] = v;
+      // the tensor's largest |scale| (magnitude bits order like the values): one atomic
+      // per warp
+      const unsigned act = __activemask();
+      const int m = __reduce_max_sync(act, valid ? int(v & 0x7FFFu) : 0);
+      if (int(threadIdx.x & 31) == __ffs(act) - 1)
+        atomicMax(&reinterpret_cast<PackedHeader*>(packed)->max_scale_bits, m);
     } else if (L.sdtype == 1) {
       uint8_t v = 127;                                                 // E8M0 1.0
       if (valid) {
@@ -151,7 +157,27 @@ __global__ void write_header_kernel(Layout L, float acc_scale, uint8_t* packed) 
   h.n_tiles = L.n_tiles; h.k_blocks = L.k_blocks; h.record_bytes = L.record_bytes;
   h.off_scales = L.off_scales; h.off_zeros = L.off_zeros; h.total_bytes = L.total_bytes;
   h.acc_scale = acc_scale;
+  h.w_prescale = 1.0f;
+  h.max_scale_bits = 0;
   *reinterpret_cast<PackedHeader*>(packed) = h;
+}
+
+// FP16-operand layouts, after the scales: k = 11 - floor(log2 max|s|), clamped to
+// [-100, 100], so that max|s| 2^k lies in [2^11, 2^12) and |q - z| s 2^k <= 15 * 2^12 stays
+// below FP16's largest finite value; the GEMM takes 2^-k back on its accumulators.
+__global__ void finish_header_f16_kernel(uint8_t* packed) {
+  PackedHeader* h = reinterpret_cast<PackedHeader*>(packed);
+  const int bits = h->max_scale_bits;
+  int k = 0;
+  if (bits != 0) {
+    const int e = (bits >> 7) & 0xFF;                 // biased BF16 exponent (0: subnormal)
+    int lg = e - 127;                                 // floor(log2 max|s|) for a normal
+    if (e == 0) lg = -127 - (__clz(bits & 0x7F) - 25);   // subnormal: the top mantissa bit
+    k = 11 - lg;
+  }
+  k = max(-100, min(100, k));
+  h->w_prescale = ldexpf(1.0f, k);
+  h->acc_scale = ldexpf(1.0f, -k);
 }
 
 static int grid_for(int64_t n) {
@@ -169,6 +195,7 @@ cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* sca
   if (L.has_zp)
     repack_zeros_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record / 2),
                           256, 0, st>>>(L, zeros, p);
+  if (f16_operands(L)) finish_header_f16_kernel<<<1, 1, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -263,6 +290,86 @@ cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, c
   const int64_t total = L.n_tiles * L.k_blocks * 4 * kTileN * 4;
   dequant_debug_kernel<<<grid_for(total), 256, 0, st>>>(L, static_cast<const uint8_t*>(packed),
                                                        static_cast<__nv_bfloat16*>(W));
+  return cudaGetLastError();
+}
+
+// --------------------------------------------------------- FP16 activations (pre-pass)
+// One block of 256 threads per row.  A row of up to 32768 elements stays in registers
+// (16-byte loads, at most 16 per thread): the maximum of |x| (BF16 magnitude bits order
+// like the values), then every element times 2^-e (exact in FP32) rounded once to FP16,
+// 16-byte stores.  Longer rows are read twice.  The block first lets dependent launches
+// start (programmatic dependent launch): the GEMM's prologue and weight stream overlap
+// this pass, and its activation reads wait for it to finish.
+constexpr int kPrepThreads = 256, kPrepVecs = 16;
+
+__device__ __forceinline__ uint32_t bf16x8_absmax(uint4 v) {
+  const uint32_t a = max(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu);
+  const uint32_t b = max(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu);
+  const uint32_t c = __vmaxu2(a, b);                  // per 16-bit half
+  return max(c & 0xFFFFu, c >> 16);
+}
+
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v, float inv) {
+  const float lo = __uint_as_float(v << 16) * inv, hi = __uint_as_float(v & 0xFFFF0000u) * inv;
+  return ptx::cvt_f16x2_f32(lo, hi);
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+prep_x_f16_kernel(const uint8_t* __restrict__ X, int64_t K, int64_t ldx_bytes,
+                  uint8_t* __restrict__ X16, float* __restrict__ rowscale) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int64_t m = blockIdx.x;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + m * ldx_bytes);
+  uint4* yr = reinterpret_cast<uint4*>(X16 + m * K * 2);
+  const int nv = int(K / 8);                          // 16-byte vectors in the row
+  const bool in_regs = nv <= kPrepThreads * kPrepVecs;
+  uint4 v[kPrepVecs];
+  uint32_t amax = 0;
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kPrepVecs; ++i) {
+      const int j = threadIdx.x + i * kPrepThreads;
+      v[i] = j < nv ? __ldg(xr + j) : make_uint4(0, 0, 0, 0);
+      amax = max(amax, bf16x8_absmax(v[i]));
+    }
+  } else {
+    for (int j = threadIdx.x; j < nv; j += kPrepThreads) amax = max(amax, bf16x8_absmax(__ldg(xr + j)));
+  }
+#pragma unroll
+  for (int d = 16; d > 0; d >>= 1) amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+  __shared__ uint32_t red[kPrepThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < kPrepThreads / 32; ++i) amax = max(amax, red[i]);
+  int e = 0;                                          // floor(log2 amax) - 14
+  const uint32_t be = (amax >> 7) & 0xFFu;
+  if (amax != 0 && be != 0xFFu) {
+    const int lg = be != 0 ? int(be) - 127 : -127 - (__clz(amax & 0x7Fu) - 25);
+    e = lg - 14;
+  }
+  const float inv = ldexpf(1.0f, -e);
+  auto cvt8 = [&](uint4 a) {
+    return make_uint4(bf16x2_to_f16x2(a.x, inv), bf16x2_to_f16x2(a.y, inv),
+                      bf16x2_to_f16x2(a.z, inv), bf16x2_to_f16x2(a.w, inv));
+  };
+  if (in_regs) {
+#pragma unroll
+    for (int i = 0; i < kPrepVecs; ++i) {
+      const int j = threadIdx.x + i * kPrepThreads;
+      if (j < nv) yr[j] = cvt8(v[i]);
+    }
+  } else {
+    for (int j = threadIdx.x; j < nv; j += kPrepThreads) yr[j] = cvt8(__ldg(xr + j));
+  }
+  if (threadIdx.x == 0) rowscale[m] = ldexpf(1.0f, e);
+}
+
+cudaError_t launch_prep_x_f16(const void* X, int64_t rows, int64_t K, int64_t ldx, void* X16,
+                              float* rowscale, cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  prep_x_f16_kernel<<<unsigned(rows), kPrepThreads, 0, st>>>(
+      static_cast<const uint8_t*>(X), K, ldx * 2, static_cast<uint8_t*>(X16), rowscale);
   return cudaGetLastError();
 }
 

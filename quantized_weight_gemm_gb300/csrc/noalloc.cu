@@ -11,6 +11,7 @@
 
 #include <mutex>
 
+#include "kernels.h"
 #include "qgemm.h"
 
 namespace {
@@ -46,18 +47,21 @@ extern "C" qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void*
                                             const void* X, int64_t M, int64_t ldx,
                                             const float* chan_scale, void* Y, int64_t ldy,
                                             void* stream) {
-  if (qgemm_check_desc(desc) != QGEMM_OK) return QGEMM_ERR_INVALID_ARG;
-  if (M <= 0)   // M == 0 is a no-op, M < 0 an argument error: no scratch involved
-    return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, Y, ldy, nullptr, 0, stream);
-  const size_t need = qgemm_workspace_bytes(desc, M);
-  if (need > size_t(QGEMM_NOALLOC_SCRATCH_BYTES)) return QGEMM_ERR_WORKSPACE;
+  // This call's own schedule decides the scratch it needs; every argument is checked
+  // before anything is enqueued.
+  int64_t need = 0, counter_off = 0, counter_bytes = 0;
+  qgemm_status s = qgemm::dense_a16_scratch(desc, packed, X, M, ldx, chan_scale, Y, ldy, &need,
+                                            &counter_off, &counter_bytes);
+  if (s != QGEMM_OK || M == 0) return s;
+  if (need > int64_t(QGEMM_NOALLOC_SCRATCH_BYTES)) return QGEMM_ERR_WORKSPACE;
   void* scratch = nullptr;
-  const qgemm_status s = scratch_address(&scratch);
-  if (s != QGEMM_OK) return s;
-  // The array keeps whatever the previous call left; the split-K tile counters must
-  // start at zero.
-  if (need > 0 && cudaMemsetAsync(scratch, 0, need, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return QGEMM_ERR_CUDA;
-  return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, Y, ldy, scratch,
-                     size_t(QGEMM_NOALLOC_SCRATCH_BYTES), stream);
+  if (need > 0) {
+    if ((s = scratch_address(&scratch)) != QGEMM_OK) return s;
+    // The array keeps whatever the previous call left; the partial-sum slots are written
+    // before they are read, but the tile arrival counters must start at zero.
+    if (cudaMemsetAsync(static_cast<unsigned char*>(scratch) + counter_off, 0,
+                        size_t(counter_bytes), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+      return QGEMM_ERR_CUDA;
+  }
+  return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, Y, ldy, scratch, size_t(need), stream);
 }

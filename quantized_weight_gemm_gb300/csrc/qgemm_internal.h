@@ -25,7 +25,7 @@
 namespace qgemm {
 
 constexpr uint32_t kPackedMagic = 0x32575147u;   // "GQW2"
-constexpr uint32_t kPackedVersion = 3;
+constexpr uint32_t kPackedVersion = 4;
 constexpr int kTileN = 128;                      // weight rows per tile (MMA M)
 constexpr int kStageK = 128;                     // K-elements per pipeline stage
 constexpr int kCodeBytes = kTileN * kStageK / 2; // 8192
@@ -42,8 +42,16 @@ struct PackedHeader {
   int64_t n_tiles, k_blocks, record_bytes;
   int64_t off_scales, off_zeros, total_bytes;    // offsets inside a record / total size
   // Factor the GEMM applies to its FP32 accumulators (NVFP4: the per-tensor scale times
-  // 2^8, the decode having left the weights 2^8 smaller; 1 for the other formats).
+  // 2^8, the decode having left the weights 2^8 smaller; INT4 with BF16 scales: 2^-k, see
+  // w_prescale; 1 for the other formats).
   float acc_scale;
+  // INT4 with BF16 scales: the power of two 2^k that the decode multiplies every scale by
+  // before rounding the weight to FP16, chosen from the largest |scale| of the tensor so
+  // that (q - z) * s * 2^k stays inside FP16's normal range; 1 for the other formats.
+  float w_prescale;
+  // INT4 with BF16 scales: the largest |scale| of the tensor as BF16 magnitude bits (the
+  // repack's reduction; k is derived from it).
+  int32_t max_scale_bits;
 };
 static_assert(sizeof(PackedHeader) <= kHeaderBytes, "header too large");
 
@@ -94,6 +102,21 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
   L->record_bytes = int32_t(round_up(L->off_zeros + (has_zp ? kTileN * L->groups_per_record / 2 : 0), 16));
   L->total_bytes = round_up(kHeaderBytes + L->n_tiles * L->k_blocks * L->record_bytes, 256);
   return true;
+}
+
+// Layouts whose GEMM runs on FP16 tensor-core operands: INT4 weights with BF16 group scales
+// (any group size) and BF16 activations.  A BF16 operand would round every dequantized
+// weight (q - z) * s, which needs up to 12 significant bits, to 8; FP16 keeps 11.  The
+// activations are then converted to FP16 exactly, with a power-of-two scale per row, by a
+// pre-pass into the workspace (prep_x_f16).
+inline bool f16_operands(const Layout& L) {
+  return L.afmt == A_BF16 && (L.wfmt == W_INT4_SYM || L.wfmt == W_UINT4_ZP);
+}
+
+// Workspace bytes of the FP16 activation copy of `rows` rows: the FP16 rows [rows][K] and
+// the FP32 row scales [rows], each rounded up to 256 bytes.
+inline int64_t prep_x_f16_bytes(int64_t rows, int64_t K) {
+  return round_up(rows * K * 2, 256) + round_up(rows * 4, 256);
 }
 
 // Device-side status codes (mirror qgemm_status values).

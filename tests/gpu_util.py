@@ -38,3 +38,30 @@ def pack(w, afmt="bf16"):
     d = desc_of(w, afmt)
     z = None if w.zeros is None else u8_tensor(w.zeros)
     return d, qg.repack(d, u8_tensor(w.codes), scales_tensor(w), z, global_scale=w.global_scale)
+
+
+def ref_bf16_weights(x_bits, w, chan_scale=None):
+    """The product on the weights rounded to BF16 (the arithmetic of a kernel that scales
+    its weights before a BF16 tensor core), for reporting beside the exact reference."""
+    import oracle
+    from oracle import formats as F
+    W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    y = oracle.gemm(F.bf16_bits_to_float(x_bits), W, chan_scale=chan_scale)
+    return y * np.float64(np.float32(w.global_scale))
+
+
+def log_parity(tag, y, ref, tol, ref_bf16=None):
+    """Append the worst error/bound against the exact reference (and, when given, against
+    the BF16-weight product) to the JSON-lines file named by QGEMM_PARITY_LOG, if set."""
+    import json
+    import os
+    import oracle
+    path = os.environ.get("QGEMM_PARITY_LOG")
+    if not path:
+        return
+    rec = {"case": tag, "tol": tol, "worst_exact": oracle.tolerance_ok(y, ref, tol)[1],
+           "outputs": int(np.asarray(ref).size)}
+    if ref_bf16 is not None:
+        rec["worst_bf16_weights"] = oracle.tolerance_ok(y, ref_bf16, tol)[1]
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")

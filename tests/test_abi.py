@@ -83,7 +83,8 @@ def test_batch_invariant_plan(L):
         p = qg.plan(d, M)
         assert (p["token_tile"], p["splits"], p["sk_tiles"], p["max_contrib"]) == (128, 1, 0, 0)
         assert p["grid"] == min(-(-M // 128) * 224, 152)
-    assert qg.workspace_bytes(d, 8192) == 0
+    # nothing is cut: the workspace is just the FP16 activation copy of INT4 with BF16 scales
+    assert qg.workspace_bytes(d, 8192) == qg.act_copy_bytes(d, 8192)
     raw = qg.WeightDesc("uint4_zp", 256, 512, 128).c()
     raw.flags = 2
     assert L.qgemm_check_desc(ctypes.byref(raw)) != 0
@@ -301,3 +302,21 @@ def test_moe_workspace_bytes(L):
     assert qg.moe_workspace_bytes(d, 8, 8 * 200) == 2 * 152 * 128 * 256 * 4 + 768
     assert qg.moe_workspace_bytes(d, 0, 8) == 0
     assert qg.moe_workspace_bytes(d, 8, 0) == 0
+
+
+def test_act_copy_bytes():
+    """INT4 with BF16 scales runs on FP16 operands: the workspace leads with an FP16 copy of
+    X ([rows][K], 256-byte rounded) and one FP32 row scale per row (256-byte rounded); no
+    other layout has one."""
+    for wfmt, group in [("int4_sym", 128), ("uint4_zp", 64), ("int4_sym", 32)]:
+        d = qg.WeightDesc(wfmt, 1000, 4096, group)
+        for rows in (1, 3, 100, 8192):
+            want = -(-rows * 4096 * 2 // 256) * 256 + -(-rows * 4 // 256) * 256
+            assert qg.act_copy_bytes(d, rows) == want
+        assert qg.act_copy_bytes(d, 0) == 0
+        assert qg.workspace_bytes(d, 8192) >= qg.act_copy_bytes(d, 8192)
+        assert qg.moe_workspace_bytes(d, 8, 1000) > qg.act_copy_bytes(d, 1000)
+    for wfmt, group, afmt in [("mxfp4", 32, "bf16"), ("mxint4", 32, "bf16"), ("nvfp4", 16, "bf16"),
+                              ("mxfp4", 32, "fp8")]:
+        d = qg.WeightDesc(wfmt, 1000, 4096, group, afmt)
+        assert qg.act_copy_bytes(d, 100) == 0

@@ -47,9 +47,26 @@ def _nan_out(M, N):
     return torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
 
 
+def _check_sampled(tag, y, x, w, ns, ms, tol=TOL_A16):
+    """Sampled outputs against the exact weights; both worst ratios (exact, BF16-rounded
+    weights) go to the parity log."""
+    from tests import gpu_util as G
+    codes, scales, zeros = _rows(w, ns)
+    ref = oracle.w4a16(x[ms], w.wfmt, w.group, codes, scales, zeros, global_scale=w.global_scale)
+    sub = WL.WeightCase(w.wfmt, w.group, len(ns), w.K, codes, scales, zeros, w.global_scale)
+    got = y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
+    G.log_parity(tag, got, ref, tol, G.ref_bf16_weights(x[ms], sub))
+    ok, worst = oracle.tolerance_ok(got, ref, tol)
+    assert ok, f"worst error / bound = {worst:.3f}"
+
+
 @pytest.mark.parametrize("N,K,M", [(28672, 8192, 1), (28672, 8192, 16), (8192, 28672, 16),
-                                   (28672, 8192, 256), (8192, 28672, 8192)])
+                                   (8192, 28672, 1), (28672, 8192, 64), (8192, 28672, 128),
+                                   (28672, 8192, 256), (28672, 8192, 1024),
+                                   (8192, 28672, 8192), (28672, 8192, 8192)])
 def test_int4_zp_bench_shapes(N, K, M):
+    """Every token tile and schedule the INT4 sweep runs, including its dominant launch
+    (N=28672, K=8192, M=8192)."""
     from tests import gpu_util as G
     import quantized_weight_gemm_gb300 as qg
     x, w = WL.int4_asym_shape(N, K, M, seed=0)
@@ -58,14 +75,11 @@ def test_int4_zp_bench_shapes(N, K, M):
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(50), N, M)
-    codes, scales, zeros = _rows(w, ns)
-    ref = oracle.w4a16(x[ms], w.wfmt, w.group, codes, scales, zeros)
-    got = y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
-    ok, worst = oracle.tolerance_ok(got, ref, TOL_A16)
-    assert ok, f"worst error / bound = {worst:.3f}"
+    _check_sampled(f"fullsize uint4_zp {N}x{K} M={M}", y, x, w, ns, ms)
 
 
-@pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 16), (4096, 7168, 2048)])
+@pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 16), (4096, 7168, 2048),
+                                   (7168, 2048, 1), (4096, 7168, 8192), (7168, 2048, 8192)])
 def test_mxfp4_bench_shapes(N, K, M):
     from tests import gpu_util as G
     import quantized_weight_gemm_gb300 as qg
@@ -75,14 +89,28 @@ def test_mxfp4_bench_shapes(N, K, M):
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(51), N, M)
-    codes, scales, _ = _rows(w, ns)
-    ref = oracle.w4a16(x[ms], w.wfmt, w.group, codes, scales)
-    got = y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
-    ok, worst = oracle.tolerance_ok(got, ref, TOL_A16)
-    assert ok, f"worst error / bound = {worst:.3f}"
+    _check_sampled(f"fullsize mxfp4 {N}x{K} M={M}", y, x, w, ns, ms)
 
 
-@pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 256), (4096, 7168, 8192)])
+@pytest.mark.parametrize("wfmt", ["mxint4", "nvfp4"])
+@pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 1), (4096, 7168, 8192),
+                                   (7168, 2048, 8192)])
+def test_mxint4_nvfp4_bench_shapes(wfmt, N, K, M):
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    r = WL.rng(0)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, wfmt, N, K)
+    d, packed = G.pack(w)
+    y = qg.w4a16(d, packed, G.bf16_tensor(x), out=_nan_out(M, N))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    ns, ms = _samples(WL.rng(53), N, M)
+    _check_sampled(f"fullsize {wfmt} {N}x{K} M={M}", y, x, w, ns, ms)
+
+
+@pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 256), (4096, 7168, 8192),
+                                   (7168, 2048, 1), (7168, 2048, 8192)])
 def test_w4a8_bench_shapes(N, K, M):
     """FP8 activations with 1% outliers, quantized by the library's own call; the oracle
     multiplies the same codes and scales (the quantization itself is checked bit for bit
@@ -102,3 +130,73 @@ def test_w4a8_bench_shapes(N, K, M):
     got = y[mi][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
     ok, worst = oracle.tolerance_ok(got, ref, TOL_A8)
     assert ok, f"worst error / bound = {worst:.3f}"
+
+
+@pytest.mark.parametrize("T", [1024, 8192])
+@pytest.mark.parametrize("skewed", [False, True])
+@pytest.mark.parametrize("gemm", ["gate_up", "down"])
+def test_moe_layer_sampled(T, skewed, gemm):
+    """Both grouped GEMMs of the 256-expert layer at prefill sizes, with the workspace the
+    bench passes (stream-K over leftover tiles where the kernel takes it): 64 weight rows
+    and 48 routed rows checked against the oracle, per expert of each sampled row."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    case = WL.moe_case(T, seed=0, skewed=skewed)
+    N, K = (2 * WL.MOE_INTER, WL.MOE_HIDDEN) if gemm == "gate_up" else (WL.MOE_HIDDEN, WL.MOE_INTER)
+    xb = case.x_bits if gemm == "gate_up" else case.down_bits
+    E = case.E
+    R = len(case.token_of_row)
+    d = qg.WeightDesc("mxfp4", N, K, 32, "bf16")
+    nb = qg.packed_bytes(d)
+    packed = torch.empty(nb * E, dtype=torch.uint8, device="cuda")
+    r = WL.rng(54)
+    ns = np.unique(np.concatenate([[0, N - 1], r.choice(N, size=62, replace=False)]))
+    valid_rows = np.nonzero(case.valid)[0]
+    ms = np.unique(np.concatenate([valid_rows[[0, -1]], r.choice(valid_rows, size=46, replace=False)]))
+    expert_of = np.searchsorted(case.offsets, ms, side="right") - 1
+    need = set(int(e) for e in expert_of)
+    rows_of = {}
+    for e, w in enumerate(WL.iter_moe_weights(E, N, K, seed=0)):
+        qg.repack(d, G.u8_tensor(w.codes), G.u8_tensor(w.scales), None,
+                  out=packed[e * nb:(e + 1) * nb])
+        if e in need:
+            rows_of[e] = (w.codes[ns], w.scales[ns])
+    X = G.bf16_tensor(xb)
+    y = qg.moe_grouped(d, packed, E, X, torch.tensor(case.offsets, device="cuda"),
+                       ws=qg.moe_workspace(d, E, R), out=_nan_out(R, N))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    ref = np.zeros((len(ms), len(ns)))
+    for i, (m, e) in enumerate(zip(ms, expert_of)):
+        codes, scales = rows_of[int(e)]
+        ref[i] = oracle.w4a16(xb[[m]], "mxfp4", 32, codes, scales)[0]
+    got = y[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
+    G.log_parity(f"fullsize moe {gemm} T={T} {'skewed' if skewed else 'uniform'}", got, ref, TOL_A16)
+    ok, worst = oracle.tolerance_ok(got, ref, TOL_A16)
+    assert ok, f"worst error / bound = {worst:.3f}"
+
+
+@pytest.mark.parametrize("wfmt", ["uint4_zp", "int4_sym", "mxint4"])
+@pytest.mark.parametrize("tile", [32, 64, 128])
+def test_cut_schedules_repeated(wfmt, tile):
+    """Stream-K at the full 28672 x 8192 shape, called five times: a missing proxy fence
+    between the dequant warps' reads of a record slot and its refill by bulk copy once
+    decoded a lane quarter of a tile from the next record in most such calls."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    N, K, M = 28672, 8192, 64
+    r = WL.rng(0)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, wfmt, N, K)
+    d, packed = G.pack(w)
+    X = G.bf16_tensor(x)
+    ns, ms = _samples(WL.rng(55), N, M)
+    qg.force_config(tile, -1)
+    try:
+        for it in range(5):
+            y = qg.w4a16(d, packed, X, out=_nan_out(M, N))
+            torch.cuda.synchronize()
+            assert qg.device_status(clear=True) == 0
+            _check_sampled(f"fullsize stream-K {wfmt} tile {tile} call {it}", y, x, w, ns, ms)
+    finally:
+        qg.force_config(0, 0)

@@ -67,10 +67,19 @@ def _assert_close(y, ref, tol):
         f"bad n-tiles {sorted(set(c // 128 for c in cols))[:8]}")
 
 
+def _check_a16(tag, y, x, w, chan=None):
+    """The bar against the exact weights; both worst ratios (exact, BF16-rounded weights)
+    go to the parity log."""
+    from tests import gpu_util as G
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros, chan_scale=chan,
+                       global_scale=w.global_scale)
+    G.log_parity(tag, y, ref, TOL_A16, G.ref_bf16_weights(x, w, chan))
+    _assert_close(y, ref, TOL_A16)
+
+
 def test_tiny_dense_workload():
     x, w = WL.tiny_dense(seed=0)
-    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales)
-    _assert_close(_run_a16(x, w), ref, TOL_A16)
+    _check_a16("tiny_dense", _run_a16(x, w), x, w)
 
 
 @pytest.mark.parametrize("wfmt,group,M,N,K", [
@@ -94,9 +103,7 @@ def test_dense_a16_parity(wfmt, group, M, N, K):
     r = WL.rng(21)
     x = WL.gen_x(r, M, K)
     w = WL.gen_weights(r, wfmt, N, K, group=group)
-    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros,
-                       global_scale=w.global_scale)
-    _assert_close(_run_a16(x, w), ref, TOL_A16)
+    _check_a16(f"dense_a16 {wfmt} g{group} {M}x{N}x{K}", _run_a16(x, w), x, w)
 
 
 def test_chan_scale():
@@ -104,8 +111,7 @@ def test_chan_scale():
     x = WL.gen_x(r, 48, 512)
     w = WL.gen_weights(r, "uint4_zp", 200, 512)
     chan = r.uniform(0.5, 2.0, 200).astype(np.float32)
-    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros, chan_scale=chan)
-    _assert_close(_run_a16(x, w, chan), ref, TOL_A16)
+    _check_a16("chan_scale uint4_zp", _run_a16(x, w, chan), x, w, chan)
 
 
 def test_nvfp4_chan_and_global_scale():
@@ -152,9 +158,14 @@ def test_one_hot_columns_exact(wfmt, group):
     x = np.zeros((len(ks), K), dtype=np.float32)
     x[np.arange(len(ks)), ks] = 1.0
     y = _run_a16(WL.to_bf16_bits(x), w)
-    W = F.round_to_bf16(oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros,
-                                       w.global_scale))
-    np.testing.assert_array_equal(y, W[:, ks].T)
+    W = oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros, w.global_scale)
+    if wfmt in ("int4_sym", "uint4_zp"):
+        # INT4 with BF16 scales runs on FP16 operands: the weight reaches the tensor core
+        # rounded to FP16's 11 significant bits (times a power of two), then Y is rounded
+        # to BF16
+        m, e = np.frexp(W)
+        W = np.ldexp(np.rint(m * 2.0 ** 11) / 2.0 ** 11, e)
+    np.testing.assert_array_equal(y, F.round_to_bf16(W)[:, ks].T)
 
 
 @pytest.mark.parametrize("wfmt", ["mxint4", "nvfp4"])

@@ -51,10 +51,10 @@ def _pack_experts(ws, afmt="bf16"):
                         global_scale=[w.global_scale for w in ws])
 
 
-def _experts_bf16(ws):
-    """The BF16 operands, times each expert's per-tensor scale (which multiplies its output,
+def _experts_a16(ws):
+    """The exact weights times each expert's per-tensor scale (which multiplies its output,
     so it may as well scale its weights: the oracle sums exactly)."""
-    return [oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales, w.zeros) *
+    return [oracle.dequant(w.wfmt, w.group, w.codes, w.scales, w.zeros) *
             np.float64(np.float32(w.global_scale)) for w in ws]
 
 
@@ -114,7 +114,7 @@ def test_moe_a16_parity(wfmt, counts, N, K, stream_k):
     R = int(off[-1])
     x = WL.gen_x(r, R, K)
     ws = [WL.gen_weights(r, wfmt, N, K) for _ in counts]
-    ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+    ref = oracle.moe_grouped(F_bits(x), off, _experts_a16(ws))
     _assert_close(_run_moe(ws, x, off, stream_k=stream_k, calls=2), ref, TOL_A16)
 
 
@@ -138,7 +138,7 @@ def test_moe_stream_k(afmt, counts, N, K):
     x = WL.gen_x(r, R, K, outliers=afmt == "fp8")
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     if afmt == "bf16":
-        ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+        ref = oracle.moe_grouped(F_bits(x), off, _experts_a16(ws))
         _assert_close(_run_moe(ws, x, off, stream_k=True, calls=2), ref, TOL_A16)
     else:
         from oracle import formats as F
@@ -158,7 +158,7 @@ def test_moe_every_token_tile(tile):
     N, K = 256, 640
     x = WL.gen_x(r, R, K)
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
-    ref = oracle.moe_grouped(F_bits(x), off, _experts_bf16(ws))
+    ref = oracle.moe_grouped(F_bits(x), off, _experts_a16(ws))
     qg.force_config(tile, 0)
     try:
         y = _run_moe(ws, x, off)
@@ -198,7 +198,7 @@ def test_moe_rows_outside_groups_untouched():
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     y = _run_moe(ws, x, off, out_fill=3.0)
     assert np.all(y[:5] == 3.0) and np.all(y[int(off[-1]):] == 3.0)
-    ref = oracle.moe_grouped(F_bits(x)[5:int(off[-1])], off - 5, _experts_bf16(ws))
+    ref = oracle.moe_grouped(F_bits(x)[5:int(off[-1])], off - 5, _experts_a16(ws))
     _assert_close(y[5:int(off[-1])], ref, TOL_A16)
 
 
@@ -246,7 +246,7 @@ def test_moe_router_workload_sampled(T):
                   out=packed[e * nb:(e + 1) * nb])
         mine = np.nonzero(expert_of == e)[0]
         if len(mine):
-            W = oracle.dequant_bf16(w.wfmt, w.group, w.codes, w.scales)
+            W = oracle.dequant(w.wfmt, w.group, w.codes, w.scales)
             ref[mine] = oracle.gemm(xf[[rows[i] for i in mine]], W)
     X = G.bf16_tensor(case.x_bits)
     y = qg.moe_grouped(d, packed, E, X, torch.tensor(off.astype(np.int32), device="cuda"),
@@ -291,7 +291,7 @@ def test_moe_indexed_router(afmt, stream_k):
     idx = case.token_of_row.astype(np.int32)
     if afmt == "bf16":
         x = case.x_tok_bits
-        ref = oracle.moe_indexed(F_bits(x), case.offsets, idx, _experts_bf16(ws))
+        ref = oracle.moe_indexed(F_bits(x), case.offsets, idx, _experts_a16(ws))
         _assert_close(_run_moe_indexed(ws, x, case.offsets, idx, stream_k=stream_k), ref, TOL_A16)
     else:
         from oracle import formats as F
@@ -313,7 +313,7 @@ def test_moe_indexed_nvfp4():
     x = WL.gen_x(r, T, K)
     ws = [WL.gen_weights(r, "nvfp4", N, K) for _ in counts]
     assert len(set(w.global_scale for w in ws)) == len(ws)
-    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_a16(ws))
     for sk in (False, True):
         _assert_close(_run_moe_indexed(ws, x, off, idx, stream_k=sk), ref, TOL_A16)
 
@@ -331,7 +331,7 @@ def test_moe_indexed_every_tile(tile):
     idx = r.integers(-1, T, size=R).astype(np.int32)          # includes -1 (padding)
     x = WL.gen_x(r, T, K)
     ws = [WL.gen_weights(r, "uint4_zp", N, K) for _ in counts]
-    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_a16(ws))
     qg.force_config(tile, 0)
     try:
         y = _run_moe_indexed(ws, x, off, idx)
@@ -351,7 +351,7 @@ def test_moe_indexed_stream_k():
     idx = r.permutation(T)[:int(off[-1])].astype(np.int32)
     x = WL.gen_x(r, T, K)
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
-    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_a16(ws))
     _assert_close(_run_moe_indexed(ws, x, off, idx, stream_k=True), ref, TOL_A16)
 
 
@@ -369,7 +369,7 @@ def test_moe_indexed_ragged_k_and_stride(tile):
     idx = r.integers(-1, T, size=int(off[-1])).astype(np.int32)
     x = WL.gen_x(r, T, K)
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
-    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_bf16(ws))
+    ref = oracle.moe_indexed(F_bits(x), off, idx, _experts_a16(ws))
     wide = torch.full((T, K + 64), float("nan"), dtype=torch.bfloat16, device="cuda")
     wide[:, :K] = G.bf16_tensor(x)
     d, packed = _pack_experts(ws)
@@ -400,7 +400,7 @@ def test_moe_indexed_index_past_end():
     x = WL.gen_x(r, T, K)
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     ok_idx = np.where(idx < T, idx, -1).astype(np.int32)
-    ref = oracle.moe_indexed(F_bits(x), off, ok_idx, _experts_bf16(ws))
+    ref = oracle.moe_indexed(F_bits(x), off, ok_idx, _experts_a16(ws))
     d, packed = _pack_experts(ws)
     qg.device_status(clear=True)
     y = qg.moe_indexed(d, packed, len(ws), G.bf16_tensor(x),
@@ -435,7 +435,7 @@ def test_moe_batch_invariant():
         y = qg.moe_grouped(d, packed, 4, G.bf16_tensor(xr),
                            torch.tensor(off, dtype=torch.int32, device="cuda"), ws=wsp)
         outs.append(G.bf16_bits_of(y)[:40])
-        ref = oracle.moe_grouped(F_bits(xr), off, _experts_bf16(ws))
+        ref = oracle.moe_grouped(F_bits(xr), off, _experts_a16(ws))
         _assert_close(G.to_f64(y), ref, TOL_A16)
     np.testing.assert_array_equal(outs[0], outs[1])
     np.testing.assert_array_equal(outs[0], outs[2])

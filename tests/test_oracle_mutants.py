@@ -100,11 +100,11 @@ def _gemm_transposed(x, w, chan_scale=None, tok_scale=None, bias=None):
     return y
 
 
-def _w4a16_exact_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None,
-                         global_scale=1.0):
+def _w4a16_bf16_weights(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None,
+                        global_scale=1.0):
     x = F.bf16_bits_to_float(x_bits)
-    return Q.gemm(x, Q.dequant(wfmt, group, codes, scales, zeros, global_scale),
-                  chan_scale=chan_scale)
+    w = F.round_to_bf16(Q.dequant(wfmt, group, codes, scales, zeros))
+    return Q.gemm(x, w, chan_scale=chan_scale) * np.float64(np.float32(global_scale))
 
 
 def _gemm_drop_tok_scale(x, w, chan_scale=None, tok_scale=None, bias=None):
@@ -133,13 +133,6 @@ def _dequant_mxint4_as_e2m1(wfmt, group, codes, scales, zeros=None, global_scale
 
 def _dequant_global_dropped(wfmt, group, codes, scales, zeros=None, global_scale=1.0):
     return _orig_dequant(wfmt, group, codes, scales, zeros)
-
-
-def _w4a16_global_inside_bf16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None,
-                              global_scale=1.0):
-    x = F.bf16_bits_to_float(x_bits)
-    w = F.round_to_bf16(_orig_dequant(wfmt, group, codes, scales, zeros, global_scale))
-    return Q.gemm(x, w, chan_scale=chan_scale)
 
 
 def _e2m1_ties_away(x):
@@ -193,12 +186,11 @@ MUTANTS = {
     "group index shifted": (Q, "dequant", _dequant_group_shift),
     "output columns permuted": (Q, "gemm", _gemm_transposed),
     "token scale dropped": (Q, "gemm", _gemm_drop_tok_scale),
-    "w4a16 without bf16 weights": (Q, "w4a16", _w4a16_exact_weights),
+    "w4a16 on bf16-rounded weights": (Q, "w4a16", _w4a16_bf16_weights),
     "zero row not guarded": (Q, "quant_act_fp8", _quant_no_zero_guard),
     "nvfp4 scale read as e8m0": (Q, "scale_values", _scale_values_nvfp4_as_e8m0),
     "mxint4 read as e2m1": (Q, "dequant", _dequant_mxint4_as_e2m1),
     "global scale dropped": (Q, "dequant", _dequant_global_dropped),
-    "global scale before bf16 rounding": (Q, "w4a16", _w4a16_global_inside_bf16),
     "e2m1 ties away from zero": (F, "round_to_e2m1_satfinite", _e2m1_ties_away),
     "mxfp4 act exponent minus one": (Q, "quant_act_mxfp4", _quant_act_mxfp4_exp_minus_one),
     "act block index shifted": (Q, "dequant_act_mxfp4", _dequant_act_block_shifted),

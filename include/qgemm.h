@@ -184,20 +184,23 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max);
 size_t qgemm_act_copy_bytes(const qgemm_wdesc* desc, int64_t x_rows);
 
 /*
- * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k]   (c = 1 when chan_scale == NULL;
- *               for NVFP4, W includes the per-tensor scale g, applied to the FP32 sum)
+ * Dense W4A16:  Y[m, n] = c[n] * sum_k X[m, k] * W[n, k] + b[n]   (c = 1 when
+ *               chan_scale == NULL, b = 0 when bias == NULL; for NVFP4, W includes the
+ *               per-tensor scale g, applied to the FP32 sum; the sum, scaled, plus the bias
+ *               is rounded to BF16 once)
  *   packed     : device, from qgemm_repack with desc->afmt == QGEMM_A_BF16
  *   X          : device BF16 [M, ldx], 16-byte aligned, ldx % 8 == 0, ldx >= K
  *   chan_scale : device float32 [N] secondary per-channel scale, or NULL
+ *   bias       : device float32 [N], 4-byte aligned, added after every scale, or NULL
  *   Y          : device BF16 [M, ldy], 4-byte aligned, ldy >= N, ldy even
  *   ws         : device workspace (see qgemm_workspace_bytes), may be NULL when
  *                qgemm_workspace_bytes(desc, M) == 0
- * "Humming wird angekündigt", section "WnA16"; fused output scaling: section
- * "Gemeinsam genutzte CUDA-Komponenten".
+ * "Humming wird angekündigt", section "WnA16"; scaling and bias addition fused into the
+ * output stage: section "Gemeinsam genutzte CUDA-Komponenten".
  */
 qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void* X, int64_t M,
-                         int64_t ldx, const float* chan_scale, void* Y, int64_t ldy, void* ws,
-                         size_t ws_bytes, void* stream);
+                         int64_t ldx, const float* chan_scale, const float* bias, void* Y,
+                         int64_t ldy, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Device staging bytes that qgemm_w4a16_host needs for any M <= M_max: two buffers of a
@@ -219,8 +222,8 @@ size_t qgemm_host_staging_bytes(const qgemm_wdesc* desc, int64_t M_max);
  *   Y_host  : host BF16 [M, ldy] (ldy >= N), same advice
  *   staging : device buffer of qgemm_host_staging_bytes(desc, M) bytes, 256-byte aligned,
  *             owned by the caller and busy until `stream` reaches the end of the call
- *   ws, chan_scale, stream : as for qgemm_w4a16 (the chunks run one after another on
- *             `stream`, so they share one workspace)
+ *   ws, chan_scale, bias, stream : as for qgemm_w4a16 (the chunks run one after another
+ *             on `stream`, so they share one workspace)
  * Errors: QGEMM_ERR_INVALID_ARG (descriptor, null pointers, ld too small, FP8 descriptor),
  * QGEMM_ERR_WORKSPACE (staging missing or too small), QGEMM_ERR_ALIGNMENT, any status of
  * qgemm_w4a16, QGEMM_ERR_CUDA when a copy or an event could not be enqueued (chunks already
@@ -231,9 +234,9 @@ size_t qgemm_host_staging_bytes(const qgemm_wdesc* desc, int64_t M_max);
  * the end-to-end measurement uses.
  */
 qgemm_status qgemm_w4a16_host(const qgemm_wdesc* desc, const void* packed, const void* X_host,
-                              int64_t M, int64_t ldx, const float* chan_scale, void* Y_host,
-                              int64_t ldy, void* staging, size_t staging_bytes, void* ws,
-                              size_t ws_bytes, void* stream);
+                              int64_t M, int64_t ldx, const float* chan_scale, const float* bias,
+                              void* Y_host, int64_t ldy, void* staging, size_t staging_bytes,
+                              void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Tokenwise FP8 activation quantization (the input of W4A8): per row m,
@@ -247,15 +250,16 @@ qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ld
 
 /*
  * Dense W4A8 (MXFP4 weights x tokenwise FP8 activations):
- *   Y[m, n] = tok_scale[m] * c[n] * sum_k e4m3(Xq[m, k]) * W[n, k]
+ *   Y[m, n] = tok_scale[m] * c[n] * sum_k e4m3(Xq[m, k]) * W[n, k] + b[n]
  *   packed : device, from qgemm_repack with desc->wfmt == MXFP4, desc->afmt == FP8E4M3_TOKEN
  *   Xq     : device uint8 e4m3 [M, ldx], 16-byte aligned, ldx % 16 == 0
  *   tok_scale : device float32 [M];  other arguments as for qgemm_w4a16.
  * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4".
  */
 qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
-                        int64_t ldx, const float* tok_scale, const float* chan_scale, void* Y,
-                        int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+                        int64_t ldx, const float* tok_scale, const float* chan_scale,
+                        const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                        void* stream);
 
 /*
  * MoE grouped GEMM over expert-sorted rows: for each expert e, rows
@@ -265,6 +269,8 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
  *   afmt           : QGEMM_A_BF16 (X is BF16) or QGEMM_A_FP8E4M3_TOKEN (X is e4m3 and
  *                    tok_scale holds one float32 per row)
  *   X              : device [R, ldx] sorted rows; padding rows should be zero
+ *   bias           : device float32 [E][N] (expert e's bias at e * N), added to that
+ *                    expert's rows after every scale, or NULL
  *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
  *   Y              : device BF16 [R, ldy]; rows of every expert are written
  *   ws, ws_bytes   : device workspace, 256-byte aligned and zero-filled before its first
@@ -281,16 +287,19 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
  */
 qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
                                int32_t afmt, const void* X, int64_t R, int64_t ldx,
-                               const float* tok_scale, const int32_t* expert_offsets,
-                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream);
+                               const float* tok_scale, const float* bias,
+                               const int32_t* expert_offsets, void* Y, int64_t ldy, void* ws,
+                               size_t ws_bytes, void* stream);
 
 /*
  * MoE GEMM over rows gathered by index (the "Indexed" MoE path): sorted position r of
  * expert e's block [expert_offsets[e], expert_offsets[e+1]) takes X row row_index[r], so
  * the caller needs no copy of X sorted by expert.
  *   Y[r, :] = X[row_index[r], :] * W_e^T   (times tok_scale[row_index[r]] for FP8 X)
- * and a padding position (row_index[r] < 0) gives a zero row.
+ *             + bias[e, :]
+ * and a padding position (row_index[r] < 0) reads a zero row of X (its output is the bias).
  *   X              : device [T, ldx] rows in token order (BF16, or e4m3 with tok_scale [T])
+ *   bias           : as for qgemm_moe_grouped ([E][N] or NULL)
  *   expert_offsets : device int32 [E+1], non-decreasing, offsets[0] = 0, offsets[E] = R
  *   row_index      : device int32 [R], values in [0, T) or negative; 4-byte aligned
  *   Y              : device BF16 [R, ldy] in sorted order
@@ -308,9 +317,10 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
  */
 qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
                                int32_t afmt, const void* X, int64_t T, int64_t ldx,
-                               const float* tok_scale, const int32_t* expert_offsets,
-                               const int32_t* row_index, int64_t R, void* Y, int64_t ldy,
-                               void* ws, size_t ws_bytes, void* stream);
+                               const float* tok_scale, const float* bias,
+                               const int32_t* expert_offsets, const int32_t* row_index,
+                               int64_t R, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                               void* stream);
 
 /*
  * Workspace bytes that let qgemm_moe_grouped or qgemm_moe_indexed use stream-K for E

@@ -123,7 +123,8 @@ def gemm(x, w, chan_scale=None, tok_scale=None, bias=None):
     return y
 
 
-def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None, global_scale=1.0):
+def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None, global_scale=1.0,
+          bias=None):
     """Dense W4A16: BF16 activations (bit patterns [M, K]) times the exact dequantized weights.
 
     The plain definition: unpack the codes, dequantize exactly in float64 and multiply with
@@ -131,10 +132,12 @@ def w4a16(x_bits, wfmt, group, codes, scales, zeros=None, chan_scale=None, globa
     exact there and applying the group scale to its FP32 accumulators (the Chinese release
     notes, v0.1.3: the "apply scale on C" path); a BF16-rounded weight is what the
     dequantization check compares (dequant_bf16), not what the product uses.  The per-tensor
-    scale (NVFP4) then multiplies the output like the per-channel one."""
+    scale (NVFP4) then multiplies the output like the per-channel one, and the bias b[n],
+    if given, is added after every scale."""
     x = F.bf16_bits_to_float(x_bits)
     y = gemm(x, dequant(wfmt, group, codes, scales, zeros), chan_scale=chan_scale)
-    return y * np.float64(np.float32(global_scale))
+    y = y * np.float64(np.float32(global_scale))
+    return y if bias is None else y + np.asarray(bias, dtype=np.float64)[None, :]
 
 
 def quant_act_fp8(x_bits):
@@ -175,28 +178,30 @@ def dequant_act_mxfp4(codes, exps, block=32):
     return F.e2m1_to_float(q) * F.e8m0_to_float(exps)[:, np.arange(q.shape[1]) // block]
 
 
-def w4a4(xq, x_exps, wfmt, group, codes, scales, zeros=None, chan_scale=None):
+def w4a4(xq, x_exps, wfmt, group, codes, scales, zeros=None, chan_scale=None, bias=None):
     """W4A4: y = sum_k dequant_act(xq)[m, k] * W[n, k] with exact weights (both operands are
-    MX values a block-scaled FP4 MMA multiplies exactly), times c[n] if given."""
+    MX values a block-scaled FP4 MMA multiplies exactly), times c[n], plus b[n], if given."""
     return gemm(dequant_act_mxfp4(xq, x_exps), dequant(wfmt, group, codes, scales, zeros),
-                chan_scale=chan_scale)
+                chan_scale=chan_scale, bias=bias)
 
 
-def w4a8(xq, tok_scale, wfmt, group, codes, scales, zeros=None, chan_scale=None):
-    """Dense W4A8: y = s_tok[m] * sum_k e4m3(xq[m, k]) * W[n, k]  (times c[n] if given)."""
+def w4a8(xq, tok_scale, wfmt, group, codes, scales, zeros=None, chan_scale=None, bias=None):
+    """Dense W4A8: y = s_tok[m] * sum_k e4m3(xq[m, k]) * W[n, k]  (times c[n], plus b[n],
+    if given)."""
     x = F.e4m3_to_float(xq)
     return gemm(x, dequant(wfmt, group, codes, scales, zeros),
-                chan_scale=chan_scale, tok_scale=tok_scale)
+                chan_scale=chan_scale, tok_scale=tok_scale, bias=bias)
 
 
-def moe_grouped(x_rows, offsets, experts, tok_scale=None, chan_scales=None):
+def moe_grouped(x_rows, offsets, experts, tok_scale=None, chan_scales=None, biases=None):
     """MoE grouped GEMM over expert-sorted rows.
 
     x_rows: activation values [R, K] sorted by expert; offsets: int [E+1], rows
     offsets[e]..offsets[e+1] belong to expert e; experts: list of E exact weights [N, K].
     Each expert's block of rows is an ordinary dense GEMM with that expert's weights
     ("Humming wird angekündigt", section "WnA16": tokens are distributed over experts and
-    the work per expert varies with the load).
+    the work per expert varies with the load).  biases: E bias vectors [N] or None, each
+    added to its expert's rows after every scale.
     """
     x_rows = np.asarray(x_rows, dtype=np.float64)
     offsets = np.asarray(offsets, dtype=np.int64)
@@ -207,11 +212,12 @@ def moe_grouped(x_rows, offsets, experts, tok_scale=None, chan_scales=None):
         if b > a:
             ts = None if tok_scale is None else np.asarray(tok_scale)[a:b]
             cs = None if chan_scales is None else chan_scales[e]
-            y[a:b] = gemm(x_rows[a:b], w, chan_scale=cs, tok_scale=ts)
+            bs = None if biases is None else biases[e]
+            y[a:b] = gemm(x_rows[a:b], w, chan_scale=cs, tok_scale=ts, bias=bs)
     return y
 
 
-def moe_indexed(x, offsets, row_index, experts, tok_scale=None):
+def moe_indexed(x, offsets, row_index, experts, tok_scale=None, biases=None):
     """MoE GEMM over rows gathered by index (the pages' "Indexed" MoE path, "Humming wird
     angekündigt", section "WnA16": the kernel reads each token's row where it lies instead
     of a copy sorted by expert).
@@ -219,9 +225,10 @@ def moe_indexed(x, offsets, row_index, experts, tok_scale=None):
     x: activation values [T, K] in token order; offsets: int [E+1] over the R sorted
     positions; row_index: int [R], the row of x that sorted position r takes, or a negative
     value for a padding position; experts: E exact weights [N, K]; tok_scale: float [T] per
-    row of x (FP8 activations) or None.  Output row r (sorted order) is x[row_index[r]] times
-    expert e's weights for the e whose block holds r, scaled by tok_scale[row_index[r]];
-    padding positions give zero rows.
+    row of x (FP8 activations) or None; biases: E bias vectors [N] or None.  Output row r
+    (sorted order) is x[row_index[r]] times expert e's weights for the e whose block holds
+    r, scaled by tok_scale[row_index[r]], plus expert e's bias; padding positions give zero
+    rows (the kernel's are unspecified).
     """
     x = np.asarray(x, dtype=np.float64)
     offsets = np.asarray(offsets, dtype=np.int64)
@@ -234,7 +241,8 @@ def moe_indexed(x, offsets, row_index, experts, tok_scale=None):
             if t < 0:
                 continue
             ts = None if tok_scale is None else np.asarray(tok_scale)[t:t + 1]
-            y[r:r + 1] = gemm(x[t:t + 1], w, tok_scale=ts)
+            bs = None if biases is None else biases[e]
+            y[r:r + 1] = gemm(x[t:t + 1], w, tok_scale=ts, bias=bs)
     return y
 
 

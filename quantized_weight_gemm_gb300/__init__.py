@@ -95,10 +95,10 @@ def lib():
         "qgemm_repack": (ctypes.c_int, [D, P, P, P, P, P]),
         "qgemm_repack_scaled": (ctypes.c_int, [D, P, P, P, ctypes.c_float, P, P]),
         "qgemm_workspace_bytes": (SZ, [D, I64]),
-        "qgemm_w4a16": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P]),
-        "qgemm_w4a8": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_w4a16": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_w4a8": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, P, I64, P, SZ, P]),
         "qgemm_quant_act_fp8": (ctypes.c_int, [P, I64, I64, I64, P, I64, P, P]),
-        "qgemm_moe_grouped": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_moe_grouped": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, P, I64, P, SZ, P]),
         "qgemm_dequant_debug": (ctypes.c_int, [D, P, P, P]),
         "qgemm_device_status": (ctypes.c_int, [I32]),
         "qgemm_force_config": (ctypes.c_int, [I32, I32]),
@@ -108,8 +108,8 @@ def lib():
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
         "qgemm_act_copy_bytes": (SZ, [D, I64]),
         "qgemm_host_staging_bytes": (SZ, [D, I64]),
-        "qgemm_moe_indexed": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, I64, P, I64, P, SZ, P]),
-        "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P, SZ, P, SZ, P]),
+        "qgemm_moe_indexed": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, P, I64, P, I64, P, SZ, P]),
+        "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P, SZ, P]),
     }
     for name, (res, args) in sigs.items():
         f = getattr(L, name)
@@ -194,7 +194,7 @@ def workspace(desc, M_max, device="cuda"):
     return torch.zeros(max(n, 256), dtype=torch.uint8, device=device)
 
 
-def w4a16(desc, packed, X, chan_scale=None, out=None, ws=None):
+def w4a16(desc, packed, X, chan_scale=None, out=None, ws=None, bias=None):
     """Y = X . dequant(W)^T (* chan_scale[n]) with BF16 X [M, K]."""
     _need(X, "X", torch.bfloat16)
     _row_major(X, "X")
@@ -209,7 +209,7 @@ def w4a16(desc, packed, X, chan_scale=None, out=None, ws=None):
         ws = workspace(desc, M, X.device)
     d = desc.c()
     _check(lib().qgemm_w4a16(ctypes.byref(d), _ptr(packed), _ptr(X), M, X.stride(0),
-                             _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(ws),
+                             _ptr(chan_scale), _ptr(bias), _ptr(out), out.stride(0), _ptr(ws),
                              ws.numel() * ws.element_size(), _stream()), "w4a16")
     return out
 
@@ -228,7 +228,7 @@ def quant_act_fp8(X, out=None, scale=None):
     return out, scale
 
 
-def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None):
+def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None, bias=None):
     """Y = diag(tok_scale) . e4m3(Xq) . dequant(W)^T (* chan_scale[n])."""
     _need(Xq, "Xq", torch.uint8)
     _row_major(Xq, "Xq")
@@ -240,7 +240,8 @@ def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None):
         ws = workspace(desc, M, Xq.device)
     d = desc.c()
     _check(lib().qgemm_w4a8(ctypes.byref(d), _ptr(packed), _ptr(Xq), M, Xq.stride(0),
-                            _ptr(tok_scale), _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(ws),
+                            _ptr(tok_scale), _ptr(chan_scale), _ptr(bias), _ptr(out), out.stride(0),
+                            _ptr(ws),
                             ws.numel() * ws.element_size(), _stream()), "w4a8")
     return out
 
@@ -255,7 +256,7 @@ def host_staging(desc, M_max, device="cuda"):
     return torch.empty(max(host_staging_bytes(desc, M_max), 256), dtype=torch.uint8, device=device)
 
 
-def w4a16_host(desc, packed, X_host, out=None, staging=None, ws=None, chan_scale=None):
+def w4a16_host(desc, packed, X_host, out=None, staging=None, ws=None, chan_scale=None, bias=None):
     """Dense W4A16 with X [M, K] and Y [M, N] in host memory (BF16, pin them for speed):
     the copies in and out overlap the GEMM chunk by chunk.  Asynchronous on the current
     stream: synchronize before reading `out`."""
@@ -271,7 +272,8 @@ def w4a16_host(desc, packed, X_host, out=None, staging=None, ws=None, chan_scale
         ws = workspace(desc, M, device=packed.device)
     d = desc.c()
     _check(lib().qgemm_w4a16_host(ctypes.byref(d), _ptr(packed), _ptr(X_host), M, X_host.stride(0),
-                                  _ptr(chan_scale), _ptr(out), out.stride(0), _ptr(staging),
+                                  _ptr(chan_scale), _ptr(bias), _ptr(out), out.stride(0),
+                                  _ptr(staging),
                                   staging.numel(), _ptr(ws), ws.numel(), _stream()), "w4a16_host")
     return out
 
@@ -298,7 +300,7 @@ def _moe_min_ws(desc, x_rows, device):
     return None if n == 0 else torch.empty(n, dtype=torch.uint8, device=device)
 
 
-def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None):
+def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None, bias=None):
     """MoE grouped GEMM over expert-sorted rows X [R, K] (BF16, or uint8 e4m3 with
     tok_scale); offsets: int32 [E+1] on the device; ws: optional moe_workspace() (without
     one, whole tiles, and for INT4 with BF16 scales just the activation copy)."""
@@ -313,12 +315,13 @@ def moe_grouped(desc, packed, E, X, offsets, tok_scale=None, out=None, ws=None):
     d = desc.c()
     wsb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().qgemm_moe_grouped(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
-                                   _ptr(X), R, X.stride(0), _ptr(tok_scale), _ptr(offsets),
+                                   _ptr(X), R, X.stride(0), _ptr(tok_scale), _ptr(bias), _ptr(offsets),
                                    _ptr(out), out.stride(0), _ptr(ws), wsb, _stream()), "moe_grouped")
     return out
 
 
-def moe_indexed(desc, packed, E, X, offsets, row_index, tok_scale=None, out=None, ws=None):
+def moe_indexed(desc, packed, E, X, offsets, row_index, tok_scale=None, out=None, ws=None,
+                bias=None):
     """MoE GEMM over rows gathered by index: X [T, K] in token order (BF16, or uint8 e4m3
     with tok_scale [T]); offsets int32 [E+1] and row_index int32 [R] on the device
     (row_index[r] < 0: padding).  Returns Y [R, N] in sorted order."""
@@ -334,7 +337,8 @@ def moe_indexed(desc, packed, E, X, offsets, row_index, tok_scale=None, out=None
     d = desc.c()
     wsb = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib().qgemm_moe_indexed(ctypes.byref(d), _ptr(packed), E, AFMT["fp8" if fp8 else "bf16"],
-                                   _ptr(X), X.shape[0], X.stride(0), _ptr(tok_scale), _ptr(offsets),
+                                   _ptr(X), X.shape[0], X.stride(0), _ptr(tok_scale), _ptr(bias),
+                                   _ptr(offsets),
                                    _ptr(row_index), R, _ptr(out), out.stride(0), _ptr(ws), wsb,
                                    _stream()), "moe_indexed")
     return out

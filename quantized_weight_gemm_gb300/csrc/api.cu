@@ -347,7 +347,7 @@ qgemm_status check_y(const void* Y, int64_t N, int64_t ldy) {
 // Every argument check of the dense calls that needs no device.
 qgemm_status check_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
                          int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
-                         const void* Y, int64_t ldy, Layout* L) {
+                         const float* bias, const void* Y, int64_t ldy, Layout* L) {
   if (!layout_of(desc, L)) return QGEMM_ERR_INVALID_ARG;
   if ((L->afmt == A_FP8) != fp8) return QGEMM_ERR_INVALID_ARG;
   if (fp8 && L->wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
@@ -358,17 +358,19 @@ qgemm_status check_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, 
   if (s != QGEMM_OK) return s;
   if ((s = check_y(Y, L->N, ldy)) != QGEMM_OK) return s;
   if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
-  if ((chan_scale && !aligned(chan_scale, 4)) || (tok_scale && !aligned(tok_scale, 4)))
+  if ((chan_scale && !aligned(chan_scale, 4)) || (tok_scale && !aligned(tok_scale, 4)) ||
+      (bias && !aligned(bias, 4)))
     return QGEMM_ERR_ALIGNMENT;
   return QGEMM_OK;
 }
 
 qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
                        int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
-                       void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+                       const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                       void* stream) {
   Layout L;
-  const qgemm_status s = check_dense(desc, fp8, packed, X, M, ldx, tok_scale, chan_scale, Y,
-                                     ldy, &L);
+  const qgemm_status s = check_dense(desc, fp8, packed, X, M, ldx, tok_scale, chan_scale, bias,
+                                     Y, ldy, &L);
   if (s != QGEMM_OK) return s;
   if (M == 0) return QGEMM_OK;
   DeviceInfo* dev = nullptr;
@@ -416,6 +418,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
     a.group_m = int(std::min<int64_t>(gm, a.m_tiles));
   }
   a.chan_scale = chan_scale;
+  a.bias = bias;
   a.tok_scale = f16 ? rowscale : tok_scale;
   a.Y = Y;
   a.ldy = ldy;
@@ -442,8 +445,8 @@ qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, cons
                                int64_t* counter_bytes) {
   *need = *counter_off = *counter_bytes = 0;
   Layout L;
-  const qgemm_status s = check_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, Y,
-                                     ldy, &L);
+  const qgemm_status s = check_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale,
+                                     nullptr, Y, ldy, &L);
   if (s != QGEMM_OK || M == 0) return s;
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
@@ -535,17 +538,18 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
 }
 
 qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void* X, int64_t M,
-                         int64_t ldx, const float* chan_scale, void* Y, int64_t ldy, void* ws,
-                         size_t ws_bytes, void* stream) {
-  return run_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, Y, ldy, ws, ws_bytes,
-                   stream);
+                         int64_t ldx, const float* chan_scale, const float* bias, void* Y,
+                         int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, bias, Y, ldy, ws,
+                   ws_bytes, stream);
 }
 
 qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
-                        int64_t ldx, const float* tok_scale, const float* chan_scale, void* Y,
-                        int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
-  return run_dense(desc, true, packed, Xq, M, ldx, tok_scale, chan_scale, Y, ldy, ws, ws_bytes,
-                   stream);
+                        int64_t ldx, const float* tok_scale, const float* chan_scale,
+                        const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                        void* stream) {
+  return run_dense(desc, true, packed, Xq, M, ldx, tok_scale, chan_scale, bias, Y, ldy, ws,
+                   ws_bytes, stream);
 }
 
 qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
@@ -570,8 +574,8 @@ namespace {
 // rows are already sorted by expert (sorted position r is X row r).
 qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int32_t afmt,
                      const void* X, int64_t x_rows, int64_t ldx, const float* tok_scale,
-                     const int32_t* expert_offsets, const int32_t* row_index, int64_t R,
-                     void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
+                     const float* bias, const int32_t* expert_offsets, const int32_t* row_index,
+                     int64_t R, void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
   Layout L;
   if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
   const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
@@ -580,7 +584,8 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   if (E < 1 || E > 1024 || packed == nullptr || expert_offsets == nullptr || R < 0 || x_rows < 0)
     return QGEMM_ERR_INVALID_ARG;
   if (row_index != nullptr && R > 0 && x_rows == 0) return QGEMM_ERR_INVALID_ARG;
-  if (!aligned(packed, 256) || !aligned(expert_offsets, 4) || !aligned(row_index, 4))
+  if (!aligned(packed, 256) || !aligned(expert_offsets, 4) || !aligned(row_index, 4) ||
+      !aligned(bias, 4))
     return QGEMM_ERR_ALIGNMENT;
   qgemm_status s = check_x(X, fp8, x_rows, L.K, ldx);
   if (s != QGEMM_OK) return s;
@@ -642,6 +647,8 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   a.E = E;
   a.M = R;
   a.splits = 1;
+  a.bias = bias;
+  a.bias_stride = L.N;
   a.tok_scale = f16 ? rowscale : tok_scale;
   a.Y = Y;
   a.ldy = ldy;
@@ -665,20 +672,22 @@ extern "C" {
 
 qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int32_t E,
                                int32_t afmt, const void* X, int64_t R, int64_t ldx,
-                               const float* tok_scale, const int32_t* expert_offsets,
-                               void* Y, int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
-  return run_moe(desc, packed, E, afmt, X, R, ldx, tok_scale, expert_offsets, nullptr, R, Y, ldy,
-                 ws, ws_bytes, stream);
+                               const float* tok_scale, const float* bias,
+                               const int32_t* expert_offsets, void* Y, int64_t ldy, void* ws,
+                               size_t ws_bytes, void* stream) {
+  return run_moe(desc, packed, E, afmt, X, R, ldx, tok_scale, bias, expert_offsets, nullptr, R,
+                 Y, ldy, ws, ws_bytes, stream);
 }
 
 qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
                                int32_t afmt, const void* X, int64_t T, int64_t ldx,
-                               const float* tok_scale, const int32_t* expert_offsets,
-                               const int32_t* row_index, int64_t R, void* Y, int64_t ldy,
-                               void* ws, size_t ws_bytes, void* stream) {
+                               const float* tok_scale, const float* bias,
+                               const int32_t* expert_offsets, const int32_t* row_index,
+                               int64_t R, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
+                               void* stream) {
   if (row_index == nullptr && R > 0) return QGEMM_ERR_INVALID_ARG;
-  return run_moe(desc, packed, E, afmt, X, T, ldx, tok_scale, expert_offsets, row_index, R, Y,
-                 ldy, ws, ws_bytes, stream);
+  return run_moe(desc, packed, E, afmt, X, T, ldx, tok_scale, bias, expert_offsets, row_index,
+                 R, Y, ldy, ws, ws_bytes, stream);
 }
 
 size_t qgemm_act_copy_bytes(const qgemm_wdesc* desc, int64_t x_rows) {

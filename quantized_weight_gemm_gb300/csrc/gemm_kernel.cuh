@@ -938,6 +938,11 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     uint32_t g = 0;                       // stage counter of this CTA at the unit's start
     Unit w;
     int e_hint = -1;
+    // Bias of output column n for the unit's expert (added after every scale).
+    auto bias_of = [&](const Unit& u, int64_t n, bool n_ok) -> float {
+      return (n_ok && a.bias != nullptr) ? __ldg(a.bias + int64_t(u.expert) * a.bias_stride + n)
+                                         : 0.0f;
+    };
     // Per-token activation scale of output row m (indexed: of the row it was gathered from).
     auto tok_scale_of = [&](int64_t m) -> float {
       if constexpr (GATHER) {
@@ -975,6 +980,15 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           // hand the accumulator back to the MMA at once, then store.
           float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
           if constexpr (DM == DM_NVFP4 || F16) cs *= acc_s;
+          const float b = bias_of(w, n, n_ok);
+          // per-token scales of this warp's columns, lane l holding column l + 32 i (columns
+          // are never gathered rows here), handed to every lane by a shuffle
+          float tk[kCols / 32];
+#pragma unroll
+          for (int i = 0; i < kCols / 32; ++i) {
+            const int64_t m = w.row0 + int64_t(eh) * kCols + i * 32 + lane;
+            tk[i] = (kTokScale && m < w.row_end) ? a.tok_scale[m] : 1.0f;
+          }
           uint32_t packed[kCols / 2];
 #pragma unroll
           for (int c = 0; c < kCols / 16; ++c) {
@@ -982,9 +996,15 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             ptx::tmem_ld16(t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * 16), v);
             ptx::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; j += 2)
-              packed[(c * 16 + j) / 2] =
-                  ptx::pack_bf16x2(__uint_as_float(v[j]) * cs, __uint_as_float(v[j + 1]) * cs);
+            for (int j = 0; j < 16; j += 2) {
+              float y0 = __uint_as_float(v[j]) * cs, y1 = __uint_as_float(v[j + 1]) * cs;
+              if constexpr (kTokScale) {
+                const int col = c * 16 + j;
+                y0 *= __shfl_sync(0xffffffffu, tk[col / 32], col % 32);
+                y1 *= __shfl_sync(0xffffffffu, tk[(col + 1) / 32], (col + 1) % 32);
+              }
+              packed[(c * 16 + j) / 2] = ptx::pack_bf16x2(y0 + b, y1 + b);
+            }
           }
           ptx::tc_fence_before();
           warp_arrive(&accempty[acc], lane);
@@ -993,16 +1013,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int64_t m = w.row0 + int64_t(eh) * kCols + j;   // (never a gathered tile)
-              if (m < w.row_end) {
-                uint16_t h = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
-                if (kTokScale) {
-                  // the per-token scale after the rounding above: FP8's rounds twice (within
-                  // its tolerance); the FP16 copy's is a power of two and commutes with it
-                  const float y = __uint_as_float(uint32_t(h) << 16);
-                  h = uint16_t(ptx::pack_bf16x2(y * a.tok_scale[m], 0.0f) & 0xFFFFu);
-                }
-                Yh[m * a.ldy] = h;
-              }
+              if (m < w.row_end)
+                Yh[m * a.ldy] = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
             }
           }
           continue;
@@ -1012,6 +1024,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         // Narrow tiles (double-buffered accumulators): convert and store chunk by chunk.
         float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
         if constexpr (DM == DM_NVFP4 || F16) cs *= acc_s;
+        const float b = bias_of(w, n, n_ok);
 #pragma unroll 1
         for (int c = 0; c < kCols / kChunk; ++c) {
           uint32_t v[32];
@@ -1027,7 +1040,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               if (m < w.row_end) {
                 float y = __uint_as_float(v[j]) * cs;
                 if (kTokScale) y *= tok_scale_of(m);
-                Y[m * a.ldy + n] = __float2bfloat16_rn(y);
+                Y[m * a.ldy + n] = __float2bfloat16_rn(y + b);
               }
             }
           }
@@ -1070,6 +1083,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
                              eh * kCols;
         float cs2 = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
         if constexpr (DM == DM_NVFP4 || F16) cs2 *= acc_s;
+        const float b2 = bias_of(w, n, n_ok);
         constexpr int kPass = kCols < 16 ? kCols : 16;
 #pragma unroll 1
         for (int c0 = 0; c0 < kCols; c0 += kPass) {
@@ -1095,7 +1109,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
               if (m < w.row_end) {
                 float y = sum[j] * cs2;
                 if (kTokScale) y *= tok_scale_of(m);
-                Y[m * a.ldy + n] = __float2bfloat16_rn(y);
+                Y[m * a.ldy + n] = __float2bfloat16_rn(y + b2);
               }
             }
           }

@@ -82,7 +82,8 @@ size_t qgemm_host_staging_bytes(const qgemm_wdesc* desc, int64_t M_max) {
 }
 
 qgemm_status qgemm_w4a16_host(const qgemm_wdesc* desc, const void* packed, const void* X_host,
-                              int64_t M, int64_t ldx, const float* chan_scale, void* Y_host,
+                              int64_t M, int64_t ldx, const float* chan_scale, const float* bias,
+                              void* Y_host,
                               int64_t ldy, void* staging, size_t staging_bytes, void* ws,
                               size_t ws_bytes, void* stream) {
   if (qgemm_check_desc(desc) != QGEMM_OK) return QGEMM_ERR_INVALID_ARG;
@@ -112,7 +113,7 @@ qgemm_status qgemm_w4a16_host(const qgemm_wdesc* desc, const void* packed, const
     if (cudaMemcpy2DAsync(xs[0], size_t(K) * 2, xh, size_t(ldx) * 2, size_t(K) * 2, size_t(M),
                           cudaMemcpyHostToDevice, st) != cudaSuccess)
       return QGEMM_ERR_CUDA;
-    const qgemm_status s = qgemm_w4a16(desc, packed, xs[0], M, K, chan_scale, ys[0], N, ws,
+    const qgemm_status s = qgemm_w4a16(desc, packed, xs[0], M, K, chan_scale, bias, ys[0], N, ws,
                                        ws_bytes, stream);
     if (s != QGEMM_OK) return s;
     if (cudaMemcpy2DAsync(yh, size_t(ldy) * 2, ys[0], size_t(N) * 2, size_t(N) * 2, size_t(M),
@@ -139,7 +140,7 @@ qgemm_status qgemm_w4a16_host(const qgemm_wdesc* desc, const void* packed, const
     // multiply, once X is in and the copy out of chunk i - 2 has read this Y buffer
     if (cudaStreamWaitEvent(st, p->copied_in[b], 0) != cudaSuccess) return QGEMM_ERR_CUDA;
     if (i >= 2 && cudaStreamWaitEvent(st, p->copied_out[b], 0) != cudaSuccess) return QGEMM_ERR_CUDA;
-    const qgemm_status s = qgemm_w4a16(desc, packed, xs[b], m, K, chan_scale, ys[b], N, ws,
+    const qgemm_status s = qgemm_w4a16(desc, packed, xs[b], m, K, chan_scale, bias, ys[b], N, ws,
                                        ws_bytes, stream);
     if (s != QGEMM_OK) return s;
     if (cudaEventRecord(p->computed[b], st) != cudaSuccess) return QGEMM_ERR_CUDA;

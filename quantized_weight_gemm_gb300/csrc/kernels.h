@@ -61,6 +61,10 @@ struct GemmArgs {
   int32_t group_m;             // token tiles per rasterization group (>= 1)
   int32_t sk_tiles;
   const float* chan_scale;     // [N] or nullptr
+  // Bias added after every scale: [N] (dense, bias_stride 0) or [E][N] (MoE, bias_stride N),
+  // or nullptr.
+  const float* bias;
+  int64_t bias_stride;
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;

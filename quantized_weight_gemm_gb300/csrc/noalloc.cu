@@ -63,5 +63,6 @@ extern "C" qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void*
                         size_t(counter_bytes), static_cast<cudaStream_t>(stream)) != cudaSuccess)
       return QGEMM_ERR_CUDA;
   }
-  return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, Y, ldy, scratch, size_t(need), stream);
+  return qgemm_w4a16(desc, packed, X, M, ldx, chan_scale, nullptr, Y, ldy, scratch, size_t(need),
+                     stream);
 }

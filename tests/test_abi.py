@@ -121,16 +121,19 @@ def test_argument_errors_before_any_launch(L):
     d = qg.WeightDesc("int4_sym", 256, 512, 128).c()
     P = ctypes.c_void_p
     # null X, null packed, negative M, ldx < K, misaligned X
-    assert L.qgemm_w4a16(ctypes.byref(d), None, P(256), 16, 512, None, P(256), 256, None, 0, None) == 1
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), None, 16, 512, None, P(256), 256, None, 0, None) == 1
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), -1, 512, None, P(256), 256, None, 0, None) == 1
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 256, None, P(256), 256, None, 0, None) == 1
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(258), 16, 512, None, P(256), 256, None, 0, None) == 3
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 516, None, P(256), 256, None, 0, None) == 3
+    assert L.qgemm_w4a16(ctypes.byref(d), None, P(256), 16, 512, None, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), None, 16, 512, None, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), -1, 512, None, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 256, None, None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(258), 16, 512, None, None, P(256), 256, None, 0, None) == 3
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 516, None, None, P(256), 256, None, 0, None) == 3
+    # misaligned bias
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 16, 512, None, P(258), P(256), 256, None, 0,
+                         None) == 3
     # M = 0 is a no-op (returns before touching any device)
-    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 0, 512, None, P(256), 256, None, 0, None) == 0
+    assert L.qgemm_w4a16(ctypes.byref(d), P(256), P(256), 0, 512, None, None, P(256), 256, None, 0, None) == 0
     # FP8 entry point with a BF16-activation descriptor
-    assert L.qgemm_w4a8(ctypes.byref(d), P(256), P(256), 4, 512, P(256), None, P(256), 256, None, 0, None) == 1
+    assert L.qgemm_w4a8(ctypes.byref(d), P(256), P(256), 4, 512, P(256), None, None, P(256), 256, None, 0, None) == 1
     assert L.qgemm_force_config(48, 0) == 1
     assert L.qgemm_force_config(0, -2) == 1
     assert L.qgemm_force_config(0, 0) == 0
@@ -169,19 +172,21 @@ def test_moe_argument_errors_before_any_launch(L):
     bf16, fp8 = 0, 1
     buf, off = P(1 << 20), P(1 << 21)
 
-    def grouped(E=4, afmt=bf16, X=buf, R=8, ldx=512, ts=None, offs=off, Y=buf, ldy=256, packed=buf):
-        return L.qgemm_moe_grouped(ctypes.byref(d), packed, E, afmt, X, R, ldx, ts, offs, Y, ldy,
-                                   None, 0, None)
+    def grouped(E=4, afmt=bf16, X=buf, R=8, ldx=512, ts=None, offs=off, Y=buf, ldy=256, packed=buf,
+                bias=None):
+        return L.qgemm_moe_grouped(ctypes.byref(d), packed, E, afmt, X, R, ldx, ts, bias, offs, Y,
+                                   ldy, None, 0, None)
 
     def indexed(T=8, R=8, idx=P(1 << 22), E=4):
-        return L.qgemm_moe_indexed(ctypes.byref(d), buf, E, bf16, buf, T, 512, None, off, idx, R,
-                                   buf, 256, None, 0, None)
+        return L.qgemm_moe_indexed(ctypes.byref(d), buf, E, bf16, buf, T, 512, None, None, off, idx,
+                                   R, buf, 256, None, 0, None)
 
     assert grouped(E=0) == 1 and grouped(E=1025) == 1           # expert count
     assert grouped(afmt=fp8) == 1                                # descriptor is BF16
     assert grouped(R=-1) == 1 and grouped(offs=None) == 1 and grouped(packed=None) == 1
     assert grouped(packed=P((1 << 20) + 16)) == 3                # packed not 256-byte aligned
     assert grouped(offs=P((1 << 21) + 2)) == 3                   # offsets not 4-byte aligned
+    assert grouped(bias=P((1 << 21) + 2)) == 3                   # bias not 4-byte aligned
     assert grouped(ldx=256) == 1                                 # ldx < K
     assert grouped(X=P((1 << 20) + 2)) == 3                      # X not 16-byte aligned
     assert grouped(ldy=128) == 1                                 # ldy < N
@@ -190,8 +195,8 @@ def test_moe_argument_errors_before_any_launch(L):
     assert indexed(idx=P((1 << 22) + 2)) == 3                    # index not 4-byte aligned
     assert indexed(R=0) == 0
     d8 = qg.WeightDesc("mxfp4", 256, 512, 32, "fp8").c()
-    assert L.qgemm_moe_grouped(ctypes.byref(d8), buf, 4, fp8, buf, 8, 512, None, off, buf, 256,
-                               None, 0, None) == 1               # FP8 without token scales
+    assert L.qgemm_moe_grouped(ctypes.byref(d8), buf, 4, fp8, buf, 8, 512, None, None, off, buf,
+                               256, None, 0, None) == 1          # FP8 without token scales
 
 
 def test_product_package_does_not_import_oracle():

@@ -416,11 +416,11 @@ def test_w4a16_host_argument_errors():
     assert need == 2 * (512 * 512 * 2 + 256 * 512 * 2)          # chunks of 512 rows
     st = torch.empty(need, dtype=torch.uint8, device="cuda")
     args = lambda stg, n: (ctypes.byref(cd), P(packed.data_ptr()), P(xh.data_ptr()), 600, 512, None,
-                           P(yh.data_ptr()), 256, stg, n, None, 0, None)
+                           None, P(yh.data_ptr()), 256, stg, n, None, 0, None)
     assert L.qgemm_w4a16_host(*args(None, 0)) == 4                    # no staging
     assert L.qgemm_w4a16_host(*args(P(st.data_ptr()), need - 1)) == 4  # too small
     assert L.qgemm_w4a16_host(*args(P(st.data_ptr() + 16), need)) == 3  # misaligned
-    assert L.qgemm_w4a16_host(ctypes.byref(cd), P(packed.data_ptr()), None, 600, 512, None,
+    assert L.qgemm_w4a16_host(ctypes.byref(cd), P(packed.data_ptr()), None, 600, 512, None, None,
                               P(yh.data_ptr()), 256, P(st.data_ptr()), need, None, 0, None) == 1
 
 

@@ -405,6 +405,44 @@ def sweep_mxfp4(device, flush, peaks, fp8):
     return rows
 
 
+def sweep_w4a4(device, flush, peaks):
+    """Dense W4A4 (MXFP4 x MXFP4 on the block-scaled FP4 MMA), the MXFP4 shapes, M in
+    M_SWEEP.  The activation quantization is a separate call, timed beside each GEMM as
+    quant_act_us.  Tensor peak: the measured BF16 peak times 6, the nominal dense FP4 / BF16
+    ratio of a GB300 (13.5 / 2.25 PFLOP/s)."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import quantized_weight_gemm_gb300 as qg
+    bw = peaks["hbm_gbs"] * 1e9
+    tc = peaks["bf16_tflops"] * 1e12 * 6.0
+    rows = []
+    Mmax = max(M_SWEEP)
+    for (N, K) in MX_SHAPES:
+        x, w = WL.mxfp4_shape(N, K, Mmax, seed=0, outliers=True)
+        d = qg.WeightDesc("mxfp4", N, K, 32, "mxfp4")
+        packed = qg.repack(d, torch.from_numpy(w.codes).to(device),
+                           torch.from_numpy(w.scales).to(device))
+        X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
+        Xq, E = qg.quant_act_mxfp4(X)
+        Xq2, E2 = torch.empty_like(Xq), torch.empty_like(E)
+        Y = torch.empty(Mmax, N, dtype=torch.bfloat16, device=device)
+        ws = qg.workspace(d, Mmax, device)
+        wb = mx_weight_bytes(N, K)
+        for M in M_SWEEP:
+            ms = time_one(lambda: qg.w4a4(d, packed, Xq[:M], E[:M], out=Y[:M], ws=ws), flush)
+            ab = wb + M * K // 2 + M * K // 32 + M * N * 2
+            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc)
+            qms = time_one(lambda: qg.quant_act_mxfp4(X[:M], out=Xq2[:M], exps=E2[:M]), flush)
+            r["quant_act_us"] = round(qms * 1e3, 2)
+            rows.append(r)
+        del packed, X, Xq, E, Y, ws
+    torch.cuda.synchronize()
+    if qg.device_status(clear=True) != 0:
+        raise RuntimeError("a W4A4 GEMM reported a device error")
+    return rows
+
+
 FMT_M = (1, 16, 128, 1024, 8192)
 
 
@@ -551,6 +589,7 @@ def bench_ours(args):
         torch.cuda.empty_cache()
         extra = {"mxfp4_a16": sweep_mxfp4(device, flush, peaks, fp8=False),
                  "mxfp4_a8": sweep_mxfp4(device, flush, peaks, fp8=True),
+                 "w4a4": sweep_w4a4(device, flush, peaks),
                  "mxint4_a16": sweep_w4a16_fmt(device, flush, peaks, "mxint4"),
                  "nvfp4_a16": sweep_w4a16_fmt(device, flush, peaks, "nvfp4"),
                  "moe": sweep_moe(device, flush, peaks)}
@@ -638,6 +677,12 @@ def bench_ours(args):
                      "(median of 5); not part of value"),
             "mxfp4_a16": {"workload": "dense W4A16 MXFP4, N x K in {4096 x 7168, 7168 x 2048}",
                           "sweep": extra["mxfp4_a16"]},
+            "w4a4": {"workload": ("dense W4A4 MXFP4 x MXFP4 (E8M0 per 32 on both operands; "
+                                  "activations with 1% outliers x20, quantized by a separate "
+                                  "call timed as quant_act_us), N x K in {4096 x 7168, "
+                                  "7168 x 2048}"),
+                     "tensor_peak": "measured BF16 x 6 (nominal dense FP4 / BF16)",
+                     "sweep": extra["w4a4"]},
             "mxfp4_a8": {"workload": ("dense W4A8 MXFP4 x per-token FP8 e4m3 (1% outliers x20), "
                                       "same shapes; quant_act_us = the separate quantization call; "
                                       "roofline tensor peak = 2 x measured bf16"),

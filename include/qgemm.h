@@ -62,14 +62,15 @@ typedef enum {
   QGEMM_W_NVFP4 = 4
 } qgemm_wfmt;
 typedef enum { QGEMM_SCALE_BF16 = 0, QGEMM_SCALE_E8M0 = 1, QGEMM_SCALE_E4M3 = 2 } qgemm_sdtype;
-typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1 } qgemm_afmt;
+typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1, QGEMM_A_MXFP4 = 2 } qgemm_afmt;
 
 /*
  * Weight descriptor ("layer config"): one quantized weight matrix W of logical shape
  * [N, K] (Y = X . W^T).  Supported combinations:
  *   wfmt INT4_SYM : sdtype BF16, has_zp 0, group_size 32 or a multiple of 64, K % group == 0
  *   wfmt UINT4_ZP : sdtype BF16, has_zp 1, group_size as above
- *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32
+ *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32 (afmt BF16, FP8E4M3_TOKEN, or
+ *                   MXFP4 for W4A4; only MXFP4 weights pair with MXFP4 activations)
  *   wfmt MXINT4   : sdtype E8M0, has_zp 0, group_size 32, afmt BF16
  *                   (w = q * 2^(e - 127), q the two's-complement nibble)
  *   wfmt NVFP4    : sdtype E4M3, has_zp 0, group_size 16, afmt BF16
@@ -260,6 +261,38 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
                         int64_t ldx, const float* tok_scale, const float* chan_scale,
                         const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
                         void* stream);
+
+/*
+ * MXFP4 activation quantization (the input of W4A4), the OCP Microscaling conversion: per
+ * row m and block of 32 K-elements b, E = floor(log2 max |X[m, 32b .. 32b+31]|) - 2 + 127
+ * clamped to [0, 254] (127 for an all-zero block), and each element X / 2^(E - 127) rounded
+ * to the nearest e2m1 value (ties to even, saturating at +-6).
+ *   X      : device BF16 [M, ldx], K % 32 == 0, ldx >= K
+ *   Xq     : device uint8 [M, ldq] codes, ldq >= K / 2, 4-byte aligned rows; element 2j
+ *            of a row in the low nibble of byte j
+ *   x_exps : device uint8 [M, ld_exps] E8M0 exponents, one per 32 K; ld_exps >=
+ *            ceil(K / 128) * 4 (blocks past K up to that are written as 127)
+ * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4" (MX formats on Blackwell's tensor
+ * cores); the conversion itself is the OCP Microscaling format's.
+ */
+qgemm_status qgemm_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                   int64_t ldq, uint8_t* x_exps, int64_t ld_exps, void* stream);
+
+/*
+ * Dense W4A4 (MXFP4 weights x MXFP4 activations, both block-scaled by E8M0 per 32 K):
+ *   Y[m, n] = c[n] * sum_k e2m1(Xq[m, k]) 2^(x_exps[m, k/32] - 127) W[n, k] + b[n]
+ * computed by the tensor cores' block-scaled FP4 MMA (kind::mxf4): both operands' products
+ * are exact, the sum is FP32, Y is rounded to BF16 once.
+ *   packed : device, from qgemm_repack with desc->wfmt == MXFP4, desc->afmt == QGEMM_A_MXFP4
+ *   Xq, ldq, x_exps, ld_exps : from qgemm_quant_act_mxfp4; Xq 16-byte aligned, ldq % 16 == 0,
+ *            x_exps 4-byte aligned, ld_exps % 4 == 0
+ *   chan_scale, bias, Y, ldy, ws, ws_bytes, stream : as for qgemm_w4a16
+ * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4" (W4A4 on B300 and SM121).
+ */
+qgemm_status qgemm_w4a4(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
+                        int64_t ldq, const uint8_t* x_exps, int64_t ld_exps,
+                        const float* chan_scale, const float* bias, void* Y, int64_t ldy,
+                        void* ws, size_t ws_bytes, void* stream);
 
 /*
  * MoE grouped GEMM over expert-sorted rows: for each expert e, rows

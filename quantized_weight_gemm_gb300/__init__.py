@@ -16,7 +16,7 @@ __all__ = [
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
     "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "host_staging_bytes",
     "host_staging", "w4a16_host", "moe_indexed", "check_desc", "WFMT", "AFMT", "EXPORTS",
-    "debug_stall", "act_copy_bytes",
+    "debug_stall", "act_copy_bytes", "w4a4", "quant_act_mxfp4",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -24,14 +24,14 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libqgemm.so")
 
 WFMT = {"int4_sym": 0, "uint4_zp": 1, "mxfp4": 2, "mxint4": 3, "nvfp4": 4}
 SDTYPE = {"int4_sym": 0, "uint4_zp": 0, "mxfp4": 1, "mxint4": 1, "nvfp4": 2}   # BF16, E8M0, E4M3
-AFMT = {"bf16": 0, "fp8": 1}
+AFMT = {"bf16": 0, "fp8": 1, "mxfp4": 2}
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
            "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host",
            "qgemm_moe_indexed", "qgemm_repack_scaled", "qgemm_debug_stall",
-           "qgemm_act_copy_bytes")
+           "qgemm_act_copy_bytes", "qgemm_w4a4", "qgemm_quant_act_mxfp4")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -107,6 +107,8 @@ def lib():
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
         "qgemm_act_copy_bytes": (SZ, [D, I64]),
+        "qgemm_w4a4": (ctypes.c_int, [D, P, P, I64, I64, P, I64, P, P, P, I64, P, SZ, P]),
+        "qgemm_quant_act_mxfp4": (ctypes.c_int, [P, I64, I64, I64, P, I64, P, I64, P]),
         "qgemm_host_staging_bytes": (SZ, [D, I64]),
         "qgemm_moe_indexed": (ctypes.c_int, [D, P, I32, I32, P, I64, I64, P, P, P, P, I64, P, I64, P, SZ, P]),
         "qgemm_w4a16_host": (ctypes.c_int, [D, P, P, I64, I64, P, P, P, I64, P, SZ, P, SZ, P]),
@@ -243,6 +245,36 @@ def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None, bias=N
                             _ptr(tok_scale), _ptr(chan_scale), _ptr(bias), _ptr(out), out.stride(0),
                             _ptr(ws),
                             ws.numel() * ws.element_size(), _stream()), "w4a8")
+    return out
+
+
+def quant_act_mxfp4(X, out=None, exps=None):
+    """MXFP4 activations of BF16 X [M, K]: (codes uint8 [M, K/2], E8M0 exponents uint8
+    [M, ceil(K/128)*4]) (see qgemm_quant_act_mxfp4)."""
+    _row_major(X, "X")
+    M, K = X.shape
+    if out is None:
+        out = torch.empty(M, K // 2, dtype=torch.uint8, device=X.device)
+    if exps is None:
+        exps = torch.empty(M, (K // 32 + 3) // 4 * 4, dtype=torch.uint8, device=X.device)
+    _check(lib().qgemm_quant_act_mxfp4(_ptr(X), M, K, X.stride(0), _ptr(out), out.stride(0),
+                                       _ptr(exps), exps.stride(0), _stream()), "quant_act_mxfp4")
+    return out, exps
+
+
+def w4a4(desc, packed, Xq, x_exps, chan_scale=None, out=None, ws=None, bias=None):
+    """Dense W4A4: MXFP4 codes Xq [M, K/2] and exponents x_exps [M, >= ceil(K/128)*4] from
+    quant_act_mxfp4, weights repacked with afmt "mxfp4"."""
+    M = Xq.shape[0]
+    if out is None:
+        out = torch.empty(M, desc.N, dtype=torch.bfloat16, device=Xq.device)
+    if ws is None:
+        ws = workspace(desc, M, Xq.device)
+    d = desc.c()
+    _check(lib().qgemm_w4a4(ctypes.byref(d), _ptr(packed), _ptr(Xq), M, Xq.stride(0), _ptr(x_exps),
+                            x_exps.stride(0), _ptr(chan_scale), _ptr(bias), _ptr(out),
+                            out.stride(0), _ptr(ws), ws.numel() * ws.element_size(), _stream()),
+           "w4a4")
     return out
 
 

@@ -332,9 +332,38 @@ bool make_x_map(CUtensorMap* m, const void* X, XType xt, int64_t rows, int64_t K
   return r == CUDA_SUCCESS;
 }
 
+// MXFP4 activation codes (W4A4): [rows][K / 2] bytes with row stride ldq bytes, loaded as
+// 64-byte rows (128 K) with the 64-byte swizzle the FP4 MMA's descriptor expects.
+bool make_x4_map(CUtensorMap* m, const void* Xq, int64_t rows, int64_t K, int64_t ldq,
+                 int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(K / 2), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ldq)};
+  cuuint32_t box[2] = {64, cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(Xq), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Exponent rows of MXFP4 activations: one byte per 32 K, the kernel reading four at a time.
+int64_t exps_row_min(int64_t K) { return (K / 32 + 3) / 4 * 4; }
+
 qgemm_status check_x(const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx) {
   if (X == nullptr || rows < 0 || rows >= (int64_t(1) << 31) || ldx < K) return QGEMM_ERR_INVALID_ARG;
   if (!aligned(X, 16) || (ldx * (fp8 ? 1 : 2)) % 16 != 0) return QGEMM_ERR_ALIGNMENT;
+  return QGEMM_OK;
+}
+
+// MXFP4 activations: codes [rows][ldq bytes] (ldq >= K / 2) and exponents [rows][lde].
+qgemm_status check_x4(const void* Xq, int64_t rows, int64_t K, int64_t ldq, const void* exps,
+                      int64_t lde) {
+  if (Xq == nullptr || exps == nullptr || rows < 0 || rows >= (int64_t(1) << 31) ||
+      ldq < K / 2 || lde < exps_row_min(K))
+    return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(Xq, 16) || ldq % 16 != 0 || !aligned(exps, 4) || lde % 4 != 0)
+    return QGEMM_ERR_ALIGNMENT;
   return QGEMM_OK;
 }
 
@@ -345,16 +374,19 @@ qgemm_status check_y(const void* Y, int64_t N, int64_t ldy) {
 }
 
 // Every argument check of the dense calls that needs no device.
-qgemm_status check_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
-                         int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
-                         const float* bias, const void* Y, int64_t ldy, Layout* L) {
+qgemm_status check_dense(const qgemm_wdesc* desc, int32_t afmt, const void* packed,
+                         const void* X, int64_t M, int64_t ldx, const float* tok_scale,
+                         const float* chan_scale, const float* bias, const void* Y, int64_t ldy,
+                         Layout* L, const uint8_t* x_exps = nullptr, int64_t ld_exps = 0) {
   if (!layout_of(desc, L)) return QGEMM_ERR_INVALID_ARG;
-  if ((L->afmt == A_FP8) != fp8) return QGEMM_ERR_INVALID_ARG;
+  if (L->afmt != afmt) return QGEMM_ERR_INVALID_ARG;
+  const bool fp8 = afmt == A_FP8;
   if (fp8 && L->wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
   if (M < 0) return QGEMM_ERR_INVALID_ARG;
   if (packed == nullptr) return QGEMM_ERR_INVALID_ARG;
   if (!aligned(packed, 256)) return QGEMM_ERR_ALIGNMENT;
-  qgemm_status s = check_x(X, fp8, M, L->K, ldx);
+  qgemm_status s = afmt == A_MXFP4 ? check_x4(X, M, L->K, ldx, x_exps, ld_exps)
+                                   : check_x(X, fp8, M, L->K, ldx);
   if (s != QGEMM_OK) return s;
   if ((s = check_y(Y, L->N, ldy)) != QGEMM_OK) return s;
   if (fp8 && tok_scale == nullptr) return QGEMM_ERR_INVALID_ARG;
@@ -364,13 +396,14 @@ qgemm_status check_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, 
   return QGEMM_OK;
 }
 
-qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, const void* X,
+qgemm_status run_dense(const qgemm_wdesc* desc, int32_t afmt, const void* packed, const void* X,
                        int64_t M, int64_t ldx, const float* tok_scale, const float* chan_scale,
                        const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
-                       void* stream) {
+                       void* stream, const uint8_t* x_exps = nullptr, int64_t ld_exps = 0) {
   Layout L;
-  const qgemm_status s = check_dense(desc, fp8, packed, X, M, ldx, tok_scale, chan_scale, bias,
-                                     Y, ldy, &L);
+  const qgemm_status s = check_dense(desc, afmt, packed, X, M, ldx, tok_scale, chan_scale, bias,
+                                     Y, ldy, &L, x_exps, ld_exps);
+  const bool fp8 = afmt == A_FP8, a4 = afmt == A_MXFP4;
   if (s != QGEMM_OK) return s;
   if (M == 0) return QGEMM_OK;
   DeviceInfo* dev = nullptr;
@@ -397,12 +430,15 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   }
   CUtensorMap tmap;
   int x3d = 0;
-  if (!make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, M, L.K, ldg, plan.token_tile,
-                  &x3d))
+  if (a4 ? !make_x4_map(&tmap, X, M, L.K, ldx, plan.token_tile)
+         : !make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, M, L.K, ldg,
+                       plan.token_tile, &x3d))
     return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
   a.x_3d = x3d;
+  a.x_exps = x_exps;
+  a.ld_exps = ld_exps;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.M = M;
@@ -413,7 +449,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, bool fp8, const void* packed, co
   // Token tiles per rasterization group: as many as keep the group's activation rows
   // within about half of L2, so that they are read from DRAM once.
   {
-    const int64_t x_tile_bytes = int64_t(plan.token_tile) * L.K * (fp8 ? 1 : 2);
+    const int64_t x_tile_bytes = int64_t(plan.token_tile) * (a4 ? L.K / 2 : L.K * (fp8 ? 1 : 2));
     const int64_t gm = std::max<int64_t>(1, (dev->l2_bytes / 2) / std::max<int64_t>(1, x_tile_bytes));
     a.group_m = int(std::min<int64_t>(gm, a.m_tiles));
   }
@@ -445,7 +481,7 @@ qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, cons
                                int64_t* counter_bytes) {
   *need = *counter_off = *counter_bytes = 0;
   Layout L;
-  const qgemm_status s = check_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale,
+  const qgemm_status s = check_dense(desc, A_BF16, packed, X, M, ldx, nullptr, chan_scale,
                                      nullptr, Y, ldy, &L);
   if (s != QGEMM_OK || M == 0) return s;
   DeviceInfo* dev = nullptr;
@@ -540,7 +576,7 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
 qgemm_status qgemm_w4a16(const qgemm_wdesc* desc, const void* packed, const void* X, int64_t M,
                          int64_t ldx, const float* chan_scale, const float* bias, void* Y,
                          int64_t ldy, void* ws, size_t ws_bytes, void* stream) {
-  return run_dense(desc, false, packed, X, M, ldx, nullptr, chan_scale, bias, Y, ldy, ws,
+  return run_dense(desc, A_BF16, packed, X, M, ldx, nullptr, chan_scale, bias, Y, ldy, ws,
                    ws_bytes, stream);
 }
 
@@ -548,8 +584,30 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
                         int64_t ldx, const float* tok_scale, const float* chan_scale,
                         const float* bias, void* Y, int64_t ldy, void* ws, size_t ws_bytes,
                         void* stream) {
-  return run_dense(desc, true, packed, Xq, M, ldx, tok_scale, chan_scale, bias, Y, ldy, ws,
+  return run_dense(desc, A_FP8, packed, Xq, M, ldx, tok_scale, chan_scale, bias, Y, ldy, ws,
                    ws_bytes, stream);
+}
+
+qgemm_status qgemm_w4a4(const qgemm_wdesc* desc, const void* packed, const uint8_t* Xq, int64_t M,
+                        int64_t ldq, const uint8_t* x_exps, int64_t ld_exps,
+                        const float* chan_scale, const float* bias, void* Y, int64_t ldy,
+                        void* ws, size_t ws_bytes, void* stream) {
+  return run_dense(desc, A_MXFP4, packed, Xq, M, ldq, nullptr, chan_scale, bias, Y, ldy, ws,
+                   ws_bytes, stream, x_exps, ld_exps);
+}
+
+qgemm_status qgemm_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                   int64_t ldq, uint8_t* x_exps, int64_t ld_exps, void* stream) {
+  if (X == nullptr || Xq == nullptr || x_exps == nullptr || M < 0 || K < 32 || K % 32 != 0 ||
+      ldx < K || ldq < K / 2 || ld_exps < exps_row_min(K) || M >= (int64_t(1) << 31))
+    return QGEMM_ERR_INVALID_ARG;
+  if (!aligned(X, 2) || !aligned(Xq, 4) || ldq % 4 != 0) return QGEMM_ERR_ALIGNMENT;
+  if (M == 0) return QGEMM_OK;
+  DeviceInfo* dev = nullptr;
+  if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
+  cudaError_t e = launch_quant_act_mxfp4(X, M, K, ldx, Xq, ldq, x_exps, ld_exps,
+                                         static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? QGEMM_OK : QGEMM_ERR_CUDA;
 }
 
 qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,

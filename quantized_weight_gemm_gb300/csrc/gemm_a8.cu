@@ -9,6 +9,7 @@ cudaError_t launch_gemm_a16_any(const GemmPlan&, const CUtensorMap&, const GemmA
 cudaError_t launch_gemm_a16_mxfp4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a16_mxint4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a16_nvfp4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_a4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
                         const GemmArgs& args, cudaStream_t st) {
@@ -19,6 +20,7 @@ cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
     case DM_MXFP4: return launch_gemm_a16_mxfp4(plan, tmap, args, st);
     case DM_MXINT4: return launch_gemm_a16_mxint4(plan, tmap, args, st);
     case DM_NVFP4: return launch_gemm_a16_nvfp4(plan, tmap, args, st);
+    case DM_W4A4: return launch_gemm_a4(plan, tmap, args, st);
     default: return launch_gemm_a16_any(plan, tmap, args, st);
   }
 }

@@ -72,12 +72,14 @@ namespace qgemm {
 // multiple of 4, so `warp & 3` is the tensor-memory lane quarter a warp may access.  Every
 // SM sub-partition holds a quarter of the warps and of the 64 K registers, so more warps
 // leave fewer registers per thread.
-template <int BNT>
+// A4 (W4A4, MXFP4 activations): no register decode -- one warpgroup moves the E8M0 scale
+// factors into tensor memory, and one issuer runs two FP4 MMAs per stage.
+template <int BNT, bool A4 = false>
 struct Roles {
-  static constexpr int kDeqWGs = BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
+  static constexpr int kDeqWGs = A4 ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
-  static constexpr int kIssuers = BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
+  static constexpr int kIssuers = A4 ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
   // Wide token tiles have one accumulator buffer (or two of 128 columns): two epilogue
   // warps per lane quarter drain it twice as fast, so the MMA waits less for it.
   static constexpr int kEpiWarps = BNT >= 128 ? 8 : 4;
@@ -97,19 +99,24 @@ constexpr int kRecTail = kTileN * 4 * 2 + kTileN * 4 / 2;           // largest s
 constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
 
-template <int BNT, bool A8>
+template <int BNT, bool A8, bool A4 = false>
 struct GemmCfg {
   // 32-K chunks per stage: full records, except BF16 x 256 tokens (half records).
-  static constexpr int kChunks = (!A8 && BNT >= 256) ? 2 : 4;
+  static constexpr int kChunks = (!A8 && !A4 && BNT >= 256) ? 2 : 4;
   static constexpr int kSubStages = 4 / kChunks;                 // stages per record
-  static constexpr int kRecSlot = kChunks * kTileN * 16 + kRecTail; // codes + tail
-  static constexpr int kSlabs = A8 ? 1 : kChunks / 2;           // 128-byte-wide X slabs
-  static constexpr int kSlabBytes = BNT * 128;
+  // codes + tail; A4: the MMA reads the codes in place, 64-byte-swizzled, so every slot
+  // starts on a 512-byte atom
+  static constexpr int kRecSlot = A4 ? 9216 : kChunks * kTileN * 16 + kRecTail;
+  // X slabs per stage: 128-byte rows (64 BF16 / 128 FP8 K); A4: one 64-byte row (128 FP4 K)
+  static constexpr int kSlabs = (A8 || A4) ? 1 : kChunks / 2;
+  static constexpr int kSlabBytes = A4 ? BNT * 64 : BNT * 128;
   static constexpr int kXBytes = kSlabs * kSlabBytes;
-  static constexpr int kACols = A8 ? 32 : kChunks * 16;          // A-operand columns / stage
-  static constexpr int kMmaPerStage = A8 ? kChunks : 2 * kChunks;
-  static_assert(A8 || kMmaPerStage % 4 == 0, "BF16 stages issue their MMAs in groups of four");
-  static constexpr int kIssuers = Roles<BNT>::kIssuers;
+  // tensor-memory columns per stage of the A ring: the A operand (BF16 / FP8), or for A4
+  // the scale factors (4 for the weights, 4 per 128 tokens for the activations)
+  static constexpr int kACols = A4 ? 4 + 4 * ((BNT + 127) / 128) : A8 ? 32 : kChunks * 16;
+  static constexpr int kMmaPerStage = A4 ? 2 : A8 ? kChunks : 2 * kChunks;
+  static_assert(A4 || A8 || kMmaPerStage % 4 == 0, "BF16 stages issue their MMAs in groups of four");
+  static constexpr int kIssuers = Roles<BNT, A4>::kIssuers;
   static constexpr int kNumSub = kIssuers;                       // partial accumulators
   static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
   static constexpr int kAccCols = kNumAcc * kNumSub * BNT;
@@ -118,13 +125,14 @@ struct GemmCfg {
   static constexpr int kSfCols = A8 ? 4 : 0;
   static constexpr int kATmemMax = (512 - kAccCols - (A8 ? 8 : 0)) / (kACols + kSfCols);
   static constexpr int kAStagesMax =
-      A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
-         : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
+      A4 ? (kATmemMax < 8 ? kATmemMax : 8)
+      : A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
+           : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
   // Stage g of the CTA goes to dequant warpgroup g % kDeqWGs and to issuer g % kIssuers.
   // A ring slot must always have the same two owners: a waiter that is not the slot's only
   // consumer could run two uses ahead, where a one-bit mbarrier phase parity cannot tell
   // the phase it needs from the one before.  So the depth is a multiple of both counts.
-  static constexpr int kDeqWGs = Roles<BNT>::kDeqWGs;
+  static constexpr int kDeqWGs = Roles<BNT, A4>::kDeqWGs;
   static constexpr int kALcm = lcm_int(kDeqWGs, kIssuers);
   static constexpr int kAStages = kAStagesMax / kALcm * kALcm;
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
@@ -338,7 +346,8 @@ struct Ring {
 // only the code it runs.  "G1": one scale (and zero point) per row per record, i.e. a
 // group of 128 K or longer, so they are read once per record.
 enum DecodeMode : int {
-  DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5
+  DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5,
+  DM_W4A4 = 6                  // MXFP4 x MXFP4: no decode, the MMA reads the codes
 };
 
 // INT4 with BF16 scales (every group size): FP16 tensor-core operands, see f16_operands().
@@ -416,14 +425,16 @@ __device__ __forceinline__ void gather_row(uint32_t dst, const uint8_t* src, uin
 }
 
 template <int BNT, bool A8, int DM, bool GATHER>
-__global__ void __launch_bounds__(Roles<BNT>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<BNT, DM == DM_W4A4>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   static_assert(!GATHER || BNT <= 64, "gathered tiles exist for token tiles up to 64");
+  constexpr bool A4 = DM == DM_W4A4;
+  static_assert(!A4 || (!A8 && !GATHER), "W4A4: its own activation format, TMA loads only");
   constexpr bool F16 = kF16Operands<A8, DM>;
   // per-token (per-row) output scale: FP8's token scale, or the FP16 copy's row scale
   constexpr bool kTokScale = A8 || F16;
-  using C = GemmCfg<BNT, A8>;
-  using RO = Roles<BNT>;
+  using C = GemmCfg<BNT, A8, A4>;
+  using RO = Roles<BNT, A4>;
   constexpr int kEpiWarp0 = RO::kEpiWarp0;
   constexpr int kDeqWGs = RO::kDeqWGs;
   constexpr int kXProducerWarp = RO::kXProducerWarp;
@@ -474,7 +485,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     misc[1] = 0;
     for (int s = 0; s < SR; ++s) {
       ptx::mbar_init(&rfull[s], 1);
-      ptx::mbar_init(&rempty[s], 4);     // one arrival per dequant warp
+      ptx::mbar_init(&rempty[s], A4 ? 1 : 4);   // per dequant warp; A4: the MMAs' commit
     }
     for (int s = 0; s < SX; ++s) {
       ptx::mbar_init(&xfull[s], GATHER ? 32 : 1);   // gathered slots: one arrival per lane
@@ -729,8 +740,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             ptx::tma_load_3d(sx, &tmap_x, 0, row0, k0 / (A8 ? 128 : 64), &xfull[rx.slot], pol_x);
           } else {
 #pragma unroll 1
-            for (int sl = 0; sl < C::kXBoxSlabs; ++sl)
-              ptx::tma_load_2d(sx + sl * C::kSlabBytes, &tmap_x, k0 + sl * (A8 ? 128 : 64), row0,
+            for (int sl = 0; sl < C::kXBoxSlabs; ++sl)   // (A4: the map counts bytes of codes)
+              ptx::tma_load_2d(sx + sl * C::kSlabBytes, &tmap_x,
+                               A4 ? k0 / 2 + sl * 64 : k0 + sl * (A8 ? 128 : 64), row0,
                                &xfull[rx.slot], pol_x);
           }
           pending |= 1u << rx.slot;
@@ -755,7 +767,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     int ui = 0;
     uint32_t g0 = 0;                      // CTA stage counter at the unit start
     bool alive = true;
-    const uint64_t desc0 = ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
+    const uint64_t desc0 = A4 ? ptx::desc_kmajor_sw64(ptx::smem_u32(s_x))
+                              : ptx::desc_kmajor_sw128(ptx::smem_u32(s_x));
     Unit w;
     int e_hint = -1;
     for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj, ++ui) {
@@ -788,6 +801,22 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           ptx::tc_fence_after();
           const uint64_t bdesc = desc0 + uint64_t((rx.slot * C::kXSlotBytes + xj * C::kXBytes) >> 4);
           const uint32_t a_tmem = tbase + uint32_t(C::kACol0 + cur.slot * C::kACols);
+          if constexpr (A4) {
+            // A is the stage's record in shared memory; the A "slot" holds its scale factors
+            const int rs = int(g % uint32_t(SR));
+            if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepMma))) { alive = false; break; }
+            ptx::tc_fence_after();
+            const uint64_t adesc = ptx::desc_kmajor_sw64(ptx::smem_u32(s_rec + rs * C::kRecSlot));
+#pragma unroll
+            for (int q = 0; q < 2; ++q)   // two 64-K steps: 32 bytes into the swizzled rows
+              ptx::mma_mxf4_ss_elect(d_tmem, adesc + uint64_t(q * 2), bdesc + uint64_t(q * 2),
+                                     ptx::idesc_mxf4(128, BNT, 2 * q, 2 * q), a_tmem, a_tmem + 4u,
+                                     q > 0 ? 1u : (first ^ 1u));
+            first = 0;
+            ptx::mma_commit_elect(&aempty[cur.slot]);   // frees the stage's scale factors
+            ptx::mma_commit_elect(&rempty[rs]);         // ... and its record
+            continue;
+          }
           if constexpr (A8) {
 #pragma unroll
             for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
@@ -824,6 +853,49 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     ptx::mma_commit_elect(drain);
     volatile int no_abort = 0;
     warp_all(ptx::mbar_wait(drain, 0, &no_abort, 200000000ull));
+  } else if (A4 && warp < kEpiWarp0) {
+    // ---------------------------------------------------------------- scale factors (A4)
+    // One warpgroup, every stage: thread r (lane l = r % 32 of lane quarter r / 32) copies
+    // into the stage's scale-factor columns
+    //  - weight row r's four E8M0 bytes (the record's tail): the MMA reads row r's factors
+    //    from lane r, column r / 32 of the group (the word is written to all four);
+    //  - the activation scale words of tokens l, l + 32, l + 64, ...: the MMA reads token
+    //    n's factors from lane n % 32, column n / 32, in every lane quarter (each quarter
+    //    holds the same copy), as a probe with one marked exponent per call showed.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
+    constexpr int kTokGroups = (BNT + 127) / 128;            // groups of 4 token columns
+    uint32_t g = 0;
+    bool alive = true;
+    Unit w;
+    int e_hint = -1;
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+      for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
+        uint32_t sfb[4 * kTokGroups];
+#pragma unroll
+        for (int c = 0; c < 4 * kTokGroups; ++c) {
+          const int j = c * 32 + lane;                   // token of column c in this lane
+          const int64_t m = w.row0 + j;
+          sfb[c] = (j < BNT && m < w.row_end)
+                       ? __ldg(reinterpret_cast<const uint32_t*>(a.x_exps + m * a.ld_exps) + kb)
+                       : 0x7F7F7F7Fu;                  // rows past the tile: 1.0 (codes are 0)
+        }
+        const int rs = int(g % uint32_t(SR)), ca = int(g % uint32_t(SA));
+        if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        const uint32_t sfa = *reinterpret_cast<const uint32_t*>(s_rec + rs * C::kRecSlot + kCodeBytes + r * 4);
+        ptx::fence_proxy_async_smem();                   // the read above before the refill
+        if (!warp_all(ptx::mbar_wait(&aempty[ca], ((g / uint32_t(SA)) & 1u) ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        ptx::tc_fence_after();
+        const uint32_t col = t_lane + uint32_t(C::kACol0 + ca * C::kACols);
+        ptx::tmem_st4(col, sfa, sfa, sfa, sfa);
+#pragma unroll
+        for (int h = 0; h < kTokGroups; ++h)
+          ptx::tmem_st4(col + 4u + 4u * h, sfb[4 * h], sfb[4 * h + 1], sfb[4 * h + 2], sfb[4 * h + 3]);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        warp_arrive(&afull[ca], lane);
+      }
+    }
   } else if (warp < kEpiWarp0) {
     // ---------------------------------------------------------------- dequant (2 WGs)
     const int wg = warp >> 2;                              // takes the stages g % kDeqWGs == wg
@@ -1132,7 +1204,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 template <int BNT, bool A8, int DM, bool GATHER>
 cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                            cudaStream_t st) {
-  using C = GemmCfg<BNT, A8>;
+  using C = GemmCfg<BNT, A8, DM == DM_W4A4>;
   // At least 120 KB of shared memory per CTA: one CTA per SM, so no CTA ever waits for
   // another one's tensor-memory allocation.
   constexpr int kSmem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
@@ -1145,7 +1217,7 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(plan.grid));
-  cfg.blockDim = dim3(Roles<BNT>::kThreads);
+  cfg.blockDim = dim3(Roles<BNT, DM == DM_W4A4>::kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1160,7 +1232,8 @@ template <bool A8, int DM>
 cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                              cudaStream_t st) {
   if (args.row_index != nullptr) {          // gathered (indexed MoE) tiles: up to 64 tokens
-    switch (plan.token_tile) {
+    if constexpr (DM == DM_W4A4) return cudaErrorInvalidValue;   // W4A4: TMA loads only
+    else switch (plan.token_tile) {
       case 16: return launch_variant<16, A8, DM, true>(plan, tmap, args, st);
       case 32: return launch_variant<32, A8, DM, true>(plan, tmap, args, st);
       case 64: return launch_variant<64, A8, DM, true>(plan, tmap, args, st);
@@ -1179,6 +1252,7 @@ cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, cons
 
 // Decode mode of a packed layout (BF16 activations).
 inline int decode_mode(const Layout& L) {
+  if (L.afmt == A_MXFP4) return DM_W4A4;
   if (L.wfmt == W_MXFP4) return DM_MXFP4;
   if (L.wfmt == W_MXINT4) return DM_MXINT4;
   if (L.wfmt == W_NVFP4) return DM_NVFP4;

@@ -32,6 +32,11 @@ cudaError_t launch_dequant_debug(const Layout& L, const void* packed, void* W, c
 // rowscale[m] = 2^e_m.  X16 is [rows][K] with leading dimension K.
 cudaError_t launch_prep_x_f16(const void* X, int64_t rows, int64_t K, int64_t ldx, void* X16,
                               float* rowscale, cudaStream_t st);
+// MXFP4 activations for W4A4: codes [M][ldq] bytes (element 2j in the low nibble of byte j)
+// and E8M0 exponents [M][lde] bytes, one per 32 K, blocks past K up to a multiple of 4
+// filled with 127.
+cudaError_t launch_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                   int64_t ldq, uint8_t* exps, int64_t lde, cudaStream_t st);
 cudaError_t launch_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
                                  int64_t ldq, float* s, cudaStream_t st);
 
@@ -66,6 +71,10 @@ struct GemmArgs {
   const float* bias;
   int64_t bias_stride;
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
+  // MXFP4 activations (W4A4): E8M0 exponents, row m at x_exps + m * ld_exps bytes, one
+  // 32-bit word (four exponents) per 128-K block
+  const uint8_t* x_exps;
+  int64_t ld_exps;
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
   // Partial sums of the tiles whose K range is cut over several CTAs: one slot per

@@ -3,6 +3,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "dequant.cuh"
 #include "kernels.h"
 #include "qgemm_internal.h"
@@ -51,12 +53,14 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
       for (int e = 0; e < 8; ++e) {
         uint32_t nib = pad ? 0u : (src >> (4 * e)) & 0xFu;   // even k in the low nibble
         if (L.wfmt == W_INT4_SYM || L.wfmt == W_MXINT4) nib ^= 8u;   // two's complement -> q + 8
-        const int pos = (L.afmt == A_FP8) ? nibble_pos_a8(e) : nibble_pos_a16(e);
+        const int pos = L.afmt == A_FP8 ? nibble_pos_a8(e)
+                        : L.afmt == A_MXFP4 ? e                        // the MMA's own order
+                                            : nibble_pos_a16(e);
         w |= nib << (4 * pos);
       }
       out[j] = w;
     }
-    uint8_t* dst = record_ptr(L, packed, nt, kb) + c * (kTileN * 16) + r * 16;
+    uint8_t* dst = record_ptr(L, packed, nt, kb) + code_piece_offset(L.afmt, r, c);
     *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
@@ -234,10 +238,22 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
     const int64_t k0 = kb * kStageK + c * 32 + j * 8;
     if (n >= L.N || k0 >= L.K) continue;
     const uint8_t* rec = packed + kHeaderBytes + (nt * L.k_blocks + kb) * int64_t(L.record_bytes);
-    const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + c * (kTileN * 16) + r * 16 + j * 4);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(rec + code_piece_offset(L.afmt, r, c) + j * 4);
     const int js = c * G / 4;                          // scale entry of chunk c
     const int ent = r * G + js;
     __nv_bfloat16* dst = W + n * L.K + k0;
+    if (L.afmt == A_MXFP4) {
+      // the MMA's operand: e2m1 codes in natural order, times 2^(E-127) (exact in bf16)
+      const uint32_t E = rec[L.off_scales + ent];
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t q = (w >> (4 * e)) & 0xFu;
+        const uint32_t mag = q & 7u;
+        float v = mag < 2 ? 0.5f * float(mag) : ldexpf(1.0f + 0.5f * float(mag & 1u), int(mag >> 1) - 1);
+        v = ldexpf(v, int(E) - 127);
+        dst[e] = __float2bfloat16_rn((q & 8u) ? -v : v);
+      }
+      continue;
+    }
     if (L.afmt == A_FP8) {
       // e2m1 -> e4m3 byte shuffle, then value = e4m3 * 2^6 * 2^(E-127) (exact in bf16)
       const uint32_t E = rec[L.off_scales + ent];
@@ -370,6 +386,58 @@ cudaError_t launch_prep_x_f16(const void* X, int64_t rows, int64_t K, int64_t ld
   if (rows <= 0) return cudaSuccess;
   prep_x_f16_kernel<<<unsigned(rows), kPrepThreads, 0, st>>>(
       static_cast<const uint8_t*>(X), K, ldx * 2, static_cast<uint8_t*>(X16), rowscale);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ MXFP4 act quantization
+// One warp per 32-element block (lane = element), 8 warps per block of rows: the block's
+// largest |x| (BF16 magnitude bits), E = floor(log2 amax) - 2 + 127 clamped to [0, 254]
+// (127 for an all-zero block), each x * 2^(127 - E) (exact in FP32) rounded to e2m1 by the
+// hardware conversion (nearest even, saturating at 6).  Codes: byte j of the block holds
+// elements 2j (low nibble) and 2j + 1; blocks of a row past K (up to the exps row's
+// padding to a multiple of 4) get E = 127.
+__global__ void quant_act_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t M, int64_t K,
+                                       int64_t ldx, uint8_t* __restrict__ Xq, int64_t ldq,
+                                       uint8_t* __restrict__ exps, int64_t lde, int64_t nblk_pad) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp_global = (int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nwarps = (int64_t(gridDim.x) * blockDim.x) >> 5;
+  const int64_t nblk = K / 32;
+  for (int64_t t = warp_global; t < M * nblk_pad; t += nwarps) {
+    const int64_t m = t / nblk_pad, b = t % nblk_pad;
+    if (b >= nblk) {                                   // padding block of the exps row
+      if (lane == 0) exps[m * lde + b] = 127;
+      continue;
+    }
+    const uint32_t bits = X[m * ldx + b * 32 + lane];
+    const uint32_t amax = __reduce_max_sync(0xffffffffu, bits & 0x7FFFu);
+    int E = 127;
+    const uint32_t be = (amax >> 7) & 0xFFu;
+    if (amax != 0) {
+      const int lg = be != 0 ? int(be) - 127 : -127 - (__clz(amax & 0x7Fu) - 25);
+      E = max(0, min(254, lg - 2 + 127));
+    }
+    const float v = ldexpf(__uint_as_float(bits << 16), 127 - E);
+    const float hi = __shfl_down_sync(0xffffffffu, v, 1);
+    uint32_t byte = ptx::cvt_e2m1x2_f32(v, hi) & 0xFFu;   // even lanes: elements 2j, 2j + 1
+    // bytes of lanes 8k, 8k+2, 8k+4, 8k+6 -> one 32-bit word at lane 8k
+    const uint32_t b1 = __shfl_down_sync(0xffffffffu, byte, 2);
+    const uint32_t b2 = __shfl_down_sync(0xffffffffu, byte, 4);
+    const uint32_t b3 = __shfl_down_sync(0xffffffffu, byte, 6);
+    if ((lane & 7) == 0)
+      *reinterpret_cast<uint32_t*>(Xq + m * ldq + b * 16 + (lane >> 3) * 4) =
+          byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+    if (lane == 0) exps[m * lde + b] = uint8_t(E);
+  }
+}
+
+cudaError_t launch_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
+                                   int64_t ldq, uint8_t* exps, int64_t lde, cudaStream_t st) {
+  const int64_t nblk_pad = (K / 32 + 3) / 4 * 4;
+  const int64_t warps = M * nblk_pad;
+  const int64_t blocks = std::min<int64_t>((warps + 7) / 8, 152 * 16);
+  quant_act_mxfp4_kernel<<<unsigned(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(
+      static_cast<const uint16_t*>(X), M, K, ldx, Xq, ldq, exps, lde, nblk_pad);
   return cudaGetLastError();
 }
 

@@ -250,6 +250,20 @@ __device__ __forceinline__ void mma_mxf8f6f4_ts_elect(uint32_t d_tmem, uint32_t 
          "r"(accumulate) : "memory");
 }
 
+// Block-scaled FP4 x FP4 MMA (kind::mxf4, one E8M0 scale per 32 K: scale_vec::2X with K = 64
+// per instruction), A and B from shared memory, under one election of a converged warp.
+__device__ __forceinline__ void mma_mxf4_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                  uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P, E;\n setp.ne.b32 P, %6, 0;\n elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%4], [%5], P;\n}\n"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate) : "memory");
+}
+
 __device__ __forceinline__ void mma_commit_elect(uint64_t* bar) {
   asm volatile(
       "{\n .reg .pred E;\n elect.sync _|E, 0xffffffff;\n"
@@ -333,6 +347,26 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor: K-major operand, 64-byte swizzle (rows of 64 bytes,
+// 8-row atoms of 512 bytes at 512-byte strides); `smem_addr` in a 512-byte aligned atom plus
+// a K offset inside the row.
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= uint64_t((smem_addr & 0x3FFFFu) >> 4);        // start address, 16-byte units
+  d |= uint64_t(1) << 16;                            // leading byte offset (unused here)
+  d |= uint64_t(512 >> 4) << 32;                     // stride byte offset: 8 rows x 64 B
+  d |= uint64_t(1) << 46;                            // descriptor version for tcgen05
+  d |= uint64_t(4) << 61;                            // swizzle: 64-byte
+  return d;
+}
+
+// Instruction descriptor, kind::mxf4: D=F32, A=B=E2M1 (format code 1), K-major, scale
+// factors UE8M0 with selectors sfa_id / sfb_id (0 or 2: the byte pair of each 64-K step).
+__host__ __device__ constexpr uint32_t idesc_mxf4(int M, int N, int sfa_id, int sfb_id) {
+  return (uint32_t(sfb_id & 3) << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) |
+         (1u << 23) | (uint32_t(M >> 4) << 24) | (uint32_t(sfa_id & 3) << 29);
+}
+
 // Instruction descriptor, kind::f16: D=F32, A=B=BF16, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
@@ -398,6 +432,13 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t mask, uint3
 __device__ __forceinline__ uint32_t cvt_bf16x2_f32(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// Two floats rounded to e2m1 (nearest even, saturating at +-6): `lo` in the low nibble.
+__device__ __forceinline__ uint32_t cvt_e2m1x2_f32(float lo, float hi) {
+  uint32_t d;
+  asm("{\n .reg .b8 t;\n cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n cvt.u32.u8 %0, t;\n}\n"
+      : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
 __device__ __forceinline__ uint16_t cvt_e4m3x2_f32(float lo, float hi) {

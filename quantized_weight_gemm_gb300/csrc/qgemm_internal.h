@@ -12,6 +12,11 @@
 //   codes  : [4 chunks][128 rows][16 B]; chunk c of row r holds K-elements 32c .. 32c+31
 //            of that row as four 32-bit words of 8 nibbles, the nibbles interleaved so one
 //            mask yields two decoded lanes (dequant.cuh);
+//            MXFP4 activations (W4A4): the tensor core reads the codes straight from shared
+//            memory instead, so they are its operand layout -- K-major rows of 64 bytes
+//            (128 K, element 2j in the low nibble of byte j), 8-row atoms of 512 bytes, the
+//            16-byte piece c of row r at position c ^ ((r >> 1) & 3) of its row (the
+//            64-byte swizzle);
 //   scales : [128 rows][G] entries of S bytes, G = max(1, 128 / group) groups per record,
 //            S = 2 (BF16) or 1 (E8M0, E4M3); a group longer than 128 repeats in each record;
 //   zeros  : (INT4 with zero points only) [128 rows x G] nibbles, entry (r, j) in nibble
@@ -21,6 +26,11 @@
 #pragma once
 
 #include <stdint.h>
+
+#ifndef __CUDACC__
+#define __host__
+#define __device__
+#endif
 
 namespace qgemm {
 
@@ -32,7 +42,13 @@ constexpr int kCodeBytes = kTileN * kStageK / 2; // 8192
 constexpr int kHeaderBytes = 256;
 
 enum WFmt : int32_t { W_INT4_SYM = 0, W_UINT4_ZP = 1, W_MXFP4 = 2, W_MXINT4 = 3, W_NVFP4 = 4 };
-enum AFmt : int32_t { A_BF16 = 0, A_FP8 = 1 };
+enum AFmt : int32_t { A_BF16 = 0, A_FP8 = 1, A_MXFP4 = 2 };
+
+// Byte offset of the 16-byte piece (row r, 32-K chunk c) inside a record's codes.
+inline __host__ __device__ int code_piece_offset(int32_t afmt, int r, int c) {
+  return afmt == A_MXFP4 ? (r >> 3) * 512 + (r & 7) * 64 + ((c ^ ((r >> 1) & 3)) << 4)
+                         : c * (kTileN * 16) + r * 16;
+}
 
 struct PackedHeader {
   uint32_t magic;
@@ -73,7 +89,8 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
                         int64_t N, int64_t K, Layout* L) {
   if (N < 1 || K < 32 || (K % 32) != 0 || N > (int64_t(1) << 31) || K > (int64_t(1) << 30))
     return false;
-  if (afmt != A_BF16 && afmt != A_FP8) return false;
+  if (afmt != A_BF16 && afmt != A_FP8 && afmt != A_MXFP4) return false;
+  if (afmt == A_MXFP4 && wfmt != W_MXFP4) return false;   // W4A4: MXFP4 x MXFP4
   if (wfmt == W_MXFP4) {
     if (sdtype != 1 || group != 32 || has_zp != 0) return false;
   } else if (wfmt == W_MXINT4 || wfmt == W_NVFP4) {

@@ -325,3 +325,32 @@ def test_act_copy_bytes():
                               ("mxfp4", 32, "fp8")]:
         d = qg.WeightDesc(wfmt, 1000, 4096, group, afmt)
         assert qg.act_copy_bytes(d, 100) == 0
+
+
+def test_w4a4_argument_errors_before_any_launch(L):
+    """W4A4 descriptors pair MXFP4 weights with MXFP4 activations only; the GEMM and the
+    activation quantization check their arguments on the host first."""
+    P = ctypes.c_void_p
+    assert qg.check_desc(qg.WeightDesc("mxfp4", 256, 512, 32, "mxfp4")) == 0
+    assert qg.check_desc(qg.WeightDesc("uint4_zp", 256, 512, 128, "mxfp4")) != 0
+    assert qg.check_desc(qg.WeightDesc("nvfp4", 256, 512, 16, "mxfp4")) != 0
+    d = qg.WeightDesc("mxfp4", 256, 512, 32, "mxfp4").c()
+    buf, ex = P(1 << 20), P(1 << 21)
+
+    def w4a4(packed=buf, X=buf, M=8, ldq=256, E=ex, lde=16, Y=buf, ldy=256, desc=d):
+        return L.qgemm_w4a4(ctypes.byref(desc), packed, X, M, ldq, E, lde, None, None, Y, ldy,
+                            None, 0, None)
+
+    assert w4a4(M=-1) == 1 and w4a4(E=None) == 1 and w4a4(packed=None) == 1
+    assert w4a4(ldq=240) == 1                       # ldq < K / 2
+    assert w4a4(lde=12) == 1                        # lde < ceil(K / 128) * 4
+    assert w4a4(X=P((1 << 20) + 8)) == 3            # codes not 16-byte aligned
+    assert w4a4(E=P((1 << 21) + 2)) == 3            # exponents not 4-byte aligned
+    assert w4a4(M=0) == 0
+    bf = qg.WeightDesc("mxfp4", 256, 512, 32, "bf16").c()
+    assert w4a4(desc=bf) == 1                       # a BF16-activation packing
+    q = L.qgemm_quant_act_mxfp4
+    assert q(buf, 4, 500, 512, buf, 256, ex, 16, None) == 1     # K % 32 != 0
+    assert q(buf, 4, 512, 512, buf, 255, ex, 16, None) == 1     # ldq < K / 2
+    assert q(buf, 4, 512, 512, buf, 256, ex, 15, None) == 1     # lde too small
+    assert q(buf, 0, 512, 512, buf, 256, ex, 16, None) == 0     # empty: a no-op

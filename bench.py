@@ -291,40 +291,66 @@ def host_copy_rates(device, nbytes=256 << 20, reps=3):
             "both": round(2 * nbytes / t_both / 1e9, 1), "bytes_per_copy": nbytes}
 
 
-def cpu_sample(seconds=12.0, threads=1):
-    """Time the oracle on a bounded sample in a fresh single-threaded process."""
+_SLAB = None
+
+
+def _oracle_worker(args):
+    """One worker of the CPU baseline: draw two seeded 512-row slabs of the INT4 sweep's
+    format and shape (K, M, group, distributions) once per process, then run the oracle on
+    512-row chunks, cycling over them, for `seconds`; return (rows, seconds)."""
+    global _SLAB
+    wid, seconds = args
+    import oracle
+    import workloads as WL
+    chunk, K, M = 512, 8192, 16
+    if _SLAB is None:
+        _SLAB = WL.int4_asym_shape(2 * chunk, K, M, seed=wid)
+    x, w = _SLAB
+    rows, t0, a = 0, time.perf_counter(), 0
+    while time.perf_counter() - t0 < seconds:
+        oracle.w4a16(x, w.wfmt, w.group, w.codes[a:a + chunk], w.scales[a:a + chunk],
+                     w.zeros[a:a + chunk])
+        rows += chunk
+        a = chunk - a
+    return rows, time.perf_counter() - t0
+
+
+def _oracle_pool(seconds, workers):
+    """Run _oracle_worker on `workers` spawned processes; print rows and wall time."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        pool.map(_oracle_worker, [(i, 0.5) for i in range(workers)])     # imports and inputs
+        t0 = time.perf_counter()
+        res = pool.map(_oracle_worker, [(i, seconds) for i in range(workers)])
+        wall = time.perf_counter() - t0
+    rows = sum(r for r, _ in res)
+    print(json.dumps({"flops": 2.0 * 16 * rows * 8192, "seconds": wall, "rows": rows}))
+
+
+def cpu_sample(seconds=12.0, workers=None):
+    """Time the oracle, as it stands, on a bounded sample in a fresh process that runs one
+    single-threaded worker process per host core; the rate is all workers' flops over the
+    wall time."""
+    if workers is None:
+        workers = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     env = dict(os.environ)
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
-        env[v] = str(threads)
-    code = f"""
-import json, sys, time
-sys.path.insert(0, {ROOT!r})
-import numpy as np
-import oracle, workloads as WL
-N, K, M, g = 28672, 8192, 16, 128
-x, w = WL.int4_asym_shape(N, K, M, seed=0)
-done_rows, flops, t_total = 0, 0.0, 0.0
-chunk = 512
-while t_total < {seconds}:
-    a = done_rows % N
-    b = min(N, a + chunk)
-    t0 = time.perf_counter()
-    y = oracle.w4a16(x, w.wfmt, w.group, w.codes[a:b], w.scales[a:b], w.zeros[a:b])
-    t_total += time.perf_counter() - t0
-    flops += 2.0 * M * (b - a) * K
-    done_rows += b - a
-print(json.dumps({{"flops": flops, "seconds": t_total, "rows": done_rows}}))
-"""
+        env[v] = "1"
+    code = (f"import sys; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"bench._oracle_pool({seconds}, {workers})")
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
-                       timeout=600)
+                       timeout=900)
     if r.returncode != 0:
         raise RuntimeError("oracle sample failed: " + r.stderr[-2000:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["flops"] / d["seconds"] / 1e12, "unit": "TFLOP/s", "cores": threads,
+    return {"value": d["flops"] / d["seconds"] / 1e12, "unit": "TFLOP/s", "cores": workers,
             "kind": "oracle",
-            "sample": (f"float64 numpy oracle, N x K = 28672 x 8192, M = 16: {d['rows']} weight "
-                       f"rows dequantized and multiplied (cycling over the 28672), "
-                       f"{d['seconds']:.1f} s, 1 thread")}
+            "sample": (f"float64 numpy oracle on the INT4 sweep's K = 8192, M = 16 (uint4 + "
+                       f"zero points, group 128): {d['rows']} weight rows dequantized and "
+                       f"multiplied in 512-row chunks by {workers} single-threaded worker "
+                       f"processes (one per host core, each cycling over two seeded 512-row "
+                       f"slabs), {d['seconds']:.1f} s of wall time")}
 
 
 # --------------------------------------------------------------------------- other workloads
@@ -354,12 +380,23 @@ def time_one(fn, flush, reps=5, warm=3):
     return statistics.median(ts)
 
 
-def _row(N, K, M, ms, wbytes, abytes, flops, bw, tc):
+# Datasheet figures of one GB300, for the second roofline fraction of every row (the first
+# is against the measured copy bandwidth and cuBLAS BF16 rate): HBM3e 7.9 TB/s, dense BF16
+# 2.25 PFLOP/s (FP8 twice, FP4 six times that).
+SPEC_HBM, SPEC_BF16 = 7.9e12, 2.25e15
+
+
+def _spec_frac(ms, abytes, flops, factor=1.0):
+    return round(max(abytes / SPEC_HBM, flops / (SPEC_BF16 * factor)) / (ms * 1e-3), 3)
+
+
+def _row(N, K, M, ms, wbytes, abytes, flops, bw, tc, factor=1.0):
     rt = max(abytes / bw, flops / tc)
     return {"N": N, "K": K, "M": M, "us": round(ms * 1e3, 2),
             "tflops": round(flops / (ms * 1e-3) / 1e12, 2),
             "weight_gbs": round(wbytes / (ms * 1e-3) / 1e9, 1),
             "roofline_frac": round(rt / (ms * 1e-3), 3),
+            "roofline_frac_spec": _spec_frac(ms, abytes, flops, factor),
             "bound": "hbm" if abytes / bw > flops / tc else "tensor"}
 
 
@@ -393,7 +430,7 @@ def sweep_mxfp4(device, flush, peaks, fp8):
             else:
                 ms = time_one(lambda: qg.w4a16(d, packed, X[:M], out=Y[:M], ws=ws), flush)
                 ab = wb + M * K * 2 + M * N * 2
-            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc)
+            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc, 2.0 if fp8 else 1.0)
             if fp8:
                 qms = time_one(lambda: qg.quant_act_fp8(X[:M], out=Xq2[:M], scale=ts2[:M]), flush)
                 r["quant_act_us"] = round(qms * 1e3, 2)
@@ -432,7 +469,7 @@ def sweep_w4a4(device, flush, peaks):
         for M in M_SWEEP:
             ms = time_one(lambda: qg.w4a4(d, packed, Xq[:M], E[:M], out=Y[:M], ws=ws), flush)
             ab = wb + M * K // 2 + M * K // 32 + M * N * 2
-            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc)
+            r = _row(N, K, M, ms, wb, ab, 2.0 * M * N * K, bw, tc, 6.0)
             qms = time_one(lambda: qg.quant_act_mxfp4(X[:M], out=Xq2[:M], exps=E2[:M]), flush)
             r["quant_act_us"] = round(qms * 1e3, 2)
             rows.append(r)
@@ -538,7 +575,8 @@ def sweep_moe(device, flush, peaks):
             r.update({"us": round(tot_ms * 1e3, 2),
                       "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 2),
                       "weight_gbs": round(tot_w / (tot_ms * 1e-3) / 1e9, 1),
-                      "roofline_frac": round(max(tot_b / bw, tot_flops / tc) / (tot_ms * 1e-3), 3)})
+                      "roofline_frac": round(max(tot_b / bw, tot_flops / tc) / (tot_ms * 1e-3), 3),
+                      "roofline_frac_spec": _spec_frac(tot_ms, tot_b, tot_flops)})
             rows.append(r)
     torch.cuda.synchronize()
     if qg.device_status(clear=True) != 0:
@@ -623,6 +661,7 @@ def bench_ours(args):
                       "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 2),
                       "weight_gbs": round(weight_bytes(N, K) / (ms * 1e-3) / 1e9, 1),
                       "roofline_frac": round(rt / (ms * 1e-3), 3),
+                      "roofline_frac_spec": _spec_frac(ms, alg_bytes(M, N, K), 2.0 * M * N * K),
                       "bound": "hbm" if alg_bytes(M, N, K) / bw > 2.0 * M * N * K / tc else "tensor",
                       "e2e_us": round(statistics.median(per_e2e[(N, K, M)]) * 1e3, 2)})
     # dominant launch: the call with the largest share of the step's time
@@ -649,7 +688,9 @@ def bench_ours(args):
         "roofline": {"bound": dom["bound"], "achieved": round(achieved_tc, 1),
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": round(achieved_tc / peaks["bf16_tflops"], 3), "traffic": traffic,
-                     "kernel": (f"qgemm_tc_kernel, 256-token tile, uint4+zp BF16: the "
+                     "frac_spec": round(achieved_tc * 1e12 / SPEC_BF16, 3),
+                     "kernel": (f"qgemm_tc_kernel, 256-token tile, uint4+zp on FP16 operands "
+                                f"(the call's time includes its FP16 activation pre-pass): the "
                                 f"N={dom['N']} K={dom['K']} M={dom['M']} call, "
                                 f"{dom['us'] / sum(r['us'] for r in sweep):.0%} of the step"),
                      "algorithmic": "2*M*N*K flops per launch",
@@ -657,6 +698,7 @@ def bench_ours(args):
         "roofline_small_m": {"bound": "hbm", "achieved": round(achieved_bw, 1),
                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
                              "frac": round(achieved_bw / peaks["hbm_gbs"], 3),
+                             "frac_spec": round(achieved_bw * 1e9 / SPEC_HBM, 3),
                              "kernel": "qgemm_tc_kernel<16, bf16> (M <= 16 calls, split-K)",
                              "peak_source": f"hbm_gbs of {peak_kind}"},
         "sweep": sweep,
@@ -718,7 +760,7 @@ def bench_case(args):
     wfmt = parts[3] if len(parts) > 3 else "uint4_zp"
     afmt = parts[4] if len(parts) > 4 else "bf16"
     r = WL.rng(0)
-    x = WL.gen_x(r, M, K)
+    x = WL.gen_x(r, M, K, outliers=afmt != "bf16")
     w = WL.gen_weights(r, wfmt, N, K)
     d = qg.WeightDesc(wfmt, N, K, w.group, afmt)
     scales = torch.from_numpy(w.scales.view(np.int16) if w.scales.dtype == np.uint16 else w.scales)
@@ -727,6 +769,8 @@ def bench_case(args):
     X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
     if afmt == "fp8":
         Xq, ts = qg.quant_act_fp8(X)
+    elif afmt == "mxfp4":
+        Xq, xe = qg.quant_act_mxfp4(X)
     ws = qg.workspace(d, M)
     Y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -739,6 +783,8 @@ def bench_case(args):
         e0.record()
         if afmt == "fp8":
             qg.w4a8(d, packed, Xq, ts, out=Y, ws=ws)
+        elif afmt == "mxfp4":
+            qg.w4a4(d, packed, Xq, xe, out=Y, ws=ws)
         else:
             qg.w4a16(d, packed, X, out=Y, ws=ws)
         e1.record()
@@ -753,6 +799,60 @@ def bench_case(args):
     print(json.dumps({"case": args.case, "us": round(ms * 1e3, 2),
                       "tflops": round(2.0 * M * N * K / (ms * 1e-3) / 1e12, 1),
                       "weight_gbs": round(wb / (ms * 1e-3) / 1e9, 1)}), flush=True)
+
+
+def bench_moe_case(args):
+    """One MoE GEMM of the 256-expert layer, timed alone (profiling aid):
+    --moe T,gate_up|down[,skewed][,indexed]."""
+    import numpy as np
+    import torch
+    import workloads as WL
+    import __graft_entry__ as ge
+    ge.build()
+    import quantized_weight_gemm_gb300 as qg
+    parts = args.moe.split(",")
+    T, gemm = int(parts[0]), parts[1]
+    skewed, indexed = "skewed" in parts[2:], "indexed" in parts[2:]
+    case = WL.moe_case(T, seed=0, skewed=skewed)
+    N, K = (2 * WL.MOE_INTER, WL.MOE_HIDDEN) if gemm == "gate_up" else (WL.MOE_HIDDEN, WL.MOE_INTER)
+    E, R = case.E, len(case.token_of_row)
+    d = qg.WeightDesc("mxfp4", N, K, 32, "bf16")
+    nb = qg.packed_bytes(d)
+    packed = torch.empty(nb * E, dtype=torch.uint8, device="cuda")
+    for e, w in enumerate(WL.iter_moe_weights(E, N, K, seed=0)):
+        qg.repack(d, torch.from_numpy(w.codes).cuda(), torch.from_numpy(w.scales).cuda(), None,
+                  out=packed[e * nb:(e + 1) * nb])
+    off = torch.tensor(case.offsets, device="cuda")
+    if indexed:
+        X = torch.from_numpy(case.x_tok_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        idx = torch.tensor(case.token_of_row.astype(np.int32), device="cuda")
+        call = lambda: qg.moe_indexed(d, packed, E, X, off, idx, out=Y, ws=wsp)
+    else:
+        xb = case.x_bits if gemm == "gate_up" else case.down_bits
+        X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+        call = lambda: qg.moe_grouped(d, packed, E, X, off, out=Y, ws=wsp)
+    wsp = qg.moe_workspace(d, E, R)
+    Y = torch.empty(R, N, dtype=torch.bfloat16, device="cuda")
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    times = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        torch.cuda._sleep(HOLD_CYCLES)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        call()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+    st = qg.device_status(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device status {st}")
+    ms = statistics.median(times)
+    active = int(np.count_nonzero(case.counts))
+    print(json.dumps({"moe": args.moe, "us": round(ms * 1e3, 2), "active_experts": active,
+                      "weight_gbs": round(active * nb / (ms * 1e-3) / 1e9, 1)}), flush=True)
 
 
 def bench_reference(args):
@@ -791,9 +891,13 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the MXFP4, W4A8 and MoE sweeps reported beside the main line")
     ap.add_argument("--case", default=None, help="N,K,M[,wfmt[,afmt]]: time one GEMM shape")
+    ap.add_argument("--moe", default=None,
+                    help="T,gate_up|down[,skewed][,indexed]: time one MoE GEMM of the layer")
     args = ap.parse_args()
     if args.case:
         bench_case(args)
+    elif args.moe:
+        bench_moe_case(args)
     elif args.impl == "reference":
         bench_reference(args)
     else:

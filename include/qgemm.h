@@ -270,8 +270,9 @@ qgemm_status qgemm_w4a8(const qgemm_wdesc* desc, const void* packed, const uint8
  *   X      : device BF16 [M, ldx], K % 32 == 0, ldx >= K
  *   Xq     : device uint8 [M, ldq] codes, ldq >= K / 2, 4-byte aligned rows; element 2j
  *            of a row in the low nibble of byte j
- *   x_exps : device uint8 [M, ld_exps] E8M0 exponents, one per 32 K; ld_exps >=
- *            ceil(K / 128) * 4 (blocks past K up to that are written as 127)
+ *   x_exps : device uint8 [M, ld_exps] E8M0 exponents, one per 32 K, 16-byte aligned;
+ *            ld_exps a multiple of 16 and >= ceil(K / 128) * 4 (blocks past K up to a whole
+ *            128-K block are written as 127; the rest of the row is not touched)
  * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4" (MX formats on Blackwell's tensor
  * cores); the conversion itself is the OCP Microscaling format's.
  */
@@ -285,7 +286,7 @@ qgemm_status qgemm_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t 
  * are exact, the sum is FP32, Y is rounded to BF16 once.
  *   packed : device, from qgemm_repack with desc->wfmt == MXFP4, desc->afmt == QGEMM_A_MXFP4
  *   Xq, ldq, x_exps, ld_exps : from qgemm_quant_act_mxfp4; Xq 16-byte aligned, ldq % 16 == 0,
- *            x_exps 4-byte aligned, ld_exps % 4 == 0
+ *            x_exps 16-byte aligned, ld_exps % 16 == 0 (both are read by TMA)
  *   chan_scale, bias, Y, ldy, ws, ws_bytes, stream : as for qgemm_w4a16
  * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4" (W4A4 on B300 and SM121).
  */

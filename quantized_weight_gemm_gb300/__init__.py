@@ -250,13 +250,14 @@ def w4a8(desc, packed, Xq, tok_scale, chan_scale=None, out=None, ws=None, bias=N
 
 def quant_act_mxfp4(X, out=None, exps=None):
     """MXFP4 activations of BF16 X [M, K]: (codes uint8 [M, K/2], E8M0 exponents uint8
-    [M, ceil(K/128)*4]) (see qgemm_quant_act_mxfp4)."""
+    [M, ceil(K/128)*4 rounded up to 16]) (see qgemm_quant_act_mxfp4)."""
     _row_major(X, "X")
     M, K = X.shape
     if out is None:
         out = torch.empty(M, K // 2, dtype=torch.uint8, device=X.device)
     if exps is None:
-        exps = torch.empty(M, (K // 32 + 3) // 4 * 4, dtype=torch.uint8, device=X.device)
+        exps = torch.empty(M, -(-((K // 32 + 3) // 4 * 4) // 16) * 16, dtype=torch.uint8,
+                           device=X.device)
     _check(lib().qgemm_quant_act_mxfp4(_ptr(X), M, K, X.stride(0), _ptr(out), out.stride(0),
                                        _ptr(exps), exps.stride(0), _stream()), "quant_act_mxfp4")
     return out, exps

@@ -347,8 +347,23 @@ bool make_x4_map(CUtensorMap* m, const void* Xq, int64_t rows, int64_t K, int64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Exponent rows of MXFP4 activations: one byte per 32 K, the kernel reading four at a time.
-int64_t exps_row_min(int64_t K) { return (K / 32 + 3) / 4 * 4; }
+// Exponent rows of MXFP4 activations: one byte per 32 K; the kernel loads them in 16-byte
+// boxes (four 128-K blocks), so a row spans a whole number of boxes.
+int64_t exps_row_min(int64_t K) { return round_up((K / 32 + 3) / 4 * 4, 16); }
+
+// The exponents [rows][ld_exps] bytes for TMA: boxes of 16 bytes x box_rows rows.
+bool make_exps_map(CUtensorMap* m, const void* exps, int64_t rows, int64_t ld_exps,
+                   int box_rows) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[2] = {cuuint64_t(ld_exps), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(ld_exps)};
+  cuuint32_t box[2] = {16, cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(exps), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 qgemm_status check_x(const void* X, bool fp8, int64_t rows, int64_t K, int64_t ldx) {
   if (X == nullptr || rows < 0 || rows >= (int64_t(1) << 31) || ldx < K) return QGEMM_ERR_INVALID_ARG;
@@ -362,7 +377,7 @@ qgemm_status check_x4(const void* Xq, int64_t rows, int64_t K, int64_t ldq, cons
   if (Xq == nullptr || exps == nullptr || rows < 0 || rows >= (int64_t(1) << 31) ||
       ldq < K / 2 || lde < exps_row_min(K))
     return QGEMM_ERR_INVALID_ARG;
-  if (!aligned(Xq, 16) || ldq % 16 != 0 || !aligned(exps, 4) || lde % 4 != 0)
+  if (!aligned(Xq, 16) || ldq % 16 != 0 || !aligned(exps, 16) || lde % 16 != 0)
     return QGEMM_ERR_ALIGNMENT;
   return QGEMM_OK;
 }
@@ -439,6 +454,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, int32_t afmt, const void* packed
   a.x_3d = x3d;
   a.x_exps = x_exps;
   a.ld_exps = ld_exps;
+  if (a4 && !make_exps_map(&a.tmap_e, x_exps, M, ld_exps, plan.token_tile)) return QGEMM_ERR_CUDA;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.M = M;
@@ -601,7 +617,9 @@ qgemm_status qgemm_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t 
   if (X == nullptr || Xq == nullptr || x_exps == nullptr || M < 0 || K < 32 || K % 32 != 0 ||
       ldx < K || ldq < K / 2 || ld_exps < exps_row_min(K) || M >= (int64_t(1) << 31))
     return QGEMM_ERR_INVALID_ARG;
-  if (!aligned(X, 2) || !aligned(Xq, 4) || ldq % 4 != 0) return QGEMM_ERR_ALIGNMENT;
+  if (!aligned(X, 2) || !aligned(Xq, 4) || ldq % 4 != 0 || !aligned(x_exps, 16) ||
+      ld_exps % 16 != 0)
+    return QGEMM_ERR_ALIGNMENT;
   if (M == 0) return QGEMM_OK;
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;

@@ -138,7 +138,10 @@ struct GemmCfg {
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
   static constexpr int kXChunk = BNT <= 32 ? 4 : BNT == 64 ? 2 : 1;
   static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
-  static constexpr int kXSlotBytes = kXChunk * kXBytes;
+  // A4: each stage's activation exponents follow the slot's codes, a 16-byte box (four
+  // 128-K blocks) per token row
+  static constexpr int kXExpBytes = A4 ? BNT * 16 : 0;
+  static constexpr int kXSlotBytes = kXChunk * (kXBytes + kXExpBytes);
   static constexpr int kXBoxSlabs = kXChunk * kSlabs;
   static constexpr int kMiscBytes = 64 + 2 * (kMaxExperts + 1) * 4 + BNT * 8;
   static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
@@ -652,6 +655,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     // ---------------------------------------------------------------- activation producer
     // FP16 operands: the activations come from the pre-pass launched just before
     if constexpr (F16) ptx::grid_dependency_wait();
+    if constexpr (A4)
+      if (lane == 0) ptx::prefetch_tmap(&a.tmap_e);
     if constexpr (GATHER) {
       // Gathered (indexed MoE) tiles: the warp copies each unit's rows out of X in token
       // order, 16 bytes per lane and copy (cp.async), straight into the 128-byte-swizzled
@@ -735,6 +740,15 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           // K offset (elements) of the chunk's first stage: records kb0.., sub-stage h
           const int k0 = w.kb0 * kStageK + i0 * (kStageK / kSub);
           ptx::mbar_arrive_expect_tx(&xfull[rx.slot], uint32_t(C::kXSlotBytes));
+          if constexpr (A4) {
+            // the exponents of each stage: x = 16-byte group of its 128-K block
+#pragma unroll 1
+            for (int sl = 0; sl < C::kXBoxSlabs; ++sl) {
+              const int kb = k0 / kStageK + sl;
+              ptx::tma_load_2d(sx + C::kXChunk * C::kXBytes + sl * C::kXExpBytes, &a.tmap_e,
+                               (kb >> 2) * 16, row0, &xfull[rx.slot], pol_x);
+            }
+          }
           if (a.x_3d) {
             // box {slab, token_tile rows, kXBoxSlabs slabs}; slab index = K / slab width
             ptx::tma_load_3d(sx, &tmap_x, 0, row0, k0 / (A8 ? 128 : 64), &xfull[rx.slot], pol_x);
@@ -867,33 +881,42 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     constexpr int kTokGroups = (BNT + 127) / 128;            // groups of 4 token columns
     uint32_t g = 0;
     bool alive = true;
+    Ring rx;                                             // the X ring, as the issuers walk it
     Unit w;
     int e_hint = -1;
     for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
-      for (int kb = w.kb0; kb < w.kb1; ++kb, ++g) {
-        uint32_t sfb[4 * kTokGroups];
+      const int nst = w.kb1 - w.kb0;
+      for (int x0 = 0; x0 < nst && alive; x0 += XQ) {
+        // the activation exponents of these stages arrive with the slot's codes
+        if (!warp_all(ptx::mbar_wait(&xfull[rx.slot], rx.phase, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        const uint8_t* ex = s_x + rx.slot * C::kXSlotBytes + XQ * C::kXBytes;
+        const int x1 = x0 + XQ < nst ? x0 + XQ : nst;
+        for (int i = x0; i < x1; ++i, ++g) {
+          const int kb = w.kb0 + i;
+          uint32_t sfb[4 * kTokGroups];
 #pragma unroll
-        for (int c = 0; c < 4 * kTokGroups; ++c) {
-          const int j = c * 32 + lane;                   // token of column c in this lane
-          const int64_t m = w.row0 + j;
-          sfb[c] = (j < BNT && m < w.row_end)
-                       ? __ldg(reinterpret_cast<const uint32_t*>(a.x_exps + m * a.ld_exps) + kb)
-                       : 0x7F7F7F7Fu;                  // rows past the tile: 1.0 (codes are 0)
+          for (int c = 0; c < 4 * kTokGroups; ++c) {
+            const int j = c * 32 + lane;                 // token of column c in this lane
+            sfb[c] = j < BNT ? *reinterpret_cast<const uint32_t*>(
+                                   ex + (i - x0) * C::kXExpBytes + j * 16 + (kb & 3) * 4)
+                             : 0x7F7F7F7Fu;              // past the tile (zero codes anyway)
+          }
+          const int rs = int(g % uint32_t(SR)), ca = int(g % uint32_t(SA));
+          if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+          const uint32_t sfa = *reinterpret_cast<const uint32_t*>(s_rec + rs * C::kRecSlot + kCodeBytes + r * 4);
+          ptx::fence_proxy_async_smem();                 // the reads above before the refills
+          if (!warp_all(ptx::mbar_wait(&aempty[ca], ((g / uint32_t(SA)) & 1u) ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+          ptx::tc_fence_after();
+          const uint32_t col = t_lane + uint32_t(C::kACol0 + ca * C::kACols);
+          ptx::tmem_st4(col, sfa, sfa, sfa, sfa);
+#pragma unroll
+          for (int h = 0; h < kTokGroups; ++h)
+            ptx::tmem_st4(col + 4u + 4u * h, sfb[4 * h], sfb[4 * h + 1], sfb[4 * h + 2], sfb[4 * h + 3]);
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          warp_arrive(&afull[ca], lane);
         }
-        const int rs = int(g % uint32_t(SR)), ca = int(g % uint32_t(SA));
-        if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
-        const uint32_t sfa = *reinterpret_cast<const uint32_t*>(s_rec + rs * C::kRecSlot + kCodeBytes + r * 4);
-        ptx::fence_proxy_async_smem();                   // the read above before the refill
-        if (!warp_all(ptx::mbar_wait(&aempty[ca], ((g / uint32_t(SA)) & 1u) ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
-        ptx::tc_fence_after();
-        const uint32_t col = t_lane + uint32_t(C::kACol0 + ca * C::kACols);
-        ptx::tmem_st4(col, sfa, sfa, sfa, sfa);
-#pragma unroll
-        for (int h = 0; h < kTokGroups; ++h)
-          ptx::tmem_st4(col + 4u + 4u * h, sfb[4 * h], sfb[4 * h + 1], sfb[4 * h + 2], sfb[4 * h + 3]);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        warp_arrive(&afull[ca], lane);
+        rx.next(SX);
       }
     }
   } else if (warp < kEpiWarp0) {
@@ -1052,30 +1075,48 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
           // hand the accumulator back to the MMA at once, then store.
           float cs = (n_ok && a.chan_scale != nullptr) ? a.chan_scale[n] : 1.0f;
           if constexpr (DM == DM_NVFP4 || F16) cs *= acc_s;
-          const float b = bias_of(w, n, n_ok);
-          // per-token scales of this warp's columns, lane l holding column l + 32 i (columns
-          // are never gathered rows here), handed to every lane by a shuffle
-          float tk[kCols / 32];
-#pragma unroll
-          for (int i = 0; i < kCols / 32; ++i) {
-            const int64_t m = w.row0 + int64_t(eh) * kCols + i * 32 + lane;
-            tk[i] = (kTokScale && m < w.row_end) ? a.tok_scale[m] : 1.0f;
-          }
           uint32_t packed[kCols / 2];
+          const bool with_bias = a.bias != nullptr;
+          if (!with_bias) {
+            // the accumulator is read, scaled by c[n] and rounded; the per-token scale comes
+            // after the release below (FP16 operands: a power of two, which commutes with the
+            // rounding; FP8: a second rounding, within that path's tolerance)
 #pragma unroll
-          for (int c = 0; c < kCols / 16; ++c) {
-            uint32_t v[16];
-            ptx::tmem_ld16(t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * 16), v);
-            ptx::tmem_wait_ld();
+            for (int c = 0; c < kCols / 16; ++c) {
+              uint32_t v[16];
+              ptx::tmem_ld16(t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * 16), v);
+              ptx::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              float y0 = __uint_as_float(v[j]) * cs, y1 = __uint_as_float(v[j + 1]) * cs;
-              if constexpr (kTokScale) {
-                const int col = c * 16 + j;
-                y0 *= __shfl_sync(0xffffffffu, tk[col / 32], col % 32);
-                y1 *= __shfl_sync(0xffffffffu, tk[(col + 1) / 32], (col + 1) % 32);
+              for (int j = 0; j < 16; j += 2)
+                packed[(c * 16 + j) / 2] =
+                    ptx::pack_bf16x2(__uint_as_float(v[j]) * cs, __uint_as_float(v[j + 1]) * cs);
+            }
+          } else {
+            // with a bias every scale comes before the single rounding: the per-token scales
+            // of this warp's columns are held one per lane (column l + 32 i in lane l; never
+            // gathered rows here) and handed out by shuffles
+            const float b = bias_of(w, n, n_ok);
+            float tk[kCols / 32];
+#pragma unroll
+            for (int i = 0; i < kCols / 32; ++i) {
+              const int64_t m = w.row0 + int64_t(eh) * kCols + i * 32 + lane;
+              tk[i] = (kTokScale && m < w.row_end) ? a.tok_scale[m] : 1.0f;
+            }
+#pragma unroll
+            for (int c = 0; c < kCols / 16; ++c) {
+              uint32_t v[16];
+              ptx::tmem_ld16(t_lane + uint32_t(acc * C::kNumSub * BNT + eh * kCols + c * 16), v);
+              ptx::tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 16; j += 2) {
+                float y0 = __uint_as_float(v[j]) * cs, y1 = __uint_as_float(v[j + 1]) * cs;
+                if constexpr (kTokScale) {
+                  const int col = c * 16 + j;
+                  y0 *= __shfl_sync(0xffffffffu, tk[col / 32], col % 32);
+                  y1 *= __shfl_sync(0xffffffffu, tk[(col + 1) / 32], (col + 1) % 32);
+                }
+                packed[(c * 16 + j) / 2] = ptx::pack_bf16x2(y0 + b, y1 + b);
               }
-              packed[(c * 16 + j) / 2] = ptx::pack_bf16x2(y0 + b, y1 + b);
             }
           }
           ptx::tc_fence_before();
@@ -1085,8 +1126,13 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 #pragma unroll
             for (int j = 0; j < kCols; ++j) {
               const int64_t m = w.row0 + int64_t(eh) * kCols + j;   // (never a gathered tile)
-              if (m < w.row_end)
-                Yh[m * a.ldy] = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
+              if (m < w.row_end) {
+                uint16_t h = uint16_t(j & 1 ? packed[j / 2] >> 16 : packed[j / 2] & 0xFFFFu);
+                if (kTokScale && !with_bias)
+                  h = uint16_t(ptx::pack_bf16x2(__uint_as_float(uint32_t(h) << 16) * a.tok_scale[m],
+                                                0.0f) & 0xFFFFu);
+                Yh[m * a.ldy] = h;
+              }
             }
           }
           continue;

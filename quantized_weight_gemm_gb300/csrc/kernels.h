@@ -72,9 +72,11 @@ struct GemmArgs {
   int64_t bias_stride;
   const float* tok_scale;      // [M] (FP8 activations) or nullptr
   // MXFP4 activations (W4A4): E8M0 exponents, row m at x_exps + m * ld_exps bytes, one
-  // 32-bit word (four exponents) per 128-K block
+  // 32-bit word (four exponents) per 128-K block; tmap_e describes them for TMA as a 2-D
+  // uint8 tensor [rows][ld_exps] loaded in boxes of 16 bytes (four blocks) x token_tile rows
   const uint8_t* x_exps;
   int64_t ld_exps;
+  CUtensorMap tmap_e;
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
   // Partial sums of the tiles whose K range is cut over several CTAs: one slot per

@@ -433,7 +433,7 @@ __global__ void quant_act_mxfp4_kernel(const uint16_t* __restrict__ X, int64_t M
 
 cudaError_t launch_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
                                    int64_t ldq, uint8_t* exps, int64_t lde, cudaStream_t st) {
-  const int64_t nblk_pad = (K / 32 + 3) / 4 * 4;
+  const int64_t nblk_pad = (K / 32 + 3) / 4 * 4;      // whole 128-K blocks (the GEMM reads words)
   const int64_t warps = M * nblk_pad;
   const int64_t blocks = std::min<int64_t>((warps + 7) / 8, 152 * 16);
   quant_act_mxfp4_kernel<<<unsigned(std::max<int64_t>(blocks, 1)), 256, 0, st>>>(

@@ -345,7 +345,8 @@ def test_w4a4_argument_errors_before_any_launch(L):
     assert w4a4(ldq=240) == 1                       # ldq < K / 2
     assert w4a4(lde=12) == 1                        # lde < ceil(K / 128) * 4
     assert w4a4(X=P((1 << 20) + 8)) == 3            # codes not 16-byte aligned
-    assert w4a4(E=P((1 << 21) + 2)) == 3            # exponents not 4-byte aligned
+    assert w4a4(E=P((1 << 21) + 8)) == 3            # exponents not 16-byte aligned
+    assert w4a4(lde=24) == 3                        # exponent rows not a multiple of 16
     assert w4a4(M=0) == 0
     bf = qg.WeightDesc("mxfp4", 256, 512, 32, "bf16").c()
     assert w4a4(desc=bf) == 1                       # a BF16-activation packing

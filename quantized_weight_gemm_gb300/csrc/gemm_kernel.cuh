@@ -29,11 +29,11 @@
 //               brings several stages at once.  Indexed MoE (the GATHER instantiations,
 //               token tiles up to 64): the whole warp copies the rows that the row index
 //               names with cp.async, 16 bytes per lane, into the same swizzled layout.
-//   record      2 warps (one thread each, alternate stages): one bulk copy per stage of the
-//   producers   packed weight record (codes, scales and zero points of 128 weight rows x
-//               128 K, see qgemm_internal.h) into the record ring, which is deep (up to 16
-//               slots) so that many weight bytes are in flight: small batches are bound by
-//               HBM.
+//   record      1 warp: one bulk copy per stage of the packed weight record (codes, scales
+//   producer    and zero points of 128 weight rows x 128 K, see qgemm_internal.h) into the
+//               record ring, four lanes issuing four consecutive stages at once.  The ring is
+//               deep (up to 16 slots) so that many weight bytes are in flight: small batches
+//               are bound by HBM.
 //
 // Every role walks the CTA's units in the same order (unit_at); the schedule is computed
 // once into shared memory after the prologue.
@@ -68,7 +68,7 @@ namespace qgemm {
 #define QGEMM_ISSUERS_NARROW 4
 #endif
 // Warp roles, in this order: the dequant warpgroups, the four epilogue warps, the MMA
-// issuers, the activation producer and the two record producers.  Groups of four start at a
+// issuers, the activation producer and the record producer.  Groups of four start at a
 // multiple of 4, so `warp & 3` is the tensor-memory lane quarter a warp may access.  Every
 // SM sub-partition holds a quarter of the warps and of the 64 K registers, so more warps
 // leave fewer registers per thread.
@@ -87,13 +87,17 @@ struct Roles {
   static constexpr int kIssuerWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kXProducerWarp = kIssuerWarp0 + kIssuers;
   static constexpr int kRecProducerWarp0 = kXProducerWarp + 1;
-  static constexpr int kWarps = kRecProducerWarp0 + 2;
+  static constexpr int kWarps = kRecProducerWarp0 + 1;
   static constexpr int kThreads = kWarps * 32;
 };
 constexpr int kMaxExperts = 1024;
 // Sleep between polls of a barrier, per role (ns): roles on the critical path poll often,
 // the others sleep longer so the dequant warps keep the issue slots.
-constexpr uint32_t kSleepDequant = 32, kSleepMma = 32, kSleepProducer = 128, kSleepEpilogue = 256;
+#ifndef QGEMM_SLEEP_EPI
+#define QGEMM_SLEEP_EPI 256
+#endif
+constexpr uint32_t kSleepDequant = 32, kSleepMma = 32, kSleepProducer = 128,
+                   kSleepEpilogue = QGEMM_SLEEP_EPI;
 constexpr int kRecTail = kTileN * 4 * 2 + kTileN * 4 / 2;           // largest scales + zeros
 
 constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
@@ -148,8 +152,8 @@ struct GemmCfg {
   static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
                                 kAStages * kBarBytesPerA + kMiscBytes + 64;
   static constexpr int kRMax0 = (227 * 1024 - kFixed) / (kRecSlot + kBarBytesPerR);
-  // record ring: producer g % 2, dequant warpgroup g % kDeqWGs (same rule as above)
-  static constexpr int kRLcm = lcm_int(2, kDeqWGs);
+  // record ring: dequant warpgroup g % kDeqWGs (same rule as above)
+  static constexpr int kRLcm = kDeqWGs;
   static constexpr int kRMax = kRMax0 / kRLcm * kRLcm;
   static constexpr int kRStages = kRMax < 16 / kRLcm * kRLcm ? kRMax : 16 / kRLcm * kRLcm;
   static constexpr int kACol0 = (kAccCols + 31) / 32 * 32;
@@ -608,48 +612,67 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   const Sched& sc = *sched;
 
   if (warp >= RO::kRecProducerWarp0) {
-    // ---------------------------------------------------------------- record producers
-    const int rp = warp - RO::kRecProducerWarp0;   // takes the stages g with g % 2 == rp
-    if (lane == 0) {
-      const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
-      const uint32_t rec_bytes = uint32_t(L.record_bytes);
-      const uint32_t tail_bytes = rec_bytes - uint32_t(kCodeBytes);     // scales + zeros
-      const uint32_t stage_tx = CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
-      Ring rr;
-      uint32_t pending = 0, pending_parity = 0;   // copies in flight, for the wind-down
-      uint32_t g = 0;                             // stage counter of this CTA
-      bool alive = true;
-      Unit w;
-      int e_hint = -1;
-      for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
-        const uint8_t* rec = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
-                             (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
-        for (int kb = w.kb0; kb < w.kb1 && alive; ++kb, rec += rec_bytes) {
-#pragma unroll 1
-          for (int h = 0; h < kSub; ++h, ++g) {
-            if ((g & 1u) != uint32_t(rp)) { rr.next(SR); continue; }
-            if (!ptx::mbar_wait(&rempty[rr.slot], rr.phase ^ 1u, abort_flag, T, kSleepProducer)) { alive = false; break; }
-            uint8_t* sr = s_rec + rr.slot * C::kRecSlot;
-            ptx::mbar_arrive_expect_tx(&rfull[rr.slot], stage_tx);
+    // ---------------------------------------------------------------- record producer
+    // One warp walks the stages in order, kCopyLanes consecutive stages of a unit at a
+    // time, one lane per stage: the lanes issue their bulk copies together.  Issuing a copy
+    // keeps its thread busy for a few hundred cycles, and copies issued by different lanes
+    // overlap, so one SM streams about twice as many bytes per cycle as from a single
+    // thread.  The warp stays converged from one group to the next, so the waits on any
+    // one slot follow the stage order, whichever lane makes them.
+    constexpr int kCopyLanes = 4;
+    const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
+    const uint32_t rec_bytes = uint32_t(L.record_bytes);
+    const uint32_t tail_bytes = rec_bytes - uint32_t(kCodeBytes);     // scales + zeros
+    const uint32_t stage_tx = CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
+    uint32_t pend = 0, pend_par = 0;    // slots with a copy in flight (warp-uniform), for the wind-down
+    uint32_t g0 = 0;                    // CTA stage counter at the unit start
+    bool alive = true;
+    Unit w;
+    int e_hint = -1;
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+      const uint8_t* rec0 = a.packed + int64_t(w.expert) * a.expert_stride + kHeaderBytes +
+                            (int64_t(w.nt) * L.k_blocks + w.kb0) * int64_t(rec_bytes);
+      const int nst = (w.kb1 - w.kb0) * kSub;
+      for (int i0 = 0; i0 < nst; i0 += kCopyLanes) {
+        const int i = i0 + lane;                        // this lane's stage of the unit
+        const uint32_t g = g0 + uint32_t(i);
+        const int slot = int(g % uint32_t(SR));
+        const uint32_t ph = (g / uint32_t(SR)) & 1u;
+        bool ok = true, issued = false;
+        if (lane < kCopyLanes && i < nst) {
+          ok = ptx::mbar_wait(&rempty[slot], ph ^ 1u, abort_flag, T, kSleepProducer);
+          if (ok) {
+            const uint8_t* rec = rec0 + int64_t(i / kSub) * rec_bytes;
+            uint8_t* sr = s_rec + slot * C::kRecSlot;
+            ptx::mbar_arrive_expect_tx(&rfull[slot], stage_tx);
             if (CH == 4) {
-              ptx::bulk_g2s(sr, rec, rec_bytes, &rfull[rr.slot], pol_w);
+              ptx::bulk_g2s(sr, rec, rec_bytes, &rfull[slot], pol_w);
             } else {
               // half record: codes of record chunks 2h, 2h+1, then the scales and zeros
-              ptx::bulk_g2s(sr, rec + h * (kCodeBytes / 2), kCodeBytes / 2, &rfull[rr.slot], pol_w);
-              ptx::bulk_g2s(sr + kTail, rec + kCodeBytes, tail_bytes, &rfull[rr.slot], pol_w);
+              const int h = i % kSub;
+              ptx::bulk_g2s(sr, rec + h * (kCodeBytes / 2), kCodeBytes / 2, &rfull[slot], pol_w);
+              ptx::bulk_g2s(sr + kTail, rec + kCodeBytes, tail_bytes, &rfull[slot], pol_w);
             }
-            pending |= 1u << rr.slot;
-            pending_parity = (pending_parity & ~(1u << rr.slot)) | (rr.phase << rr.slot);
-            rr.next(SR);
+            issued = true;
           }
         }
+        // the slots of this group's copies, the same in every lane
+        const uint32_t iss = __ballot_sync(0xffffffffu, issued);
+        for (uint32_t m = iss; m != 0; m &= m - 1) {
+          const uint32_t gj = g0 + uint32_t(i0 + __ffs(m) - 1);
+          const uint32_t sj = gj % uint32_t(SR);
+          pend |= 1u << sj;
+          pend_par = (pend_par & ~(1u << sj)) | (((gj / uint32_t(SR)) & 1u) << sj);
+        }
+        if (!warp_all(ok)) { alive = false; break; }
       }
-      if (!alive) {
-        volatile int no_abort = 0;      // let every copy this thread issued land first
-        for (int s = 0; s < SR; ++s)
-          if (pending & (1u << s))
-            ptx::mbar_wait(&rfull[s], (pending_parity >> s) & 1u, &no_abort, 200000000ull);
-      }
+      g0 += uint32_t(nst);
+    }
+    if (!alive && lane == 0) {
+      volatile int no_abort = 0;        // let every copy the warp issued land first (each
+      for (int s = 0; s < SR; ++s)      // slot's last use: earlier ones were consumed)
+        if (pend & (1u << s))
+          ptx::mbar_wait(&rfull[s], (pend_par >> s) & 1u, &no_abort, 200000000ull);
     }
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer

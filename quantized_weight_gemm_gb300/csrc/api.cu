@@ -95,7 +95,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Schedules (T = m_tiles * n_tiles tiles of k_blocks 128-K records each):
 //   uniform  every tile cut into s equal K parts (s = 1: plain data-parallel), unit u on
 //            CTA u % P: time ~ T0 + ceil(T s / P) (ceil(k_blocks / s) stage + unit
-//                                                  + [s > 1] s tile reduce)
+//                                                  + [s > 1] (reduce + s tile reduce))
 //   stream-K the records of the T mod P leftover tiles (all T when T < P) are dealt out
 //            evenly over the P CTAs, which then take the remaining whole tiles:
 //            time ~ T0 + (records per CTA) stage + (units per CTA) unit
@@ -108,6 +108,10 @@ constexpr int kTiles[5] = {16, 32, 64, 128, 256};
 constexpr double kStageUs[5] = {0.326, 0.330, 0.353, 0.401, 0.657};  // per 128-K block
 constexpr double kUnitUs[5] = {3.08, 6.11, 7.88, 10.05, 17.59};      // per unit
 constexpr double kReduceUsPerSplitRow = 0.0716;
+// A cut tile's last contributor also waits for the others' partial tiles and reads them
+// back from L2: 1 to 1.5 us more than a whole tile's epilogue (per-CTA timestamps of
+// 16-token tiles cut in two).
+constexpr double kReduceFixedUs = 1.0;
 constexpr double kCallUs = 6.44;
 constexpr int kMaxContrib = 8;       // stream-K (unforced): at most this many CTAs per tile
 }  // namespace
@@ -151,7 +155,7 @@ double plan_cost_us(const Layout& L, int64_t M, int ti, int splits, int sms) {
   const int64_t per_cta = (units + sms - 1) / sms;
   const int64_t kpu = (L.k_blocks + splits - 1) / splits;
   double unit = double(kpu) * kStageUs[ti] + kUnitUs[ti];
-  if (splits > 1) unit += double(splits) * double(tt) * kReduceUsPerSplitRow;
+  if (splits > 1) unit += kReduceFixedUs + double(splits) * double(tt) * kReduceUsPerSplitRow;
   return kCallUs + double(per_cta) * unit;
 }
 
@@ -170,7 +174,7 @@ double sk_cost_us(const Layout& L, int64_t M, int ti, int sms, SkShape* out) {
   *out = sh;
   if (sh.sk_tiles == 0 || (sh.max_contrib > kMaxContrib && g_force_splits >= 0)) return 1e300;
   double c = kCallUs + double(sh.max_records) * kStageUs[ti] + double(sh.max_units) * kUnitUs[ti];
-  if (T < sms) c += double(sh.max_contrib) * double(tt) * kReduceUsPerSplitRow;
+  if (T < sms) c += kReduceFixedUs + double(sh.max_contrib) * double(tt) * kReduceUsPerSplitRow;
   return c;
 }
 

@@ -400,9 +400,11 @@ def _row(N, K, M, ms, wbytes, abytes, flops, bw, tc, factor=1.0):
             "bound": "hbm" if abytes / bw > flops / tc else "tensor"}
 
 
-def sweep_mxfp4(device, flush, peaks, fp8):
-    """The MXFP4 dense sweep: W4A16 (BF16 X) or W4A8 (per-token FP8 X with 1% outliers),
-    N x K in {4096 x 7168, 7168 x 2048}, M = 1..8192."""
+def sweep_mxfp4(device, flush, peaks, afmt):
+    """The MXFP4 dense sweep: W4A16 (afmt "bf16": BF16 X) or W4A8 (per-token FP8 X with 1%
+    outliers; afmt "fp8": weights widened to e4m3 in registers, "fp8n": weights as FP4
+    tensor-core operands), N x K in {4096 x 7168, 7168 x 2048}, M = 1..8192."""
+    fp8 = afmt != "bf16"
     import numpy as np
     import torch
     import workloads as WL
@@ -413,7 +415,7 @@ def sweep_mxfp4(device, flush, peaks, fp8):
     Mmax = max(M_SWEEP)
     for (N, K) in MX_SHAPES:
         x, w = WL.mxfp4_shape(N, K, Mmax, seed=0, outliers=fp8)
-        d = qg.WeightDesc("mxfp4", N, K, 32, "fp8" if fp8 else "bf16")
+        d = qg.WeightDesc("mxfp4", N, K, 32, afmt)
         packed = qg.repack(d, torch.from_numpy(w.codes).to(device),
                            torch.from_numpy(w.scales).to(device))
         X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(device)
@@ -625,8 +627,9 @@ def bench_ours(args):
     if not args.no_extra:
         del cases
         torch.cuda.empty_cache()
-        extra = {"mxfp4_a16": sweep_mxfp4(device, flush, peaks, fp8=False),
-                 "mxfp4_a8": sweep_mxfp4(device, flush, peaks, fp8=True),
+        extra = {"mxfp4_a16": sweep_mxfp4(device, flush, peaks, "bf16"),
+                 "mxfp4_a8": sweep_mxfp4(device, flush, peaks, "fp8"),
+                 "mxfp4_a8n": sweep_mxfp4(device, flush, peaks, "fp8n"),
                  "w4a4": sweep_w4a4(device, flush, peaks),
                  "mxint4_a16": sweep_w4a16_fmt(device, flush, peaks, "mxint4"),
                  "nvfp4_a16": sweep_w4a16_fmt(device, flush, peaks, "nvfp4"),
@@ -729,6 +732,10 @@ def bench_ours(args):
                                       "same shapes; quant_act_us = the separate quantization call; "
                                       "roofline tensor peak = 2 x measured bf16"),
                          "sweep": extra["mxfp4_a8"]},
+            "mxfp4_a8n": {"workload": ("dense W4A8 as mxfp4_a8, the e2m1 weights fed to the "
+                                       "tensor core as FP4 operands of the block-scaled "
+                                       "FP8/FP6/FP4 MMA (no register decode)"),
+                          "sweep": extra["mxfp4_a8n"]},
             "mxint4_a16": {"workload": ("dense W4A16 MXINT4 (two's-complement nibbles, E8M0 per "
                                         "32), same shapes"),
                            "sweep": extra["mxint4_a16"]},
@@ -767,7 +774,7 @@ def bench_case(args):
     packed = qg.repack(d, torch.from_numpy(w.codes).cuda(), scales.cuda(),
                        None if w.zeros is None else torch.from_numpy(w.zeros).cuda())
     X = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
-    if afmt == "fp8":
+    if afmt in ("fp8", "fp8n"):
         Xq, ts = qg.quant_act_fp8(X)
     elif afmt == "mxfp4":
         Xq, xe = qg.quant_act_mxfp4(X)
@@ -781,7 +788,7 @@ def bench_case(args):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
-        if afmt == "fp8":
+        if afmt in ("fp8", "fp8n"):
             qg.w4a8(d, packed, Xq, ts, out=Y, ws=ws)
         elif afmt == "mxfp4":
             qg.w4a4(d, packed, Xq, xe, out=Y, ws=ws)

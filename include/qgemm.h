@@ -62,15 +62,19 @@ typedef enum {
   QGEMM_W_NVFP4 = 4
 } qgemm_wfmt;
 typedef enum { QGEMM_SCALE_BF16 = 0, QGEMM_SCALE_E8M0 = 1, QGEMM_SCALE_E4M3 = 2 } qgemm_sdtype;
-typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1, QGEMM_A_MXFP4 = 2 } qgemm_afmt;
+typedef enum {
+  QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1, QGEMM_A_MXFP4 = 2,
+  QGEMM_A_FP8E4M3_TOKEN_FP4MMA = 3
+} qgemm_afmt;
 
 /*
  * Weight descriptor ("layer config"): one quantized weight matrix W of logical shape
  * [N, K] (Y = X . W^T).  Supported combinations:
  *   wfmt INT4_SYM : sdtype BF16, has_zp 0, group_size 32 or a multiple of 64, K % group == 0
  *   wfmt UINT4_ZP : sdtype BF16, has_zp 1, group_size as above
- *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32 (afmt BF16, FP8E4M3_TOKEN, or
- *                   MXFP4 for W4A4; only MXFP4 weights pair with MXFP4 activations)
+ *   wfmt MXFP4    : sdtype E8M0, has_zp 0, group_size 32 (afmt BF16, FP8E4M3_TOKEN,
+ *                   FP8E4M3_TOKEN_FP4MMA, or MXFP4 for W4A4; only MXFP4 weights pair with
+ *                   FP8 or MXFP4 activations)
  *   wfmt MXINT4   : sdtype E8M0, has_zp 0, group_size 32, afmt BF16
  *                   (w = q * 2^(e - 127), q the two's-complement nibble)
  *   wfmt NVFP4    : sdtype E4M3, has_zp 0, group_size 16, afmt BF16
@@ -78,7 +82,13 @@ typedef enum { QGEMM_A_BF16 = 0, QGEMM_A_FP8E4M3_TOKEN = 1, QGEMM_A_MXFP4 = 2 } 
  * K must be a multiple of 32; N >= 1 is arbitrary (the packed form pads it).
  * MXINT4 and NVFP4 are the formats of the B300 MoE results in "Humming wird
  * angekündigt", section "WnA16".
- * afmt names the activation format the packed weights will be multiplied with.
+ * afmt names the activation format the packed weights will be multiplied with.  The two FP8
+ * forms are two W4A8 kernels for the same arithmetic: FP8E4M3_TOKEN widens each e2m1 weight
+ * to an e4m3 byte in registers and feeds the tensor core FP8 x FP8; FP8E4M3_TOKEN_FP4MMA
+ * keeps the weights as they are and feeds them to the tensor core as FP4 operands of the
+ * block-scaled FP8/FP6/FP4 MMA (no decode, the weight codes go from HBM to shared memory by
+ * TMA).  qgemm_w4a8 and the MoE calls with QGEMM_A_FP8E4M3_TOKEN activations accept either
+ * packing.
  * flags: QGEMM_FLAG_BATCH_INVARIANT (below) or 0; other bits are invalid.  The packed form
  * does not depend on flags.
  */
@@ -252,7 +262,8 @@ qgemm_status qgemm_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ld
 /*
  * Dense W4A8 (MXFP4 weights x tokenwise FP8 activations):
  *   Y[m, n] = tok_scale[m] * c[n] * sum_k e4m3(Xq[m, k]) * W[n, k] + b[n]
- *   packed : device, from qgemm_repack with desc->wfmt == MXFP4, desc->afmt == FP8E4M3_TOKEN
+ *   packed : device, from qgemm_repack with desc->wfmt == MXFP4 and desc->afmt ==
+ *            FP8E4M3_TOKEN or FP8E4M3_TOKEN_FP4MMA (the kernel follows the packing)
  *   Xq     : device uint8 e4m3 [M, ldx], 16-byte aligned, ldx % 16 == 0
  *   tok_scale : device float32 [M];  other arguments as for qgemm_w4a16.
  * "Humming wird angekündigt", section "W8A8 / W4A8 / W4A4".
@@ -301,7 +312,7 @@ qgemm_status qgemm_w4a4(const qgemm_wdesc* desc, const void* packed, const uint8
  *   desc           : per-expert weight descriptor (all experts share it)
  *   packed         : device, E packed matrices, expert e at e * qgemm_packed_bytes(desc)
  *   afmt           : QGEMM_A_BF16 (X is BF16) or QGEMM_A_FP8E4M3_TOKEN (X is e4m3 and
- *                    tok_scale holds one float32 per row)
+ *                    tok_scale holds one float32 per row; desc->afmt either FP8 form)
  *   X              : device [R, ldx] sorted rows; padding rows should be zero
  *   bias           : device float32 [E][N] (expert e's bias at e * N), added to that
  *                    expert's rows after every scale, or NULL

@@ -24,7 +24,7 @@ _LIB_PATH = os.path.join(_PKG, "_lib", "libqgemm.so")
 
 WFMT = {"int4_sym": 0, "uint4_zp": 1, "mxfp4": 2, "mxint4": 3, "nvfp4": 4}
 SDTYPE = {"int4_sym": 0, "uint4_zp": 0, "mxfp4": 1, "mxint4": 1, "nvfp4": 2}   # BF16, E8M0, E4M3
-AFMT = {"bf16": 0, "fp8": 1, "mxfp4": 2}
+AFMT = {"bf16": 0, "fp8": 1, "mxfp4": 2, "fp8n": 3}   # fp8n: W4A8 on FP4 tensor-core operands
 EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packed_bytes",
            "qgemm_repack", "qgemm_workspace_bytes", "qgemm_w4a16", "qgemm_quant_act_fp8",
            "qgemm_w4a8", "qgemm_moe_grouped", "qgemm_dequant_debug", "qgemm_device_status",

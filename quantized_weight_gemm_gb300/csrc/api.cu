@@ -90,6 +90,11 @@ bool layout_of(const qgemm_wdesc* d, Layout* L) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+// FP4-operand records are addressed by a 32-bit tensor coordinate.
+bool fp4_operand_records_fit(const Layout& L) {
+  return L.afmt != A_FP8N || L.n_tiles * L.k_blocks < (int64_t(1) << 31);
+}
+
 // ---------------------------------------------------------------- dispatch
 // Token tile and schedule from a cost model of one call on a persistent grid of P CTAs.
 // Schedules (T = m_tiles * n_tiles tiles of k_blocks 128-K records each):
@@ -351,6 +356,24 @@ bool make_x4_map(CUtensorMap* m, const void* Xq, int64_t rows, int64_t K, int64_
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// FP8 activations on FP4 operands: the packed codes of E experts as a 4-D tensor of 4-bit
+// elements [E][records][128 rows][128], rows 64 bytes apart, records record_bytes and experts
+// expert_stride bytes apart; a box is one record, which the TMA writes as 128-byte rows (16
+// elements in the first 8 bytes of every 16) with the 128-byte swizzle.
+bool make_w4_map(CUtensorMap* m, const Layout& L, const void* packed, int32_t E,
+                 int64_t expert_stride) {
+  EncodeFn enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[4] = {128, 128, cuuint64_t(L.n_tiles * L.k_blocks), cuuint64_t(E)};
+  cuuint64_t strides[3] = {64, cuuint64_t(L.record_bytes), cuuint64_t(expert_stride)};
+  cuuint32_t box[4] = {128, 128, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  void* base = const_cast<uint8_t*>(static_cast<const uint8_t*>(packed) + kHeaderBytes);
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 4, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Exponent rows of MXFP4 activations: one byte per 32 K; the kernel loads them in 16-byte
 // boxes (four 128-K blocks), so a row spans a whole number of boxes.
 int64_t exps_row_min(int64_t K) { return round_up((K / 32 + 3) / 4 * 4, 16); }
@@ -398,8 +421,10 @@ qgemm_status check_dense(const qgemm_wdesc* desc, int32_t afmt, const void* pack
                          const float* chan_scale, const float* bias, const void* Y, int64_t ldy,
                          Layout* L, const uint8_t* x_exps = nullptr, int64_t ld_exps = 0) {
   if (!layout_of(desc, L)) return QGEMM_ERR_INVALID_ARG;
-  if (L->afmt != afmt) return QGEMM_ERR_INVALID_ARG;
   const bool fp8 = afmt == A_FP8;
+  // FP8 activations run on either W4A8 packing: register-decoded or FP4 operands
+  if (L->afmt != afmt && !(fp8 && L->afmt == A_FP8N)) return QGEMM_ERR_INVALID_ARG;
+  if (!fp4_operand_records_fit(*L)) return QGEMM_ERR_UNSUPPORTED;
   if (fp8 && L->wfmt != W_MXFP4) return QGEMM_ERR_UNSUPPORTED;
   if (M < 0) return QGEMM_ERR_INVALID_ARG;
   if (packed == nullptr) return QGEMM_ERR_INVALID_ARG;
@@ -459,6 +484,7 @@ qgemm_status run_dense(const qgemm_wdesc* desc, int32_t afmt, const void* packed
   a.x_exps = x_exps;
   a.ld_exps = ld_exps;
   if (a4 && !make_exps_map(&a.tmap_e, x_exps, M, ld_exps, plan.token_tile)) return QGEMM_ERR_CUDA;
+  if (L.afmt == A_FP8N && !make_w4_map(&a.tmap_w, L, packed, 1, L.total_bytes)) return QGEMM_ERR_CUDA;
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.M = M;
@@ -660,7 +686,8 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   if (!layout_of(desc, &L)) return QGEMM_ERR_INVALID_ARG;
   const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
   if (afmt != QGEMM_A_BF16 && !fp8) return QGEMM_ERR_INVALID_ARG;
-  if (L.afmt != afmt) return QGEMM_ERR_INVALID_ARG;
+  if (L.afmt != afmt && !(fp8 && L.afmt == A_FP8N)) return QGEMM_ERR_INVALID_ARG;
+  if (!fp4_operand_records_fit(L)) return QGEMM_ERR_UNSUPPORTED;
   if (E < 1 || E > 1024 || packed == nullptr || expert_offsets == nullptr || R < 0 || x_rows < 0)
     return QGEMM_ERR_INVALID_ARG;
   if (row_index != nullptr && R > 0 && x_rows == 0) return QGEMM_ERR_INVALID_ARG;
@@ -722,6 +749,7 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   a.L = L;
   a.packed = static_cast<const uint8_t*>(packed);
   a.expert_stride = L.total_bytes;
+  if (L.afmt == A_FP8N && !make_w4_map(&a.tmap_w, L, packed, E, L.total_bytes)) return QGEMM_ERR_CUDA;
   a.offsets = expert_offsets;
   a.row_index = row_index;
   a.E = E;

@@ -10,10 +10,13 @@ cudaError_t launch_gemm_a16_mxfp4(const GemmPlan&, const CUtensorMap&, const Gem
 cudaError_t launch_gemm_a16_mxint4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a16_nvfp4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_a8n(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
                         const GemmArgs& args, cudaStream_t st) {
-  if (fp8) return launch_gemm_impl<true, DM_MXFP4>(plan, tmap, args, st);
+  if (fp8)
+    return decode_mode(args.L) == DM_W4A8N ? launch_gemm_a8n(plan, tmap, args, st)
+                                           : launch_gemm_impl<true, DM_MXFP4>(plan, tmap, args, st);
   switch (decode_mode(args.L)) {
     case DM_INT4_ZP_G1: return launch_gemm_a16_zp_g1(plan, tmap, args, st);
     case DM_INT4_SYM_G1: return launch_gemm_a16_sym_g1(plan, tmap, args, st);

@@ -72,14 +72,15 @@ namespace qgemm {
 // multiple of 4, so `warp & 3` is the tensor-memory lane quarter a warp may access.  Every
 // SM sub-partition holds a quarter of the warps and of the 64 K registers, so more warps
 // leave fewer registers per thread.
-// A4 (W4A4, MXFP4 activations): no register decode -- one warpgroup moves the E8M0 scale
-// factors into tensor memory, and one issuer runs two FP4 MMAs per stage.
-template <int BNT, bool A4 = false>
+// Direct operands (W4A4, and FP8 activations on FP4 operands): no register decode -- the
+// MMA reads the weight codes from shared memory, one warpgroup moves the E8M0 scale
+// factors into tensor memory, and one issuer runs the stage's MMAs.
+template <int BNT, bool D = false>
 struct Roles {
-  static constexpr int kDeqWGs = A4 ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
+  static constexpr int kDeqWGs = D ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
-  static constexpr int kIssuers = A4 ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
+  static constexpr int kIssuers = D ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
   // Wide token tiles have one accumulator buffer (or two of 128 columns): two epilogue
   // warps per lane quarter drain it twice as fast, so the MMA waits less for it.
   static constexpr int kEpiWarps = BNT >= 128 ? 8 : 4;
@@ -103,24 +104,29 @@ constexpr int kRecTail = kTileN * 4 * 2 + kTileN * 4 / 2;           // largest s
 constexpr int gcd_int(int a, int b) { return b == 0 ? a : gcd_int(b, a % b); }
 constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
 
-template <int BNT, bool A8, bool A4 = false>
+// A4: W4A4 (MXFP4 activations).  N8: FP8 activations on FP4 operands (A8 as well).
+template <int BNT, bool A8, bool A4 = false, bool N8 = false>
 struct GemmCfg {
+  static_assert(!N8 || A8, "FP4-operand W4A8 has FP8 activations");
+  static constexpr bool kDirect = A4 || N8;                      // weights read from smem
   // 32-K chunks per stage: full records, except BF16 x 256 tokens (half records).
   static constexpr int kChunks = (!A8 && !A4 && BNT >= 256) ? 2 : 4;
   static constexpr int kSubStages = 4 / kChunks;                 // stages per record
   // codes + tail; A4: the MMA reads the codes in place, 64-byte-swizzled, so every slot
-  // starts on a 512-byte atom
-  static constexpr int kRecSlot = A4 ? 9216 : kChunks * kTileN * 16 + kRecTail;
+  // starts on a 512-byte atom; N8: the padded codes (128 rows x 128 bytes, 128-byte
+  // swizzle, 1024-byte aligned), the scales in a ring of their own
+  static constexpr int kRecSlot = A4 ? 9216 : N8 ? kTileN * 128 : kChunks * kTileN * 16 + kRecTail;
+  static constexpr int kTailBytes = N8 ? kTileN * 4 : 0;       // N8: a row's four E8M0 bytes
   // X slabs per stage: 128-byte rows (64 BF16 / 128 FP8 K); A4: one 64-byte row (128 FP4 K)
   static constexpr int kSlabs = (A8 || A4) ? 1 : kChunks / 2;
   static constexpr int kSlabBytes = A4 ? BNT * 64 : BNT * 128;
   static constexpr int kXBytes = kSlabs * kSlabBytes;
   // tensor-memory columns per stage of the A ring: the A operand (BF16 / FP8), or for A4
   // the scale factors (4 for the weights, 4 per 128 tokens for the activations)
-  static constexpr int kACols = A4 ? 4 + 4 * ((BNT + 127) / 128) : A8 ? 32 : kChunks * 16;
+  static constexpr int kACols = A4 ? 4 + 4 * ((BNT + 127) / 128) : N8 ? 0 : A8 ? 32 : kChunks * 16;
   static constexpr int kMmaPerStage = A4 ? 2 : A8 ? kChunks : 2 * kChunks;
   static_assert(A4 || A8 || kMmaPerStage % 4 == 0, "BF16 stages issue their MMAs in groups of four");
-  static constexpr int kIssuers = Roles<BNT, A4>::kIssuers;
+  static constexpr int kIssuers = Roles<BNT, kDirect>::kIssuers;
   static constexpr int kNumSub = kIssuers;                       // partial accumulators
   static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
   static constexpr int kAccCols = kNumAcc * kNumSub * BNT;
@@ -129,19 +135,21 @@ struct GemmCfg {
   static constexpr int kSfCols = A8 ? 4 : 0;
   static constexpr int kATmemMax = (512 - kAccCols - (A8 ? 8 : 0)) / (kACols + kSfCols);
   static constexpr int kAStagesMax =
-      A4 ? (kATmemMax < 8 ? kATmemMax : 8)
+      kDirect ? (kATmemMax < 8 ? kATmemMax : 8)
       : A8 ? (BNT >= 128 ? 5 : (kATmemMax < 10 ? kATmemMax : 10))
            : (BNT >= 256 ? 5 : (kATmemMax < 7 ? kATmemMax : 7));
   // Stage g of the CTA goes to dequant warpgroup g % kDeqWGs and to issuer g % kIssuers.
   // A ring slot must always have the same two owners: a waiter that is not the slot's only
   // consumer could run two uses ahead, where a one-bit mbarrier phase parity cannot tell
   // the phase it needs from the one before.  So the depth is a multiple of both counts.
-  static constexpr int kDeqWGs = Roles<BNT, A4>::kDeqWGs;
+  static constexpr int kDeqWGs = Roles<BNT, kDirect>::kDeqWGs;
   static constexpr int kALcm = lcm_int(kDeqWGs, kIssuers);
   static constexpr int kAStages = kAStagesMax / kALcm * kALcm;
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
   static constexpr int kXChunk = BNT <= 32 ? 4 : BNT == 64 ? 2 : 1;
-  static constexpr int kXSlots = kXChunk > 1 ? 3 : kAStages;
+  // (N8: only the issuer walks the X ring, which needs no more slots than the record ring
+  // keeps stages in flight)
+  static constexpr int kXSlots = kXChunk > 1 ? 3 : N8 ? (BNT >= 256 ? 3 : 4) : kAStages;
   // A4: each stage's activation exponents follow the slot's codes, a 16-byte box (four
   // 128-K blocks) per token row
   static constexpr int kXExpBytes = A4 ? BNT * 16 : 0;
@@ -151,7 +159,7 @@ struct GemmCfg {
   static constexpr int kBarBytesPerR = 16, kBarBytesPerA = 16, kBarBytesPerX = 16;
   static constexpr int kFixed = 1024 + kXSlots * (kXSlotBytes + kBarBytesPerX) +
                                 kAStages * kBarBytesPerA + kMiscBytes + 64;
-  static constexpr int kRMax0 = (227 * 1024 - kFixed) / (kRecSlot + kBarBytesPerR);
+  static constexpr int kRMax0 = (227 * 1024 - kFixed) / (kRecSlot + kTailBytes + kBarBytesPerR);
   // record ring: dequant warpgroup g % kDeqWGs (same rule as above)
   static constexpr int kRLcm = kDeqWGs;
   static constexpr int kRMax = kRMax0 / kRLcm * kRLcm;
@@ -171,7 +179,7 @@ struct GemmCfg {
   static constexpr int kBarBytes = kRStages * kBarBytesPerR + kAStages * kBarBytesPerA +
                                    kXSlots * kBarBytesPerX + (2 * kNumAcc + 2) * 8;
   static constexpr int kSmemBytes =
-      1024 + kXSlots * kXSlotBytes + kRStages * kRecSlot + kBarBytes + kMiscBytes;
+      1024 + kXSlots * kXSlotBytes + kRStages * (kRecSlot + kTailBytes) + kBarBytes + kMiscBytes;
   static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 };
 
@@ -354,7 +362,8 @@ struct Ring {
 // group of 128 K or longer, so they are read once per record.
 enum DecodeMode : int {
   DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5,
-  DM_W4A4 = 6                  // MXFP4 x MXFP4: no decode, the MMA reads the codes
+  DM_W4A4 = 6,                 // MXFP4 x MXFP4: no decode, the MMA reads the codes
+  DM_W4A8N = 7                 // MXFP4 x FP8 on FP4 operands: no decode either
 };
 
 // INT4 with BF16 scales (every group size): FP16 tensor-core operands, see f16_operands().
@@ -432,16 +441,19 @@ __device__ __forceinline__ void gather_row(uint32_t dst, const uint8_t* src, uin
 }
 
 template <int BNT, bool A8, int DM, bool GATHER>
-__global__ void __launch_bounds__(Roles<BNT, DM == DM_W4A4>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   static_assert(!GATHER || BNT <= 64, "gathered tiles exist for token tiles up to 64");
   constexpr bool A4 = DM == DM_W4A4;
+  constexpr bool N8 = DM == DM_W4A8N;
+  constexpr bool kDirect = A4 || N8;       // the MMA reads the weight codes from shared memory
   static_assert(!A4 || (!A8 && !GATHER), "W4A4: its own activation format, TMA loads only");
+  static_assert(!N8 || A8, "FP4-operand W4A8: FP8 activations");
   constexpr bool F16 = kF16Operands<A8, DM>;
   // per-token (per-row) output scale: FP8's token scale, or the FP16 copy's row scale
   constexpr bool kTokScale = A8 || F16;
-  using C = GemmCfg<BNT, A8, A4>;
-  using RO = Roles<BNT, A4>;
+  using C = GemmCfg<BNT, A8, A4, N8>;
+  using RO = Roles<BNT, kDirect>;
   constexpr int kEpiWarp0 = RO::kEpiWarp0;
   constexpr int kDeqWGs = RO::kDeqWGs;
   constexpr int kXProducerWarp = RO::kXProducerWarp;
@@ -457,7 +469,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* s_x = smem;                                   // [SX][kXSlotBytes], 1024-aligned
   uint8_t* s_rec = s_x + SX * C::kXSlotBytes;            // [SR][kRecSlot]
-  uint64_t* rfull = reinterpret_cast<uint64_t*>(s_rec + SR * C::kRecSlot);
+  uint8_t* s_tail = s_rec + SR * C::kRecSlot;            // N8: [SR][kTailBytes] scales
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(s_tail + SR * C::kTailBytes);
   uint64_t* rempty = rfull + SR;
   uint64_t* xfull = rempty + SR;
   uint64_t* xempty = xfull + SX;
@@ -492,7 +505,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     misc[1] = 0;
     for (int s = 0; s < SR; ++s) {
       ptx::mbar_init(&rfull[s], 1);
-      ptx::mbar_init(&rempty[s], A4 ? 1 : 4);   // per dequant warp; A4: the MMAs' commit
+      ptx::mbar_init(&rempty[s], kDirect ? 1 : 4);   // per dequant warp; direct: the MMAs' commit
     }
     for (int s = 0; s < SX; ++s) {
       ptx::mbar_init(&xfull[s], GATHER ? 32 : 1);   // gathered slots: one arrival per lane
@@ -529,6 +542,8 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   }
   if constexpr (!GATHER)
     if (warp == kXProducerWarp && lane == 0) ptx::prefetch_tmap(&tmap_x);
+  if constexpr (N8)
+    if (warp == RO::kRecProducerWarp0 && lane == 0) ptx::prefetch_tmap(&a.tmap_w);
   int num_units = a.num_units;
   if (a.offsets != nullptr && warp == 0) {
     // MoE schedule: m-tiles per expert and their exclusive prefix (one warp).  All offsets
@@ -600,10 +615,12 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 
   if (A8 && warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {    // first lane quarter set
     // Activation-side block scale: a constant 2^6 (E8M0 133) that returns the factor 2^-6
-    // of the e2m1 -> e4m3 byte shuffle.  Filled over every lane of its columns.
+    // of the e2m1 -> e4m3 byte shuffle; on FP4 operands 1 (E8M0 127).  Filled over every
+    // lane of its columns.
     const uint32_t tl = tbase + (uint32_t((warp & 3) * 32) << 16);
-    ptx::tmem_st4(tl + C::kSfbCol0, 0x85858585u, 0x85858585u, 0x85858585u, 0x85858585u);
-    ptx::tmem_st4(tl + C::kSfbCol0 + 4, 0x85858585u, 0x85858585u, 0x85858585u, 0x85858585u);
+    constexpr uint32_t sfb = N8 ? 0x7F7F7F7Fu : 0x85858585u;
+    ptx::tmem_st4(tl + C::kSfbCol0, sfb, sfb, sfb, sfb);
+    ptx::tmem_st4(tl + C::kSfbCol0 + 4, sfb, sfb, sfb, sfb);
     ptx::tmem_wait_st();
     ptx::tc_fence_before();
   }
@@ -623,7 +640,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
     const uint32_t rec_bytes = uint32_t(L.record_bytes);
     const uint32_t tail_bytes = rec_bytes - uint32_t(kCodeBytes);     // scales + zeros
-    const uint32_t stage_tx = CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
+    // (N8: the tensor copy counts the packed bytes it reads, not the padded ones it writes)
+    const uint32_t stage_tx = N8 ? uint32_t(kCodeBytes + C::kTailBytes)
+                              : CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
     uint32_t pend = 0, pend_par = 0;    // slots with a copy in flight (warp-uniform), for the wind-down
     uint32_t g0 = 0;                    // CTA stage counter at the unit start
     bool alive = true;
@@ -645,7 +664,14 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             const uint8_t* rec = rec0 + int64_t(i / kSub) * rec_bytes;
             uint8_t* sr = s_rec + slot * C::kRecSlot;
             ptx::mbar_arrive_expect_tx(&rfull[slot], stage_tx);
-            if (CH == 4) {
+            if constexpr (N8) {
+              // the codes through the tensor map, which writes them as padded 128-byte rows;
+              // the scales as plain bytes into the slot's tail
+              const int32_t ridx = int32_t(int64_t(w.nt) * L.k_blocks + w.kb0 + i);
+              ptx::tma_load_4d(sr, &a.tmap_w, 0, 0, ridx, w.expert, &rfull[slot], pol_w);
+              ptx::bulk_g2s(s_tail + slot * C::kTailBytes, rec + kCodeBytes, C::kTailBytes,
+                            &rfull[slot], pol_w);
+            } else if (CH == 4) {
               ptx::bulk_g2s(sr, rec, rec_bytes, &rfull[slot], pol_w);
             } else {
               // half record: codes of record chunks 2h, 2h+1, then the scales and zeros
@@ -854,6 +880,25 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             ptx::mma_commit_elect(&rempty[rs]);         // ... and its record
             continue;
           }
+          if constexpr (N8) {
+            // A is the stage's padded e2m1 codes in shared memory, B the FP8 tile: four
+            // K = 32 MMAs, each with its byte of the rows' E8M0 scale words
+            const int rs = int(g % uint32_t(SR));
+            if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepMma))) { alive = false; break; }
+            ptx::tc_fence_after();
+            const uint64_t adesc = ptx::desc_kmajor_sw128(ptx::smem_u32(s_rec + rs * C::kRecSlot));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)   // 32 bytes (32 K) into the 128-byte rows
+              ptx::mma_mxf8f6f4_ss_elect(d_tmem, adesc + uint64_t(kk * 2), bdesc + uint64_t(kk * 2),
+                                         ptx::idesc_mxf8_e2m1_e4m3(128, BNT, kk, 0),
+                                         tbase + uint32_t(C::kSfaCol0 + 4 * cur.slot),
+                                         tbase + uint32_t(C::kSfbCol0),
+                                         kk > 0 ? 1u : (first ^ 1u));
+            first = 0;
+            ptx::mma_commit_elect(&aempty[cur.slot]);   // frees the stage's scale factors
+            ptx::mma_commit_elect(&rempty[rs]);         // ... and its record
+            continue;
+          }
           if constexpr (A8) {
 #pragma unroll
             for (int kk = 0; kk < C::kMmaPerStage; ++kk) {
@@ -942,7 +987,33 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         rx.next(SX);
       }
     }
-  } else if (warp < kEpiWarp0) {
+  } else if (N8 && warp < kEpiWarp0) {
+    // ---------------------------------------------------------------- scale factors (N8)
+    // One warpgroup, every stage: thread r copies weight row r's four E8M0 bytes (the
+    // stage's scale tail) into the stage's four scale-factor columns of lane r, as for the
+    // register-decoded FP8 path; the activation side is the constant set in the prologue.
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t t_lane = tbase + (uint32_t((warp & 3) * 32) << 16);
+    uint32_t g = 0;
+    bool alive = true;
+    Unit w;
+    int e_hint = -1;
+    for (int uj = 0; alive && unit_at(uj, a, sc, BNT, prefix, offs, e_hint, w); ++uj) {
+      const int nst = w.kb1 - w.kb0;
+      for (int i = 0; i < nst; ++i, ++g) {
+        const int rs = int(g % uint32_t(SR)), ca = int(g % uint32_t(SA));
+        if (!warp_all(ptx::mbar_wait(&rfull[rs], (g / uint32_t(SR)) & 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        const uint32_t sfa = *reinterpret_cast<const uint32_t*>(s_tail + rs * C::kTailBytes + r * 4);
+        ptx::fence_proxy_async_smem();                 // the read above before the refill
+        if (!warp_all(ptx::mbar_wait(&aempty[ca], ((g / uint32_t(SA)) & 1u) ^ 1u, abort_flag, T, kSleepDequant))) { alive = false; break; }
+        ptx::tc_fence_after();
+        ptx::tmem_st4(t_lane + uint32_t(C::kSfaCol0 + 4 * ca), sfa, sfa, sfa, sfa);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        warp_arrive(&afull[ca], lane);
+      }
+    }
+  } else if (!kDirect && warp < kEpiWarp0) {
     // ---------------------------------------------------------------- dequant (2 WGs)
     const int wg = warp >> 2;                              // takes the stages g % kDeqWGs == wg
     const int r = (warp & 3) * 32 + lane;                  // weight row = TMEM lane
@@ -1273,7 +1344,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
 template <int BNT, bool A8, int DM, bool GATHER>
 cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const GemmArgs& args,
                            cudaStream_t st) {
-  using C = GemmCfg<BNT, A8, DM == DM_W4A4>;
+  using C = GemmCfg<BNT, A8, DM == DM_W4A4, DM == DM_W4A8N>;
   // At least 120 KB of shared memory per CTA: one CTA per SM, so no CTA ever waits for
   // another one's tensor-memory allocation.
   constexpr int kSmem = C::kSmemBytes > 120 * 1024 ? C::kSmemBytes : 120 * 1024;
@@ -1286,7 +1357,7 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(plan.grid));
-  cfg.blockDim = dim3(Roles<BNT, DM == DM_W4A4>::kThreads);
+  cfg.blockDim = dim3(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N>::kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -1322,6 +1393,7 @@ cudaError_t launch_gemm_impl(const GemmPlan& plan, const CUtensorMap& tmap, cons
 // Decode mode of a packed layout (BF16 activations).
 inline int decode_mode(const Layout& L) {
   if (L.afmt == A_MXFP4) return DM_W4A4;
+  if (L.afmt == A_FP8N) return DM_W4A8N;
   if (L.wfmt == W_MXFP4) return DM_MXFP4;
   if (L.wfmt == W_MXINT4) return DM_MXINT4;
   if (L.wfmt == W_NVFP4) return DM_NVFP4;

@@ -77,6 +77,10 @@ struct GemmArgs {
   const uint8_t* x_exps;
   int64_t ld_exps;
   CUtensorMap tmap_e;
+  // FP8 activations on FP4 operands (afmt A_FP8N): the packed codes as a 4-D tensor
+  // [experts][records][128 rows][128 e2m1] (strides expert_stride, record_bytes, 64 bytes),
+  // loaded one record at a time into the padded 128-byte rows the MMA reads
+  CUtensorMap tmap_w;
   void* Y;                     // bf16 [M, ldy]
   int64_t ldy;
   // Partial sums of the tiles whose K range is cut over several CTAs: one slot per

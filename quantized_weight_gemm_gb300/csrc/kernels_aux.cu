@@ -54,8 +54,8 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
         uint32_t nib = pad ? 0u : (src >> (4 * e)) & 0xFu;   // even k in the low nibble
         if (L.wfmt == W_INT4_SYM || L.wfmt == W_MXINT4) nib ^= 8u;   // two's complement -> q + 8
         const int pos = L.afmt == A_FP8 ? nibble_pos_a8(e)
-                        : L.afmt == A_MXFP4 ? e                        // the MMA's own order
-                                            : nibble_pos_a16(e);
+                        : (L.afmt == A_MXFP4 || L.afmt == A_FP8N) ? e   // the MMA's own order
+                                                                   : nibble_pos_a16(e);
         w |= nib << (4 * pos);
       }
       out[j] = w;
@@ -242,7 +242,7 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
     const int js = c * G / 4;                          // scale entry of chunk c
     const int ent = r * G + js;
     __nv_bfloat16* dst = W + n * L.K + k0;
-    if (L.afmt == A_MXFP4) {
+    if (L.afmt == A_MXFP4 || L.afmt == A_FP8N) {
       // the MMA's operand: e2m1 codes in natural order, times 2^(E-127) (exact in bf16)
       const uint32_t E = rec[L.off_scales + ent];
       for (int e = 0; e < 8; ++e) {

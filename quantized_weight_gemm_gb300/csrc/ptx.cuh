@@ -147,6 +147,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int32_t
          "l"(policy) : "memory");
 }
 
+// 4-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, int32_t c3, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
+      :: "r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar)),
+         "l"(policy) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" :: "l"(tmap) : "memory");
 }
@@ -259,6 +270,20 @@ __device__ __forceinline__ void mma_mxf4_ss_elect(uint32_t d_tmem, uint64_t a_de
   asm volatile(
       "{\n .reg .pred P, E;\n setp.ne.b32 P, %6, 0;\n elect.sync _|E, 0xffffffff;\n"
       " @E tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X"
+      " [%0], %1, %2, %3, [%4], [%5], P;\n}\n"
+      :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+         "r"(accumulate) : "memory");
+}
+
+// Block-scaled FP8/FP6/FP4 MMA (kind::mxf8f6f4, one E8M0 scale per 32 K) with A and B from
+// shared memory, under one election of a converged warp.
+__device__ __forceinline__ void mma_mxf8f6f4_ss_elect(uint32_t d_tmem, uint64_t a_desc,
+                                                      uint64_t b_desc, uint32_t idesc,
+                                                      uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                      uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred P, E;\n setp.ne.b32 P, %6, 0;\n elect.sync _|E, 0xffffffff;\n"
+      " @E tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
       " [%0], %1, %2, %3, [%4], [%5], P;\n}\n"
       :: "r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
          "r"(accumulate) : "memory");
@@ -381,6 +406,14 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
 // selectors sfa_id / sfb_id, shape M x N.
 __host__ __device__ constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int sfa_id, int sfb_id) {
   return (uint32_t(sfb_id & 3) << 4) | (0u << 7) | (0u << 10) | (uint32_t(N >> 3) << 17) |
+         (1u << 23) | (uint32_t(M >> 4) << 24) | (uint32_t(sfa_id & 3) << 29);
+}
+
+// Instruction descriptor, kind::mxf8f6f4: D=F32, A=E2M1 (format code 5), B=E4M3 (0), scale
+// factors UE8M0 with byte selectors sfa_id / sfb_id, shape M x N.  The e2m1 operand sits in
+// shared memory in the padded form (16 elements in the first 8 of every 16 bytes).
+__host__ __device__ constexpr uint32_t idesc_mxf8_e2m1_e4m3(int M, int N, int sfa_id, int sfb_id) {
+  return (uint32_t(sfb_id & 3) << 4) | (5u << 7) | (0u << 10) | (uint32_t(N >> 3) << 17) |
          (1u << 23) | (uint32_t(M >> 4) << 24) | (uint32_t(sfa_id & 3) << 29);
 }
 

@@ -17,6 +17,10 @@
 //            (128 K, element 2j in the low nibble of byte j), 8-row atoms of 512 bytes, the
 //            16-byte piece c of row r at position c ^ ((r >> 1) & 3) of its row (the
 //            64-byte swizzle);
+//            FP8 activations on FP4 operands (A_FP8N): plain K-major rows of 64 bytes, the
+//            same nibble order, row r at byte 64 r -- a tensor the TMA loads with its
+//            "16 x 4-bit in 16 bytes" expansion, which writes the padded shared-memory
+//            layout the block-scaled FP8/FP6/FP4 MMA reads e2m1 operands from;
 //   scales : [128 rows][G] entries of S bytes, G = max(1, 128 / group) groups per record,
 //            S = 2 (BF16) or 1 (E8M0, E4M3); a group longer than 128 repeats in each record;
 //   zeros  : (INT4 with zero points only) [128 rows x G] nibbles, entry (r, j) in nibble
@@ -42,12 +46,15 @@ constexpr int kCodeBytes = kTileN * kStageK / 2; // 8192
 constexpr int kHeaderBytes = 256;
 
 enum WFmt : int32_t { W_INT4_SYM = 0, W_UINT4_ZP = 1, W_MXFP4 = 2, W_MXINT4 = 3, W_NVFP4 = 4 };
-enum AFmt : int32_t { A_BF16 = 0, A_FP8 = 1, A_MXFP4 = 2 };
+// A_FP8N: FP8 activations with the e2m1 weights fed to the tensor core as FP4 operands
+// (no register decode; see the codes layout above).
+enum AFmt : int32_t { A_BF16 = 0, A_FP8 = 1, A_MXFP4 = 2, A_FP8N = 3 };
 
 // Byte offset of the 16-byte piece (row r, 32-K chunk c) inside a record's codes.
 inline __host__ __device__ int code_piece_offset(int32_t afmt, int r, int c) {
   return afmt == A_MXFP4 ? (r >> 3) * 512 + (r & 7) * 64 + ((c ^ ((r >> 1) & 3)) << 4)
-                         : c * (kTileN * 16) + r * 16;
+         : afmt == A_FP8N ? r * 64 + c * 16
+                          : c * (kTileN * 16) + r * 16;
 }
 
 struct PackedHeader {
@@ -89,8 +96,8 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
                         int64_t N, int64_t K, Layout* L) {
   if (N < 1 || K < 32 || (K % 32) != 0 || N > (int64_t(1) << 31) || K > (int64_t(1) << 30))
     return false;
-  if (afmt != A_BF16 && afmt != A_FP8 && afmt != A_MXFP4) return false;
-  if (afmt == A_MXFP4 && wfmt != W_MXFP4) return false;   // W4A4: MXFP4 x MXFP4
+  if (afmt != A_BF16 && afmt != A_FP8 && afmt != A_MXFP4 && afmt != A_FP8N) return false;
+  if ((afmt == A_MXFP4 || afmt == A_FP8N) && wfmt != W_MXFP4) return false;   // e2m1 operands
   if (wfmt == W_MXFP4) {
     if (sdtype != 1 || group != 32 || has_zp != 0) return false;
   } else if (wfmt == W_MXINT4 || wfmt == W_NVFP4) {
@@ -101,7 +108,7 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
   } else if (wfmt == W_INT4_SYM || wfmt == W_UINT4_ZP) {
     if (sdtype != 0 || has_zp != (wfmt == W_UINT4_ZP ? 1 : 0)) return false;
     if (!(group == 32 || (group >= 64 && group % 64 == 0))) return false;
-    if (afmt == A_FP8) return false;    // FP8 activations pair with MXFP4 weights only
+    if (afmt == A_FP8 || afmt == A_FP8N) return false;   // FP8 activations: MXFP4 weights only
   } else {
     return false;
   }

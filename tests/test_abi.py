@@ -47,6 +47,7 @@ def test_status_strings(L):
     ("mxint4", 32, "bf16", True), ("nvfp4", 16, "bf16", True),
     ("mxint4", 64, "bf16", False), ("nvfp4", 32, "bf16", False),
     ("mxint4", 32, "fp8", False), ("nvfp4", 16, "fp8", False),
+    ("mxfp4", 32, "fp8n", True), ("uint4_zp", 128, "fp8n", False), ("mxint4", 32, "fp8n", False),
 ])
 def test_check_desc(L, wfmt, group, afmt, ok):
     d = qg.WeightDesc(wfmt, 256, 512, group, afmt)

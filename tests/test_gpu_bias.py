@@ -90,8 +90,9 @@ def test_bias_alone_is_exact():
     np.testing.assert_array_equal(y, np.broadcast_to(F.round_to_bf16(bias.astype(np.float64)), (M, N)))
 
 
+@pytest.mark.parametrize("afmt", ["fp8", "fp8n"])
 @pytest.mark.parametrize("tile,splits", [(16, 1), (32, -1), (64, 3), (128, 1), (256, 1)])
-def test_bias_w4a8(tile, splits):
+def test_bias_w4a8(tile, splits, afmt):
     """FP8 activations: token scale, channel scale and bias in one output expression."""
     from tests import gpu_util as G
     qg = _qg()
@@ -101,7 +102,7 @@ def test_bias_w4a8(tile, splits):
     w = WL.gen_weights(r, "mxfp4", N, K)
     chan = r.uniform(0.5, 2.0, N).astype(np.float32)
     bias = r.standard_normal(N).astype(np.float32)
-    d, packed = G.pack(w, afmt="fp8")
+    d, packed = G.pack(w, afmt=afmt)
     xq, ts = oracle.quant_act_fp8(x)
     qg.force_config(tile, splits)
     try:

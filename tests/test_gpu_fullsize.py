@@ -109,16 +109,17 @@ def test_mxint4_nvfp4_bench_shapes(wfmt, N, K, M):
     _check_sampled(f"fullsize {wfmt} {N}x{K} M={M}", y, x, w, ns, ms)
 
 
+@pytest.mark.parametrize("afmt", ["fp8", "fp8n"])
 @pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 256), (4096, 7168, 8192),
                                    (7168, 2048, 1), (7168, 2048, 8192)])
-def test_w4a8_bench_shapes(N, K, M):
+def test_w4a8_bench_shapes(N, K, M, afmt):
     """FP8 activations with 1% outliers, quantized by the library's own call; the oracle
     multiplies the same codes and scales (the quantization itself is checked bit for bit
     against the oracle in test_gpu_gemm)."""
     from tests import gpu_util as G
     import quantized_weight_gemm_gb300 as qg
     x, w = WL.mxfp4_shape(N, K, M, seed=0, outliers=True)
-    d, packed = G.pack(w, afmt="fp8")
+    d, packed = G.pack(w, afmt=afmt)
     Xq, ts = qg.quant_act_fp8(G.bf16_tensor(x))
     y = qg.w4a8(d, packed, Xq, ts, out=_nan_out(M, N))
     torch.cuda.synchronize()

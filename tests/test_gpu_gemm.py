@@ -189,7 +189,7 @@ def test_new_formats_every_tile(wfmt, tile, splits):
 
 
 @pytest.mark.parametrize("wfmt,afmt", [("uint4_zp", "bf16"), ("mxfp4", "bf16"),
-                                       ("nvfp4", "bf16"), ("mxfp4", "fp8")])
+                                       ("nvfp4", "bf16"), ("mxfp4", "fp8"), ("mxfp4", "fp8n")])
 def test_batch_invariant_rows(wfmt, afmt):
     """With the batch-invariant flag, row m of Y is the same bits for every M (the default
     schedules change token tile and K cuts with M), and the largest call matches the oracle."""
@@ -197,13 +197,13 @@ def test_batch_invariant_rows(wfmt, afmt):
     qg = _qg()
     r = WL.rng(27)
     Mmax, N, K = 1000, 384, 1536
-    x = WL.gen_x(r, Mmax, K, outliers=(afmt == "fp8"))
+    x = WL.gen_x(r, Mmax, K, outliers=(afmt != "bf16"))
     w = WL.gen_weights(r, wfmt, N, K)
     d = qg.WeightDesc(wfmt, N, K, w.group, afmt, batch_invariant=True)
     z = None if w.zeros is None else G.u8_tensor(w.zeros)
     packed = qg.repack(d, G.u8_tensor(w.codes), G.scales_tensor(w), z, global_scale=w.global_scale)
     X = G.bf16_tensor(x)
-    if afmt == "fp8":
+    if afmt != "bf16":
         Xq, ts = qg.quant_act_fp8(X)
         run = lambda M: qg.w4a8(d, packed, Xq[:M], ts[:M])
     else:
@@ -214,7 +214,7 @@ def test_batch_invariant_rows(wfmt, afmt):
     torch.cuda.synchronize()
     assert qg.device_status(clear=True) == 0
     y = F.bf16_bits_to_float(full)
-    if afmt == "fp8":
+    if afmt != "bf16":
         xq, s = oracle.quant_act_fp8(x)
         ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
         _assert_close(y, ref, TOL_A8)
@@ -315,10 +315,15 @@ def test_quant_act_fp8_bitexact(M, K):
     np.testing.assert_array_equal(codes.cpu().numpy(), ref_codes)
 
 
-def _run_a8(xq, s, w, chan=None):
+# The two W4A8 kernels: e2m1 -> e4m3 in registers ("fp8"), and the e2m1 codes as FP4
+# tensor-core operands ("fp8n").
+A8_FORMS = ["fp8", "fp8n"]
+
+
+def _run_a8(xq, s, w, chan=None, afmt="fp8"):
     from tests import gpu_util as G
     qg = _qg()
-    d, packed = G.pack(w, afmt="fp8")
+    d, packed = G.pack(w, afmt=afmt)
     cs = None if chan is None else torch.from_numpy(chan.astype(np.float32)).cuda()
     out = torch.full((xq.shape[0], w.N), float("nan"), dtype=torch.bfloat16, device="cuda")
     y = qg.w4a8(d, packed, G.u8_tensor(xq), torch.from_numpy(s).cuda(), chan_scale=cs, out=out)
@@ -327,18 +332,20 @@ def _run_a8(xq, s, w, chan=None):
     return G.to_f64(y)
 
 
+@pytest.mark.parametrize("afmt", A8_FORMS)
 @pytest.mark.parametrize("M,N,K", [(1, 256, 512), (16, 300, 1024), (40, 512, 2048),
                                    (130, 256, 384), (300, 640, 1024)])
-def test_dense_a8_parity(M, N, K):
+def test_dense_a8_parity(M, N, K, afmt):
     r = WL.rng(27)
     x = WL.gen_x(r, M, K, outliers=True)
     w = WL.gen_weights(r, "mxfp4", N, K)
     xq, s = oracle.quant_act_fp8(x)
     ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
-    _assert_close(_run_a8(xq, s, w), ref, TOL_A8)
+    _assert_close(_run_a8(xq, s, w, afmt=afmt), ref, TOL_A8)
 
 
-def test_a8_integer_inputs_exact():
+@pytest.mark.parametrize("afmt", A8_FORMS)
+def test_a8_integer_inputs_exact(afmt):
     r = WL.rng(28)
     M, N, K = 8, 256, 256
     xq = F.e4m3_encode(r.integers(-4, 5, size=(M, K)).astype(np.float64))
@@ -346,12 +353,13 @@ def test_a8_integer_inputs_exact():
     w = WL.gen_weights(r, "mxfp4", N, K)
     w.scales[:] = r.integers(124, 130, size=w.scales.shape, dtype=np.uint8)
     ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales)
-    np.testing.assert_array_equal(_run_a8(xq, s, w), F.round_to_bf16(ref))
+    np.testing.assert_array_equal(_run_a8(xq, s, w, afmt=afmt), F.round_to_bf16(ref))
 
 
-@pytest.mark.parametrize("tile", [16, 64, 256])
-@pytest.mark.parametrize("splits", [1, 3])
-def test_a8_dispatch_entries(tile, splits):
+@pytest.mark.parametrize("afmt", A8_FORMS)
+@pytest.mark.parametrize("tile", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("splits", [1, 3, -1])
+def test_a8_dispatch_entries(tile, splits, afmt):
     qg = _qg()
     r = WL.rng(29)
     M, N, K = 100, 384, 1024
@@ -362,7 +370,7 @@ def test_a8_dispatch_entries(tile, splits):
     ref = oracle.w4a8(xq, s, w.wfmt, w.group, w.codes, w.scales, chan_scale=chan)
     qg.force_config(tile, splits)
     try:
-        y = _run_a8(xq, s, w, chan)
+        y = _run_a8(xq, s, w, chan, afmt=afmt)
     finally:
         qg.force_config(0, 0)
     _assert_close(y, ref, TOL_A8)

@@ -128,6 +128,7 @@ def F_bits(x_bits):
     ("bf16", [1, 1, 1, 1, 1, 1, 1, 1], 2048, 2560),     # 128 tiles, all cut (20 K blocks each)
     ("bf16", [40, 3, 0, 17, 9, 1, 0, 22], 1536, 2688),  # several m-tiles per expert
     ("fp8", [12, 0, 41, 200, 1], 2048, 3584),           # 64-row tiles, FP8 activations
+    ("fp8n", [12, 0, 41, 200, 1], 2048, 3584),          # ... on FP4 tensor-core operands
 ])
 def test_moe_stream_k(afmt, counts, N, K):
     """MoE calls whose leftover tiles hold at least 16 K blocks per SM, so that the kernel
@@ -135,7 +136,7 @@ def test_moe_stream_k(afmt, counts, N, K):
     r = WL.rng(46)
     off = _offsets(counts)
     R = int(off[-1])
-    x = WL.gen_x(r, R, K, outliers=afmt == "fp8")
+    x = WL.gen_x(r, R, K, outliers=afmt != "bf16")
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     if afmt == "bf16":
         ref = oracle.moe_grouped(F_bits(x), off, _experts_a16(ws))
@@ -144,7 +145,7 @@ def test_moe_stream_k(afmt, counts, N, K):
         from oracle import formats as F
         xq, sc = oracle.quant_act_fp8(x)
         ref = oracle.moe_grouped(F.e4m3_to_float(xq), off, _experts_exact(ws), tok_scale=sc)
-        _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=sc, stream_k=True, calls=2),
+        _assert_close(_run_moe(ws, xq, off, afmt=afmt, tok_scale=sc, stream_k=True, calls=2),
                       ref, TOL_A8)
 
 
@@ -202,8 +203,9 @@ def test_moe_rows_outside_groups_untouched():
     _assert_close(y[5:int(off[-1])], ref, TOL_A16)
 
 
+@pytest.mark.parametrize("afmt", ["fp8", "fp8n"])
 @pytest.mark.parametrize("stream_k", [False, True])
-def test_moe_a8_parity(stream_k):
+def test_moe_a8_parity(stream_k, afmt):
     r = WL.rng(45)
     counts = [12, 0, 41, 200, 1]
     off = _offsets(counts)
@@ -214,7 +216,7 @@ def test_moe_a8_parity(stream_k):
     ws = [WL.gen_weights(r, "mxfp4", N, K) for _ in counts]
     from oracle import formats as F
     ref = oracle.moe_grouped(F.e4m3_to_float(xq), off, _experts_exact(ws), tok_scale=s)
-    _assert_close(_run_moe(ws, xq, off, afmt="fp8", tok_scale=s, stream_k=stream_k, calls=2),
+    _assert_close(_run_moe(ws, xq, off, afmt=afmt, tok_scale=s, stream_k=stream_k, calls=2),
                   ref, TOL_A8)
 
 
@@ -281,7 +283,7 @@ def _run_moe_indexed(ws, x_bits, offsets, row_index, afmt="bf16", tok_scale=None
 
 
 @pytest.mark.parametrize("stream_k", [False, True])
-@pytest.mark.parametrize("afmt", ["bf16", "fp8"])
+@pytest.mark.parametrize("afmt", ["bf16", "fp8", "fp8n"])
 def test_moe_indexed_router(afmt, stream_k):
     """Routed tokens gathered from X in token order (padding positions index -1), against
     the oracle; FP8 rows take the scale of the row they come from."""
@@ -298,7 +300,7 @@ def test_moe_indexed_router(afmt, stream_k):
         xq, s = oracle.quant_act_fp8(WL.gen_x(WL.rng(48), case.T, 256, outliers=True))
         ref = oracle.moe_indexed(F.e4m3_to_float(xq), case.offsets, idx, _experts_exact(ws),
                                  tok_scale=s)
-        y = _run_moe_indexed(ws, xq, case.offsets, idx, afmt="fp8", tok_scale=s, stream_k=stream_k)
+        y = _run_moe_indexed(ws, xq, case.offsets, idx, afmt=afmt, tok_scale=s, stream_k=stream_k)
         _assert_close(y, ref, TOL_A8)
 
 

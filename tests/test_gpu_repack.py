@@ -51,10 +51,11 @@ def test_repack_roundtrip_bitexact(wfmt, group, N, K):
     _check(w)
 
 
+@pytest.mark.parametrize("afmt", ["fp8", "fp8n"])
 @pytest.mark.parametrize("N,K", [(256, 512), (200, 160)])
-def test_repack_roundtrip_fp8_layout(N, K):
+def test_repack_roundtrip_fp8_layout(N, K, afmt):
     w = WL.gen_weights(WL.rng(12), "mxfp4", N, K)
-    _check(w, afmt="fp8")
+    _check(w, afmt=afmt)
 
 
 def test_mxfp4_all_exponents():
@@ -65,6 +66,7 @@ def test_mxfp4_all_exponents():
     w.scales[:] = np.arange(255, dtype=np.uint8)[:, None]
     _check(w)
     _check(w, afmt="fp8")
+    _check(w, afmt="fp8n")
 
 
 def test_mxint4_all_exponents():

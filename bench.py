@@ -810,7 +810,9 @@ def bench_case(args):
 
 def bench_moe_case(args):
     """One MoE GEMM of the 256-expert layer, timed alone (profiling aid):
-    --moe T,gate_up|down[,skewed][,indexed]."""
+    --moe T,gate_up|down[,skewed][,indexed][,E<experts>][,top<k>] -- fewer experts (and a
+    smaller top-k) keep the rows per expert, and so the kernel's tiles, of the full layer
+    with a fraction of its weights on the device."""
     import numpy as np
     import torch
     import workloads as WL
@@ -820,7 +822,10 @@ def bench_moe_case(args):
     parts = args.moe.split(",")
     T, gemm = int(parts[0]), parts[1]
     skewed, indexed = "skewed" in parts[2:], "indexed" in parts[2:]
-    case = WL.moe_case(T, seed=0, skewed=skewed)
+    E_opt = [int(p[1:]) for p in parts[2:] if p.startswith("E")]
+    k_opt = [int(p[3:]) for p in parts[2:] if p.startswith("top")]
+    case = WL.moe_case(T, seed=0, skewed=skewed, E=E_opt[0] if E_opt else WL.MOE_E,
+                       topk=k_opt[0] if k_opt else WL.MOE_TOPK)
     N, K = (2 * WL.MOE_INTER, WL.MOE_HIDDEN) if gemm == "gate_up" else (WL.MOE_HIDDEN, WL.MOE_INTER)
     E, R = case.E, len(case.token_of_row)
     d = qg.WeightDesc("mxfp4", N, K, 32, "bf16")

@@ -636,15 +636,18 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
     // overlap, so one SM streams about twice as many bytes per cycle as from a single
     // thread.  The warp stays converged from one group to the next, so the waits on any
     // one slot follow the stage order, whichever lane makes them.
-    constexpr int kCopyLanes = 4;
+    // (wide token tiles run at large M, where the weight stream is no limit: one lane)
+    constexpr int kCopyLanes = BNT >= 128 ? 1 : 4;
+    constexpr uint32_t kLaneMask = (1u << kCopyLanes) - 1u;
+    if (lane < kCopyLanes) {
     const uint64_t pol_w = a.m_tiles <= 1 ? ptx::policy_evict_first() : ptx::policy_evict_normal();
     const uint32_t rec_bytes = uint32_t(L.record_bytes);
     const uint32_t tail_bytes = rec_bytes - uint32_t(kCodeBytes);     // scales + zeros
     // (N8: the tensor copy counts the packed bytes it reads, not the padded ones it writes)
     const uint32_t stage_tx = N8 ? uint32_t(kCodeBytes + C::kTailBytes)
                               : CH == 4 ? rec_bytes : uint32_t(kCodeBytes / 2) + tail_bytes;
-    uint32_t pend = 0, pend_par = 0;    // slots with a copy in flight (warp-uniform), for the wind-down
     uint32_t g0 = 0;                    // CTA stage counter at the unit start
+    uint32_t fail_g = 0, fail_iss = 0;  // on a failed wait: the group's first stage and its issued lanes
     bool alive = true;
     Unit w;
     int e_hint = -1;
@@ -658,7 +661,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
         const int slot = int(g % uint32_t(SR));
         const uint32_t ph = (g / uint32_t(SR)) & 1u;
         bool ok = true, issued = false;
-        if (lane < kCopyLanes && i < nst) {
+        if (i < nst) {
           ok = ptx::mbar_wait(&rempty[slot], ph ^ 1u, abort_flag, T, kSleepProducer);
           if (ok) {
             const uint8_t* rec = rec0 + int64_t(i / kSub) * rec_bytes;
@@ -682,23 +685,30 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
             issued = true;
           }
         }
-        // the slots of this group's copies, the same in every lane
-        const uint32_t iss = __ballot_sync(0xffffffffu, issued);
-        for (uint32_t m = iss; m != 0; m &= m - 1) {
-          const uint32_t gj = g0 + uint32_t(i0 + __ffs(m) - 1);
-          const uint32_t sj = gj % uint32_t(SR);
-          pend |= 1u << sj;
-          pend_par = (pend_par & ~(1u << sj)) | (((gj / uint32_t(SR)) & 1u) << sj);
+        if (!__all_sync(kLaneMask, ok)) {
+          alive = false;
+          fail_g = g0 + uint32_t(i0);
+          fail_iss = __ballot_sync(kLaneMask, issued);
+          break;
         }
-        if (!warp_all(ok)) { alive = false; break; }
       }
       g0 += uint32_t(nst);
     }
     if (!alive && lane == 0) {
-      volatile int no_abort = 0;        // let every copy the warp issued land first (each
-      for (int s = 0; s < SR; ++s)      // slot's last use: earlier ones were consumed)
-        if (pend & (1u << s))
-          ptx::mbar_wait(&rfull[s], (pend_par >> s) & 1u, &no_abort, 200000000ull);
+      // Let every copy the warp issued land first.  Every stage before fail_g was issued,
+      // and of the group at fail_g the lanes in fail_iss; each slot's last fill is waited
+      // for (an earlier fill of the slot was consumed, so it has landed).
+      volatile int no_abort = 0;
+      const uint32_t lo = fail_g > uint32_t(SR) ? fail_g - uint32_t(SR) : 0u;
+      for (uint32_t g = lo; g < fail_g + uint32_t(kCopyLanes); ++g) {
+        const bool in_group = g >= fail_g;
+        if (in_group && !((fail_iss >> (g - fail_g)) & 1u)) continue;       // not issued
+        if (!in_group && g + uint32_t(SR) >= fail_g && g + uint32_t(SR) < fail_g + uint32_t(kCopyLanes) &&
+            ((fail_iss >> (g + uint32_t(SR) - fail_g)) & 1u))
+          continue;                                                         // refilled later
+        ptx::mbar_wait(&rfull[g % uint32_t(SR)], (g / uint32_t(SR)) & 1u, &no_abort, 200000000ull);
+      }
+    }
     }
   } else if (warp == kXProducerWarp) {
     // ---------------------------------------------------------------- activation producer

@@ -16,14 +16,16 @@ roofline: the dominant launch (the call with the largest share of the step time,
           tensor-bound M = 8192 call): 2*M*N*K / its event time against the measured bf16
           peak; the HBM-bound small-M calls (M <= 16: weight + X + Y bytes / time against
           the measured copy bandwidth) are reported beside it
-other_workloads: the MXFP4 W4A16, MXFP4 W4A8, MXINT4 W4A16 and NVFP4 W4A16 sweeps and the
-          MoE sweep (grouped, and indexed gate_up up to 1024 tokens), measured once after the
-          timed region (--no-extra skips them)
+other_workloads: the MXFP4 W4A16, MXFP4 W4A8 (both packings: weights widened to e4m3 in
+          registers, and e2m1 weights as FP4 tensor-core operands), W4A4, MXINT4 W4A16 and
+          NVFP4 W4A16 sweeps and the MoE sweep (grouped, and the indexed gate_up), measured
+          once after the timed region (--no-extra skips them)
+cpu_baseline: the float64 numpy oracle on every host core (one single-threaded worker
+          process per core) on a bounded sample of the workload
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (float64 numpy, one thread) on a bounded sample of
-the same workload.  Multi-GPU runs (torchrun) execute independent replicas (weak scaling);
+--impl reference times the same CPU oracle on a bounded sample of the same workload.  Multi-GPU runs (torchrun) execute independent replicas (weak scaling);
 the GEMM has no exchange step.
 """
 import argparse
@@ -520,9 +522,10 @@ def sweep_w4a16_fmt(device, flush, peaks, wfmt):
 def sweep_moe(device, flush, peaks):
     """The MoE layer (E = 256 MXFP4 experts, top-8, hidden 7168, intermediate 2048):
     gate_up [4096 x 7168] and down [7168 x 2048] grouped GEMMs over expert-sorted rows,
-    T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone.  For
-    T <= 1024 the gate_up GEMM is also timed on the indexed path (token-order X gathered by
-    index), reported as gate_up_indexed_us beside the grouped time."""
+    T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone.  The
+    gate_up GEMM is also timed on the indexed path (token-order X gathered by index, with
+    the indexed workspace: from 2048 rows on the call gathers into it and runs the grouped
+    kernel), reported as gate_up_indexed_us beside the grouped time."""
     import numpy as np
     import torch
     import workloads as WL
@@ -564,16 +567,16 @@ def sweep_moe(device, flush, peaks):
                 tot_w += wb
                 tot_b += wb + valid * K * 2 + valid * N * 2
             # the same gate_up GEMM on the indexed path: X in token order [T, hidden], rows
-            # gathered by index (padding positions -1), no sorted copy of X
-            if T <= 1024:
-                N, K, _ = shapes["gate_up"]
-                Xt = torch.from_numpy(case.x_tok_bits.view(np.int16)).view(torch.bfloat16).to(device)
-                idx = torch.from_numpy(case.token_of_row.astype(np.int32)).to(device)
-                Y = torch.empty(R, N, dtype=torch.bfloat16, device=device)
-                d, p = descs["gate_up"], packs["gate_up"]
-                wsp = qg.moe_workspace(d, E, R, device=device)
-                ms = time_one(lambda: qg.moe_indexed(d, p, E, Xt, off, idx, out=Y, ws=wsp), flush)
-                r["gate_up_indexed_us"] = round(ms * 1e3, 2)
+            # gathered by index (padding positions -1), no sorted copy of X from the caller
+            N, K, _ = shapes["gate_up"]
+            Xt = torch.from_numpy(case.x_tok_bits.view(np.int16)).view(torch.bfloat16).to(device)
+            idx = torch.from_numpy(case.token_of_row.astype(np.int32)).to(device)
+            Y = torch.empty(R, N, dtype=torch.bfloat16, device=device)
+            d, p = descs["gate_up"], packs["gate_up"]
+            wsp = qg.moe_indexed_workspace(d, E, T, R, device=device)
+            ms = time_one(lambda: qg.moe_indexed(d, p, E, Xt, off, idx, out=Y, ws=wsp), flush)
+            r["gate_up_indexed_us"] = round(ms * 1e3, 2)
+            del wsp
             r.update({"us": round(tot_ms * 1e3, 2),
                       "tflops": round(tot_flops / (tot_ms * 1e-3) / 1e12, 2),
                       "weight_gbs": round(tot_w / (tot_ms * 1e-3) / 1e9, 1),
@@ -843,7 +846,7 @@ def bench_moe_case(args):
         xb = case.x_bits if gemm == "gate_up" else case.down_bits
         X = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
         call = lambda: qg.moe_grouped(d, packed, E, X, off, out=Y, ws=wsp)
-    wsp = qg.moe_workspace(d, E, R)
+    wsp = qg.moe_indexed_workspace(d, E, case.T, R) if indexed else qg.moe_workspace(d, E, R)
     Y = torch.empty(R, N, dtype=torch.bfloat16, device="cuda")
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     times = []

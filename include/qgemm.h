@@ -350,14 +350,18 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
  *   Y              : device BF16 [R, ldy] in sorted order
  *   ws, ws_bytes   : as for qgemm_moe_grouped, with the activation copy for the T rows
  *                    of X: qgemm_act_copy_bytes(desc, T) at least for INT4 weights with
- *                    BF16 scales, and qgemm_moe_workspace_bytes(desc, E, max(R, T)) for
- *                    stream-K
- * The kernel copies the indexed rows into its activation tiles itself (token tiles of 16,
- * 32 or 64 rows, from R / E), which suits the few rows per expert of decode-sized routing;
- * for large batches the grouped call's wider tiles are faster.  An index >= T is an error
+ *                    BF16 scales; qgemm_moe_indexed_workspace_bytes(desc, E, afmt, T, R)
+ *                    for the fastest schedule (below)
+ * Up to 2047 rows, or with less workspace, the kernel copies the indexed rows into its
+ * activation tiles itself (token tiles of 16, 32 or 64 rows, from R / E), which suits the
+ * few rows per expert of decode-sized routing.  From 2048 rows on, given
+ * qgemm_moe_indexed_workspace_bytes, a gather kernel first writes the rows (and their token
+ * or row scales) in sorted order into the workspace, and the grouped kernel with its wider
+ * tiles runs on that copy: the same result, one more launch, and the rows are read from X
+ * once per call instead of once per weight tile.  An index >= T is an error
  * (QGEMM_ERR_BAD_VALUE in the device status word, see qgemm_device_status) and that row
  * reads as zeros.  QGEMM_ERR_UNSUPPORTED when qgemm_force_config forces a token tile
- * above 64.
+ * above 64 (a forced token tile also keeps the in-kernel gather).
  * "Humming wird angekündigt", section "WnA16" (Indexed and Grouped MoE paths).
  */
 qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int32_t E,
@@ -375,6 +379,17 @@ qgemm_status qgemm_moe_indexed(const qgemm_wdesc* desc, const void* packed, int3
  * E < 1 or R <= 0.
  */
 size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R);
+
+/*
+ * Workspace bytes for the fastest schedule of qgemm_moe_indexed with afmt activations
+ * (QGEMM_A_BF16 or QGEMM_A_FP8E4M3_TOKEN), T rows of X and R sorted positions: the FP16
+ * activation copy of the T rows for INT4 weights with BF16 scales, then from R = 2048 on the
+ * sorted copy of the R rows (R * K * 2 bytes, or R * K for FP8, each part rounded up to 256)
+ * and their FP32 scales (FP8 or FP16 activations), then the stream-K slots as in
+ * qgemm_moe_workspace_bytes.  0 for an invalid descriptor or afmt, E < 1, T < 0 or R <= 0.
+ */
+size_t qgemm_moe_indexed_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int32_t afmt,
+                                         int64_t T, int64_t R);
 
 /*
  * Test hook: unpack a packed matrix back to BF16 W[n, k] = RNE_bf16(dequant) through the

@@ -14,7 +14,8 @@ import torch
 __all__ = [
     "QGemmError", "WeightDesc", "lib", "lib_path", "packed_bytes", "repack", "workspace_bytes",
     "w4a16", "w4a8", "quant_act_fp8", "moe_grouped", "dequant_debug", "device_status",
-    "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "host_staging_bytes",
+    "force_config", "plan", "moe_workspace_bytes", "moe_workspace", "moe_indexed_workspace_bytes",
+    "moe_indexed_workspace", "host_staging_bytes",
     "host_staging", "w4a16_host", "moe_indexed", "check_desc", "WFMT", "AFMT", "EXPORTS",
     "debug_stall", "act_copy_bytes", "w4a4", "quant_act_mxfp4",
 ]
@@ -31,7 +32,8 @@ EXPORTS = ("qgemm_version", "qgemm_status_str", "qgemm_check_desc", "qgemm_packe
            "qgemm_force_config", "qgemm_w4a16_noalloc", "qgemm_plan",
            "qgemm_moe_workspace_bytes", "qgemm_host_staging_bytes", "qgemm_w4a16_host",
            "qgemm_moe_indexed", "qgemm_repack_scaled", "qgemm_debug_stall",
-           "qgemm_act_copy_bytes", "qgemm_w4a4", "qgemm_quant_act_mxfp4")
+           "qgemm_act_copy_bytes", "qgemm_w4a4", "qgemm_quant_act_mxfp4",
+           "qgemm_moe_indexed_workspace_bytes")
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "alignment", 4: "workspace",
           5: "bad packed", 6: "cuda error", 7: "timeout", 8: "no device", 9: "bad value"}
@@ -106,6 +108,7 @@ def lib():
         "qgemm_w4a16_noalloc": (ctypes.c_int, [D, P, P, I64, I64, P, P, I64, P]),
         "qgemm_plan": (ctypes.c_int, [D, I64, P]),
         "qgemm_moe_workspace_bytes": (SZ, [D, I32, I64]),
+        "qgemm_moe_indexed_workspace_bytes": (SZ, [D, I32, I32, I64, I64]),
         "qgemm_act_copy_bytes": (SZ, [D, I64]),
         "qgemm_w4a4": (ctypes.c_int, [D, P, P, I64, I64, P, I64, P, P, P, I64, P, SZ, P]),
         "qgemm_quant_act_mxfp4": (ctypes.c_int, [P, I64, I64, I64, P, I64, P, I64, P]),
@@ -319,6 +322,18 @@ def moe_workspace_bytes(desc, E, R):
 def moe_workspace(desc, E, R, device="cuda"):
     """A zero-filled workspace that lets qgemm_moe_grouped use stream-K (reusable)."""
     return torch.zeros(max(moe_workspace_bytes(desc, E, R), 256), dtype=torch.uint8, device=device)
+
+
+def moe_indexed_workspace_bytes(desc, E, T, R, fp8=False):
+    d = desc.c()
+    return int(lib().qgemm_moe_indexed_workspace_bytes(ctypes.byref(d), int(E),
+                                                       AFMT["fp8" if fp8 else "bf16"], int(T), int(R)))
+
+
+def moe_indexed_workspace(desc, E, T, R, fp8=False, device="cuda"):
+    """A zero-filled workspace for qgemm_moe_indexed's fastest schedule (reusable)."""
+    return torch.zeros(max(moe_indexed_workspace_bytes(desc, E, T, R, fp8), 256), dtype=torch.uint8,
+                       device=device)
 
 
 def act_copy_bytes(desc, x_rows):

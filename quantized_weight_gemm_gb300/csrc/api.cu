@@ -285,6 +285,16 @@ int64_t moe_ws_bytes(int tt, int sms) {
   return 2 * int64_t(sms) * slot_bytes(tt) + round_up(int64_t(sms) * 4, 256);
 }
 
+// Indexed MoE over many rows: the rows gathered into the workspace in sorted order (and,
+// for FP8 or FP16 activations, their scales) for the grouped kernel.  The in-kernel gather
+// copies about 6 bytes per cycle per SM; at prefill sizes the copy first is faster.
+constexpr int64_t kIndexedCopyMinRows = 2048;
+
+int64_t indexed_copy_bytes(const Layout& L, int64_t R, bool fp8) {
+  const int64_t esz = fp8 ? 1 : 2;
+  return round_up(R * L.K * esz, 256) + ((fp8 || f16_operands(L)) ? round_up(R * 4, 256) : 0);
+}
+
 typedef PFN_cuTensorMapEncodeTiled_v12000 EncodeFn;
 
 EncodeFn encode_fn() {
@@ -704,43 +714,62 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   GemmPlan plan;
   const bool inv = batch_invariant(desc);
   if (inv && row_index != nullptr) return QGEMM_ERR_UNSUPPORTED;
-  const int tt = inv ? kInvariantTile
-                     : row_index != nullptr ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
-  if (row_index != nullptr && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathering kernels: <= 64
-  plan.token_tile = tt;
-  plan.splits = 1;
-  plan.sk_tiles = 0;
-  plan.max_contrib = 0;
-  plan.grid = dev->sms;
   // FP16 operands: the pre-pass's FP16 copy of the x_rows rows of X and their row scales
   // lead the workspace, which is then required
   const bool f16 = f16_operands(L);
   const int64_t prep = f16 ? prep_x_f16_bytes(x_rows, L.K) : 0;
   if (f16 && (ws == nullptr || int64_t(ws_bytes) < prep)) return QGEMM_ERR_WORKSPACE;
-  if (f16 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+  if ((f16 || ws != nullptr) && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
+  // Indexed calls over many rows gather them into the workspace first and run the grouped
+  // kernel on the sorted copy, when the workspace holds it.
+  const bool copy = row_index != nullptr && R >= kIndexedCopyMinRows &&
+                    int64_t(ws_bytes) >= prep + indexed_copy_bytes(L, R, fp8) && g_force_tile == 0;
+  const bool gather = row_index != nullptr && !copy;     // the gathering kernel
+  const int tt = inv ? kInvariantTile : gather ? moe_indexed_token_tile(R, E) : moe_token_tile(R, E);
+  if (gather && tt > 64) return QGEMM_ERR_UNSUPPORTED;   // gathering kernels: <= 64
+  plan.token_tile = tt;
+  plan.splits = 1;
+  plan.sk_tiles = 0;
+  plan.max_contrib = 0;
+  plan.grid = dev->sms;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
   const void* xg = X;
   int64_t ldg = ldx;
-  float* rowscale = nullptr;
+  const float* tok = tok_scale;
   if (f16) {
-    rowscale = reinterpret_cast<float*>(wsb + round_up(x_rows * L.K * 2, 256));
-    if (launch_prep_x_f16(X, x_rows, L.K, ldx, wsb, rowscale,
-                          static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    float* rowscale = reinterpret_cast<float*>(wsb + round_up(x_rows * L.K * 2, 256));
+    if (launch_prep_x_f16(X, x_rows, L.K, ldx, wsb, rowscale, st) != cudaSuccess)
       return QGEMM_ERR_CUDA;
     xg = wsb;
     ldg = L.K;
+    tok = rowscale;
     plan.pdl = 1;
+  }
+  int64_t head = prep;                                   // workspace bytes before the slots
+  if (copy) {
+    const int64_t esz = fp8 ? 1 : 2;
+    uint8_t* sorted = wsb + prep;
+    float* sorted_scale = (fp8 || f16) ? reinterpret_cast<float*>(sorted + round_up(R * L.K * esz, 256))
+                                       : nullptr;
+    if (launch_gather_rows(xg, ldg * esz, x_rows, row_index, R, L.K * esz, sorted, L.K * esz,
+                           tok, sorted_scale, dev->status, st) != cudaSuccess)
+      return QGEMM_ERR_CUDA;
+    xg = sorted;
+    ldg = L.K;
+    tok = sorted_scale;
+    plan.pdl = 0;                      // the GEMM follows the gather, not the pre-pass
+    head += indexed_copy_bytes(L, R, fp8);
   }
   // the gathering kernel copies X rows itself and never reads a tensor map
   CUtensorMap tmap;
   memset(&tmap, 0, sizeof(tmap));
   int x3d = 0;
-  if (row_index == nullptr &&
-      !make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, R, L.K, ldg, tt, &x3d))
+  if (!gather && !make_x_map(&tmap, xg, fp8 ? X_FP8 : f16 ? X_F16 : X_BF16, R, L.K, ldg, tt, &x3d))
     return QGEMM_ERR_CUDA;
   GemmArgs a;
   memset(&a, 0, sizeof(a));
-  if (row_index != nullptr) {
+  if (gather) {
     a.x = static_cast<const uint8_t*>(xg);
     a.ldx_bytes = ldg * (fp8 ? 1 : 2);
     a.x_rows = x_rows;
@@ -751,22 +780,21 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   a.expert_stride = L.total_bytes;
   if (L.afmt == A_FP8N && !make_w4_map(&a.tmap_w, L, packed, E, L.total_bytes)) return QGEMM_ERR_CUDA;
   a.offsets = expert_offsets;
-  a.row_index = row_index;
+  a.row_index = gather ? row_index : nullptr;
   a.E = E;
   a.M = R;
   a.splits = 1;
   a.bias = bias;
   a.bias_stride = L.N;
-  a.tok_scale = f16 ? rowscale : tok_scale;
+  a.tok_scale = tok;
   a.Y = Y;
   a.ldy = ldy;
-  // Stream-K needs the whole bound after the activation copy; a smaller (or no) workspace
-  // keeps whole tiles.
+  // Stream-K needs the whole bound after the activation copies; a smaller (or no)
+  // workspace keeps whole tiles.
   if (ws != nullptr && !inv && g_force_splits != 1 && sk_fits(L, plan.grid) &&
-      int64_t(ws_bytes) >= prep + moe_ws_bytes(tt, plan.grid)) {
-    if (!aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
-    a.ws = reinterpret_cast<float*>(wsb + prep);
-    a.counters = reinterpret_cast<int32_t*>(wsb + prep + 2 * int64_t(plan.grid) * slot_bytes(tt));
+      int64_t(ws_bytes) >= head + moe_ws_bytes(tt, plan.grid)) {
+    a.ws = reinterpret_cast<float*>(wsb + head);
+    a.counters = reinterpret_cast<int32_t*>(wsb + head + 2 * int64_t(plan.grid) * slot_bytes(tt));
   }
   a.status = dev->status;
   a.timeout_ns = timeout_ns();
@@ -810,6 +838,18 @@ size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R) 
   const int tt = std::max(moe_token_tile(R, E), std::min(moe_indexed_token_tile(R, E), 64));
   const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(R, L.K) : 0;
   return size_t(prep + moe_ws_bytes(tt, sms_or_default()));
+}
+
+size_t qgemm_moe_indexed_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int32_t afmt,
+                                         int64_t T, int64_t R) {
+  Layout L;
+  if (!layout_of(desc, &L) || E < 1 || R <= 0 || T < 0) return 0;
+  if (afmt != QGEMM_A_BF16 && afmt != QGEMM_A_FP8E4M3_TOKEN) return 0;
+  const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
+  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(T, L.K) : 0;
+  const int64_t copy = R >= kIndexedCopyMinRows ? indexed_copy_bytes(L, R, fp8) : 0;
+  const int tt = copy > 0 ? moe_token_tile(R, E) : std::min(moe_indexed_token_tile(R, E), 64);
+  return size_t(prep + copy + moe_ws_bytes(tt, sms_or_default()));
 }
 
 qgemm_status qgemm_dequant_debug(const qgemm_wdesc* desc, const void* packed, void* W_out,

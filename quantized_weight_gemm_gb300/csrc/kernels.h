@@ -39,6 +39,14 @@ cudaError_t launch_quant_act_mxfp4(const void* X, int64_t M, int64_t K, int64_t 
                                    int64_t ldq, uint8_t* exps, int64_t lde, cudaStream_t st);
 cudaError_t launch_quant_act_fp8(const void* X, int64_t M, int64_t K, int64_t ldx, uint8_t* Xq,
                                  int64_t ldq, float* s, cudaStream_t st);
+// Indexed MoE: dst row r (dst_ld bytes apart) = src row idx[r] (src_ld bytes apart, src_rows
+// rows), row_bytes bytes (a multiple of 16, both pointers and strides 16-byte aligned); a
+// negative index gives a zero row, an index >= src_rows sets kStatusBadValue in *status and
+// gives a zero row.  If dst_scale is given, dst_scale[r] = src_scale[idx[r]] (0 for padding).
+cudaError_t launch_gather_rows(const void* src, int64_t src_ld, int64_t src_rows,
+                               const int32_t* idx, int64_t R, int64_t row_bytes, void* dst,
+                               int64_t dst_ld, const float* src_scale, float* dst_scale,
+                               int* status, cudaStream_t st);
 
 // Arguments of the tensor-core GEMM kernel (dense and MoE grouped).
 struct GemmArgs {

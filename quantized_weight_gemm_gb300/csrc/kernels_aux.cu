@@ -389,6 +389,52 @@ cudaError_t launch_prep_x_f16(const void* X, int64_t rows, int64_t K, int64_t ld
   return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ indexed MoE: row gather
+// One warp per sorted position r: dst row r = src row idx[r] (row_bytes bytes, 16-byte
+// vectors), or zeros for a negative index; an index past the end sets the bad-value status
+// and gives zeros.  With scales, dst_scale[r] = src_scale[idx[r]] (0 for padding).
+constexpr int kGatherWarps = 8;
+
+__global__ void __launch_bounds__(kGatherWarps * 32)
+gather_rows_kernel(const uint8_t* __restrict__ src, int64_t src_ld, int64_t src_rows,
+                   const int32_t* __restrict__ idx, int64_t R, int64_t row_bytes,
+                   uint8_t* __restrict__ dst, int64_t dst_ld, const float* __restrict__ src_scale,
+                   float* __restrict__ dst_scale, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = int64_t(blockIdx.x) * kGatherWarps + (threadIdx.x >> 5);
+  if (r >= R) return;
+  const int32_t t = idx[r];
+  const bool ok = t >= 0 && t < src_rows;
+  if (lane == 0 && t >= src_rows) atomicCAS(status, 0, kStatusBadValue);
+  uint4* d = reinterpret_cast<uint4*>(dst + r * dst_ld);
+  const int64_t nv = row_bytes / 16;
+  if (ok) {
+    const uint4* s = reinterpret_cast<const uint4*>(src + int64_t(t) * src_ld);
+    int64_t v = lane;
+    for (; v + 96 < nv; v += 128) {        // four 16-byte loads in flight per lane
+      const uint4 a0 = __ldg(s + v), a1 = __ldg(s + v + 32), a2 = __ldg(s + v + 64),
+                  a3 = __ldg(s + v + 96);
+      d[v] = a0; d[v + 32] = a1; d[v + 64] = a2; d[v + 96] = a3;
+    }
+    for (; v < nv; v += 32) d[v] = __ldg(s + v);
+  } else {
+    for (int64_t v = lane; v < nv; v += 32) d[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (dst_scale != nullptr && lane == 0) dst_scale[r] = ok ? src_scale[t] : 0.0f;
+}
+
+cudaError_t launch_gather_rows(const void* src, int64_t src_ld, int64_t src_rows,
+                               const int32_t* idx, int64_t R, int64_t row_bytes, void* dst,
+                               int64_t dst_ld, const float* src_scale, float* dst_scale,
+                               int* status, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  const int64_t blocks = (R + kGatherWarps - 1) / kGatherWarps;
+  gather_rows_kernel<<<unsigned(blocks), kGatherWarps * 32, 0, st>>>(
+      static_cast<const uint8_t*>(src), src_ld, src_rows, idx, R, row_bytes,
+      static_cast<uint8_t*>(dst), dst_ld, src_scale, dst_scale, status);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------ MXFP4 act quantization
 // One warp per 32-element block (lane = element), 8 warps per block of rows: the block's
 // largest |x| (BF16 magnitude bits), E = floor(log2 amax) - 2 + 127 clamped to [0, 254]

@@ -304,6 +304,53 @@ def test_moe_indexed_router(afmt, stream_k):
         _assert_close(y, ref, TOL_A8)
 
 
+@pytest.mark.parametrize("wfmt,afmt", [("mxfp4", "bf16"), ("uint4_zp", "bf16"), ("mxfp4", "fp8"),
+                                       ("mxfp4", "fp8n")])
+@pytest.mark.parametrize("copy", [False, True])
+def test_moe_indexed_many_rows(wfmt, afmt, copy):
+    """Indexed calls of 2048 rows or more: with the indexed workspace the rows are gathered
+    into it first and the grouped kernel runs on the copy; with a forced token tile the
+    gathering kernel runs instead.  Both against the oracle, twice on one workspace."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    case = WL.moe_case(T=320, seed=9, E=16, topk=8, hidden=512, inter=64)
+    r = WL.rng(49)
+    ws = [WL.gen_weights(r, wfmt, 256, 512) for _ in range(16)]
+    idx = case.token_of_row.astype(np.int32)
+    R, T = len(idx), case.T
+    assert R >= 2048
+    fp8 = afmt != "bf16"
+    d, packed = _pack_experts(ws, afmt)
+    off = torch.tensor(np.asarray(case.offsets, dtype=np.int32), device="cuda")
+    it = torch.tensor(idx, device="cuda")
+    wsp = qg.moe_indexed_workspace(d, 16, T, R, fp8=fp8)
+    if fp8:
+        from oracle import formats as F
+        xq, s = oracle.quant_act_fp8(WL.gen_x(WL.rng(50), T, 512, outliers=True))
+        ref = oracle.moe_indexed(F.e4m3_to_float(xq), case.offsets, idx, _experts_exact(ws),
+                                 tok_scale=s)
+        X = G.u8_tensor(xq)
+        ts = torch.from_numpy(s).cuda()
+    else:
+        x = case.x_tok_bits
+        ref = oracle.moe_indexed(F_bits(x), case.offsets, idx, _experts_a16(ws))
+        X = G.bf16_tensor(x)
+        ts = None
+    out = torch.empty(R, 256, dtype=torch.bfloat16, device="cuda")
+    if not copy:
+        qg.force_config(32, 0)       # a forced token tile keeps the in-kernel gather
+    try:
+        for _ in range(2):
+            out.fill_(float("nan"))
+            y = qg.moe_indexed(d, packed, 16, X, off, it, tok_scale=ts, out=out, ws=wsp)
+            torch.cuda.synchronize()
+            assert qg.device_status(clear=True) == 0
+            valid = idx >= 0
+            _assert_close(G.to_f64(y)[valid], ref[valid], TOL_A8 if fp8 else TOL_A16)
+    finally:
+        qg.force_config(0, 0)
+
+
 def test_moe_indexed_nvfp4():
     """Indexed rows with NVFP4 experts, each with its own per-tensor scale, with and without
     stream-K (K blocks enough to cut the leftover tiles)."""

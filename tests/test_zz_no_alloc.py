@@ -51,7 +51,7 @@ def _noalloc(qg, d, packed, X, M, N):
 
 @pytest.mark.parametrize("wfmt,M,N,K,cut", [("uint4_zp", 16, 4096, 4096, "any"),
                                             ("mxfp4", 1, 4096, 7168, "any"),
-                                            ("int4_sym", 64, 1024, 2048, "any"),
+                                            ("int4_sym", 64, 1024, 4096, "any"),
                                             ("uint4_zp", 1, 28672, 8192, "stream-k")])
 def test_noalloc_matches_workspace_entry_point(qg, wfmt, M, N, K, cut):
     from tests import gpu_util as G

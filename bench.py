@@ -71,20 +71,19 @@ def alg_bytes(M, N, K):
 # (N, K, M), with the digest of the kernel sources they were taken on; a changed kernel
 # reports null until it is captured again.
 CAPTURED_TRAFFIC = {
-    # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch),
-    # captured at digest beff4503...; the sources changed since only in host code that this
-    # launch does not take (descriptor flags and the batch-invariant plan), so the digest
-    # below re-keys the same counters
-    "csrc_sha256": "64dccaa118d5c8b9876b19255cb290b4ed61b6884299c60385d5e67e436bba29",
-    "launches": {"28672,8192,8192": 2983337000 + 926694656},
+    # profiles/qgemm_tc_kernel_tile256_w4a16_28672x8192_m8192.md (ncu --set full, one launch of
+    # the GEMM kernel; dram__bytes_read.sum + dram__bytes_write.sum)
+    "csrc_sha256": "e692841234ffe4850398c8a6d9298ddf256c756fd5bc073440b62f5fc921cf38",
+    "launches": {"28672,8192,8192": 2434685000 + 495768064},
 }
 
 
-# Sources that define the GEMM kernel and its launch plan (not the repack, quantization or
-# no-alloc wrappers).
+# Sources that define the GEMM kernel, its activation pre-pass and its launch plan (not the
+# no-alloc or host-buffer wrappers).
 GEMM_SOURCES = ("api.cu", "dequant.cuh", "gemm_a16_any.cu", "gemm_a16_mxfp4.cu",
-                "gemm_a16_sym_g1.cu", "gemm_a16_zp_g1.cu", "gemm_a8.cu", "gemm_kernel.cuh",
-                "kernels.h", "ptx.cuh", "qgemm_internal.h")
+                "gemm_a16_mxint4.cu", "gemm_a16_nvfp4.cu", "gemm_a16_sym_g1.cu",
+                "gemm_a16_zp_g1.cu", "gemm_a4.cu", "gemm_a8.cu", "gemm_a8n.cu",
+                "gemm_kernel.cuh", "kernels.h", "kernels_aux.cu", "ptx.cuh", "qgemm_internal.h")
 
 
 def _code_only(text):

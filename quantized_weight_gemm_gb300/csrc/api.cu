@@ -285,6 +285,12 @@ int64_t moe_ws_bytes(int tt, int sms) {
   return 2 * int64_t(sms) * slot_bytes(tt) + round_up(int64_t(sms) * 4, 256);
 }
 
+// MXFP4 with BF16 activations: the calls that may run on FP16 operands (given the
+// workspace for the activation copy), by their token tile; see mx_f16_capable().
+bool mx_f16_call(const Layout& L, int token_tile, bool invariant) {
+  return mx_f16_capable(L) && !invariant && token_tile <= kMxF16MaxTile;
+}
+
 // Indexed MoE over many rows: the rows gathered into the workspace in sorted order (and,
 // for FP8 or FP16 activations, their scales) for the grouped kernel.  The in-kernel gather
 // copies about 6 bytes per cycle per SM; at prefill sizes the copy first is faster.
@@ -292,7 +298,7 @@ constexpr int64_t kIndexedCopyMinRows = 2048;
 
 int64_t indexed_copy_bytes(const Layout& L, int64_t R, bool fp8) {
   const int64_t esz = fp8 ? 1 : 2;
-  return round_up(R * L.K * esz, 256) + ((fp8 || f16_operands(L)) ? round_up(R * 4, 256) : 0);
+  return round_up(R * L.K * esz, 256) + round_up(R * 4, 256);   // rows, then their scales
 }
 
 typedef PFN_cuTensorMapEncodeTiled_v12000 EncodeFn;
@@ -463,10 +469,15 @@ qgemm_status run_dense(const qgemm_wdesc* desc, int32_t afmt, const void* packed
   DeviceInfo* dev = nullptr;
   if (!current_device(&dev)) return QGEMM_ERR_NO_DEVICE;
   GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
-  // FP16 operands: the pre-pass's FP16 rows and row scales lead the workspace
-  const bool f16 = f16_operands(L);
+  // FP16 operands: the pre-pass's FP16 rows and row scales lead the workspace (INT4 with
+  // BF16 scales always; MXFP4 in small calls when the workspace holds the copy)
+  const int64_t split = split_ws_bytes(L, M, plan);
+  const bool f16 = f16_operands(L) ||
+                   (mx_f16_call(L, plan.token_tile, batch_invariant(desc)) && ws != nullptr &&
+                    int64_t(ws_bytes) >= prep_x_f16_bytes(M, L.K) + split);
+  plan.mx_f16 = f16 && !f16_operands(L);
   const int64_t prep = f16 ? prep_x_f16_bytes(M, L.K) : 0;
-  const int64_t need = prep + split_ws_bytes(L, M, plan);
+  const int64_t need = prep + split;
   if (need > 0 && (ws == nullptr || int64_t(ws_bytes) < need)) return QGEMM_ERR_WORKSPACE;
   if (need > 0 && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
   uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -533,8 +544,8 @@ namespace qgemm {
 
 qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, const void* X,
                                int64_t M, int64_t ldx, const float* chan_scale, const void* Y,
-                               int64_t ldy, int64_t* need, int64_t* counter_off,
-                               int64_t* counter_bytes) {
+                               int64_t ldy, int64_t capacity, int64_t* need,
+                               int64_t* counter_off, int64_t* counter_bytes) {
   *need = *counter_off = *counter_bytes = 0;
   Layout L;
   const qgemm_status s = check_dense(desc, A_BF16, packed, X, M, ldx, nullptr, chan_scale,
@@ -545,8 +556,13 @@ qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, cons
   const GemmPlan plan = plan_dense(L, M, dev->sms, batch_invariant(desc));
   int64_t slots, counters;
   cut_sizes(L, M, plan, &slots, &counters);
-  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(M, L.K) : 0;
   const int64_t split = split_ws_bytes(L, M, plan);
+  // the same choice as run_dense makes with a workspace of `need` bytes: INT4 with BF16
+  // scales always takes the activation copy, small MXFP4 calls when it fits the capacity
+  const bool f16 = f16_operands(L) ||
+                   (mx_f16_call(L, plan.token_tile, batch_invariant(desc)) &&
+                    prep_x_f16_bytes(M, L.K) + split <= capacity);
+  const int64_t prep = f16 ? prep_x_f16_bytes(M, L.K) : 0;
   *need = prep + split;
   if (split > 0) {
     *counter_off = prep + slots * slot_bytes(plan.token_tile);
@@ -621,10 +637,14 @@ size_t qgemm_workspace_bytes(const qgemm_wdesc* desc, int64_t M_max) {
   int64_t best = 0;
   const int64_t top = std::min<int64_t>(M_max, kSplitMaxM);
   const bool inv = batch_invariant(desc);
-  for (int64_t M = 1; M <= top; ++M)
-    best = std::max(best, split_ws_bytes(L, M, plan_dense(L, M, sms, inv)));
-  best = std::max(best, split_ws_bytes(L, M_max, plan_dense(L, M_max, sms, inv)));
-  // FP16 operands: the activation copy, largest at M_max
+  // (MXFP4: narrow-tile calls also hold their FP16 activation copy)
+  auto need = [&](int64_t M) {
+    const GemmPlan p = plan_dense(L, M, sms, inv);
+    return split_ws_bytes(L, M, p) + (mx_f16_call(L, p.token_tile, inv) ? prep_x_f16_bytes(M, L.K) : 0);
+  };
+  for (int64_t M = 1; M <= top; ++M) best = std::max(best, need(M));
+  best = std::max(best, need(M_max));
+  // FP16 operands (INT4 with BF16 scales): the activation copy, largest at M_max
   if (f16_operands(L)) best += prep_x_f16_bytes(M_max, L.K);
   return size_t(best);
 }
@@ -715,8 +735,12 @@ qgemm_status run_moe(const qgemm_wdesc* desc, const void* packed, int32_t E, int
   const bool inv = batch_invariant(desc);
   if (inv && row_index != nullptr) return QGEMM_ERR_UNSUPPORTED;
   // FP16 operands: the pre-pass's FP16 copy of the x_rows rows of X and their row scales
-  // lead the workspace, which is then required
-  const bool f16 = f16_operands(L);
+  // lead the workspace, which is then required (INT4 with BF16 scales); MXFP4 experts take
+  // them for narrow token tiles when the workspace holds the copy
+  const bool mx = !fp8 && mx_f16_call(L, moe_token_tile(R, E), inv) && ws != nullptr &&
+                  int64_t(ws_bytes) >= prep_x_f16_bytes(x_rows, L.K);
+  const bool f16 = f16_operands(L) || mx;
+  plan.mx_f16 = mx ? 1 : 0;
   const int64_t prep = f16 ? prep_x_f16_bytes(x_rows, L.K) : 0;
   if (f16 && (ws == nullptr || int64_t(ws_bytes) < prep)) return QGEMM_ERR_WORKSPACE;
   if ((f16 || ws != nullptr) && !aligned(ws, 256)) return QGEMM_ERR_ALIGNMENT;
@@ -836,7 +860,8 @@ size_t qgemm_moe_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int64_t R) 
   Layout L;
   if (!layout_of(desc, &L) || E < 1 || R <= 0) return 0;
   const int tt = std::max(moe_token_tile(R, E), std::min(moe_indexed_token_tile(R, E), 64));
-  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(R, L.K) : 0;
+  const bool f16 = f16_operands(L) || mx_f16_call(L, moe_token_tile(R, E), false);
+  const int64_t prep = f16 ? prep_x_f16_bytes(R, L.K) : 0;
   return size_t(prep + moe_ws_bytes(tt, sms_or_default()));
 }
 
@@ -846,7 +871,8 @@ size_t qgemm_moe_indexed_workspace_bytes(const qgemm_wdesc* desc, int32_t E, int
   if (!layout_of(desc, &L) || E < 1 || R <= 0 || T < 0) return 0;
   if (afmt != QGEMM_A_BF16 && afmt != QGEMM_A_FP8E4M3_TOKEN) return 0;
   const bool fp8 = afmt == QGEMM_A_FP8E4M3_TOKEN;
-  const int64_t prep = f16_operands(L) ? prep_x_f16_bytes(T, L.K) : 0;
+  const bool f16 = f16_operands(L) || (!fp8 && mx_f16_call(L, moe_token_tile(R, E), false));
+  const int64_t prep = f16 ? prep_x_f16_bytes(T, L.K) : 0;
   const int64_t copy = R >= kIndexedCopyMinRows ? indexed_copy_bytes(L, R, fp8) : 0;
   const int tt = copy > 0 ? moe_token_tile(R, E) : std::min(moe_indexed_token_tile(R, E), 64);
   return size_t(prep + copy + moe_ws_bytes(tt, sms_or_default()));

@@ -15,7 +15,9 @@
 //   1024.0 = 0x6400 has a unit last place, so 0x6400 | u is 1024 + u): one FP16 multiply
 //   by s * 2^k rounds (u - z) * s * 2^k to 11 significant bits, where BF16 would keep 8
 //   of the up to 12 that the product has.
-//   MXFP4: the e2m1 magnitude bits (e1 e0 m) are moved to bf16 bits 8..6 and the sign to
+//   MXFP4 (codes in natural order, one byte = two elements): a byte permute places the
+//   byte's two nibbles at bits 0..3 and 16..19; then the e2m1 magnitude bits (e1 e0 m) are
+//   moved to bf16 bits 8..6 and the sign to
 //   bit 15, which is the bf16 number e2m1(q) * 2^-126 (a subnormal for e = 0); multiplying
 //   by 2^(E-1) (or by 2^127 and then 2^(E-128) when E > 128) gives e2m1(q) * 2^(E-127),
 //   exact unless it overflows bf16.
@@ -76,6 +78,42 @@ __device__ __forceinline__ void decode_mxfp4_word(uint32_t w, uint32_t sa, uint3
     if (two_step) r = ptx::bf16x2_mul(r, sb);
     out[i] = r;
   }
+}
+
+// MXFP4 word in natural order (element 2j in the low nibble of byte j) -> 4 bf16x2: the low
+// and the high nibbles of all four bytes are masked out once (u, v); one byte permute then
+// takes byte j of u to byte 0 and byte j of v to byte 2, with zero bytes between (the
+// selector's sign-replicate bit on a byte below 16), which puts pair j's two codes at bits
+// 0..3 and 16..19; then the bit move above.
+__device__ __forceinline__ void decode_mxfp4_word_nat(uint32_t w, uint32_t sa, uint32_t sb,
+                                                      bool two_step, uint32_t* out) {
+  const uint32_t u = w & 0x0F0F0F0Fu, v = (w >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ptx::prmt(u, v, 0x8080u | uint32_t(i) | (uint32_t(4 + i) << 8));
+    const uint32_t x = (t * 0x1040u) & 0x81C081C0u;
+    uint32_t r = ptx::bf16x2_mul(x, sa);
+    if (two_step) r = ptx::bf16x2_mul(r, sb);
+    out[i] = r;
+  }
+}
+
+// MXFP4 word in natural order -> 4 f16x2: the hardware e2m1x2 -> f16x2 conversion (exact),
+// then one FP16 multiply by f2 = the block's 2^(E - 127 + k) (exact while the product stays
+// on FP16's grid, see PackedHeader::w_prescale).
+__device__ __forceinline__ void decode_mxfp4_word_f16(uint32_t w, uint32_t f2, uint32_t* out) {
+  out[0] = ptx::f16x2_mul(ptx::cvt_f16x2_e2m1x2<0>(w), f2);
+  out[1] = ptx::f16x2_mul(ptx::cvt_f16x2_e2m1x2<1>(w), f2);
+  out[2] = ptx::f16x2_mul(ptx::cvt_f16x2_e2m1x2<2>(w), f2);
+  out[3] = ptx::f16x2_mul(ptx::cvt_f16x2_e2m1x2<3>(w), f2);
+}
+
+// f16x2 of 2^(E - 127) * p for an E8M0 exponent E and a power of two p (FP32 2^(E-127) is
+// exact, also the subnormal 2^-127 for E = 0; the product rounds once to FP16, to 0 far
+// below FP16's range).
+__device__ __forceinline__ uint32_t e8m0_f16x2(uint32_t E, float p) {
+  const float v = __uint_as_float(E != 0u ? (E << 23) : 0x00400000u) * p;
+  return ptx::cvt_f16x2_f32(v, v);
 }
 
 // bf16x2 factors applying 2^(E-127) to the subnormal-offset e2m1 value (see above).

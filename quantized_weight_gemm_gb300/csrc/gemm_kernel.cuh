@@ -363,13 +363,16 @@ struct Ring {
 enum DecodeMode : int {
   DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5,
   DM_W4A4 = 6,                 // MXFP4 x MXFP4: no decode, the MMA reads the codes
-  DM_W4A8N = 7                 // MXFP4 x FP8 on FP4 operands: no decode either
+  DM_W4A8N = 7,                // MXFP4 x FP8 on FP4 operands: no decode either
+  DM_MXFP4_F16 = 8             // MXFP4 x BF16 activations on FP16 operands (small calls)
 };
 
-// INT4 with BF16 scales (every group size): FP16 tensor-core operands, see f16_operands().
+// INT4 with BF16 scales (every group size) and MXFP4 in small calls: FP16 tensor-core
+// operands, see f16_operands() and mx_f16_capable().
 template <bool A8, int DM>
 constexpr bool kF16Operands =
-    !A8 && (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1 || DM == DM_INT4_ANY);
+    !A8 && (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1 || DM == DM_INT4_ANY ||
+            DM == DM_MXFP4_F16);
 
 // Decode two 32-K chunks of weight row r into 32 registers of 16-bit pairs (pair order):
 // FP16 for INT4 with BF16 scales (the scale times w_pre = 2^k), BF16 for the other formats.
@@ -404,7 +407,11 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
         mxfp4_factors(E, sa, sb, big);
         const bool two = __any_sync(0xffffffffu, big);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) decode_mxfp4_word(wd[j], sa, sb, two, &regs[16 * c + 4 * j]);
+        for (int j = 0; j < 4; ++j) decode_mxfp4_word_nat(wd[j], sa, sb, two, &regs[16 * c + 4 * j]);
+      } else if constexpr (DM == DM_MXFP4_F16) {
+        const uint32_t f2 = e8m0_f16x2(rec[tail + r * 4 + rchunk0 + c], w_pre);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) decode_mxfp4_word_f16(wd[j], f2, &regs[16 * c + 4 * j]);
       } else if constexpr (DM == DM_MXINT4) {
         const uint32_t s2 = e8m0_bf16x2(rec[tail + r * 4 + rchunk0 + c]);   // one E8M0 per 32 K
 #pragma unroll
@@ -1166,7 +1173,10 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       // NVFP4 and the FP16 operands: the accumulator scale of the unit's expert, from its
       // packed header
       float acc_s = 1.0f;
-      if constexpr (DM == DM_NVFP4 || F16)
+      if constexpr (DM == DM_MXFP4_F16)     // (the header's acc_scale serves the BF16 decode)
+        acc_s = 1.0f / __ldg(&reinterpret_cast<const PackedHeader*>(
+                                a.packed + int64_t(w.expert) * a.expert_stride)->w_prescale);
+      else if constexpr (DM == DM_NVFP4 || F16)
         acc_s = __ldg(&reinterpret_cast<const PackedHeader*>(
                           a.packed + int64_t(w.expert) * a.expert_stride)->acc_scale);
       // Partial accumulators of the issuers that had a stage in this unit: the unit's

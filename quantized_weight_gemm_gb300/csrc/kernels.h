@@ -11,14 +11,16 @@
 namespace qgemm {
 
 // The scratch that the dense W4A16 call would use for these arguments under its own plan
-// for M: *need bytes in all (0 when the plan cuts no tile's K range), of which the arrival
+// for M, given at most `capacity` bytes: *need bytes in all (the FP16 activation copy where
+// the call makes one -- always for INT4 with BF16 scales, for small MXFP4 calls when it fits
+// the capacity -- then the partial sums of cut tiles; 0 for neither), of which the arrival
 // counters, [*counter_off, *counter_off + *counter_bytes), must be zero at launch.  Checks
 // every argument as qgemm_w4a16 does and returns its error, if any, before looking at the
-// device.
+// device.  qgemm_w4a16 given exactly *need bytes of workspace runs the same schedule.
 qgemm_status dense_a16_scratch(const qgemm_wdesc* desc, const void* packed, const void* X,
                                int64_t M, int64_t ldx, const float* chan_scale, const void* Y,
-                               int64_t ldy, int64_t* need, int64_t* counter_off,
-                               int64_t* counter_bytes);
+                               int64_t ldy, int64_t capacity, int64_t* need,
+                               int64_t* counter_off, int64_t* counter_bytes);
 
 int* device_status_ptr();
 
@@ -116,6 +118,9 @@ struct GemmPlan {
   // activation pre-pass): its prologue and weight stream start early, and its reads of the
   // pre-pass's output wait for that kernel (griddepcontrol.wait).
   int pdl = 0;
+  // MXFP4 weights with BF16 activations: FP16 operands (the activation copy made by the
+  // pre-pass, the weights decoded by the hardware e2m1 conversion); see mx_f16_capable().
+  int mx_f16 = 0;
 };
 
 // Launch the tcgen05 GEMM for the given plan.  tmap describes X (BF16 or E4M3, K-major,

@@ -53,9 +53,11 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
       for (int e = 0; e < 8; ++e) {
         uint32_t nib = pad ? 0u : (src >> (4 * e)) & 0xFu;   // even k in the low nibble
         if (L.wfmt == W_INT4_SYM || L.wfmt == W_MXINT4) nib ^= 8u;   // two's complement -> q + 8
-        const int pos = L.afmt == A_FP8 ? nibble_pos_a8(e)
-                        : (L.afmt == A_MXFP4 || L.afmt == A_FP8N) ? e   // the MMA's own order
-                                                                   : nibble_pos_a16(e);
+        // natural order: the MMA's own (W4A4, FP4 operands) or the hardware e2m1x2
+        // conversion's input (MXFP4 with BF16 activations)
+        const bool natural = L.afmt == A_MXFP4 || L.afmt == A_FP8N ||
+                             (L.wfmt == W_MXFP4 && L.afmt == A_BF16);
+        const int pos = L.afmt == A_FP8 ? nibble_pos_a8(e) : natural ? e : nibble_pos_a16(e);
         w |= nib << (4 * pos);
       }
       out[j] = w;
@@ -109,6 +111,12 @@ __global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
         if (v == 255) set_status(kStatusBadValue);
       }
       dst[r * G + j] = v;
+      if (mx_f16_capable(L)) {            // the tensor's largest exponent, one atomic per warp
+        const unsigned act = __activemask();
+        const int m = __reduce_max_sync(act, valid ? int(v) : 0);
+        if (int(threadIdx.x & 31) == __ffs(act) - 1)
+          atomicMax(&reinterpret_cast<PackedHeader*>(packed)->max_scale_bits, m);
+      }
     } else {
       uint8_t v = 0x38;                                                // E4M3 1.0
       if (valid) {
@@ -184,6 +192,16 @@ __global__ void finish_header_f16_kernel(uint8_t* packed) {
   h->acc_scale = ldexpf(1.0f, -k);
 }
 
+// MXFP4 with BF16 activations, after the scales: k = 140 - (largest E8M0), clamped to
+// [-126, 126], so that e2m1 * 2^(E - 127 + k) <= 6 * 2^13 (FP16's range) for every block;
+// blocks down to 36 exponents below the largest stay exact in FP16.  The BF16 decode does
+// not use it (acc_scale stays 1); the FP16-operand GEMM takes 2^-k back itself.
+__global__ void finish_header_mxfp4_kernel(uint8_t* packed) {
+  PackedHeader* h = reinterpret_cast<PackedHeader*>(packed);
+  const int k = max(-126, min(126, 140 - h->max_scale_bits));
+  h->w_prescale = ldexpf(1.0f, k);
+}
+
 static int grid_for(int64_t n) {
   const int64_t b = (n + 255) / 256;
   return int(b < 65536 ? (b > 0 ? b : 1) : 65536);
@@ -200,6 +218,7 @@ cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* sca
     repack_zeros_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record / 2),
                           256, 0, st>>>(L, zeros, p);
   if (f16_operands(L)) finish_header_f16_kernel<<<1, 1, 0, st>>>(p);
+  if (mx_f16_capable(L)) finish_header_mxfp4_kernel<<<1, 1, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -287,7 +306,7 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
       uint32_t sa, sb;
       bool big;
       mxfp4_factors(E, sa, sb, big);
-      decode_mxfp4_word(w, sa, sb, big, out);
+      decode_mxfp4_word_nat(w, sa, sb, big, out);
     } else if (L.wfmt == W_MXINT4) {
       decode_int4_word(w, 0x43084308u, e8m0_bf16x2(rec[L.off_scales + ent]), out);
     } else {

@@ -50,7 +50,8 @@ extern "C" qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void*
   // This call's own schedule decides the scratch it needs; every argument is checked
   // before anything is enqueued.
   int64_t need = 0, counter_off = 0, counter_bytes = 0;
-  qgemm_status s = qgemm::dense_a16_scratch(desc, packed, X, M, ldx, chan_scale, Y, ldy, &need,
+  qgemm_status s = qgemm::dense_a16_scratch(desc, packed, X, M, ldx, chan_scale, Y, ldy,
+                                            int64_t(QGEMM_NOALLOC_SCRATCH_BYTES), &need,
                                             &counter_off, &counter_bytes);
   if (s != QGEMM_OK || M == 0) return s;
   if (need > int64_t(QGEMM_NOALLOC_SCRATCH_BYTES)) return QGEMM_ERR_WORKSPACE;

@@ -425,6 +425,31 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
+// prmt.b32 (default mode): result byte i is byte (c >> 4i) & 7 of {b, a} (a the low word);
+// when bit 3 of that selector nibble is set, the byte is replaced by copies of its sign bit.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Byte B of w (two e2m1 codes, the low nibble first) -> f16x2 (exact), by the hardware
+// conversion.
+template <int B>
+__device__ __forceinline__ uint32_t cvt_f16x2_e2m1x2(uint32_t w) {
+  static_assert(B >= 0 && B < 4, "byte index");
+  uint32_t r;
+  if constexpr (B == 0)
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b0;\n}\n" : "=r"(r) : "r"(w));
+  else if constexpr (B == 1)
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b1;\n}\n" : "=r"(r) : "r"(w));
+  else if constexpr (B == 2)
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b2;\n}\n" : "=r"(r) : "r"(w));
+  else
+    asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %1;\n cvt.rn.f16x2.e2m1x2 %0, b3;\n}\n" : "=r"(r) : "r"(w));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));

@@ -11,7 +11,9 @@
 // single bulk copy:
 //   codes  : [4 chunks][128 rows][16 B]; chunk c of row r holds K-elements 32c .. 32c+31
 //            of that row as four 32-bit words of 8 nibbles, the nibbles interleaved so one
-//            mask yields two decoded lanes (dequant.cuh);
+//            mask yields two decoded lanes (dequant.cuh); MXFP4 weights for BF16
+//            activations keep the natural order instead (element 2j in the low nibble of
+//            byte j, the input of the hardware e2m1x2 conversion);
 //            MXFP4 activations (W4A4): the tensor core reads the codes straight from shared
 //            memory instead, so they are its operand layout -- K-major rows of 64 bytes
 //            (128 K, element 2j in the low nibble of byte j), 8-row atoms of 512 bytes, the
@@ -39,7 +41,7 @@
 namespace qgemm {
 
 constexpr uint32_t kPackedMagic = 0x32575147u;   // "GQW2"
-constexpr uint32_t kPackedVersion = 4;
+constexpr uint32_t kPackedVersion = 5;
 constexpr int kTileN = 128;                      // weight rows per tile (MMA M)
 constexpr int kStageK = 128;                     // K-elements per pipeline stage
 constexpr int kCodeBytes = kTileN * kStageK / 2; // 8192
@@ -70,10 +72,13 @@ struct PackedHeader {
   float acc_scale;
   // INT4 with BF16 scales: the power of two 2^k that the decode multiplies every scale by
   // before rounding the weight to FP16, chosen from the largest |scale| of the tensor so
-  // that (q - z) * s * 2^k stays inside FP16's normal range; 1 for the other formats.
+  // that (q - z) * s * 2^k stays inside FP16's normal range.  MXFP4 (BF16 activations):
+  // 2^k with k = 140 - (largest E8M0), so that e2m1 * 2^(E - 127 + k) <= 6 * 2^13 for
+  // the FP16-operand decode of small calls (whose GEMM takes 2^-k back on its
+  // accumulators; acc_scale stays 1 for the BF16 decode).  1 for the other formats.
   float w_prescale;
-  // INT4 with BF16 scales: the largest |scale| of the tensor as BF16 magnitude bits (the
-  // repack's reduction; k is derived from it).
+  // INT4 with BF16 scales: the largest |scale| of the tensor as BF16 magnitude bits; MXFP4:
+  // the largest E8M0 exponent (the repack's reduction; k is derived from it).
   int32_t max_scale_bits;
 };
 static_assert(sizeof(PackedHeader) <= kHeaderBytes, "header too large");
@@ -135,6 +140,18 @@ inline bool make_layout(int32_t wfmt, int32_t sdtype, int32_t group, int32_t has
 // pre-pass into the workspace (prep_x_f16).
 inline bool f16_operands(const Layout& L) {
   return L.afmt == A_BF16 && (L.wfmt == W_INT4_SYM || L.wfmt == W_UINT4_ZP);
+}
+
+// MXFP4 weights with BF16 activations: calls with token tiles of up to 64 rows (dense and
+// MoE) whose workspace also holds the FP16 activation copy run on FP16 operands, the
+// weights decoded by the hardware e2m1x2 -> f16x2 conversion (twice the rate of the BF16
+// bit construction, where the narrow tiles make the decode the limit); wider tiles keep
+// BF16 operands and need no pre-pass.  Exact like the BF16 decode for blocks with
+// E >= max E - 36; blocks further below the tensor's largest scale fall under FP16's
+// subnormal grid.
+constexpr int kMxF16MaxTile = 64;
+inline __host__ __device__ bool mx_f16_capable(const Layout& L) {
+  return L.wfmt == W_MXFP4 && L.afmt == A_BF16;
 }
 
 // Workspace bytes of the FP16 activation copy of `rows` rows: the FP16 rows [rows][K] and

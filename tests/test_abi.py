@@ -304,7 +304,11 @@ def test_plan_defaults_are_valid(L):
 
 def test_moe_workspace_bytes(L):
     d = qg.WeightDesc("mxfp4", 4096, 7168, 32)
-    assert qg.moe_workspace_bytes(d, 256, 8) == 2 * 152 * 128 * 16 * 4 + 768   # 16-row tiles, counters rounded up to 256 B
+    # 16-row tiles, counters rounded up to 256 B; narrow MXFP4 tiles also hold the FP16
+    # activation copy of the 8 rows (7168 x 2 bytes each, then 8 row scales, each part
+    # rounded up to 256 B) that lets them run on FP16 operands
+    copy8 = 8 * 7168 * 2 + 256
+    assert qg.moe_workspace_bytes(d, 256, 8) == 2 * 152 * 128 * 16 * 4 + 768 + copy8
     assert qg.moe_workspace_bytes(d, 8, 8 * 200) == 2 * 152 * 128 * 256 * 4 + 768
     assert qg.moe_workspace_bytes(d, 0, 8) == 0
     assert qg.moe_workspace_bytes(d, 8, 0) == 0

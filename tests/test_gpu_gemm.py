@@ -67,6 +67,43 @@ def _assert_close(y, ref, tol):
         f"bad n-tiles {sorted(set(c // 128 for c in cols))[:8]}")
 
 
+def test_mxfp4_small_calls_fp16_operands():
+    """MXFP4 weights with BF16 activations: a small call given a workspace runs on FP16
+    operands (the hardware e2m1 conversion, the activations copied to FP16 by the
+    pre-pass); with a workspace too small for that copy it runs on BF16 operands.  Both meet the bar against the exact
+    weights.  Weight rows 0..127 have E8M0 exponents 165..200, rows 128..255 exponents
+    100..110, more than 36 below the tensor's largest: on FP16 operands those blocks fall
+    under FP16's subnormal grid (the rows' outputs become 0), far below the bar's
+    max(|y|, rms(y)) scale, and the two paths differ exactly there."""
+    from tests import gpu_util as G
+    qg = _qg()
+    r = WL.rng(38)
+    M, N, K = 16, 256, 512
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    w.scales[:128] = r.integers(165, 201, size=(128, K // 32), dtype=np.uint8)
+    w.scales[128:] = r.integers(100, 111, size=(128, K // 32), dtype=np.uint8)
+    d, packed = G.pack(w)
+    X = G.bf16_tensor(x)
+    qg.force_config(16, 1)                     # whole tiles: no workspace needed for cuts
+    try:
+        outs = {}
+        # (a workspace too small for the activation copy keeps BF16 operands)
+        small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+        for name, ws in (("f16", qg.workspace(d, M)), ("bf16", small)):
+            out = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
+            outs[name] = G.to_f64(qg.w4a16(d, packed, X, out=out, ws=ws))
+            torch.cuda.synchronize()
+            assert qg.device_status(clear=True) == 0
+    finally:
+        qg.force_config(0, 0)
+    ref = oracle.w4a16(x, w.wfmt, w.group, w.codes, w.scales, w.zeros)
+    for name in outs:
+        _assert_close(outs[name], ref, TOL_A16)
+    np.testing.assert_array_equal(outs["f16"][:, :128], outs["bf16"][:, :128])
+    assert np.all(outs["f16"][:, 128:] == 0) and np.any(outs["bf16"][:, 128:] != 0)
+
+
 def _check_a16(tag, y, x, w, chan=None):
     """The bar against the exact weights; both worst ratios (exact, BF16-rounded weights)
     go to the parity log."""

@@ -82,6 +82,7 @@ CAPTURED_TRAFFIC = {
 # no-alloc or host-buffer wrappers).
 GEMM_SOURCES = ("api.cu", "dequant.cuh", "gemm_a16_any.cu", "gemm_a16_mxfp4.cu",
                 "gemm_a16_mxfp4f16.cu", "gemm_a16_mxint4.cu", "gemm_a16_nvfp4.cu",
+                "gemm_a16_nvfp4f16.cu",
                 "gemm_a16_sym_g1.cu",
                 "gemm_a16_zp_g1.cu", "gemm_a4.cu", "gemm_a8.cu", "gemm_a8n.cu",
                 "gemm_kernel.cuh", "kernels.h", "kernels_aux.cu", "ptx.cuh", "qgemm_internal.h")

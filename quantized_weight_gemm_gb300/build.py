@@ -19,7 +19,8 @@ CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_lib")
 LIB = os.path.join(OUT_DIR, "libqgemm.so")
 SOURCES = ["gemm_a16_zp_g1.cu", "gemm_a16_sym_g1.cu", "gemm_a16_any.cu", "gemm_a16_mxfp4.cu",
-           "gemm_a16_mxint4.cu", "gemm_a16_nvfp4.cu", "gemm_a16_mxfp4f16.cu", "gemm_a8.cu",
+           "gemm_a16_mxint4.cu", "gemm_a16_nvfp4.cu", "gemm_a16_mxfp4f16.cu", "gemm_a16_nvfp4f16.cu",
+           "gemm_a8.cu",
            "gemm_a8n.cu", "gemm_a4.cu",
            "kernels_aux.cu",
            "api.cu",

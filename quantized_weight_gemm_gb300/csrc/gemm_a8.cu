@@ -12,6 +12,7 @@ cudaError_t launch_gemm_a16_nvfp4(const GemmPlan&, const CUtensorMap&, const Gem
 cudaError_t launch_gemm_a4(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a8n(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 cudaError_t launch_gemm_a16_mxfp4f16(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
+cudaError_t launch_gemm_a16_nvfp4f16(const GemmPlan&, const CUtensorMap&, const GemmArgs&, cudaStream_t);
 
 cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
                         const GemmArgs& args, cudaStream_t st) {
@@ -25,7 +26,9 @@ cudaError_t launch_gemm(bool fp8, const GemmPlan& plan, const CUtensorMap& tmap,
       return plan.mx_f16 ? launch_gemm_a16_mxfp4f16(plan, tmap, args, st)
                          : launch_gemm_a16_mxfp4(plan, tmap, args, st);
     case DM_MXINT4: return launch_gemm_a16_mxint4(plan, tmap, args, st);
-    case DM_NVFP4: return launch_gemm_a16_nvfp4(plan, tmap, args, st);
+    case DM_NVFP4:
+      return plan.mx_f16 ? launch_gemm_a16_nvfp4f16(plan, tmap, args, st)
+                         : launch_gemm_a16_nvfp4(plan, tmap, args, st);
     case DM_W4A4: return launch_gemm_a4(plan, tmap, args, st);
     default: return launch_gemm_a16_any(plan, tmap, args, st);
   }

@@ -364,7 +364,8 @@ enum DecodeMode : int {
   DM_INT4_ZP_G1 = 0, DM_INT4_SYM_G1 = 1, DM_INT4_ANY = 2, DM_MXFP4 = 3, DM_MXINT4 = 4, DM_NVFP4 = 5,
   DM_W4A4 = 6,                 // MXFP4 x MXFP4: no decode, the MMA reads the codes
   DM_W4A8N = 7,                // MXFP4 x FP8 on FP4 operands: no decode either
-  DM_MXFP4_F16 = 8             // MXFP4 x BF16 activations on FP16 operands (small calls)
+  DM_MXFP4_F16 = 8,            // MXFP4 x BF16 activations on FP16 operands (narrow tiles)
+  DM_NVFP4_F16 = 9             // NVFP4, likewise
 };
 
 // INT4 with BF16 scales (every group size) and MXFP4 in small calls: FP16 tensor-core
@@ -372,7 +373,7 @@ enum DecodeMode : int {
 template <bool A8, int DM>
 constexpr bool kF16Operands =
     !A8 && (DM == DM_INT4_ZP_G1 || DM == DM_INT4_SYM_G1 || DM == DM_INT4_ANY ||
-            DM == DM_MXFP4_F16);
+            DM == DM_MXFP4_F16 || DM == DM_NVFP4_F16);
 
 // Decode two 32-K chunks of weight row r into 32 registers of 16-bit pairs (pair order):
 // FP16 for INT4 with BF16 scales (the scale times w_pre = 2^k), BF16 for the other formats.
@@ -422,7 +423,15 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
         const uint32_t s0 = e4m3_bf16x2_p118(sp & 0xFFu), s1 = e4m3_bf16x2_p118(sp >> 8);
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          decode_mxfp4_word(wd[j], j < 2 ? s0 : s1, 0u, false, &regs[16 * c + 4 * j]);
+          decode_mxfp4_word_nat(wd[j], j < 2 ? s0 : s1, 0u, false, &regs[16 * c + 4 * j]);
+      } else if constexpr (DM == DM_NVFP4_F16) {
+        // the chunk's two E4M3 scales (16 K each) -> f16x2, times 16 (exact: e2m1 x E4M3 x 16
+        // stays within FP16's normal range), each broadcast to both halves
+        const uint32_t sp = reinterpret_cast<const uint16_t*>(rec + tail)[r * 4 + rchunk0 + c];
+        const uint32_t ss = ptx::f16x2_mul(ptx::cvt_f16x2_e4m3x2(sp), 0x4C004C00u);
+        const uint32_t s0 = ptx::prmt(ss, ss, 0x1010u), s1 = ptx::prmt(ss, ss, 0x3232u);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) decode_mxfp4_word_f16(wd[j], j < 2 ? s0 : s1, &regs[16 * c + 4 * j]);
       } else {
         const int ent = r * G + ((rchunk0 + c) * G) / 4;      // scale entry of this chunk
         const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[ent];
@@ -1176,6 +1185,9 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
       if constexpr (DM == DM_MXFP4_F16)     // (the header's acc_scale serves the BF16 decode)
         acc_s = 1.0f / __ldg(&reinterpret_cast<const PackedHeader*>(
                                 a.packed + int64_t(w.expert) * a.expert_stride)->w_prescale);
+      else if constexpr (DM == DM_NVFP4_F16)  // g 2^8 of the BF16 decode -> g 2^-4 (weights x 16)
+        acc_s = 0x1p-12f * __ldg(&reinterpret_cast<const PackedHeader*>(
+                                     a.packed + int64_t(w.expert) * a.expert_stride)->acc_scale);
       else if constexpr (DM == DM_NVFP4 || F16)
         acc_s = __ldg(&reinterpret_cast<const PackedHeader*>(
                           a.packed + int64_t(w.expert) * a.expert_stride)->acc_scale);

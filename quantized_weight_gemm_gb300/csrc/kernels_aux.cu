@@ -55,8 +55,7 @@ __global__ void repack_codes_kernel(Layout L, const uint8_t* __restrict__ codes,
         if (L.wfmt == W_INT4_SYM || L.wfmt == W_MXINT4) nib ^= 8u;   // two's complement -> q + 8
         // natural order: the MMA's own (W4A4, FP4 operands) or the hardware e2m1x2
         // conversion's input (MXFP4 with BF16 activations)
-        const bool natural = L.afmt == A_MXFP4 || L.afmt == A_FP8N ||
-                             (L.wfmt == W_MXFP4 && L.afmt == A_BF16);
+        const bool natural = L.afmt == A_MXFP4 || L.afmt == A_FP8N || mx_f16_capable(L);
         const int pos = L.afmt == A_FP8 ? nibble_pos_a8(e) : natural ? e : nibble_pos_a16(e);
         w |= nib << (4 * pos);
       }
@@ -111,7 +110,7 @@ __global__ void repack_scales_kernel(Layout L, const void* __restrict__ scales,
         if (v == 255) set_status(kStatusBadValue);
       }
       dst[r * G + j] = v;
-      if (mx_f16_capable(L)) {            // the tensor's largest exponent, one atomic per warp
+      if (L.wfmt == W_MXFP4 && mx_f16_capable(L)) {   // the largest exponent, one atomic per warp
         const unsigned act = __activemask();
         const int m = __reduce_max_sync(act, valid ? int(v) : 0);
         if (int(threadIdx.x & 31) == __ffs(act) - 1)
@@ -218,7 +217,7 @@ cudaError_t launch_repack(const Layout& L, const uint8_t* codes, const void* sca
     repack_zeros_kernel<<<grid_for(L.n_tiles * L.k_blocks * kTileN * L.groups_per_record / 2),
                           256, 0, st>>>(L, zeros, p);
   if (f16_operands(L)) finish_header_f16_kernel<<<1, 1, 0, st>>>(p);
-  if (mx_f16_capable(L)) finish_header_mxfp4_kernel<<<1, 1, 0, st>>>(p);
+  if (L.wfmt == W_MXFP4 && mx_f16_capable(L)) finish_header_mxfp4_kernel<<<1, 1, 0, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -293,7 +292,7 @@ __global__ void dequant_debug_kernel(Layout L, const uint8_t* __restrict__ packe
       // the GEMM's decode (e2m1 x s x 2^-8, exact), then the accumulator factor (2^8 times
       // the per-tensor scale) in double and one rounding to BF16
       const uint32_t s = e4m3_bf16x2_p118(rec[L.off_scales + r * G + c * 2 + j / 2]);
-      decode_mxfp4_word(w, s, 0u, false, out);
+      decode_mxfp4_word_nat(w, s, 0u, false, out);
       const double f = double(reinterpret_cast<const PackedHeader*>(packed)->acc_scale);
       for (int e = 0; e < 8; ++e) {
         const uint32_t hb = (out[e >> 1] >> (16 * (e & 1))) & 0xFFFFu;

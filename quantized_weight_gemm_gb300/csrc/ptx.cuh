@@ -433,6 +433,14 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t c) {
   return d;
 }
 
+// Two E4M3 codes (the low byte first) -> f16x2 (exact), by the hardware conversion.
+__device__ __forceinline__ uint32_t cvt_f16x2_e4m3x2(uint32_t pair) {
+  uint32_t r;
+  const unsigned short p16 = static_cast<unsigned short>(pair & 0xFFFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(p16));
+  return r;
+}
+
 // Byte B of w (two e2m1 codes, the low nibble first) -> f16x2 (exact), by the hardware
 // conversion.
 template <int B>

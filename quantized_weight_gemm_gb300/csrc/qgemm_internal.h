@@ -11,7 +11,7 @@
 // single bulk copy:
 //   codes  : [4 chunks][128 rows][16 B]; chunk c of row r holds K-elements 32c .. 32c+31
 //            of that row as four 32-bit words of 8 nibbles, the nibbles interleaved so one
-//            mask yields two decoded lanes (dequant.cuh); MXFP4 weights for BF16
+//            mask yields two decoded lanes (dequant.cuh); MXFP4 and NVFP4 weights for BF16
 //            activations keep the natural order instead (element 2j in the low nibble of
 //            byte j, the input of the hardware e2m1x2 conversion);
 //            MXFP4 activations (W4A4): the tensor core reads the codes straight from shared
@@ -142,16 +142,17 @@ inline bool f16_operands(const Layout& L) {
   return L.afmt == A_BF16 && (L.wfmt == W_INT4_SYM || L.wfmt == W_UINT4_ZP);
 }
 
-// MXFP4 weights with BF16 activations: calls with token tiles of up to 64 rows (dense and
-// MoE) whose workspace also holds the FP16 activation copy run on FP16 operands, the
-// weights decoded by the hardware e2m1x2 -> f16x2 conversion (twice the rate of the BF16
-// bit construction, where the narrow tiles make the decode the limit); wider tiles keep
-// BF16 operands and need no pre-pass.  Exact like the BF16 decode for blocks with
-// E >= max E - 36; blocks further below the tensor's largest scale fall under FP16's
-// subnormal grid.
+// MXFP4 and NVFP4 weights with BF16 activations: calls with token tiles of up to 64 rows
+// (dense and MoE) whose workspace also holds the FP16 activation copy run on FP16
+// operands, the weights decoded by the hardware e2m1x2 -> f16x2 conversion (twice the rate
+// of the BF16 bit construction, where the narrow tiles make the decode the limit); wider
+// tiles keep BF16 operands and need no pre-pass.  NVFP4 is exact in FP16 (e2m1 * E4M3 *
+// 16 has at most 6 significant bits and stays in FP16's normal range); MXFP4 is exact like
+// the BF16 decode for blocks with E >= max E - 36, blocks further below the tensor's
+// largest scale falling under FP16's subnormal grid.
 constexpr int kMxF16MaxTile = 64;
 inline __host__ __device__ bool mx_f16_capable(const Layout& L) {
-  return L.wfmt == W_MXFP4 && L.afmt == A_BF16;
+  return (L.wfmt == W_MXFP4 || L.wfmt == W_NVFP4) && L.afmt == A_BF16;
 }
 
 // Workspace bytes of the FP16 activation copy of `rows` rows: the FP16 rows [rows][K] and

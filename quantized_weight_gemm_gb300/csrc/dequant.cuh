@@ -51,14 +51,18 @@ __device__ __forceinline__ void decode_int4_word(uint32_t w, uint32_t zz, uint32
   }
 }
 
-// INT4 word -> 4 f16x2 (pairs 0..3).  zz = f16x2(1024 + z), s2 = f16x2(scale * 2^k).
-__device__ __forceinline__ void decode_int4_word_f16(uint32_t w, uint32_t zz, uint32_t s2,
-                                                     uint32_t* out) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t t = ptx::lop3_and_or(w >> (4 * i), 0x000F000Fu, 0x64006400u);
-    out[i] = ptx::f16x2_mul(ptx::f16x2_sub(t, zz), s2);
-  }
+// INT4 word -> 4 f16x2 (pairs 0..3).  zz = f16x2(1024 + z), zz64 = f16x2(64 + z),
+// s2 = f16x2(scale * 2^k).  Pairs 0 and 2 sit in nibbles 0 / 4 (of w and of w >> 8): ORed
+// into the mantissa of 1024.0 they give 1024 + q.  Pairs 1 and 3 sit in nibbles 1 / 5, bits
+// 4..7 of each half: ORed into 64.0 (0x5400, whose last place is 1/16) they give 64 + q, so
+// no shift is needed for them.  Subtracting the matching 1024 + z or 64 + z is exact.
+__device__ __forceinline__ void decode_int4_word_f16(uint32_t w, uint32_t zz, uint32_t zz64,
+                                                     uint32_t s2, uint32_t* out) {
+  const uint32_t w8 = w >> 8;
+  out[0] = ptx::f16x2_mul(ptx::f16x2_sub(ptx::lop3_and_or(w, 0x000F000Fu, 0x64006400u), zz), s2);
+  out[1] = ptx::f16x2_mul(ptx::f16x2_sub(ptx::lop3_and_or(w, 0x00F000F0u, 0x54005400u), zz64), s2);
+  out[2] = ptx::f16x2_mul(ptx::f16x2_sub(ptx::lop3_and_or(w8, 0x000F000Fu, 0x64006400u), zz), s2);
+  out[3] = ptx::f16x2_mul(ptx::f16x2_sub(ptx::lop3_and_or(w8, 0x00F000F0u, 0x54005400u), zz64), s2);
 }
 
 // f16x2 of a BF16 scale (bits) times the power of two p, rounded once to FP16.

@@ -387,14 +387,14 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
     const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[r];
     uint32_t z = 8;
     if constexpr (DM == DM_INT4_ZP_G1) z = (rec[tail + zoff + (r >> 1)] >> (4 * (r & 1))) & 0xFu;
-    const uint32_t zz = (0x6400u | z) * 0x00010001u;
+    const uint32_t zz = (0x6400u | z) * 0x00010001u, zz64 = (0x5400u | (z << 4)) * 0x00010001u;
     const uint32_t s2 = scale_f16x2(s, w_pre);
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
       const uint4 q = *reinterpret_cast<const uint4*>(rec + (slot0 + c) * (kTileN * 16) + r * 16);
       const uint32_t wd[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+      for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, zz64, s2, &regs[16 * c + 4 * j]);
     }
   } else {
 #pragma unroll
@@ -437,10 +437,10 @@ __device__ __forceinline__ void decode_two_chunks_a16(const uint8_t* rec, int ta
         const uint32_t s = reinterpret_cast<const uint16_t*>(rec + tail)[ent];
         uint32_t z = 8;
         if (has_zp) z = (rec[tail + zoff + (ent >> 1)] >> (4 * (ent & 1))) & 0xFu;
-        const uint32_t zz = (0x6400u | z) * 0x00010001u;
+        const uint32_t zz = (0x6400u | z) * 0x00010001u, zz64 = (0x5400u | (z << 4)) * 0x00010001u;
         const uint32_t s2 = scale_f16x2(s, w_pre);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, s2, &regs[16 * c + 4 * j]);
+        for (int j = 0; j < 4; ++j) decode_int4_word_f16(wd[j], zz, zz64, s2, &regs[16 * c + 4 * j]);
       }
     }
   }

@@ -623,14 +623,15 @@ def bench_ours(args):
     clocks = sampler.stop(t0, t1)
     # end-to-end leg: the same warm-up as the kernel-only leg, then the timed steps.  The
     # host enqueues every call while the GPU runs, so a pause of this Python harness lands
-    # inside a call's events; the garbage collector is held off while the steps run (as
-    # timeit does), its pauses of about 0.2 ms being the harness's, not the library's.
+    # inside a call's events; the garbage collector is held off while the warm-up and the
+    # timed steps run (as timeit does), its pauses of about 0.2 ms being the harness's, not
+    # the library's, and the one collection before them lies outside both.
     import gc
-    for _ in range(args.warmup):
-        run_step(cases, flush, e2e=True)
     gc.collect()
     gc.disable()
     try:
+        for _ in range(args.warmup):
+            run_step(cases, flush, e2e=True)
         e2e_steps = [run_step(cases, flush, e2e=True) for _ in range(max(1, args.steps))]
         torch.cuda.synchronize()
     finally:

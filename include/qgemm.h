@@ -174,7 +174,9 @@ qgemm_status qgemm_repack_scaled(const qgemm_wdesc* desc, const uint8_t* codes,
  *     the GEMM, and the epilogue takes the powers of two back;
  *   - the FP32 partial sums of the output tiles whose K range the schedule cuts over
  *     several CTAs (split-K or stream-K; one 128 x token-tile slot per contributing CTA)
- *     and one arrival counter per cut tile.
+ *     and one arrival counter per cut tile.  Cuts are made up to M = 1024; above it only
+ *     stream-K over the leftover tiles, for K >= 16384, and only when the workspace
+ *     passed holds its partial sums (a smaller one gets whole tiles, never an error).
  * 0 when neither applies to any M <= M_max.  The workspace must be 256-byte aligned and
  * zero-filled before its first use; every successful call leaves the counters zero again
  * (the partial sums and the activation copy are overwritten by every call), so one
@@ -418,9 +420,9 @@ qgemm_status qgemm_device_status(int32_t clear);
  * Same arguments and result as qgemm_w4a16 without `ws`/`ws_bytes`: the split-K scratch
  * is a fixed QGEMM_NOALLOC_SCRATCH_BYTES device array inside the library, held by every
  * GPU that loads it until the process exits.  A call needs only what its own schedule for
- * this M uses (qgemm_plan): the partial sums of the tiles it cuts (none above M = 1024 by
- * default), after the FP16 activation copy for INT4 weights with BF16 scales
- * (qgemm_act_copy_bytes).  A call that needs more than the array returns
+ * this M uses (qgemm_plan): the partial sums of the tiles it cuts (above M = 1024 only a
+ * stream-K schedule, which gives way to whole tiles when the array cannot hold it), after
+ * the FP16 activation copy for INT4 weights with BF16 scales (qgemm_act_copy_bytes).  A call that needs more than the array returns
  * QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a workspace for it.  Arguments are
  * checked as qgemm_w4a16 checks them, before anything is enqueued.
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library routine.  The first
@@ -437,7 +439,7 @@ qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, co
 
 /*
  * The schedule qgemm_w4a16 / qgemm_w4a8 would run for M rows on the current device (152
- * SMs assumed when no device is visible): out[0] token tile, out[1] uniform K cut (1 = none),
+ * SMs assumed when no device is visible), given a workspace of qgemm_workspace_bytes(desc, M): out[0] token tile, out[1] uniform K cut (1 = none),
  * out[2] stream-K tiles (0 = none), out[3] partial-sum slots per cut tile, out[4] CTAs.
  * Host-only (launches nothing); honours qgemm_force_config.
  * The choice is the pages' Tuning Config (tile shape, Stream-K planning; "Humming wird

@@ -290,6 +290,33 @@ def test_default_plans_match_the_contributor_model(L):
                     assert qg.workspace_bytes(d, M) >= T * p["splits"] * 128 * tt * 4
 
 
+def test_large_m_stream_k_plans_and_workspace(L):
+    """Above M = 1024, stream-K is planned only for K >= 16384 (128 blocks), agrees with the
+    record-walk model, and a workspace sized for M_max covers the plan of every M <= M_max."""
+    P = 152
+    for (N, K) in [(8192, 28672), (4096, 16384), (28672, 8192), (4096, 7168)]:
+        d = qg.WeightDesc("uint4_zp", N, K, 128)
+        kb = -(-K // 128)
+        copy = qg.act_copy_bytes(d, 4096)
+        ws = qg.workspace_bytes(d, 4096)
+        seen = 0
+        for M in range(1025, 4097, 7):
+            p = qg.plan(d, M)
+            if kb < 128:
+                assert p["sk_tiles"] == 0 and p["splits"] == 1, (N, K, M, p)
+                continue
+            assert p["splits"] == 1
+            if p["sk_tiles"] > 0:
+                seen += 1
+                tt = p["token_tile"]
+                T = -(-M // tt) * -(-N // 128)
+                assert p["sk_tiles"] == T % P
+                c = _sk_contributors(p["sk_tiles"], kb, P)
+                assert p["max_contrib"] == (c if c > 1 else 0) and c <= 8
+                assert ws - copy >= (p["sk_tiles"] + p["grid"]) * 128 * tt * 4 + 4 * p["sk_tiles"]
+        assert kb < 128 or seen > 0
+
+
 def test_plan_defaults_are_valid(L):
     for (N, K) in [(28672, 8192), (8192, 28672), (4096, 7168), (7168, 2048)]:
         d = qg.WeightDesc("uint4_zp", N, K, 128)

@@ -63,7 +63,8 @@ def _check_sampled(tag, y, x, w, ns, ms, tol=TOL_A16):
 @pytest.mark.parametrize("N,K,M", [(28672, 8192, 1), (28672, 8192, 16), (8192, 28672, 16),
                                    (8192, 28672, 1), (28672, 8192, 64), (8192, 28672, 128),
                                    (28672, 8192, 256), (28672, 8192, 1024),
-                                   (8192, 28672, 8192), (28672, 8192, 8192)])
+                                   (8192, 28672, 2048), (8192, 28672, 8192),
+                                   (28672, 8192, 8192)])
 def test_int4_zp_bench_shapes(N, K, M):
     """Every token tile and schedule the INT4 sweep runs, including its dominant launch
     (N=28672, K=8192, M=8192)."""
@@ -76,6 +77,31 @@ def test_int4_zp_bench_shapes(N, K, M):
     assert qg.device_status(clear=True) == 0
     ns, ms = _samples(WL.rng(50), N, M)
     _check_sampled(f"fullsize uint4_zp {N}x{K} M={M}", y, x, w, ns, ms)
+
+
+def test_large_m_stream_k_gives_way_to_a_small_workspace():
+    """Above M = 1024 with K >= 16384 the default plan runs stream-K over the leftover tiles;
+    a workspace that holds only the activation copy gets whole tiles instead of an error.
+    Both against the oracle on the same samples, and with each other."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    N, K, M = 8192, 28672, 1536
+    x, w = WL.int4_asym_shape(N, K, M, seed=3)
+    d, packed = G.pack(w)
+    p = qg.plan(d, M)
+    assert p["sk_tiles"] > 0 and p["max_contrib"] > 1
+    X = G.bf16_tensor(x)
+    ns, ms = _samples(WL.rng(52), N, M)
+    y_sk = qg.w4a16(d, packed, X, out=_nan_out(M, N), ws=qg.workspace(d, M))
+    small = torch.zeros(qg.act_copy_bytes(d, M), dtype=torch.uint8, device="cuda")
+    y_whole = qg.w4a16(d, packed, X, out=_nan_out(M, N), ws=small)
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    _check_sampled(f"fullsize stream-K large M {N}x{K} M={M}", y_sk, x, w, ns, ms)
+    _check_sampled(f"fullsize whole tiles large M {N}x{K} M={M}", y_whole, x, w, ns, ms)
+    # the two schedules sum the same FP32 products in a different order
+    diff = (y_sk.float() - y_whole.float()).abs().max().item()
+    assert diff <= 8e-3 * y_whole.float().abs().max().item()
 
 
 @pytest.mark.parametrize("N,K,M", [(4096, 7168, 1), (7168, 2048, 16), (4096, 7168, 2048),

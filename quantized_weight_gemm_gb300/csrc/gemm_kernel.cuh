@@ -64,6 +64,12 @@ namespace qgemm {
 #ifndef QGEMM_DEQ_WGS_NARROW
 #define QGEMM_DEQ_WGS_NARROW 4
 #endif
+#ifndef QGEMM_DEQ_WGS_128
+#define QGEMM_DEQ_WGS_128 4
+#endif
+#ifndef QGEMM_DEQ_WGS_256
+#define QGEMM_DEQ_WGS_256 2
+#endif
 #ifndef QGEMM_ISSUERS_NARROW
 #define QGEMM_ISSUERS_NARROW 4
 #endif
@@ -77,7 +83,12 @@ namespace qgemm {
 // factors into tensor memory, and one issuer runs the stage's MMAs.
 template <int BNT, bool D = false>
 struct Roles {
-  static constexpr int kDeqWGs = D ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW : 2;   // round-robin stages
+  // Dequant warpgroups, round-robin over the stages: four up to 128-token tiles, two for
+  // 256-token tiles, whose epilogue needs more registers than 27 warps leave (with four it
+  // spills and ran up to 15% slower; the 128-token tile with four instead of two ran up to
+  // 8% faster where it is chosen, M = 96 ... 1024).
+  static constexpr int kDeqWGs = D ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW
+                                      : BNT == 128 ? QGEMM_DEQ_WGS_128 : QGEMM_DEQ_WGS_256;
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
   static constexpr int kIssuers = D ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;

@@ -70,6 +70,9 @@ namespace qgemm {
 #ifndef QGEMM_DEQ_WGS_256
 #define QGEMM_DEQ_WGS_256 2
 #endif
+#ifndef QGEMM_EPI_WARPS_256
+#define QGEMM_EPI_WARPS_256 16
+#endif
 #ifndef QGEMM_ISSUERS_NARROW
 #define QGEMM_ISSUERS_NARROW 4
 #endif
@@ -92,9 +95,12 @@ struct Roles {
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
   static constexpr int kIssuers = D ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
-  // Wide token tiles have one accumulator buffer (or two of 128 columns): two epilogue
-  // warps per lane quarter drain it twice as fast, so the MMA waits less for it.
-  static constexpr int kEpiWarps = BNT >= 128 ? 8 : 4;
+  // Wide token tiles have one accumulator buffer (or two of 128 columns): several epilogue
+  // warps per lane quarter drain it faster, so the MMA waits less for it -- two for
+  // 128-token tiles, four for 256-token tiles (64 columns each: the MMA gets the
+  // accumulator back after four tensor-memory loads per warp instead of eight, and the
+  // kernel needs 72 registers without spilling instead of 96 with).
+  static constexpr int kEpiWarps = BNT == 256 ? QGEMM_EPI_WARPS_256 : BNT >= 128 ? 8 : 4;
   static constexpr int kEpiWarp0 = 4 * kDeqWGs;
   static constexpr int kIssuerWarp0 = kEpiWarp0 + kEpiWarps;
   static constexpr int kXProducerWarp = kIssuerWarp0 + kIssuers;

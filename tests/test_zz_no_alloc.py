@@ -8,8 +8,9 @@ checks, through the C ABI:
     a workspace (both run the same schedule) and pass the W4A16 bar against the oracle,
     for uniform K cuts and for stream-K;
   * a call needs only what its own schedule uses, whatever smaller M would need (above
-    M = 1024 nothing is cut: INT4 with BF16 scales needs its FP16 activation copy, MXFP4
-    nothing);
+    M = 1024 nothing is cut below K = 16384: INT4 with BF16 scales needs its FP16
+    activation copy, MXFP4 nothing; with longer K the stream-K schedule there gives way
+    to whole tiles when its partial sums do not fit the array);
   * a call whose schedule needs more scratch than the built-in array is refused with
     QGEMM_ERR_WORKSPACE.
 """
@@ -118,3 +119,27 @@ def test_noalloc_refuses_oversized_plan(qg):
         assert st == 4
     finally:
         qg.force_config(0, 0)
+
+
+def test_noalloc_long_k_large_m_keeps_whole_tiles(qg):
+    """K >= 16384 above M = 1024: the default schedule runs stream-K, whose partial sums do
+    not fit the array, so the no-alloc call runs whole tiles instead of refusing -- the
+    same bits as qgemm_w4a16 with a workspace too small for stream-K."""
+    from tests import gpu_util as G
+    N, K, M = 4096, 16384, 2048
+    r = WL.rng(35)
+    x = WL.gen_x(r, M, K)
+    w = WL.gen_weights(r, "mxfp4", N, K)
+    d, packed = G.pack(w)
+    p = qg.plan(d, M)
+    assert p["sk_tiles"] > 0 and p["max_contrib"] > 1
+    assert qg.workspace_bytes(d, M) > SCRATCH_BYTES
+    X = G.bf16_tensor(x)
+    st, y = _noalloc(qg, d, packed, X, M, N)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    small = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    ref_dev = qg.w4a16(d, packed, X, ws=small)
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), ref_dev.view(torch.int16))

@@ -422,16 +422,17 @@ qgemm_status qgemm_device_status(int32_t clear);
  * GPU that loads it until the process exits.  A call needs only what its own schedule for
  * this M uses (qgemm_plan): the partial sums of the tiles it cuts (above M = 1024 only a
  * stream-K schedule, which gives way to whole tiles when the array cannot hold it), after
- * the FP16 activation copy for INT4 weights with BF16 scales (qgemm_act_copy_bytes).  A call that needs more than the array returns
- * QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a workspace for it.  Arguments are
- * checked as qgemm_w4a16 checks them, before anything is enqueued.
+ * the FP16 activation copy for INT4 weights with BF16 scales (qgemm_act_copy_bytes).  A
+ * call that needs more than the array returns QGEMM_ERR_WORKSPACE; use qgemm_w4a16 with a
+ * workspace for it.  Arguments are checked as qgemm_w4a16 checks them, before anything is
+ * enqueued.
  * Allocates nothing: no cudaMalloc/cudaFree or allocating library routine.  The first
  * call on a device that needs scratch looks up the array's device address (once per
  * device, with that device current); make that first call before any stream capture.
  * Such a call zeroes the arrival counters of its schedule inside the array, on `stream`
- * (the partial sums are written before they are read).  All calls share the one array, so calls that
- * may overlap on the GPU (different streams, or different host threads) race and give
- * wrong results; serialize them on one stream.
+ * (the partial sums are written before they are read).  All calls share the one array, so
+ * calls that may overlap on the GPU (different streams, or different host threads) race and
+ * give wrong results; serialize them on one stream.
  */
 qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, const void* X,
                                  int64_t M, int64_t ldx, const float* chan_scale, void* Y,
@@ -439,8 +440,9 @@ qgemm_status qgemm_w4a16_noalloc(const qgemm_wdesc* desc, const void* packed, co
 
 /*
  * The schedule qgemm_w4a16 / qgemm_w4a8 would run for M rows on the current device (152
- * SMs assumed when no device is visible), given a workspace of qgemm_workspace_bytes(desc, M): out[0] token tile, out[1] uniform K cut (1 = none),
- * out[2] stream-K tiles (0 = none), out[3] partial-sum slots per cut tile, out[4] CTAs.
+ * SMs assumed when no device is visible), given a workspace of qgemm_workspace_bytes(desc,
+ * M): out[0] token tile, out[1] uniform K cut (1 = none), out[2] stream-K tiles (0 = none),
+ * out[3] partial-sum slots per cut tile, out[4] CTAs.
  * Host-only (launches nothing); honours qgemm_force_config.
  * The choice is the pages' Tuning Config (tile shape, Stream-K planning; "Humming wird
  * angekündigt", sections "Tuning und JIT-Kompilierung für jeden Workload" and

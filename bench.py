@@ -525,7 +525,7 @@ def sweep_moe(device, flush, peaks):
     gate_up [4096 x 7168] and down [7168 x 2048] grouped GEMMs over expert-sorted rows,
     T in {1, 16, 128, 1024, 8192}, uniform and skewed routing; each GEMM timed alone.  The
     gate_up GEMM is also timed on the indexed path (token-order X gathered by index, with
-    the indexed workspace: from 2048 rows on the call gathers into it and runs the grouped
+    the indexed workspace: from 256 rows on the call gathers into it and runs the grouped
     kernel), reported as gate_up_indexed_us beside the grouped time."""
     import numpy as np
     import torch

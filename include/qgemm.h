@@ -354,9 +354,9 @@ qgemm_status qgemm_moe_grouped(const qgemm_wdesc* desc, const void* packed, int3
  *                    of X: qgemm_act_copy_bytes(desc, T) at least for INT4 weights with
  *                    BF16 scales; qgemm_moe_indexed_workspace_bytes(desc, E, afmt, T, R)
  *                    for the fastest schedule (below)
- * Up to 2047 rows, or with less workspace, the kernel copies the indexed rows into its
+ * Up to 255 rows, or with less workspace, the kernel copies the indexed rows into its
  * activation tiles itself (token tiles of 16, 32 or 64 rows, from R / E), which suits the
- * few rows per expert of decode-sized routing.  From 2048 rows on, given
+ * few rows of decode-sized routing.  From 256 rows on, given
  * qgemm_moe_indexed_workspace_bytes, a gather kernel first writes the rows (and their token
  * or row scales) in sorted order into the workspace, and the grouped kernel with its wider
  * tiles runs on that copy: the same result, one more launch, and the rows are read from X

@@ -308,7 +308,7 @@ def test_moe_indexed_router(afmt, stream_k):
                                        ("mxfp4", "fp8n")])
 @pytest.mark.parametrize("copy", [False, True])
 def test_moe_indexed_many_rows(wfmt, afmt, copy):
-    """Indexed calls of 2048 rows or more: with the indexed workspace the rows are gathered
+    """Indexed calls of 256 rows or more (here over 2048): with the indexed workspace the rows are gathered
     into it first and the grouped kernel runs on the copy; with a forced token tile the
     gathering kernel runs instead.  Both against the oracle, twice on one workspace."""
     from tests import gpu_util as G

@@ -284,14 +284,14 @@ bool large_m_sk_fits(const Layout& L, int64_t M, const GemmPlan& p, int64_t avai
 // MoE: the token tile from the average rows per expert (padding included); the stream-K
 // workspace holds 2 * SMs slots and SMs counters.  Every m-tile of an expert streams the
 // expert's weights again, and an expert a little above a multiple of the tile pays for a
-// nearly empty one, so 128-token tiles are kept up to 320 rows per expert (64 experts of
-// MXFP4 4096 x 7168, top-2: at 131 rows per expert 571 against 654 us with 256-token tiles,
-// 696 against 875 skewed; at 259 rows 909 against 932, 1024 against 1113 skewed; at 387
-// rows 256-token tiles led by 5% uniform and trailed by 6% skewed; from 512 rows on they
-// led).
+// nearly empty one, so 128-token tiles are kept up to 192 rows per expert (64 experts of
+// MXFP4 4096 x 7168, top-2, at 131 rows per expert: 571 against 654 us with 256-token tiles,
+// 696 against 875 skewed).  Above that the 256-token tiles' fewer weight re-reads win on
+// experts with many rows: 256 experts, top-8, 259 rows per expert, skewed routing, gate_up
+// 3536 against 3993 us and down 1947 against 2387 us; uniform down 1945 against 2107 us.
 int moe_token_tile(int64_t R, int32_t E) {
   const int64_t avg = R / E;
-  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 320 ? 128 : 256;
+  int tt = avg <= 16 ? 16 : avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 192 ? 128 : 256;
   if (g_force_tile) tt = g_force_tile;
   return tt;
 }

@@ -336,9 +336,9 @@ def test_moe_workspace_bytes(L):
     # rounded up to 256 B) that lets them run on FP16 operands
     copy8 = 8 * 7168 * 2 + 256
     assert qg.moe_workspace_bytes(d, 256, 8) == 2 * 152 * 128 * 16 * 4 + 768 + copy8
-    # 128-token tiles up to 320 rows per expert, 256-token tiles above
-    assert qg.moe_workspace_bytes(d, 8, 8 * 200) == 2 * 152 * 128 * 128 * 4 + 768
-    assert qg.moe_workspace_bytes(d, 8, 8 * 400) == 2 * 152 * 128 * 256 * 4 + 768
+    # 128-token tiles up to 192 rows per expert, 256-token tiles above
+    assert qg.moe_workspace_bytes(d, 8, 8 * 150) == 2 * 152 * 128 * 128 * 4 + 768
+    assert qg.moe_workspace_bytes(d, 8, 8 * 200) == 2 * 152 * 128 * 256 * 4 + 768
     assert qg.moe_workspace_bytes(d, 0, 8) == 0
     assert qg.moe_workspace_bytes(d, 8, 0) == 0
 

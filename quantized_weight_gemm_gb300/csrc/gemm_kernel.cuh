@@ -84,14 +84,16 @@ namespace qgemm {
 // Direct operands (W4A4, and FP8 activations on FP4 operands): no register decode -- the
 // MMA reads the weight codes from shared memory, one warpgroup moves the E8M0 scale
 // factors into tensor memory, and one issuer runs the stage's MMAs.
-template <int BNT, bool D = false>
+template <int BNT, bool D = false, bool A8 = false>
 struct Roles {
   // Dequant warpgroups, round-robin over the stages: four up to 128-token tiles, two for
   // 256-token tiles, whose epilogue needs more registers than 27 warps leave (with four it
-  // spills and ran up to 15% slower; the 128-token tile with four instead of two ran up to
-  // 8% faster where it is chosen, M = 96 ... 1024).
+  // spills and ran up to 15% slower).  The 128-token tile with four instead of two ran up
+  // to 8% faster where it is chosen (M = 96 ... 1024) on BF16/FP16 activations and 3-5%
+  // slower on FP8 ones (whose decode is a byte shuffle), which keep two.
   static constexpr int kDeqWGs = D ? 1 : BNT <= 64 ? QGEMM_DEQ_WGS_NARROW
-                                      : BNT == 128 ? QGEMM_DEQ_WGS_128 : QGEMM_DEQ_WGS_256;
+                                      : BNT == 128 ? (A8 ? 2 : QGEMM_DEQ_WGS_128)
+                                                   : QGEMM_DEQ_WGS_256;
   // An issuing thread needs a few dozen cycles per MMA whatever its size, so narrow token
   // tiles spread the stages over several issuing warps, each with a partial accumulator.
   static constexpr int kIssuers = D ? 1 : BNT <= 64 ? QGEMM_ISSUERS_NARROW : 1;
@@ -143,7 +145,7 @@ struct GemmCfg {
   static constexpr int kACols = A4 ? 4 + 4 * ((BNT + 127) / 128) : N8 ? 0 : A8 ? 32 : kChunks * 16;
   static constexpr int kMmaPerStage = A4 ? 2 : A8 ? kChunks : 2 * kChunks;
   static_assert(A4 || A8 || kMmaPerStage % 4 == 0, "BF16 stages issue their MMAs in groups of four");
-  static constexpr int kIssuers = Roles<BNT, kDirect>::kIssuers;
+  static constexpr int kIssuers = Roles<BNT, kDirect, A8>::kIssuers;
   static constexpr int kNumSub = kIssuers;                       // partial accumulators
   static constexpr int kNumAcc = (BNT <= 32 || BNT == 128) ? 2 : 1;  // unit double-buffering
   static constexpr int kAccCols = kNumAcc * kNumSub * BNT;
@@ -159,7 +161,7 @@ struct GemmCfg {
   // A ring slot must always have the same two owners: a waiter that is not the slot's only
   // consumer could run two uses ahead, where a one-bit mbarrier phase parity cannot tell
   // the phase it needs from the one before.  So the depth is a multiple of both counts.
-  static constexpr int kDeqWGs = Roles<BNT, kDirect>::kDeqWGs;
+  static constexpr int kDeqWGs = Roles<BNT, kDirect, A8>::kDeqWGs;
   static constexpr int kALcm = lcm_int(kDeqWGs, kIssuers);
   static constexpr int kAStages = kAStagesMax / kALcm * kALcm;
   // X ring: slots of kXChunk stages (one 3-D load per slot for narrow token tiles).
@@ -474,7 +476,7 @@ __device__ __forceinline__ void gather_row(uint32_t dst, const uint8_t* src, uin
 }
 
 template <int BNT, bool A8, int DM, bool GATHER>
-__global__ void __launch_bounds__(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N>::kThreads, 1)
+__global__ void __launch_bounds__(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N, A8>::kThreads, 1)
 qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constant__ GemmArgs a) {
   static_assert(!GATHER || BNT <= 64, "gathered tiles exist for token tiles up to 64");
   constexpr bool A4 = DM == DM_W4A4;
@@ -486,7 +488,7 @@ qgemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_x, const __grid_constan
   // per-token (per-row) output scale: FP8's token scale, or the FP16 copy's row scale
   constexpr bool kTokScale = A8 || F16;
   using C = GemmCfg<BNT, A8, A4, N8>;
-  using RO = Roles<BNT, kDirect>;
+  using RO = Roles<BNT, kDirect, A8>;
   constexpr int kEpiWarp0 = RO::kEpiWarp0;
   constexpr int kDeqWGs = RO::kDeqWGs;
   constexpr int kXProducerWarp = RO::kXProducerWarp;
@@ -1406,7 +1408,7 @@ cudaError_t launch_variant(const GemmPlan& plan, const CUtensorMap& tmap, const 
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(plan.grid));
-  cfg.blockDim = dim3(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N>::kThreads);
+  cfg.blockDim = dim3(Roles<BNT, DM == DM_W4A4 || DM == DM_W4A8N, A8>::kThreads);
   cfg.dynamicSmemBytes = kSmem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

@@ -343,6 +343,20 @@ def test_moe_workspace_bytes(L):
     assert qg.moe_workspace_bytes(d, 8, 0) == 0
 
 
+def test_moe_indexed_workspace_holds_the_copy_from_256_rows(L):
+    """The indexed MoE call gathers its rows into the workspace from 256 sorted rows on: the
+    workspace it asks for grows by exactly the sorted copy of the rows and their scales
+    there, and not below."""
+    d = qg.WeightDesc("mxfp4", 4096, 7168, 32)
+    for fp8, esz in ((False, 2), (True, 1)):
+        dd = qg.WeightDesc("mxfp4", 4096, 7168, 32, afmt="fp8") if fp8 else d
+        below = qg.moe_indexed_workspace_bytes(dd, 256, 40, 255, fp8=fp8)
+        at = qg.moe_indexed_workspace_bytes(dd, 256, 40, 256, fp8=fp8)
+        copy = -(-256 * 7168 * esz // 256) * 256 + -(-256 * 4 // 256) * 256
+        assert at - below == copy, (fp8, at, below)
+        assert qg.moe_indexed_workspace_bytes(dd, 256, 40, 200, fp8=fp8) == below
+
+
 def test_act_copy_bytes():
     """INT4 with BF16 scales runs on FP16 operands: the workspace leads with an FP16 copy of
     X ([rows][K], 256-byte rounded) and one FP32 row scale per row (256-byte rounded); no

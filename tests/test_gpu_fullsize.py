@@ -203,6 +203,55 @@ def test_moe_layer_sampled(T, skewed, gemm):
     assert ok, f"worst error / bound = {worst:.3f}"
 
 
+@pytest.mark.parametrize("T", [16, 128])
+@pytest.mark.parametrize("skewed", [False, True])
+def test_moe_indexed_layer_matches_grouped(T, skewed):
+    """The gate_up GEMM of the 256-expert layer at decode-to-prefill sizes on the indexed path
+    with the bench's indexed workspace (from 256 sorted rows on: the rows gathered into it,
+    then the grouped kernel; narrow tiles on FP16 operands): the same bits as the grouped
+    call on the sorted rows, which matches the oracle on sampled rows."""
+    from tests import gpu_util as G
+    import quantized_weight_gemm_gb300 as qg
+    case = WL.moe_case(T, seed=1, skewed=skewed)
+    N, K, E = 2 * WL.MOE_INTER, WL.MOE_HIDDEN, case.E
+    R = len(case.token_of_row)
+    assert R >= 256
+    d = qg.WeightDesc("mxfp4", N, K, 32, "bf16")
+    nb = qg.packed_bytes(d)
+    packed = torch.empty(nb * E, dtype=torch.uint8, device="cuda")
+    r = WL.rng(55)
+    ns = np.unique(np.concatenate([[0, N - 1], r.choice(N, size=62, replace=False)]))
+    valid_rows = np.nonzero(case.valid)[0]
+    ms = np.unique(np.concatenate([valid_rows[[0, -1]],
+                                   r.choice(valid_rows, size=min(46, len(valid_rows)), replace=False)]))
+    expert_of = np.searchsorted(case.offsets, ms, side="right") - 1
+    need = set(int(e) for e in expert_of)
+    rows_of = {}
+    for e, w in enumerate(WL.iter_moe_weights(E, N, K, seed=0)):
+        qg.repack(d, G.u8_tensor(w.codes), G.u8_tensor(w.scales), None,
+                  out=packed[e * nb:(e + 1) * nb])
+        if e in need:
+            rows_of[e] = (w.codes[ns], w.scales[ns])
+    off = torch.tensor(case.offsets, device="cuda")
+    y = qg.moe_grouped(d, packed, E, G.bf16_tensor(case.x_bits), off,
+                       ws=qg.moe_workspace(d, E, R), out=_nan_out(R, N))
+    idx = torch.from_numpy(case.token_of_row.astype(np.int32)).cuda()
+    yi = qg.moe_indexed(d, packed, E, G.bf16_tensor(case.x_tok_bits), off, idx,
+                        ws=qg.moe_indexed_workspace(d, E, T, R), out=_nan_out(R, N))
+    torch.cuda.synchronize()
+    assert qg.device_status(clear=True) == 0
+    assert torch.equal(y.view(torch.int16), yi.view(torch.int16))
+    ref = np.zeros((len(ms), len(ns)))
+    for i, (m, e) in enumerate(zip(ms, expert_of)):
+        codes, scales = rows_of[int(e)]
+        ref[i] = oracle.w4a16(case.x_bits[[m]], "mxfp4", 32, codes, scales)[0]
+    got = yi[torch.from_numpy(ms).cuda()][:, torch.from_numpy(ns).cuda()].double().cpu().numpy()
+    G.log_parity(f"fullsize moe indexed gate_up T={T} {'skewed' if skewed else 'uniform'}", got, ref,
+                 TOL_A16)
+    ok, worst = oracle.tolerance_ok(got, ref, TOL_A16)
+    assert ok, f"worst error / bound = {worst:.3f}"
+
+
 @pytest.mark.parametrize("wfmt", ["uint4_zp", "int4_sym", "mxint4"])
 @pytest.mark.parametrize("tile", [32, 64, 128])
 def test_cut_schedules_repeated(wfmt, tile):

@@ -918,7 +918,7 @@ def main():
                     help="skip the MXFP4, W4A8 and MoE sweeps reported beside the main line")
     ap.add_argument("--case", default=None, help="N,K,M[,wfmt[,afmt]]: time one GEMM shape")
     ap.add_argument("--moe", default=None,
-                    help="T,gate_up|down[,skewed][,indexed]: time one MoE GEMM of the layer")
+                    help="T,gate_up|down[,skewed][,indexed][,E<experts>][,top<k>]: time one MoE GEMM of the layer")
     args = ap.parse_args()
     if args.case:
         bench_case(args)
